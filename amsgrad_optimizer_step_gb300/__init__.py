@@ -1,0 +1,293 @@
+"""GB300 fused AdamW / AMSGrad step: thin Python binding of ``libfused_adamw.so``.
+
+Every function here marshals torch tensors into the C ABI of
+``include/fused_adamw.h`` under the same name; all arithmetic runs in the CUDA
+kernels of the library.  PyTorch supplies device memory and streams only.
+Layout checks that raw pointers cannot express (contiguity, strides, dtype,
+device) are made here, as the adapter's job ("実験的なデバイス上の融合 AdamW /
+AMSGrad", section "ネイティブ PyTorch ストレージと階層統計": the adapter validates
+shape, alias, lifetime and queue).
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  # noqa: F401
+                   FaStepReport, FusedAdamWError, check)
+
+__all__ = [
+    "fa_abi_version", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
+    "fa_adamw_step_inplace", "fa_bucket_step", "fa_stats_plan", "fa_stats_rows",
+    "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_read_report", "fa_clip_decision",
+    "fa_clip_decide", "fa_bucket_step_clipped", "options", "control", "stats_buffer",
+    "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
+]
+
+_TORCH_GRAD = {torch.float32: FA_F32, torch.float16: FA_F16, torch.bfloat16: FA_BF16}
+STATS_WORDS = 3  # a 12-byte record is three 32-bit words
+
+
+def _L():
+    return _lib.load()
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dense(name: str, t: torch.Tensor, n: int, dtypes, device=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.layout != torch.strided:
+        raise ValueError(f"{name}: sparse or non-strided tensors are not supported")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous() or (t.numel() > 1 and 0 in t.stride()):
+        raise ValueError(f"{name}: must be dense and contiguous (no strides, no broadcast)")
+    if t.numel() != n:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {n}")
+    if device is not None and t.numel() and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
+def options(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=1e-4, amsgrad=False,
+            maximize=False) -> FaOptions:
+    return FaOptions(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                     int(bool(amsgrad)), int(bool(maximize)))
+
+
+def control(gradient_scale: float = 1.0, skip_update: bool = False) -> FaStepControl:
+    return FaStepControl(float(gradient_scale), int(bool(skip_update)))
+
+
+def bytes_per_param(grad_bytes: int, amsgrad: bool, first_step: bool) -> int:
+    """Algorithmic HBM bytes one update moves per parameter.
+
+    FP32 parameter read and write; gradient read; m and v written, and read
+    unless this is the first step; AMSGrad adds the max state the same way
+    ("実験的なデバイス上の融合 AdamW / AMSGrad", section "割り当てとパフォーマンスのモデル":
+    28 bytes = 4 FP32 reads + 3 FP32 writes for an FP32 gradient).
+    """
+    states = 3 if amsgrad else 2
+    reads = 4 + grad_bytes + (0 if first_step else 4 * states)
+    writes = 4 + 4 * states
+    return reads + writes
+
+
+# ---- host-only -----------------------------------------------------------------
+
+def fa_abi_version() -> int:
+    return _L().fa_abi_version()
+
+
+def fa_options_default() -> FaOptions:
+    return _L().fa_options_default()
+
+
+def fa_step_coefficients(opts: FaOptions, t: int, gradient_scale: float = 1.0,
+                         grad_mult: float = 1.0) -> list[float]:
+    out = (ctypes.c_float * 9)()
+    check("fa_step_coefficients",
+          _L().fa_step_coefficients(ctypes.byref(opts), t, gradient_scale, grad_mult, out))
+    return list(out)
+
+
+def fa_stats_plan(rows: int) -> tuple[int, int]:
+    k = ctypes.c_int32()
+    e = ctypes.c_int64()
+    check("fa_stats_plan", _L().fa_stats_plan(rows, ctypes.byref(k), ctypes.byref(e)))
+    return k.value, e.value
+
+
+def _segments(seg_offsets: Optional[Sequence[int]]):
+    if seg_offsets is None:
+        return None, 0
+    arr = (ctypes.c_int64 * len(seg_offsets))(*[int(x) for x in seg_offsets])
+    return arr, len(seg_offsets) - 1
+
+
+def fa_stats_rows(n: int, row_len: int, seg_offsets: Optional[Sequence[int]] = None) -> int:
+    seg, nseg = _segments(seg_offsets)
+    r = ctypes.c_int64()
+    check("fa_stats_rows", _L().fa_stats_rows(n, row_len, seg, nseg, ctypes.byref(r)))
+    return r.value
+
+
+def fa_clip_decision(sum_sq_stored: float, nonfinite: int, gradient_scale: float,
+                     max_grad_norm: float) -> tuple[bool, float, float]:
+    s = ctypes.c_int32()
+    nrm = ctypes.c_double()
+    c = ctypes.c_double()
+    check("fa_clip_decision",
+          _L().fa_clip_decision(sum_sq_stored, nonfinite, gradient_scale, max_grad_norm,
+                                ctypes.byref(s), ctypes.byref(nrm), ctypes.byref(c)))
+    return bool(s.value), nrm.value, c.value
+
+
+# ---- the update ------------------------------------------------------------------
+
+def fa_adamw_step(p: torch.Tensor, g: torch.Tensor, m: Optional[torch.Tensor],
+                  v: Optional[torch.Tensor], vmax: Optional[torch.Tensor], t: int,
+                  opts: FaOptions, ctl: FaStepControl, stream=None):
+    """Out-of-place step.  Returns (p, m, v, vmax, t, updated).
+
+    Skip and empty steps allocate nothing and return the inputs unchanged.
+    """
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    for name, x in (("m", m), ("v", v), ("vmax", vmax)):
+        if x is not None:
+            _dense(name, x, n, (torch.float32,), p.device)
+    if n == 0 or ctl.skip_update:
+        # the library still validates; no output buffer is allocated
+        tout, upd = ctypes.c_uint64(), ctypes.c_int32()
+        check("fa_adamw_step", _L().fa_adamw_step(
+            n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
+            ctypes.byref(opts), ctl, None, None, None, None, ctypes.byref(tout),
+            ctypes.byref(upd), _stream(stream)))
+        return p, m, v, vmax, tout.value, False
+    p_out = torch.empty_like(p)
+    m_out = torch.empty_like(p)
+    v_out = torch.empty_like(p)
+    vmax_out = torch.empty_like(p) if opts.amsgrad else None
+    tout, upd = ctypes.c_uint64(), ctypes.c_int32()
+    check("fa_adamw_step", _L().fa_adamw_step(
+        n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
+        ctypes.byref(opts), ctl, _ptr(p_out), _ptr(m_out), _ptr(v_out), _ptr(vmax_out),
+        ctypes.byref(tout), ctypes.byref(upd), _stream(stream)))
+    return p_out, m_out, v_out, vmax_out, tout.value, bool(upd.value)
+
+
+def fa_adamw_step_inplace(p, g, m, v, vmax, t: int, opts: FaOptions, ctl: FaStepControl,
+                          grad_mult: float = 1.0, stream=None) -> tuple[int, bool]:
+    """In-place step on preallocated storage.  Returns (t, updated)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    tt, upd = ctypes.c_uint64(t), ctypes.c_int32()
+    check("fa_adamw_step_inplace", _L().fa_adamw_step_inplace(
+        n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, ctypes.byref(upd),
+        _stream(stream)))
+    return tt.value, bool(upd.value)
+
+
+def fa_bucket_step(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions, ctl: FaStepControl,
+                   grad_mult: float = 1.0, stream=None) -> tuple[int, bool]:
+    """One update launch over a pre-flattened bucket.  Returns (t, updated)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    seg, nseg = _segments(seg_offsets)
+    tt, upd = ctypes.c_uint64(t), ctypes.c_int32()
+    check("fa_bucket_step", _L().fa_bucket_step(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, ctypes.byref(upd),
+        _stream(stream)))
+    return tt.value, bool(upd.value)
+
+
+# ---- statistics ------------------------------------------------------------------
+
+def stats_buffer(rows: int, device) -> torch.Tensor:
+    """Device buffer of ``rows`` 12-byte records, as int32 [rows, 3]."""
+    return torch.empty((max(rows, 1), STATS_WORDS), dtype=torch.int32, device=device)
+
+
+def scratch_buffer(rows: int, device) -> torch.Tensor:
+    """Device scratch (FP32 elements) for merging ``rows`` records."""
+    _, e = fa_stats_plan(rows)
+    return torch.empty(max(e, 1), dtype=torch.float32, device=device)
+
+
+def _stats_tensor(name, t):
+    if t.dtype != torch.int32 or t.dim() != 2 or t.shape[1] != STATS_WORDS or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous int32 [rows, 3] stats buffer")
+
+
+def fa_analyze_gradient(g: torch.Tensor, row_len: int, rows_out: torch.Tensor,
+                        seg_offsets: Optional[Sequence[int]] = None, stream=None) -> int:
+    """Per-row statistics of ``g`` into ``rows_out``.  Returns the row count."""
+    _dense("g", g, g.numel(), tuple(_TORCH_GRAD))
+    _stats_tensor("rows_out", rows_out)
+    seg, nseg = _segments(seg_offsets)
+    rows = fa_stats_rows(g.numel(), row_len, seg_offsets)
+    check("fa_analyze_gradient", _L().fa_analyze_gradient(
+        _ptr(g), _TORCH_GRAD[g.dtype], g.numel(), row_len, seg, nseg, _ptr(rows_out),
+        rows_out.shape[0], _stream(stream)))
+    return rows
+
+
+def fa_merge_gradient_stats(rows_in: torch.Tensor, rows: int, scratch: Optional[torch.Tensor],
+                            report: torch.Tensor, stream=None) -> None:
+    _stats_tensor("rows_in", rows_in)
+    _stats_tensor("report", report)
+    if scratch is not None and (scratch.dtype != torch.float32 or not scratch.is_contiguous()):
+        raise ValueError("scratch: expected contiguous float32")
+    check("fa_merge_gradient_stats", _L().fa_merge_gradient_stats(
+        _ptr(rows_in), rows, _ptr(scratch), 0 if scratch is None else scratch.numel(),
+        _ptr(report), _stream(stream)))
+
+
+def fa_read_report(report: torch.Tensor, stream=None) -> FaStats:
+    _stats_tensor("report", report)
+    h = FaStats()
+    check("fa_read_report", _L().fa_read_report(_ptr(report), ctypes.byref(h), _stream(stream)))
+    return h
+
+
+def fa_clip_decide(report: torch.Tensor, gradient_scale: float, max_grad_norm: float,
+                   stream=None) -> tuple[bool, float, float]:
+    _stats_tensor("report", report)
+    s = ctypes.c_int32()
+    nrm = ctypes.c_double()
+    c = ctypes.c_double()
+    check("fa_clip_decide", _L().fa_clip_decide(
+        _ptr(report), gradient_scale, max_grad_norm, ctypes.byref(s), ctypes.byref(nrm),
+        ctypes.byref(c), _stream(stream)))
+    return bool(s.value), nrm.value, c.value
+
+
+def fa_bucket_step_clipped(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                           ctl: FaStepControl, max_grad_norm: float, row_len: int,
+                           rows_buf: torch.Tensor, scratch: Optional[torch.Tensor],
+                           report: torch.Tensor, stream=None) -> tuple[int, FaStepReport]:
+    """Analyse, merge, read back, decide, then update or skip.  Returns (t, report)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _stats_tensor("rows_buf", rows_buf)
+    _stats_tensor("report", report)
+    seg, nseg = _segments(seg_offsets)
+    tt = ctypes.c_uint64(t)
+    rep = FaStepReport()
+    check("fa_bucket_step_clipped", _L().fa_bucket_step_clipped(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, max_grad_norm, row_len, _ptr(rows_buf),
+        rows_buf.shape[0], _ptr(scratch), 0 if scratch is None else scratch.numel(),
+        _ptr(report), ctypes.byref(rep), _stream(stream)))
+    return tt.value, rep

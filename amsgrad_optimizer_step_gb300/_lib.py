@@ -1,0 +1,104 @@
+"""ctypes declarations of ``libfused_adamw.so`` (mirrors include/fused_adamw.h).
+
+Loading fails loudly when the library has not been built: there is no
+fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+c_i32, c_i64, c_u64, c_f64, c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
+                                    ctypes.c_double, ctypes.c_void_p)
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_DTYPE", 3: "FA_ERR_SIZE",
+                4: "FA_ERR_OPTION", 5: "FA_ERR_ALIAS", 6: "FA_ERR_POINTER", 7: "FA_ERR_ALIGN",
+                8: "FA_ERR_PLAN", 9: "FA_ERR_CUDA", 10: "FA_ERR_SEGMENTS"}
+FA_F32, FA_F16, FA_BF16 = 0, 1, 2
+
+
+class FaOptions(ctypes.Structure):
+    _fields_ = [("lr", c_f64), ("beta1", c_f64), ("beta2", c_f64), ("eps", c_f64),
+                ("weight_decay", c_f64), ("amsgrad", c_i32), ("maximize", c_i32)]
+
+
+class FaStepControl(ctypes.Structure):
+    _fields_ = [("gradient_scale", c_f64), ("skip_update", c_i32)]
+
+
+class FaStats(ctypes.Structure):
+    _fields_ = [("sum_sq", ctypes.c_float), ("nonfinite", ctypes.c_uint32),
+                ("sum_sq_lo", ctypes.c_float)]
+
+
+class FaStepReport(ctypes.Structure):
+    _fields_ = [("updated", c_i32), ("skipped_nonfinite", c_i32), ("nonfinite", c_u64),
+                ("grad_norm", c_f64), ("clip_coef", c_f64)]
+
+
+P = c_vp
+PI64 = ctypes.POINTER(c_i64)
+PU64 = ctypes.POINTER(c_u64)
+PI32 = ctypes.POINTER(c_i32)
+PF64 = ctypes.POINTER(c_f64)
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "fa_abi_version": (c_i32, []),
+    "fa_status_string": (ctypes.c_char_p, [c_i32]),
+    "fa_options_default": (FaOptions, []),
+    "fa_step_coefficients": (c_i32, [ctypes.POINTER(FaOptions), c_u64, c_f64, c_f64,
+                                     ctypes.POINTER(ctypes.c_float)]),
+    "fa_adamw_step": (c_i32, [c_i64, P, P, c_i32, P, P, P, c_u64, ctypes.POINTER(FaOptions),
+                              FaStepControl, P, P, P, P, PU64, PI32, P]),
+    "fa_adamw_step_inplace": (c_i32, [c_i64, P, P, c_i32, P, P, P, PU64,
+                                      ctypes.POINTER(FaOptions), FaStepControl, c_f64, PI32, P]),
+    "fa_bucket_step": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
+                               ctypes.POINTER(FaOptions), FaStepControl, c_f64, PI32, P]),
+    "fa_stats_plan": (c_i32, [c_i64, PI32, PI64]),
+    "fa_stats_rows": (c_i32, [c_i64, c_i32, PI64, c_i32, PI64]),
+    "fa_analyze_gradient": (c_i32, [P, c_i32, c_i64, c_i32, PI64, c_i32, P, c_i64, P]),
+    "fa_merge_gradient_stats": (c_i32, [P, c_i64, P, c_i64, P, P]),
+    "fa_read_report": (c_i32, [P, ctypes.POINTER(FaStats), P]),
+    "fa_clip_decision": (c_i32, [c_f64, c_u64, c_f64, c_f64, PI32, PF64, PF64]),
+    "fa_clip_decide": (c_i32, [P, c_f64, c_f64, PI32, PF64, PF64, P]),
+    "fa_bucket_step_clipped": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
+                                       ctypes.POINTER(FaOptions), FaStepControl, c_f64, c_i32,
+                                       P, c_i64, P, c_i64, P, ctypes.POINTER(FaStepReport), P]),
+}
+
+_LIB = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{os.path.basename(path)} is not built: run amsgrad_optimizer_step_gb300.build.build() "
+            "(nvcc, sm_103a). There is no CPU or library fallback.")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+class FusedAdamWError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = load().fa_status_string(status).decode()
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({msg})")
+
+
+def check(fn: str, status: int) -> None:
+    if status != FA_OK:
+        raise FusedAdamWError(fn, status)

@@ -1,0 +1,586 @@
+// C-ABI host layer: validation, FP64 host coefficients, the statistics plan,
+// the skip / clip decision, and kernel launches.  Everything that touches the
+// device goes through the kernels in update_kernels.cu and stats_kernels.cu.
+//
+// Contract sources (RUDA documentation pages):
+//   "実験的なデバイス上の融合 AdamW / AMSGrad" (ja/docs/fused-adamw): "この演算子を使用する
+//     理由" (formula, host FP64 coefficients, defaults), "サポートされている契約"
+//     (flattened buckets share options and step; no host pointers), "低レベルの使用"
+//     (AdamWOptions, StepControl, validation leaves inputs untouched, success =
+//     enqueued), "ネイティブ PyTorch ストレージと階層統計" (storage kernels, StatsPlan).
+//   "实验性融合 AdamW / AMSGrad" (zh/docs/fused-adamw): "增加的实际能力" (dtypes; empty
+//     tensor or skip_update launches nothing and does not advance the step).
+//   "训练与状态保存" (zh/docs/training): "在 ruda:0 上进行原生 PyTorch 训练" (12-byte
+//     report read back first, non-finite skip, global clip after unscale).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "fused_adamw.h"
+#include "internal.h"
+
+namespace fa {
+
+int sm_count(int device) {
+    static int cache[64] = {0};  // immutable device property
+    if (device >= 0 && device < 64 && cache[device] > 0) return cache[device];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return 0;
+    if (device >= 0 && device < 64) cache[device] = n;
+    return n;
+}
+
+}  // namespace fa
+
+namespace {
+
+using fa::Coef;
+
+bool is_finite(double x) { return std::isfinite(x); }
+
+// beta^t as an FP64 integer power (binary exponentiation).
+double int_pow(double beta, uint64_t t) {
+    double r = 1.0, b = beta;
+    while (t) {
+        if (t & 1) r *= b;
+        b *= b;
+        t >>= 1;
+    }
+    return r;
+}
+
+fa_status check_options(const fa_options *o) {
+    if (!o) return FA_ERR_NULL;
+    if (!is_finite(o->lr) || o->lr < 0) return FA_ERR_OPTION;
+    if (!is_finite(o->beta1) || o->beta1 < 0 || o->beta1 >= 1) return FA_ERR_OPTION;
+    if (!is_finite(o->beta2) || o->beta2 < 0 || o->beta2 >= 1) return FA_ERR_OPTION;
+    if (!is_finite(o->eps) || o->eps < 0) return FA_ERR_OPTION;
+    if (!is_finite(o->weight_decay) || o->weight_decay < 0) return FA_ERR_OPTION;
+    if ((o->amsgrad != 0 && o->amsgrad != 1) || (o->maximize != 0 && o->maximize != 1))
+        return FA_ERR_OPTION;
+    return FA_OK;
+}
+
+fa_status check_control(const fa_step_control &c) {
+    if (!is_finite(c.gradient_scale) || c.gradient_scale <= 0) return FA_ERR_OPTION;
+    if (c.skip_update != 0 && c.skip_update != 1) return FA_ERR_OPTION;
+    return FA_OK;
+}
+
+bool valid_dtype(fa_dtype d) { return d == FA_F32 || d == FA_F16 || d == FA_BF16; }
+size_t dtype_bytes(fa_dtype d) { return d == FA_F32 ? 4 : 2; }
+
+// Device of the stream (current device for the legacy default stream).
+fa_status stream_device(void *stream, int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    if (stream) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_POINTER;
+        }
+        if (sdev != *dev) return FA_ERR_POINTER;
+    }
+    return FA_OK;
+}
+
+// Device (or managed) memory of device ``dev``, aligned to ``align`` bytes.
+fa_status check_device_ptr(const void *p, int dev, size_t align) {
+    if (!p) return FA_ERR_NULL;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_POINTER;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return FA_ERR_POINTER;
+    if (at.device != dev) return FA_ERR_POINTER;
+    if (reinterpret_cast<uintptr_t>(p) % align) return FA_ERR_ALIGN;
+    return FA_OK;
+}
+
+struct Range {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlap(Range a, Range b) {
+    if (!a.p || !b.p || !a.bytes || !b.bytes) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool any_overlap(const Range *r, int count) {
+    for (int i = 0; i < count; ++i)
+        for (int j = i + 1; j < count; ++j)
+            if (overlap(r[i], r[j])) return true;
+    return false;
+}
+
+fa_status make_coef(const fa_options *o, uint64_t t, double scale, double grad_mult, Coef *c) {
+    if (t == 0) return FA_ERR_OPTION;
+    if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
+    const double bc1 = 1.0 - int_pow(o->beta1, t);
+    const double bc2 = 1.0 - int_pow(o->beta2, t);
+    if (!(bc1 > 0) || !(bc2 > 0)) return FA_ERR_OPTION;  // beta == 0 is fine; bc = 1
+    c->b1 = static_cast<float>(o->beta1);
+    c->omb1 = static_cast<float>(1.0 - o->beta1);
+    c->b2 = static_cast<float>(o->beta2);
+    c->omb2 = static_cast<float>(1.0 - o->beta2);
+    c->step_size = static_cast<float>(o->lr / bc1);
+    c->rbc2 = static_cast<float>(1.0 / bc2);
+    c->eps = static_cast<float>(o->eps);
+    c->decay = static_cast<float>(1.0 - o->lr * o->weight_decay);
+    c->gmul = static_cast<float>((o->maximize ? -1.0 : 1.0) * grad_mult / scale);
+    return FA_OK;
+}
+
+// First element index at which every pointer is 16-byte aligned (-1: none).
+int64_t vector_head(const void *const *ptrs, const size_t *esize, int count, int64_t n) {
+    for (int64_t h = 0; h < 8; ++h) {
+        bool ok = true;
+        for (int i = 0; i < count && ok; ++i)
+            if (ptrs[i] && (reinterpret_cast<uintptr_t>(ptrs[i]) + h * esize[i]) % 16) ok = false;
+        if (ok) return h < n ? h : n;
+    }
+    return -1;
+}
+
+// Shared by the out-of-place, in-place and bucket entry points: all pointers
+// already validated.
+fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt, const float *m,
+                         const float *v, const float *vmax, float *p_out, float *m_out,
+                         float *v_out, float *vmax_out, const fa_options *o, uint64_t t_new,
+                         double scale, double grad_mult, void *stream) {
+    Coef c;
+    fa_status st = make_coef(o, t_new, scale, grad_mult, &c);
+    if (st != FA_OK) return st;
+    const bool first = t_new == 1;
+    fa::UpdateArgs a;
+    a.p_in = p;
+    a.m_in = first ? nullptr : m;
+    a.v_in = first ? nullptr : v;
+    a.vmax_in = (first || !o->amsgrad) ? nullptr : vmax;
+    a.g = g;
+    a.p_out = p_out;
+    a.m_out = m_out;
+    a.v_out = v_out;
+    a.vmax_out = o->amsgrad ? vmax_out : nullptr;
+    a.n = n;
+    const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g,
+                          a.p_out, a.m_out, a.v_out, a.vmax_out};
+    const size_t es[] = {4, 4, 4, 4, dtype_bytes(gdt), 4, 4, 4, 4};
+    const int64_t head = vector_head(ptrs, es, 9, n);
+    const bool vec = head >= 0;
+    a.head = vec ? head : 0;
+    a.nvec = vec ? (n - a.head) / 8 : 0;
+    cudaError_t err = fa::launch_update(a, c, gdt, o->amsgrad != 0, first, vec,
+                                        static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Validates the in-place argument set; fills the ranges for alias checks.
+fa_status check_inplace(int64_t n, float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                        float *vmax, const fa_options *o, int dev) {
+    fa_status st;
+    if ((st = check_device_ptr(p, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(g, dev, dtype_bytes(gdt))) != FA_OK) return st;
+    if ((st = check_device_ptr(m, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(v, dev, 4)) != FA_OK) return st;
+    if (o->amsgrad && (st = check_device_ptr(vmax, dev, 4)) != FA_OK) return st;
+    if (!o->amsgrad && vmax) return FA_ERR_NULL;
+    const size_t b = static_cast<size_t>(n) * 4;
+    const Range r[] = {{p, b}, {g, static_cast<size_t>(n) * dtype_bytes(gdt)}, {m, b}, {v, b},
+                       {o->amsgrad ? vmax : nullptr, b}};
+    if (any_overlap(r, 5)) return FA_ERR_ALIAS;
+    return FA_OK;
+}
+
+fa_status check_segments(const int64_t *seg, int32_t nseg, int64_t n) {
+    if (nseg < 0) return FA_ERR_SEGMENTS;
+    if (nseg == 0) return FA_OK;
+    if (!seg) return FA_ERR_NULL;
+    if (seg[0] != 0 || seg[nseg] != n) return FA_ERR_SEGMENTS;
+    for (int32_t k = 0; k < nseg; ++k)
+        if (seg[k + 1] < seg[k]) return FA_ERR_SEGMENTS;
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t fa_abi_version(void) { return FA_ABI_VERSION; }
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL: return "null pointer, or state pointers inconsistent with the step count";
+        case FA_ERR_DTYPE: return "unsupported gradient dtype";
+        case FA_ERR_SIZE: return "negative size or buffer too small";
+        case FA_ERR_OPTION: return "option or control value out of range";
+        case FA_ERR_ALIAS: return "buffers overlap";
+        case FA_ERR_POINTER: return "not device memory of the current device";
+        case FA_ERR_ALIGN: return "pointer not aligned to its element size";
+        case FA_ERR_PLAN: return "statistics rows outside 1..4194304";
+        case FA_ERR_CUDA: return "CUDA error";
+        case FA_ERR_SEGMENTS: return "malformed segment table";
+    }
+    return "unknown status";
+}
+
+fa_options fa_options_default(void) {
+    fa_options o;
+    o.lr = 1e-3;
+    o.beta1 = 0.9;
+    o.beta2 = 0.999;
+    o.eps = 1e-5;
+    o.weight_decay = 1e-4;
+    o.amsgrad = 0;
+    o.maximize = 0;
+    return o;
+}
+
+fa_status fa_step_coefficients(const fa_options *options, uint64_t t, double gradient_scale,
+                               double grad_mult, float coef_out[9]) {
+    fa_status st = check_options(options);
+    if (st != FA_OK) return st;
+    if (!coef_out) return FA_ERR_NULL;
+    fa_step_control ctl{gradient_scale, 0};
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    Coef c;
+    if ((st = make_coef(options, t, gradient_scale, grad_mult, &c)) != FA_OK) return st;
+    const float v[9] = {c.b1, c.omb1, c.b2, c.omb2, c.step_size, c.rbc2, c.eps, c.decay, c.gmul};
+    std::memcpy(coef_out, v, sizeof v);
+    return FA_OK;
+}
+
+fa_status fa_adamw_step(int64_t n, const float *p, const void *g, fa_dtype gdt, const float *m,
+                        const float *v, const float *vmax, uint64_t t_in,
+                        const fa_options *options, fa_step_control ctl, float *p_out,
+                        float *m_out, float *v_out, float *vmax_out, uint64_t *t_out,
+                        int32_t *updated, void *stream) {
+    fa_status st;
+    if (!t_out || !updated) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n < 0) return FA_ERR_SIZE;
+    if (n == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
+        *t_out = t_in;
+        *updated = 0;
+        return FA_OK;
+    }
+    const bool ams = options->amsgrad != 0;
+    // State is None before the first update: all moment pointers NULL.
+    if (t_in == 0) {
+        if (m || v || vmax) return FA_ERR_NULL;
+    } else {
+        if (!m || !v || (ams != (vmax != nullptr))) return FA_ERR_NULL;
+    }
+    if (t_in == UINT64_MAX) return FA_ERR_OPTION;
+    {
+        int dev = 0;
+        if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+        const size_t gb = dtype_bytes(gdt);
+        if ((st = check_device_ptr(p, dev, 4)) != FA_OK) return st;
+        if ((st = check_device_ptr(g, dev, gb)) != FA_OK) return st;
+        if (t_in > 0) {
+            if ((st = check_device_ptr(m, dev, 4)) != FA_OK) return st;
+            if ((st = check_device_ptr(v, dev, 4)) != FA_OK) return st;
+            if (ams && (st = check_device_ptr(vmax, dev, 4)) != FA_OK) return st;
+        }
+        if ((st = check_device_ptr(p_out, dev, 4)) != FA_OK) return st;
+        if ((st = check_device_ptr(m_out, dev, 4)) != FA_OK) return st;
+        if ((st = check_device_ptr(v_out, dev, 4)) != FA_OK) return st;
+        if (ams && (st = check_device_ptr(vmax_out, dev, 4)) != FA_OK) return st;
+        if (!ams && vmax_out) return FA_ERR_NULL;
+        const size_t b = static_cast<size_t>(n) * 4;
+        const Range outs[] = {{p_out, b}, {m_out, b}, {v_out, b}, {ams ? vmax_out : nullptr, b}};
+        const Range ins[] = {{p, b}, {g, static_cast<size_t>(n) * gb}, {m, b}, {v, b},
+                             {ams ? vmax : nullptr, b}};
+        if (any_overlap(outs, 4)) return FA_ERR_ALIAS;
+        for (const Range &o : outs)
+            for (const Range &i : ins)
+                if (overlap(o, i)) return FA_ERR_ALIAS;
+    }
+    st = enqueue_update(n, p, g, gdt, m, v, vmax, p_out, m_out, v_out, vmax_out, options,
+                        t_in + 1, ctl.gradient_scale, 1.0, stream);
+    if (st != FA_OK) return st;
+    *t_out = t_in + 1;
+    *updated = 1;
+    return FA_OK;
+}
+
+fa_status fa_adamw_step_inplace(int64_t n, float *p, const void *g, fa_dtype gdt, float *m,
+                                float *v, float *vmax, uint64_t *t,
+                                const fa_options *options, fa_step_control ctl,
+                                double grad_mult, int32_t *updated, void *stream) {
+    fa_status st;
+    if (!t || !updated) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n < 0) return FA_ERR_SIZE;
+    if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
+    if (n == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
+        *updated = 0;
+        return FA_OK;
+    }
+    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    st = enqueue_update(n, p, g, gdt, m, v, vmax, p, m, v, vmax, options, *t + 1,
+                        ctl.gradient_scale, grad_mult, stream);
+    if (st != FA_OK) return st;
+    *t += 1;
+    *updated = 1;
+    return FA_OK;
+}
+
+fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_total, float *p,
+                         const void *g, fa_dtype gdt, float *m, float *v, float *vmax,
+                         uint64_t *t, const fa_options *options, fa_step_control ctl,
+                         double grad_mult, int32_t *updated, void *stream) {
+    if (n_total < 0) return FA_ERR_SIZE;
+    fa_status st = check_segments(seg_offsets, nseg, n_total);
+    if (st != FA_OK) return st;
+    return fa_adamw_step_inplace(n_total, p, g, gdt, m, v, vmax, t, options, ctl, grad_mult,
+                                 updated, stream);
+}
+
+// ---- statistics ---------------------------------------------------------------
+
+fa_status fa_stats_plan(int64_t rows, int32_t *merge_kernels, int64_t *scratch_elements) {
+    if (!merge_kernels || !scratch_elements) return FA_ERR_NULL;
+    if (rows < 1 || rows > fa::kMaxRows) return FA_ERR_PLAN;
+    int32_t k = 0;
+    int64_t scratch_records = 0;
+    for (int64_t c = rows;;) {
+        c = (c + fa::kFanIn - 1) / fa::kFanIn;
+        ++k;
+        if (c == 1) break;
+        scratch_records += c;
+    }
+    *merge_kernels = k;
+    *scratch_elements = 3 * scratch_records;  // 12-byte records = 3 FP32 words
+    return FA_OK;
+}
+
+fa_status fa_stats_rows(int64_t n, int32_t row_len, const int64_t *seg_offsets, int32_t nseg,
+                        int64_t *rows) {
+    if (!rows) return FA_ERR_NULL;
+    if (n < 0 || row_len <= 0) return FA_ERR_SIZE;
+    fa_status st = check_segments(seg_offsets, nseg, n);
+    if (st != FA_OK) return st;
+    int64_t r = 0;
+    if (nseg == 0) {
+        r = (n + row_len - 1) / row_len;
+    } else {
+        for (int32_t k = 0; k < nseg; ++k)
+            r += (seg_offsets[k + 1] - seg_offsets[k] + row_len - 1) / row_len;
+    }
+    *rows = r;
+    return FA_OK;
+}
+
+fa_status fa_analyze_gradient(const void *g, fa_dtype gdt, int64_t n, int32_t row_len,
+                              const int64_t *seg_offsets, int32_t nseg, fa_stats *rows_out,
+                              int64_t rows_capacity, void *stream) {
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    int64_t rows = 0;
+    fa_status st = fa_stats_rows(n, row_len, seg_offsets, nseg, &rows);
+    if (st != FA_OK) return st;
+    if (rows < 1 || rows > fa::kMaxRows) return FA_ERR_PLAN;
+    if (rows_capacity < rows) return FA_ERR_SIZE;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    const size_t gb = dtype_bytes(gdt);
+    if ((st = check_device_ptr(g, dev, gb)) != FA_OK) return st;
+    if ((st = check_device_ptr(rows_out, dev, 4)) != FA_OK) return st;
+    if (overlap({g, static_cast<size_t>(n) * gb}, {rows_out, static_cast<size_t>(rows) * 12}))
+        return FA_ERR_ALIAS;
+
+    const int64_t one[2] = {0, n};
+    const int64_t *seg = nseg == 0 ? one : seg_offsets;
+    const int32_t ns = nseg == 0 ? 1 : nseg;
+    // 16-byte loads need every row start aligned: aligned base, segment starts
+    // and row length all multiples of 16 bytes.
+    bool vec = reinterpret_cast<uintptr_t>(g) % 16 == 0 && (row_len * gb) % 16 == 0;
+    for (int32_t k = 0; k < ns && vec; ++k) vec = (seg[k] * gb) % 16 == 0;
+
+    int64_t row_base = 0;
+    for (int32_t k0 = 0; k0 < ns; k0 += fa::kMaxSegPerLaunch) {
+        const int32_t cnt = ns - k0 < fa::kMaxSegPerLaunch ? ns - k0 : fa::kMaxSegPerLaunch;
+        fa::AnalyzeArgs a;
+        a.g = g;
+        a.out = rows_out + row_base;
+        a.row_len = row_len;
+        a.nseg = cnt;
+        int64_t r = 0;
+        for (int32_t j = 0; j <= cnt; ++j) {
+            a.seg_start[j] = seg[k0 + j];
+            a.row_start[j] = r;
+            if (j < cnt) r += (seg[k0 + j + 1] - seg[k0 + j] + row_len - 1) / row_len;
+        }
+        a.rows = r;
+        if (r > 0) {
+            cudaError_t err = fa::launch_analyze(a, gdt, vec, static_cast<cudaStream_t>(stream));
+            if (err != cudaSuccess) return FA_ERR_CUDA;
+        }
+        row_base += r;
+    }
+    return FA_OK;
+}
+
+fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *scratch,
+                                  int64_t scratch_elements, fa_stats *report, void *stream) {
+    int32_t kernels = 0;
+    int64_t need = 0;
+    fa_status st = fa_stats_plan(rows, &kernels, &need);
+    if (st != FA_OK) return st;
+    if (scratch_elements < need || (need > 0 && !scratch)) return FA_ERR_SIZE;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(rows_in, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(report, dev, 4)) != FA_OK) return st;
+    if (need > 0 && (st = check_device_ptr(scratch, dev, 4)) != FA_OK) return st;
+    const Range r[] = {{rows_in, static_cast<size_t>(rows) * 12},
+                       {scratch, static_cast<size_t>(need) * 4},
+                       {report, 12}};
+    if (any_overlap(r, 3)) return FA_ERR_ALIAS;
+
+    const fa_stats *in = rows_in;
+    int64_t count = rows;
+    fa_stats *next = reinterpret_cast<fa_stats *>(scratch);
+    for (int32_t level = 0; level < kernels; ++level) {
+        const int64_t out_count = (count + fa::kFanIn - 1) / fa::kFanIn;
+        fa_stats *out = out_count == 1 ? report : next;
+        cudaError_t err = fa::launch_merge(in, count, out, static_cast<cudaStream_t>(stream));
+        if (err != cudaSuccess) return FA_ERR_CUDA;
+        in = out;
+        count = out_count;
+        next = out + out_count;
+    }
+    return FA_OK;
+}
+
+fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream) {
+    if (!report_host) return FA_ERR_NULL;
+    int dev = 0;
+    fa_status st = stream_device(stream, &dev);
+    if (st != FA_OK) return st;
+    if ((st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
+    fa_stats tmp;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&tmp, report_dev, sizeof tmp, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    *report_host = tmp;
+    return FA_OK;
+}
+
+fa_status fa_clip_decision(double sum_sq_stored, uint64_t nonfinite, double gradient_scale,
+                           double max_grad_norm, int32_t *skip, double *grad_norm,
+                           double *clip_coef) {
+    if (!skip || !grad_norm || !clip_coef) return FA_ERR_NULL;
+    if (!is_finite(gradient_scale) || gradient_scale <= 0) return FA_ERR_OPTION;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    const int32_t s = nonfinite > 0;
+    const double norm = std::sqrt(sum_sq_stored) / gradient_scale;
+    double coef = 1.0;
+    if (!s && max_grad_norm > 0 && norm > max_grad_norm) coef = max_grad_norm / norm;
+    *skip = s;
+    *grad_norm = norm;
+    *clip_coef = coef;
+    return FA_OK;
+}
+
+fa_status fa_clip_decide(const fa_stats *report_dev, double gradient_scale, double max_grad_norm,
+                         int32_t *skip, double *grad_norm, double *clip_coef, void *stream) {
+    if (!skip || !grad_norm || !clip_coef) return FA_ERR_NULL;
+    fa_stats h;
+    fa_status st = fa_read_report(report_dev, &h, stream);
+    if (st != FA_OK) return st;
+    const double sum = static_cast<double>(h.sum_sq) + static_cast<double>(h.sum_sq_lo);
+    return fa_clip_decision(sum, h.nonfinite, gradient_scale, max_grad_norm, skip, grad_norm,
+                            clip_coef);
+}
+
+fa_status fa_bucket_step_clipped(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                 float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                                 float *vmax, uint64_t *t, const fa_options *options,
+                                 fa_step_control ctl, double max_grad_norm, int32_t row_len,
+                                 fa_stats *rows_buf, int64_t rows_capacity, float *scratch,
+                                 int64_t scratch_elements, fa_stats *report_dev,
+                                 fa_step_report *out, void *stream) {
+    fa_status st;
+    if (!t || !out) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n_total < 0) return FA_ERR_SIZE;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    fa_step_report rep{0, 0, 0, 0.0, 1.0};
+    if (n_total == 0 || ctl.skip_update) {
+        *out = rep;
+        return FA_OK;
+    }
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    int64_t rows = 0;
+    if ((st = fa_stats_rows(n_total, row_len, seg_offsets, nseg, &rows)) != FA_OK) return st;
+    int32_t kernels = 0;
+    int64_t need = 0;
+    if ((st = fa_stats_plan(rows, &kernels, &need)) != FA_OK) return st;
+    if (rows_capacity < rows || scratch_elements < need) return FA_ERR_SIZE;
+    const size_t b = static_cast<size_t>(n_total) * 4;
+    const Range r[] = {{p, b}, {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b},
+                       {v, b}, {options->amsgrad ? vmax : nullptr, b},
+                       {rows_buf, static_cast<size_t>(rows) * 12},
+                       {scratch, static_cast<size_t>(need) * 4}, {report_dev, 12}};
+    if (any_overlap(r, 8)) return FA_ERR_ALIAS;
+
+    if ((st = fa_analyze_gradient(g, gdt, n_total, row_len, seg_offsets, nseg, rows_buf,
+                                  rows_capacity, stream)) != FA_OK)
+        return st;
+    if ((st = fa_merge_gradient_stats(rows_buf, rows, scratch, scratch_elements, report_dev,
+                                      stream)) != FA_OK)
+        return st;
+    fa_stats h;
+    if ((st = fa_read_report(report_dev, &h, stream)) != FA_OK) return st;
+    int32_t skip = 0;
+    double norm = 0, coef = 1;
+    const double sum = static_cast<double>(h.sum_sq) + static_cast<double>(h.sum_sq_lo);
+    if ((st = fa_clip_decision(sum, h.nonfinite, ctl.gradient_scale, max_grad_norm, &skip, &norm,
+                               &coef)) != FA_OK)
+        return st;
+    rep.nonfinite = h.nonfinite;
+    rep.grad_norm = norm;
+    rep.clip_coef = coef;
+    if (skip) {
+        rep.skipped_nonfinite = 1;
+        *out = rep;
+        return FA_OK;
+    }
+    st = enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, *t + 1,
+                        ctl.gradient_scale, coef, stream);
+    if (st != FA_OK) return st;
+    *t += 1;
+    rep.updated = 1;
+    *out = rep;
+    return FA_OK;
+}
+
+}  // extern "C"

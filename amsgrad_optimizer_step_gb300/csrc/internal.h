@@ -1,0 +1,62 @@
+// Internal interface between the C-ABI host layer (abi.cpp) and the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "fused_adamw.h"
+
+namespace fa {
+
+constexpr int kThreads = 256;            // threads per CTA for every kernel here
+constexpr int kFanIn = 1024;             // merge fan-in
+constexpr int64_t kMaxRows = 4194304;    // largest statistics plan
+constexpr int kMaxSegPerLaunch = 240;    // segment table entries carried in kernel parameters
+
+// FP32 coefficients of one update, computed on the host in FP64.
+struct Coef {
+    float b1, omb1, b2, omb2;
+    float step_size;  // lr / (1 - beta1^t)
+    float rbc2;       // 1 / (1 - beta2^t)
+    float eps;
+    float decay;      // 1 - lr * weight_decay
+    float gmul;       // (maximize ? -1 : 1) * grad_mult / gradient_scale
+};
+
+// Pointers of one update launch.  In place: *_out == *_in.
+struct UpdateArgs {
+    const float *p_in, *m_in, *v_in, *vmax_in;
+    const void *g;
+    float *p_out, *m_out, *v_out, *vmax_out;
+    int64_t n;     // elements
+    int64_t head;  // scalar elements before the 16-byte aligned vector body
+    int64_t nvec;  // 8-element vectors in the body
+};
+
+// Enqueues one update kernel over a.n elements.  vector_ok: every pointer is
+// 16-byte aligned at element a.head.  Returns the CUDA launch status.
+cudaError_t launch_update(const UpdateArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,
+                          bool first, bool vector_ok, cudaStream_t stream);
+
+// Row-statistics launch over up to kMaxSegPerLaunch segments.
+struct AnalyzeArgs {
+    const void *g;
+    fa_stats *out;        // first row record of this launch
+    int64_t row_len;
+    int64_t rows;         // rows in this launch
+    int32_t nseg;         // segments in this launch
+    int64_t seg_start[kMaxSegPerLaunch + 1];  // element offsets; [nseg] = end of the last
+    int64_t row_start[kMaxSegPerLaunch + 1];  // first row of each segment; [nseg] = rows
+};
+
+cudaError_t launch_analyze(const AnalyzeArgs &a, fa_dtype gdt, bool vector_ok,
+                           cudaStream_t stream);
+
+// One merge level: ceil(count / kFanIn) output records from count input records.
+cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream);
+
+// SM count of the current device (cached per device).
+int sm_count(int device);
+
+}  // namespace fa

@@ -1,0 +1,236 @@
+// Gradient statistics for sm_103a: per-row analysis and the fan-in-1024 merge.
+//
+// Follows RUDA "训练与状态保存" (zh/docs/training), section "在 ruda:0 上进行原生
+// PyTorch 训练" (read-only gradient analysis; a 12-byte report read back before
+// the update; any non-finite gradient skips the step; hierarchical statistics
+// at fan-in 1024 change the reduction order only) and "実験的なデバイス上の融合
+// AdamW / AMSGrad" (ja/docs/fused-adamw), section "ネイティブ PyTorch ストレージと
+// 階層統計" (analyze_gradient, merge_gradient_stats, up to 4,194,304 rows).
+//
+// Record layout (12 bytes): {sum_sq: f32, nonfinite: u32, sum_sq_lo: f32}.
+// A row's sum of squares is accumulated in FP32 (8 values per lane, then a
+// warp shuffle tree) -- at 256 elements per row its relative error stays
+// below 1e-6.  Merges widen to FP64, add, and hand the FP64 total to the next
+// level as a (hi, lo) pair of floats, so later levels lose nothing.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kVec = 8;
+constexpr int kRowsPerWarp = 4;  // rows a warp analyses concurrently
+
+// Widened value and whether the stored pattern is NaN or +-Inf (exponent all ones).
+template <int GT>
+struct StatIO;
+
+template <>
+struct StatIO<FA_F32> {
+    static __device__ __forceinline__ void acc1(uint32_t b, float &s, uint32_t &c) {
+        const bool bad = (b & 0x7f800000u) == 0x7f800000u;
+        const float x = __uint_as_float(b);
+        c += bad;
+        s = bad ? s : fmaf(x, x, s);
+    }
+    static __device__ __forceinline__ void acc8(const void *g, int64_t i, float &s, uint32_t &c) {
+        const uint4 *q = reinterpret_cast<const uint4 *>(static_cast<const float *>(g) + i);
+        uint4 a = __ldcs(q);
+        uint4 b = __ldcs(q + 1);
+        acc1(a.x, s, c); acc1(a.y, s, c); acc1(a.z, s, c); acc1(a.w, s, c);
+        acc1(b.x, s, c); acc1(b.y, s, c); acc1(b.z, s, c); acc1(b.w, s, c);
+    }
+    static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
+        acc1(__ldcs(reinterpret_cast<const unsigned int *>(g) + i), s, c);
+    }
+};
+
+template <>
+struct StatIO<FA_BF16> {
+    static __device__ __forceinline__ void acc1(uint32_t h, float &s, uint32_t &c) {
+        const bool bad = (h & 0x7f80u) == 0x7f80u;
+        const float x = __uint_as_float(h << 16);
+        c += bad;
+        s = bad ? s : fmaf(x, x, s);
+    }
+    static __device__ __forceinline__ void acc8(const void *g, int64_t i, float &s, uint32_t &c) {
+        uint4 r = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + i));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc1(w[k] & 0xffffu, s, c);
+            acc1(w[k] >> 16, s, c);
+        }
+    }
+    static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
+        acc1(__ldcs(static_cast<const unsigned short *>(g) + i), s, c);
+    }
+};
+
+template <>
+struct StatIO<FA_F16> {
+    static __device__ __forceinline__ void acc1(uint32_t h, float &s, uint32_t &c) {
+        const bool bad = (h & 0x7c00u) == 0x7c00u;
+        const float x = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+        c += bad;
+        s = bad ? s : fmaf(x, x, s);
+    }
+    static __device__ __forceinline__ void acc8(const void *g, int64_t i, float &s, uint32_t &c) {
+        uint4 r = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + i));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc1(w[k] & 0xffffu, s, c);
+            acc1(w[k] >> 16, s, c);
+        }
+    }
+    static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
+        acc1(__ldcs(static_cast<const unsigned short *>(g) + i), s, c);
+    }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Segment holding launch-relative row r (binary search; warp-uniform).
+__device__ __forceinline__ int find_segment(const AnalyzeArgs &a, int64_t r) {
+    int lo = 0, hi = a.nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.row_start[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// One warp per row, kRowsPerWarp rows in flight per warp.  Lane l reads
+// elements [l*8, l*8+8) of each 256-element stretch of its rows.
+template <int GT, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+analyze_kernel(const __grid_constant__ AnalyzeArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+
+    for (int64_t r0 = warp * kRowsPerWarp; r0 < a.rows; r0 += nwarps * kRowsPerWarp) {
+        float s[kRowsPerWarp];
+        uint32_t c[kRowsPerWarp];
+#pragma unroll
+        for (int j = 0; j < kRowsPerWarp; ++j) {
+            s[j] = 0.f;
+            c[j] = 0;
+            const int64_t r = r0 + j;
+            if (r < a.rows) {
+                const int k = a.nseg == 1 ? 0 : find_segment(a, r);
+                const int64_t start = a.seg_start[k] + (r - a.row_start[k]) * a.row_len;
+                const int64_t seg_end = a.seg_start[k + 1];
+                const int64_t end = start + a.row_len < seg_end ? start + a.row_len : seg_end;
+                for (int64_t i = start + lane * kVec; i < end; i += 32 * kVec) {
+                    if (VEC && i + kVec <= end) {
+                        StatIO<GT>::acc8(a.g, i, s[j], c[j]);
+                    } else {
+                        const int64_t e = i + kVec < end ? i + kVec : end;
+                        for (int64_t q = i; q < e; ++q) StatIO<GT>::accs(a.g, q, s[j], c[j]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kRowsPerWarp; ++j) {
+            const float tot = warp_sum(s[j]);
+            const uint32_t cnt = __reduce_add_sync(0xffffffffu, c[j]);
+            const int64_t r = r0 + j;
+            if (lane == j && r < a.rows) {
+                fa_stats rec;
+                rec.sum_sq = tot;
+                rec.nonfinite = cnt;
+                rec.sum_sq_lo = 0.f;
+                a.out[r] = rec;
+            }
+        }
+    }
+}
+
+// One CTA per group of kFanIn input records.
+__global__ void __launch_bounds__(kThreads)
+merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
+    __shared__ double s_sum[kThreads / 32];
+    __shared__ unsigned long long s_cnt[kThreads / 32];
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kFanIn;
+    const int64_t g1 = g0 + kFanIn < count ? g0 + kFanIn : count;
+
+    double s = 0.0;
+    unsigned long long c = 0;
+    for (int64_t i = g0 + threadIdx.x; i < g1; i += kThreads) {
+        const fa_stats r = in[i];
+        s += static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
+        c += r.nonfinite;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        s_sum[w] = s;
+        s_cnt[w] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double ts = 0.0;
+        unsigned long long tc = 0;
+        for (int k = 0; k < kThreads / 32; ++k) {
+            ts += s_sum[k];
+            tc += s_cnt[k];
+        }
+        fa_stats rec;
+        rec.sum_sq = static_cast<float>(ts);
+        rec.sum_sq_lo = static_cast<float>(ts - static_cast<double>(rec.sum_sq));
+        rec.nonfinite = tc > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(tc);
+        out[blockIdx.x] = rec;
+    }
+}
+
+template <int GT>
+cudaError_t launch_analyze_typed(const AnalyzeArgs &a, bool vec, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t warps_needed = (a.rows + kRowsPerWarp - 1) / kRowsPerWarp;
+    const int64_t need = (warps_needed * 32 + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs (64 warps) per SM
+    const int grid = static_cast<int>(need < cap ? need : cap);
+    if (grid == 0) return cudaSuccess;
+    if (vec) analyze_kernel<GT, true><<<grid, kThreads, 0, stream>>>(a);
+    else analyze_kernel<GT, false><<<grid, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_analyze(const AnalyzeArgs &a, fa_dtype gdt, bool vector_ok,
+                           cudaStream_t stream) {
+    switch (gdt) {
+        case FA_F32: return launch_analyze_typed<FA_F32>(a, vector_ok, stream);
+        case FA_F16: return launch_analyze_typed<FA_F16>(a, vector_ok, stream);
+        case FA_BF16: return launch_analyze_typed<FA_BF16>(a, vector_ok, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream) {
+    const int64_t grid = (count + kFanIn - 1) / kFanIn;
+    if (grid <= 0) return cudaSuccess;
+    merge_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(in, count, out);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

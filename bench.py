@@ -1,0 +1,367 @@
+#!/usr/bin/env python3
+"""Throughput of the fused AdamW step with its gradient statistics on GB300.
+
+One step is the whole hot path on the 1,073,741,824-parameter FP32 bucket with
+BF16 gradients: row analysis (4,194,304 rows of 256), the fan-in-1024 merge,
+the 12-byte report read back, the skip / global-norm clip decision
+(max_grad_norm 1.0), and the fused update.  Inputs are synthetic and seeded,
+resident in HBM before the timed region; each step moves ~30 GB, far more than
+the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU, each rank holding its own
+1.07e9-parameter shard of an N x larger bucket (weak scaling); the ranks
+exchange only the 12-byte statistics per step to take one global decision.
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload (the pages publish no implementation to run).
+Prints one JSON line (rank 0).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused AdamW params/sec and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n", type=int, default=0, help="override the parameter count (testing)")
+    return ap.parse_args()
+
+
+def workload(n_override=0):
+    from synthetic.configs import CONFIG5
+    w = CONFIG5
+    if n_override:
+        w = w.scaled(n_override)
+    return w
+
+
+def config_dict(w):
+    return {"workload": w.name, "params": w.n, "param_dtype": "f32", "grad_dtype": w.grad_dtype,
+            "optimizer": "adamw", "lr": w.lr, "betas": [w.beta1, w.beta2], "eps": w.eps,
+            "weight_decay": w.weight_decay, "row_len": w.row_len, "merge_fan_in": 1024,
+            "max_grad_norm": w.max_grad_norm, "gradient_scale": w.gradient_scale,
+            "l2_policy": "inputs larger than L2 (about 30 GB moved per step), no flush"}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- clocks during the timed region -------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd[1:1] = ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---- CPU baseline: the oracle ---------------------------------------------------
+
+def oracle_steps(w, sample: int, steps: int, warmup: int):
+    """Times the oracle's whole step (global stats, decision, update) on ``sample``
+    elements of the workload; returns (seconds per step, cores used)."""
+    import numpy as np
+    import oracle
+    lib = oracle.lib()
+    idx = np.arange(sample)
+    grads = [w.grad_host(c, idx) for c in (1, 2)]
+    o = oracle.OracleAdamW(w.params_host(idx), w.options(), storage="f32", lib_=lib)
+    times = []
+    for k in range(warmup + steps):
+        g = grads[k % 2]
+        t0 = time.perf_counter()
+        s, c = lib.gradient_stats(g, "bf16", w.gradient_scale)
+        skip, _, coef = lib.clip_decision(s, c, w.max_grad_norm)
+        o.step(g, "bf16", w.gradient_scale, skip_update=skip, clip_coef=coef)
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times[warmup:]), 1
+
+
+def cpu_baseline(w, target_s=12.0):
+    sample = 1 << 22
+    sec, cores = oracle_steps(w, sample, steps=1, warmup=0)
+    steps = max(2, int(target_s / max(sec, 1e-3)))
+    sec, cores = oracle_steps(w, sample, steps=steps, warmup=1)
+    return {"value": sample / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{sample} elements of the {w.name} recipe (BF16 gradients, FP32 state), "
+                      f"{steps} full steps (global stats + decision + update), single-threaded "
+                      "FP64 C loop, median step"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = workload(args.n)
+    sample = 1 << 22
+    sec, cores = oracle_steps(w, sample, steps=args.steps, warmup=args.warmup)
+    value = sample / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{sample} elements per step of the {w.name} recipe"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- the GPU arm -----------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import amsgrad_optimizer_step_gb300 as fa
+    from amsgrad_optimizer_step_gb300 import build, sharded
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    build.build()
+    w = workload(args.n)
+    n = w.n
+    row_len = w.row_len
+    opts = fa.options(**w.options())
+    ctl = fa.control(w.gradient_scale)
+
+    # resident inputs: this rank's shard (weak scaling: same size on every rank)
+    p = torch.empty(n, dtype=torch.float32, device=dev)
+    w.fill_params_device(p)
+    m = torch.empty_like(p)
+    v = torch.empty_like(p)
+    g = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    w.fill_grad_device(1, g)
+    rows = fa.fa_stats_rows(n, row_len)
+    rows_buf = fa.stats_buffer(rows, dev)
+    scratch = fa.scratch_buffer(rows, dev)
+    report = fa.stats_buffer(1, dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    state = {"t": 0}
+    launches = {"n": 0}
+    merge_kernels, _ = fa.fa_stats_plan(rows)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        fa.fa_analyze_gradient(g, row_len, rows_buf)
+        fa.fa_merge_gradient_stats(rows_buf, rows, scratch, report)
+        if ev: ev[1].record(stream)
+        rep = fa.fa_read_report(report)
+        skip, norm, coef = sharded.global_clip_decision(rep, w.gradient_scale, w.max_grad_norm,
+                                                        device=dev)
+        if ev: ev[2].record(stream)
+        launches["n"] += 1 + merge_kernels
+        if not skip:
+            state["t"], _ = fa.fa_bucket_step(None, p, g, m, v, None, state["t"], opts, ctl, coef)
+            launches["n"] += 1
+        if ev: ev[3].record(stream)
+        return norm
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = None
+    clocks = ClockSampler(gpu_uuid if rank == 0 else None)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.5)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    launches["n"] = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    clock_info = clocks.stop() if rank == 0 else None
+    timed_launches = launches["n"]
+
+    stats_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    update_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # end to end through the public C-ABI call, gradient from pinned host memory
+    e2e = None
+    if args.e2e_steps > 0:
+        g_host = g.cpu().pin_memory()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            g.copy_(g_host, non_blocking=True)
+            if world > 1:
+                fa.fa_analyze_gradient(g, row_len, rows_buf)
+                fa.fa_merge_gradient_stats(rows_buf, rows, scratch, report)
+                rep = fa.fa_read_report(report)
+                skip, _, coef = sharded.global_clip_decision(rep, w.gradient_scale,
+                                                             w.max_grad_norm, device=dev)
+                if not skip:
+                    state["t"], _ = fa.fa_bucket_step(None, p, g, m, v, None, state["t"], opts,
+                                                      ctl, coef)
+            else:
+                state["t"], _ = fa.fa_bucket_step_clipped(None, p, g, m, v, None, state["t"], opts,
+                                                          ctl, w.max_grad_norm, row_len, rows_buf,
+                                                          scratch, report)
+        torch.cuda.synchronize(dev)
+        e2e_s = time.perf_counter() - t0
+        if world > 1:
+            tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        e2e = {"value": world * n * args.e2e_steps / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": n * 2, "d2h_bytes_per_step": 12,
+               "ms_per_step": e2e_s * 1e3 / args.e2e_steps,
+               "what": "pinned-host BF16 gradient copied in, then the C-ABI statistics-guarded "
+                       "step (analyse, merge, 12-byte report read back, decide, update)"}
+
+    if rank == 0:
+        ms_step = total_ms / args.steps
+        bpp = fa.bytes_per_param(2, False, False)
+        upd_ms = statistics.median(update_ms)
+        st_ms = statistics.median(stats_ms)
+        peak, peak_kind = measured_peaks()
+        achieved = bpp * n / (upd_ms * 1e-3) / 1e9
+        step_bytes = bpp * n + 2 * n + rows * 12 * 2
+        line = {
+            "metric": METRIC, "value": world * n / (ms_step * 1e-3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_dict(w),
+            "achieved_gbs_step": step_bytes / (ms_step * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "update_vec_kernel (fused AdamW, BF16 grad)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "bytes_per_param": bpp, "traffic": None,
+                         "kernel_ms_median": upd_ms, "kernel_ms_min": min(update_ms)},
+            "stats_path": {"ms_median": st_ms, "analyze_bytes": n * 2 + rows * 12,
+                           "achieved_gbs": (n * 2 + rows * 12) / (st_ms * 1e-3) / 1e9},
+            "gpu_launches": timed_launches,
+            "clocks": clock_info,
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

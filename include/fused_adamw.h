@@ -1,0 +1,265 @@
+/*
+ * fused_adamw.h -- C ABI of the GB300 fused AdamW / AMSGrad step and of the
+ * gradient statistics that feed its skip and global-norm clip.
+ *
+ * Sources (RUDA documentation pages; section names as printed):
+ *   [FA-ja] "実験的なデバイス上の融合 AdamW / AMSGrad"   (ja/docs/fused-adamw)
+ *   [FA-zh] "实验性融合 AdamW / AMSGrad"                  (zh/docs/fused-adamw)
+ *   [TR-zh] "训练与状态保存"                                (zh/docs/training)
+ *
+ * General contract (applies to every entry point below):
+ *   - Pointers named "device" must be CUDA device (or managed) memory of the
+ *     current device.  Host pointers are rejected with FA_ERR_POINTER
+ *     ([FA-ja] "サポートされている契約": no arbitrary host pointers).
+ *   - ``stream`` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  All device work is enqueued on it, in call order.
+ *   - FA_OK from an enqueuing call means the work was ENQUEUED, not that it
+ *     finished ([FA-ja] "低レベルの使用"; [FA-zh] "用法"): check the stream's
+ *     completion before trusting or checkpointing outputs; after a device
+ *     failure discard them.
+ *   - Validation happens before anything is enqueued or written; on any
+ *     error no output (host or device) is modified ([FA-ja] "低レベルの使用").
+ *   - The library never allocates device memory and keeps no mutable global
+ *     state: buffers (outputs, row statistics, scratch, report) belong to the
+ *     caller.
+ *   - Parameters and moments are dense contiguous FP32; gradients are dense
+ *     contiguous FP32, FP16 or BF16 of the same element count
+ *     ([FA-zh] "增加的实际能力").  Strides, broadcasts and sparse gradients
+ *     cannot be expressed through this ABI; the Python binding rejects them.
+ */
+#ifndef FUSED_ADAMW_H
+#define FUSED_ADAMW_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_ABI_VERSION 1
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_NULL = 1,      /* a required pointer is NULL, or state pointers disagree with t  */
+    FA_ERR_DTYPE = 2,     /* unknown gradient dtype                                          */
+    FA_ERR_SIZE = 3,      /* negative count, or a buffer too small for the request           */
+    FA_ERR_OPTION = 4,    /* option/control out of range (non-finite lr, beta outside [0,1),  */
+                          /* eps < 0, scale <= 0, t would overflow, ...)                     */
+    FA_ERR_ALIAS = 5,     /* buffers that must be distinct overlap                           */
+    FA_ERR_POINTER = 6,   /* host pointer, or device memory of another device/stream device  */
+    FA_ERR_ALIGN = 7,     /* pointer not aligned to its element size                         */
+    FA_ERR_PLAN = 8,      /* statistics rows outside 1..4,194,304                            */
+    FA_ERR_CUDA = 9,      /* a CUDA call failed (launch error, copy error)                   */
+    FA_ERR_SEGMENTS = 10  /* segment table not non-decreasing from 0 to n                    */
+} fa_status;
+
+typedef enum fa_dtype { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+/* Hyper-parameters, as doubles ([FA-ja] "低レベルの使用": AdamWOptions).
+ * Valid ranges: lr >= 0, 0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0,
+ * weight_decay >= 0, all finite; amsgrad and maximize are 0 or 1. */
+typedef struct fa_options {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;
+    int32_t amsgrad;
+    int32_t maximize;
+} fa_options;
+
+/* Per-call control ([FA-ja] "低レベルの使用": StepControl).  gradient_scale
+ * divides the stored gradient (finite, > 0); skip_update is the caller's
+ * found_inf flag -- this call does not compute it. */
+typedef struct fa_step_control {
+    double gradient_scale;
+    int32_t skip_update;
+} fa_step_control;
+
+/* 12-byte statistics record ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": a 12-byte
+ * report).  Row records, intermediate merge records and the final report all
+ * use it.  sum_sq + sum_sq_lo (added in FP64) is the sum of squares of the
+ * STORED (still scaled) finite gradient values; nonfinite counts stored NaN
+ * and +-Inf values, saturating at 2^32-1. */
+typedef struct fa_stats {
+    float sum_sq;
+    uint32_t nonfinite;
+    float sum_sq_lo;
+} fa_stats;
+
+/* Outcome of a step that ran the statistics path. */
+typedef struct fa_step_report {
+    int32_t updated;           /* 1 when the update kernel was enqueued                 */
+    int32_t skipped_nonfinite; /* 1 when the step was skipped for a non-finite gradient */
+    uint64_t nonfinite;        /* non-finite stored gradient values found               */
+    double grad_norm;          /* global L2 norm of the unscaled gradient               */
+    double clip_coef;          /* factor applied to the unscaled gradient (1 = none)    */
+} fa_step_report;
+
+/* ---- host-only helpers ---------------------------------------------------- */
+
+int32_t fa_abi_version(void);
+const char *fa_status_string(fa_status status);
+
+/* Defaults ([FA-ja] "この演算子を使用する理由": betas (0.9, 0.999), eps 1e-5,
+ * weight_decay 1e-4, matching RUDA's AdamWConfig).  The pages state no default
+ * learning rate; 1e-3 is used.  amsgrad = maximize = 0. */
+fa_options fa_options_default(void);
+
+/* Host coefficients of one update, FP64 then cast to FP32 ([FA-ja]
+ * "この演算子を使用する理由": the host computes the bias corrections once per call
+ * from FP64 integer powers and casts them to FP32).  ``t`` is the 1-based step
+ * of the update; ``grad_mult`` an extra factor on the unscaled gradient.
+ * Writes 9 floats: beta1, 1-beta1, beta2, 1-beta2, lr/(1-beta1^t),
+ * 1/(1-beta2^t), eps, 1-lr*weight_decay, (maximize ? -1 : 1)*grad_mult/scale. */
+fa_status fa_step_coefficients(const fa_options *options, uint64_t t, double gradient_scale,
+                               double grad_mult, float coef_out[9]);
+
+/* ---- the fused update ----------------------------------------------------- */
+
+/*
+ * Out-of-place step ([FA-ja] "低レベルの使用" adamw_step and "割り当てとパフォーマンスの
+ * モデル"; [FA-zh] "增加的实际能力").  Per element, one HBM pass:
+ *   g = stored/gradient_scale, negated if maximize;
+ *   m = beta1*m + (1-beta1)*g;  v = beta2*v + (1-beta2)*g*g;
+ *   AMSGrad: vmax = max(vmax, v) (uncorrected) and v_used = vmax, else v_used = v;
+ *   p = p*(1-lr*wd) - lr*(m/(1-beta1^t)) / (sqrt(v_used/(1-beta2^t)) + eps).
+ *
+ *   n               element count (>= 0)
+ *   p, g, gdt       device inputs: FP32 parameters, gradient of type gdt
+ *   m, v, vmax      device state; all NULL iff t_in == 0 (no state yet: the
+ *                   first update writes the moments without reading them);
+ *                   vmax NULL unless options->amsgrad
+ *   t_in            completed updates so far
+ *   p_out, m_out, v_out, vmax_out
+ *                   device outputs (vmax_out NULL unless amsgrad); distinct,
+ *                   and overlapping no input
+ *   t_out, updated  host outputs: t_in+1 and 1 when an update was enqueued;
+ *                   t_in and 0 when n == 0 or ctl.skip_update: then nothing is
+ *                   launched, no buffer is checked or touched, and the output
+ *                   pointers may be NULL (the caller need not allocate them).
+ */
+fa_status fa_adamw_step(int64_t n, const float *p, const void *g, fa_dtype gdt,
+                        const float *m, const float *v, const float *vmax, uint64_t t_in,
+                        const fa_options *options, fa_step_control ctl,
+                        float *p_out, float *m_out, float *v_out, float *vmax_out,
+                        uint64_t *t_out, int32_t *updated, void *stream);
+
+/*
+ * In-place step on caller-owned storage ([FA-ja] "ネイティブ PyTorch ストレージと
+ * 階層統計": adamw_scaled on framework-preallocated storage).  Same arithmetic as
+ * fa_adamw_step; p, m, v (and vmax with AMSGrad) are read and rewritten in
+ * place and must not overlap each other or g.  ``*t`` is the completed step
+ * count on entry and is advanced on an update; when *t == 0 the moments are
+ * only written.  ``grad_mult`` multiplies the unscaled gradient (the global
+ * clip coefficient; 1 = none; finite, >= 0).  n == 0 or ctl.skip_update:
+ * nothing is launched or checked, *t is unchanged and *updated = 0.
+ */
+fa_status fa_adamw_step_inplace(int64_t n, float *p, const void *g, fa_dtype gdt,
+                                float *m, float *v, float *vmax, uint64_t *t,
+                                const fa_options *options, fa_step_control ctl,
+                                double grad_mult, int32_t *updated, void *stream);
+
+/*
+ * Pre-flattened multi-tensor bucket ([FA-ja] "サポートされている契約": a flattened
+ * bucket is valid only when every element shares the options and the step
+ * count).  ``seg_offsets`` (host, nseg+1 entries, non-decreasing from 0 to
+ * n_total) records the tensors packed in the bucket; the update itself is ONE
+ * launch over the flat buffers, identical element by element to updating
+ * each tensor on its own.  Other arguments as fa_adamw_step_inplace.
+ */
+fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                         float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                         float *vmax, uint64_t *t, const fa_options *options,
+                         fa_step_control ctl, double grad_mult, int32_t *updated,
+                         void *stream);
+
+/* ---- gradient statistics -------------------------------------------------- */
+
+/*
+ * Reduction plan ([FA-ja] "ネイティブ PyTorch ストレージと階層統計": StatsPlan::new(rows)
+ * accepts 1..=4,194,304 rows at fan-in 1024; scratch_elements counts FP32
+ * elements, excluding the initial statistics and the final report; at most
+ * 49,200 bytes).  Each merge kernel reduces groups of 1024 records, until one
+ * record is left.  merge_kernels is 1 for rows <= 1024, 2 up to 1,048,576 and
+ * 3 above ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": at most two extra merge
+ * kernels, none at <= 1024 rows).  FA_ERR_PLAN outside 1..4,194,304.
+ */
+fa_status fa_stats_plan(int64_t rows, int32_t *merge_kernels, int64_t *scratch_elements);
+
+/* Row count of an analysis: each segment [seg[k], seg[k+1]) is cut into rows
+ * of row_len elements, its last row possibly shorter; rows never span
+ * segments.  seg_offsets NULL / nseg 0 means one segment [0, n).  Host only. */
+fa_status fa_stats_rows(int64_t n, int32_t row_len, const int64_t *seg_offsets, int32_t nseg,
+                        int64_t *rows);
+
+/*
+ * Read-only gradient analysis ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练":
+ * read-only gradient analysis; [FA-ja] "ネイティブ PyTorch ストレージと階層統計":
+ * analyze_gradient).  Writes one fa_stats per row (rows as fa_stats_rows) to the
+ * device array rows_out (capacity rows_capacity >= rows; FA_ERR_SIZE else).
+ * The row count must be a valid plan size (FA_ERR_PLAN else).  The gradient
+ * is not modified.
+ */
+fa_status fa_analyze_gradient(const void *g, fa_dtype gdt, int64_t n, int32_t row_len,
+                              const int64_t *seg_offsets, int32_t nseg, fa_stats *rows_out,
+                              int64_t rows_capacity, void *stream);
+
+/*
+ * Hierarchical merge ([FA-ja] "ネイティブ PyTorch ストレージと階層統計":
+ * merge_gradient_stats; [TR-zh]: fan-in 1024, changes the reduction order, not
+ * the clip policy).  Reduces ``rows`` device records to one device report, in
+ * fa_stats_plan's merge kernels.  ``scratch`` is caller-owned device memory of
+ * at least fa_stats_plan's scratch_elements floats (may be NULL when that is
+ * 0); its contents on entry do not matter.  Sums are carried in FP64 inside
+ * each kernel and passed between levels as (sum_sq, sum_sq_lo) pairs.
+ */
+fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *scratch,
+                                  int64_t scratch_elements, fa_stats *report, void *stream);
+
+/* Copies the 12-byte device report to host memory and waits for the stream
+ * ([TR-zh]: the report is read back before any update).  Synchronises. */
+fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream);
+
+/*
+ * Host decision ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": any non-finite gradient
+ * skips the whole step; optional global L2 clipping after unscale).
+ * sum_sq_stored is the sum of squares of the stored gradient (a report's
+ * sum_sq + sum_sq_lo, or the sum of several ranks' reports).  Outputs:
+ * skip = nonfinite > 0; grad_norm = sqrt(sum_sq_stored)/gradient_scale;
+ * clip_coef = max_grad_norm/grad_norm when max_grad_norm > 0 and the norm
+ * exceeds it, else 1.  Host only.
+ */
+fa_status fa_clip_decision(double sum_sq_stored, uint64_t nonfinite, double gradient_scale,
+                           double max_grad_norm, int32_t *skip, double *grad_norm,
+                           double *clip_coef);
+
+/* fa_read_report followed by fa_clip_decision.  Synchronises the stream. */
+fa_status fa_clip_decide(const fa_stats *report_dev, double gradient_scale, double max_grad_norm,
+                         int32_t *skip, double *grad_norm, double *clip_coef, void *stream);
+
+/*
+ * The whole statistics-guarded step on a bucket ([TR-zh] "在 ruda:0 上进行原生
+ * PyTorch 训练": ruda_torch.AdamW(fused_step=True, max_grad_norm, hierarchical_stats
+ * =True) -- analyse, merge, read back 12 bytes, then update or skip).
+ *   1. ctl.skip_update or n_total == 0: nothing is launched; t unchanged.
+ *   2. fa_analyze_gradient over segment-aligned rows of row_len into rows_buf.
+ *   3. fa_merge_gradient_stats into report_dev, using scratch.
+ *   4. fa_clip_decide (synchronises the stream).
+ *   5. Non-finite found: skip, t unchanged.  Else one fa_bucket_step with
+ *      grad_mult = clip_coef (max_grad_norm <= 0: no clipping).
+ * ``out`` (host) receives the decision.  Buffers as in the calls above.
+ */
+fa_status fa_bucket_step_clipped(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                 float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                                 float *vmax, uint64_t *t, const fa_options *options,
+                                 fa_step_control ctl, double max_grad_norm, int32_t row_len,
+                                 fa_stats *rows_buf, int64_t rows_capacity, float *scratch,
+                                 int64_t scratch_elements, fa_stats *report_dev,
+                                 fa_step_report *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSED_ADAMW_H */

@@ -1,0 +1,225 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and
+its host-only logic (plan, row count, coefficients, clip decision, validation,
+skip/empty) agrees with the pinned oracle and the pages.  No kernel is launched."""
+
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, read_golden
+
+import amsgrad_optimizer_step_gb300 as fa
+from amsgrad_optimizer_step_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} missing from the Python binding"
+
+
+def test_binding_names_match_header():
+    assert sorted(_lib.SIGNATURES) == declared_functions()
+    for name in declared_functions():
+        if name != "fa_status_string":
+            assert hasattr(fa, name), name
+
+
+def test_abi_version_and_defaults(lib):
+    assert fa.fa_abi_version() == 1
+    d = fa.fa_options_default()
+    assert (d.beta1, d.beta2, d.eps, d.weight_decay, d.amsgrad, d.maximize) == \
+        (0.9, 0.999, 1e-5, 1e-4, 0, 0)
+    for s in range(11):
+        assert lib.fa_status_string(s)
+
+
+def test_stats_plan_matches_oracle_and_pages(oracle_lib):
+    gold = read_golden("stats_plan.txt")
+    rows_list = [1, 2, 1023, 1024, 1025, 4096, 1048575, 1048576, 1048577, 3_000_000,
+                 4_194_303, 4_194_304] + list(np.random.default_rng(5).integers(1, 4_194_305, 200))
+    for rows in rows_list:
+        k, e = fa.fa_stats_plan(int(rows))
+        ok, oe, _ = oracle_lib.stats_plan(int(rows))
+        assert (k, e) == (ok, oe)
+        assert 4 * e <= gold["max_extra_scratch_bytes"]
+        assert k - 1 <= gold["max_extra_merge_kernels"]
+    assert fa.fa_stats_plan(4_194_304) == (3, 12_300)
+    for bad in (0, -1, gold["max_rows"] + 1):
+        with pytest.raises(fa.FusedAdamWError) as e:
+            fa.fa_stats_plan(bad)
+        assert e.value.status == 8
+
+
+def test_stats_rows_matches_oracle(oracle_lib):
+    from synthetic.configs import CONFIG4
+    cases = [(1000, 256, None), (257, 256, None), (1, 7, None), (2000, 128, [0, 5, 5, 700, 1300, 2000]),
+             (CONFIG4.n, 256, list(CONFIG4.segments)), (CONFIG4.n, 512, list(CONFIG4.segments))]
+    for n, row_len, seg in cases:
+        want = None
+        if n < 100000:
+            want = len(oracle_lib.row_stats(np.zeros(n, np.float32), "f32", row_len, seg)[0])
+        else:  # count rows per segment by the same rule, without materialising the gradient
+            want = sum(-(-(b - a) // row_len) for a, b in zip(seg[:-1], seg[1:]))
+        assert fa.fa_stats_rows(n, row_len, seg) == want
+    # the decoder bucket at 256-element rows exceeds the plan; 512 fits
+    assert fa.fa_stats_rows(CONFIG4.n, 256, list(CONFIG4.segments)) > 4_194_304
+    assert fa.fa_stats_rows(CONFIG4.n, 512, list(CONFIG4.segments)) <= 4_194_304
+    with pytest.raises(fa.FusedAdamWError):
+        fa.fa_stats_rows(10, 4, [0, 6, 5, 10])
+
+
+def test_clip_decision_matches_oracle(oracle_lib):
+    rng = np.random.default_rng(6)
+    for _ in range(200):
+        s = float(rng.uniform(0, 10) ** 4)
+        cnt = int(rng.integers(0, 3))
+        scale = float(2.0 ** rng.integers(0, 10))
+        mx = float(rng.choice([0.0, 1.0, 5.0, 100.0]))
+        skip, norm, coef = fa.fa_clip_decision(s, cnt, scale, mx)
+        o_skip, o_norm, o_coef = oracle_lib.clip_decision(s / scale ** 2, cnt, mx)
+        assert skip == o_skip
+        assert math.isclose(norm, o_norm, rel_tol=1e-15)
+        assert math.isclose(coef, o_coef, rel_tol=1e-15)
+
+
+def test_step_coefficients_are_fp64_then_fp32():
+    o = fa.options(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=0.01,
+                   maximize=True)
+    for t in (1, 2, 7, 1000):
+        c = fa.fa_step_coefficients(o, t, gradient_scale=128.0, grad_mult=0.5)
+        bc1 = 1 - 0.9 ** t
+        bc2 = 1 - 0.999 ** t
+        want = [0.9, 1 - 0.9, 0.999, 1 - 0.999, 1e-3 / bc1, 1 / bc2, 1e-5, 1 - 1e-3 * 0.01,
+                -0.5 / 128.0]
+        for got, w in zip(c, want):
+            assert got == float(np.float32(w)) or abs(got - w) <= 2 ** -24 * abs(w)
+    # (1 - beta2) formed in FP64 then cast, not fp32(1) - fp32(beta2)
+    c = fa.fa_step_coefficients(o, 1)
+    assert c[3] == float(np.float32(1 - 0.999))
+    assert c[3] != float(np.float32(1) - np.float32(0.999))
+
+
+def _call_step(lib, n, opts, ctl, t_in=0, p=None, g=None):
+    tout = ctypes.c_uint64(12345)
+    upd = ctypes.c_int32(7)
+    st = lib.fa_adamw_step(n, p, g, 0, None, None, None, t_in, ctypes.byref(opts), ctl,
+                           None, None, None, None, ctypes.byref(tout), ctypes.byref(upd), None)
+    return st, tout.value, upd.value
+
+
+def test_skip_and_empty_touch_nothing(lib):
+    o = fa.options()
+    # empty tensor: OK, t unchanged, nothing launched (NULL pointers accepted)
+    assert _call_step(lib, 0, o, fa.control(), t_in=3, p=None) == (0, 3, 0)
+    # skip_update: OK, t unchanged, outputs not needed
+    assert _call_step(lib, 1000, o, fa.control(skip_update=True), t_in=5) == (0, 5, 0)
+    t = ctypes.c_uint64(9)
+    upd = ctypes.c_int32(3)
+    st = lib.fa_adamw_step_inplace(10, None, None, 0, None, None, None, ctypes.byref(t),
+                                   ctypes.byref(o), fa.control(skip_update=True), 1.0,
+                                   ctypes.byref(upd), None)
+    assert (st, t.value, upd.value) == (0, 9, 0)
+
+
+@pytest.mark.parametrize("field,value", [("lr", -1.0), ("lr", float("nan")), ("beta1", 1.0),
+                                         ("beta2", -0.1), ("eps", -1e-8),
+                                         ("weight_decay", float("inf")), ("amsgrad", 2)])
+def test_bad_options_rejected_before_anything(lib, field, value):
+    o = fa.options()
+    setattr(o, field, value)
+    st, tout, upd = _call_step(lib, 0, o, fa.control())
+    assert st == 4 and tout == 12345 and upd == 7  # outputs untouched
+
+
+@pytest.mark.parametrize("scale", [0.0, -1.0, float("inf"), float("nan")])
+def test_bad_scale_rejected(lib, scale):
+    st, tout, upd = _call_step(lib, 0, fa.options(), fa.control(gradient_scale=scale))
+    assert st == 4 and tout == 12345 and upd == 7
+
+
+def test_state_pointers_must_match_t(lib):
+    o = fa.options()
+    tout = ctypes.c_uint64(0)
+    upd = ctypes.c_int32(0)
+    fake = ctypes.c_void_p(0x1000)
+    # t_in == 0 (no state) but a moment pointer given
+    st = lib.fa_adamw_step(4, fake, fake, 0, fake, None, None, 0, ctypes.byref(o), fa.control(),
+                           None, None, None, None, ctypes.byref(tout), ctypes.byref(upd), None)
+    assert st == 1
+    # t_in > 0 but moments missing
+    st = lib.fa_adamw_step(4, fake, fake, 0, None, None, None, 3, ctypes.byref(o), fa.control(),
+                           None, None, None, None, ctypes.byref(tout), ctypes.byref(upd), None)
+    assert st == 1
+    # bad dtype
+    st = lib.fa_adamw_step(4, fake, fake, 9, None, None, None, 0, ctypes.byref(o), fa.control(),
+                           None, None, None, None, ctypes.byref(tout), ctypes.byref(upd), None)
+    assert st == 2
+
+
+def test_segment_table_validation(lib):
+    for seg, n in (([0, 5, 3, 10], 10), ([1, 10], 10), ([0, 9], 10)):
+        arr = (ctypes.c_int64 * len(seg))(*seg)
+        r = ctypes.c_int64()
+        assert lib.fa_stats_rows(n, 4, arr, len(seg) - 1, ctypes.byref(r)) == 10
+
+
+def test_binding_rejects_bad_layouts():
+    import torch
+    p = torch.zeros(16)
+    g = torch.zeros(32)[::2]  # strided view
+    with pytest.raises(ValueError):
+        fa.fa_adamw_step(p, g, None, None, None, 0, fa.options(), fa.control())
+    with pytest.raises(TypeError):
+        fa.fa_adamw_step(p, torch.zeros(16, dtype=torch.int32), None, None, None, 0,
+                         fa.options(), fa.control())
+    with pytest.raises(ValueError):
+        fa.fa_adamw_step(p, torch.zeros(15), None, None, None, 0, fa.options(), fa.control())
+    with pytest.raises(ValueError):
+        fa.fa_adamw_step(p, torch.zeros(1).expand(16), None, None, None, 0, fa.options(),
+                         fa.control())
+
+
+def test_host_memory_is_rejected_not_computed():
+    """CPU tensors reach the library and are refused: there is no CPU fallback."""
+    import torch
+    p = torch.zeros(64)
+    g = torch.zeros(64)
+    with pytest.raises(fa.FusedAdamWError) as e:
+        fa.fa_adamw_step(p, g, None, None, None, 0, fa.options(), fa.control(), stream=0)
+    assert e.value.status in (6, 9)  # not device memory / no CUDA device here
+    assert not p.any()
+
+
+def test_byte_model_matches_pages():
+    gold = read_golden("byte_model.txt")
+    assert fa.bytes_per_param(4, False, False) == gold["fused_adamw_f32grad_steady"]
+    assert fa.bytes_per_param(4, True, False) == gold["fused_amsgrad_f32grad_steady"]
+    assert fa.bytes_per_param(2, False, False) == 26
+    assert fa.bytes_per_param(2, True, False) == 34
+    assert fa.bytes_per_param(4, False, True) == 20
+    assert fa.bytes_per_param(2, False, True) == 18
+    assert fa.bytes_per_param(2, True, True) == 22

@@ -1,0 +1,445 @@
+"""CUDA path vs the oracle, through the C ABI, on the five seeded workloads.
+
+Small and scaled sizes are compared element by element on every call; the full
+sizes (124M, the 1.196e9 decoder bucket, 1.07e9 with statistics) are compared
+on sampled indices, which is exact because elements are independent, and the
+statistics against the oracle's sum over the whole gradient.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import amsgrad_optimizer_step_gb300 as fa
+from gpu_harness import run_workload
+from synthetic.configs import (CONFIG1, CONFIG2, CONFIG3, CONFIG4, CONFIG4_MAX, CONFIG5,
+                               decoder_bucket_shapes)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from amsgrad_optimizer_step_gb300 import build
+    build.build()
+    torch.cuda.init()
+
+
+def sample_indices(n, k=40000, seed=0, extra=()):
+    rng = np.random.default_rng(seed)
+    base = set(rng.integers(0, n, k).tolist())
+    for b in (0, 1, 2, 7, 8, 9, 4095, 4096, 4097, n - 9, n - 8, n - 7, n - 2, n - 1, *extra):
+        if 0 <= b < n:
+            base.add(int(b))
+    return np.array(sorted(base), dtype=np.int64)
+
+
+def small_decoder_offsets(scale=32):
+    sizes = []
+    for _, shape in decoder_bucket_shapes()[:1 + 9 * 3]:  # embed + 3 layers
+        sizes.append(int(np.prod([max(1, d // scale) for d in shape])))
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+
+
+# ---- the five workloads ---------------------------------------------------------
+
+def test_config1_out_of_place_full():
+    s = run_workload(CONFIG1, CONFIG1.n, "oop", DEV, guard=1024)
+    assert s["updates"] == 10 and s["t"] == 10
+
+
+def test_config2_bf16_scaled_amsgrad_with_skip_full():
+    s = run_workload(CONFIG2, CONFIG2.n, "oop", DEV, guard=1024)
+    assert s["skips"] == 1 and s["updates"] == 19 and s["t"] == 19
+
+
+@pytest.mark.parametrize("api", ["inplace", "oop"])
+def test_config3_scaled_ragged(api):
+    w = dataclasses.replace(CONFIG3, calls=12, inplace=api == "inplace")
+    s = run_workload(w, 1_000_003, api, DEV, guard=1024)
+    assert s["t"] == 12
+
+
+def test_config3_full_size_sampled():
+    idx = sample_indices(CONFIG3.n, seed=3)
+    s = run_workload(CONFIG3, CONFIG3.n, "inplace", DEV, idx=idx)
+    assert s["t"] == 50
+
+
+@pytest.mark.parametrize("w", [CONFIG4, CONFIG4_MAX], ids=["maximize_off", "maximize_on"])
+def test_config4_scaled_decoder_bucket(w):
+    off = small_decoder_offsets()
+    s = run_workload(w, int(off[-1]), "bucket", DEV, segments=off, guard=1024)
+    assert s["t"] == 10
+
+
+@pytest.mark.parametrize("w", [CONFIG4, CONFIG4_MAX], ids=["maximize_off", "maximize_on"])
+def test_config4_full_size_sampled(w):
+    idx = sample_indices(w.n, seed=4, extra=list(w.segments[1:-1]) + [x - 1 for x in w.segments[1:-1]])
+    s = run_workload(w, w.n, "bucket", DEV, idx=idx)
+    assert s["t"] == 10
+
+
+def test_config5_scaled_stats_clip_and_inf_skip():
+    n = 256 * 5000 + 77
+    s = run_workload(CONFIG5, n, "clipped", DEV, row_len=256, guard=1024)
+    assert s["skips"] == 1 and s["updates"] == 4 and s["t"] == 4
+    # norm well above 1: the clip is active in every update
+    assert all(r[1] > 1.0 for r in s["reports"] if r[3] == 0)
+
+
+def test_config5_full_size_sampled():
+    idx = sample_indices(CONFIG5.n, seed=5, extra=[CONFIG5.inf_index()])
+    s = run_workload(CONFIG5, CONFIG5.n, "clipped", DEV, idx=idx, row_len=256,
+                     full_grad_on_host=False)
+    assert s["skips"] == 1 and s["t"] == 4
+    inf_reports = [r for r in s["reports"] if r[3] > 0]
+    assert len(inf_reports) == 1 and inf_reports[0][2] == 1
+
+
+# ---- sizes, dtypes, alignment ---------------------------------------------------
+
+@pytest.mark.parametrize("gdt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("ams", [False, True])
+@pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 15, 16, 17, 255, 4095, 4097, 65537])
+def test_edge_sizes(gdt, ams, n):
+    w = dataclasses.replace(CONFIG1, grad_dtype=gdt, amsgrad=ams, calls=3, inplace=True)
+    run_workload(w, n, "inplace", DEV, guard=64)
+
+
+@pytest.mark.parametrize("gdt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("offsets", [(1, 1, 1, 1, 1), (3, 3, 3, 3, 3), (0, 1, 2, 3, 5),
+                                     (2, 0, 0, 0, 0), (0, 0, 0, 0, 3)])
+def test_misaligned_views(gdt, offsets):
+    """Views starting off a 16-byte boundary: common offset -> vector body after a
+    scalar head; mixed offsets -> all-scalar kernel.  Both must match the oracle."""
+    n = 10_001
+    w = dataclasses.replace(CONFIG2, grad_dtype=gdt, calls=3, skip_calls=(), amsgrad=True,
+                            inplace=True)
+    import oracle
+    lib = oracle.lib()
+    idx = np.arange(n)
+    bufs = []
+    names = ("p", "m", "v", "vmax")
+    views = {}
+    for name, off in zip(names, offsets[:4]):
+        full = torch.zeros(n + 16, dtype=torch.float32, device=DEV)
+        bufs.append(full)
+        views[name] = full[off:off + n]
+    gfull = torch.zeros(n + 16, dtype={"f32": torch.float32, "f16": torch.float16,
+                                       "bf16": torch.bfloat16}[gdt], device=DEV)
+    g = gfull[offsets[4]:offsets[4] + n]
+    w.fill_params_device(views["p"])
+    traj = oracle.OracleAdamW(w.params_host(idx), w.options(), lib_=lib)
+    t = 0
+    for call in range(1, 4):
+        w.fill_grad_device(call, g)
+        t, upd = fa.fa_adamw_step_inplace(views["p"], g, views["m"], views["v"], views["vmax"], t,
+                                          fa.options(**w.options()),
+                                          fa.control(w.gradient_scale))
+        traj.step(w.grad_host(call, idx), gdt, w.gradient_scale)
+    torch.cuda.synchronize()
+    from gpu_harness import gate
+    gate(views["p"].cpu().numpy(), traj.p, 1e-6, "p")
+    gate(views["vmax"].cpu().numpy(), traj.state.vmax, 1e-6, "vmax")
+
+
+# ---- bitwise invariants ---------------------------------------------------------
+
+def _fresh(n, gdt, seed, ams=True):
+    w = dataclasses.replace(CONFIG2, grad_dtype=gdt, amsgrad=ams, seed=seed, skip_calls=(),
+                            inplace=True, gradient_scale=1.0, grad_premul=1.0)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p) if n == w.n else w.scaled(n).fill_params_device(p)
+    return w if n == w.n else w.scaled(n), p
+
+
+def _grads(w, call):
+    g = torch.empty(w.n, dtype={"f32": torch.float32, "f16": torch.float16,
+                                "bf16": torch.bfloat16}[w.grad_dtype], device=DEV)
+    w.fill_grad_device(call, g)
+    return g
+
+
+def _zeros(n, k):
+    return [torch.zeros(n, device=DEV) for _ in range(k)]
+
+
+@pytest.mark.parametrize("gdt", ["f32", "bf16", "f16"])
+def test_inplace_equals_out_of_place_bitwise(gdt):
+    w, p0 = _fresh(70_001, gdt, 11)
+    o = fa.options(**w.options())
+    pa = p0.clone()
+    ma, va, vma = _zeros(w.n, 3)
+    pb, mb, vb, vmb, tb = p0.clone(), None, None, None, 0
+    ta = 0
+    for call in range(1, 6):
+        g = _grads(w, call)
+        ta, _ = fa.fa_adamw_step_inplace(pa, g, ma, va, vma, ta, o, fa.control())
+        pb, mb, vb, vmb, tb, _ = fa.fa_adamw_step(pb, g, mb, vb, vmb, tb, o, fa.control())
+    torch.cuda.synchronize()
+    assert ta == tb == 5
+    for a, b in ((pa, pb), (ma, mb), (va, vb), (vma, vmb)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_bucket_equals_per_tensor_bitwise():
+    off = small_decoder_offsets(16)
+    n = int(off[-1])
+    w, p0 = _fresh(n, "f16", 12)
+    o = fa.options(**w.options())
+    pa, pb = p0.clone(), p0.clone()
+    ma, va, vma = _zeros(n, 3)
+    mb, vb, vmb = _zeros(n, 3)
+    ta = 0
+    tb = [0] * (len(off) - 1)
+    for call in range(1, 4):
+        g = _grads(w, call)
+        ta, _ = fa.fa_bucket_step(list(off), pa, g, ma, va, vma, ta, o, fa.control())
+        for k in range(len(off) - 1):
+            s = slice(int(off[k]), int(off[k + 1]))
+            tb[k], _ = fa.fa_adamw_step_inplace(pb[s], g[s], mb[s], vb[s], vmb[s], tb[k], o,
+                                                fa.control())
+    torch.cuda.synchronize()
+    for a, b in ((pa, pb), (ma, mb), (va, vb), (vma, vmb)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_maximize_equals_negated_gradient_bitwise(gdt):
+    w, p0 = _fresh(33_333, gdt, 13)
+    pa, pb = p0.clone(), p0.clone()
+    sa, sb = _zeros(w.n, 3), _zeros(w.n, 3)
+    ta = tb = 0
+    oa = fa.options(**dict(w.options(), maximize=True))
+    ob = fa.options(**dict(w.options(), maximize=False))
+    for call in range(1, 4):
+        g = _grads(w, call)
+        gneg = g.clone()
+        if gdt == "f32":
+            gneg.neg_()
+        else:
+            gneg.view(torch.int16).bitwise_xor_(torch.tensor(-32768, dtype=torch.int16, device=DEV))
+        ta, _ = fa.fa_adamw_step_inplace(pa, g, *sa, ta, oa, fa.control())
+        tb, _ = fa.fa_adamw_step_inplace(pb, gneg, *sb, tb, ob, fa.control())
+    torch.cuda.synchronize()
+    assert torch.equal(pa, pb) and all(torch.equal(x, y) for x, y in zip(sa, sb))
+    assert not torch.equal(pa, p0)
+
+
+def test_power_of_two_scale_bitwise():
+    w, p0 = _fresh(20_000, "bf16", 14)
+    pa, pb = p0.clone(), p0.clone()
+    sa, sb = _zeros(w.n, 3), _zeros(w.n, 3)
+    o = fa.options(**w.options())
+    ta = tb = 0
+    for call in range(1, 4):
+        g = _grads(w, call)
+        g128 = (g.float() * 128).to(torch.bfloat16)  # exact: power of two, no overflow
+        ta, _ = fa.fa_adamw_step_inplace(pa, g, *sa, ta, o, fa.control(1.0))
+        tb, _ = fa.fa_adamw_step_inplace(pb, g128, *sb, tb, o, fa.control(128.0))
+    torch.cuda.synchronize()
+    assert torch.equal(pa, pb) and all(torch.equal(x, y) for x, y in zip(sa, sb))
+
+
+def test_checkpoint_export_import_bitwise():
+    """10 straight steps == 5 steps, export state, restore into fresh buffers, 5 steps."""
+    w, p0 = _fresh(50_001, "f16", 15)
+    o = fa.options(**w.options())
+    grads = [_grads(w, c) for c in range(1, 11)]
+    pa = p0.clone()
+    sa = _zeros(w.n, 3)
+    ta = 0
+    for g in grads:
+        ta, _ = fa.fa_adamw_step_inplace(pa, g, *sa, ta, o, fa.control())
+    pb = p0.clone()
+    sb = _zeros(w.n, 3)
+    tb = 0
+    for g in grads[:5]:
+        tb, _ = fa.fa_adamw_step_inplace(pb, g, *sb, tb, o, fa.control())
+    torch.cuda.synchronize()
+    saved = {"t": tb, "p": pb.cpu(), "m": sb[0].cpu(), "v": sb[1].cpu(), "vmax": sb[2].cpu()}
+    del pb, sb
+    pc = saved["p"].to(DEV)
+    sc = [saved[k].to(DEV) for k in ("m", "v", "vmax")]
+    tc = saved["t"]
+    for g in grads[5:]:
+        tc, _ = fa.fa_adamw_step_inplace(pc, g, *sc, tc, o, fa.control())
+    torch.cuda.synchronize()
+    assert ta == tc == 10
+    assert torch.equal(pa, pc) and all(torch.equal(x, y) for x, y in zip(sa, sc))
+
+
+def test_skip_and_empty_launch_nothing():
+    w, p0 = _fresh(1000, "f32", 16)
+    o = fa.options(**w.options())
+    g = _grads(w, 1)
+    # out of place, skip: returns the very same tensors, allocates nothing
+    before = torch.cuda.memory_allocated()
+    p2, m2, v2, vm2, t2, upd = fa.fa_adamw_step(p0, g, None, None, None, 0, o,
+                                                fa.control(skip_update=True))
+    assert p2 is p0 and m2 is None and t2 == 0 and not upd
+    assert torch.cuda.memory_allocated() == before
+    e = torch.empty(0, device=DEV)
+    p3, _, _, _, t3, upd3 = fa.fa_adamw_step(e, e, None, None, None, 4, o, fa.control())
+    assert t3 == 4 and not upd3
+
+
+# ---- statistics kernels ---------------------------------------------------------
+
+def _planted_grad(n, gdt, seed, bad_idx, sigma=1e-2):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal(n) * sigma).astype(np.float32)
+    vals = [np.inf, -np.inf, np.nan]
+    for j, i in enumerate(bad_idx):
+        x[i] = vals[j % 3]
+    t = torch.from_numpy(x)
+    t = t.to({"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[gdt])
+    bits = t.numpy() if gdt == "f32" else t.view(torch.int16).numpy().view(np.uint16)
+    return t.to(DEV), bits
+
+
+@pytest.mark.parametrize("gdt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("n,row_len,segs", [
+    (256 * 1000, 256, None), (256 * 777 + 5, 256, None), (12_345, 100, None), (3, 256, None),
+    (100_000, 256, [0, 1, 2049, 70_000, 70_000, 100_000]), (65_536, 7, None)])
+def test_analyze_rows_match_oracle(gdt, n, row_len, segs, oracle_lib):
+    bad = [0, n // 3, n - 1] if n > 3 else [1]
+    g, bits = _planted_grad(n, gdt, 21, bad)
+    rows = fa.fa_stats_rows(n, row_len, segs)
+    buf = fa.stats_buffer(rows, DEV)
+    got = fa.fa_analyze_gradient(g, row_len, buf, segs)
+    torch.cuda.synchronize()
+    assert got == rows
+    rs, rc = oracle_lib.row_stats(bits, gdt, row_len, segs)
+    host = buf.cpu()
+    dev_s = host[:rows, 0].view(torch.float32).double().numpy()
+    dev_c = host[:rows, 1].numpy().astype(np.int64)
+    dev_lo = host[:rows, 2].view(torch.float32).double().numpy()
+    assert np.array_equal(dev_c, rc.astype(np.int64))
+    ok = rc == 0
+    assert np.all(np.abs(dev_s + dev_lo - rs)[ok] <= 2e-6 * rs[ok] + 1e-30)
+
+
+@pytest.mark.parametrize("rows", [1, 2, 1023, 1024, 1025, 4096, 1_048_575, 1_048_576,
+                                  1_048_577, 4_194_304])
+def test_merge_matches_exact_sum(rows):
+    """The merge only reorders the sum: compare with math.fsum of the records."""
+    import math
+    rng = np.random.default_rng(rows)
+    s = (rng.random(rows) * 10).astype(np.float32)
+    lo = (rng.random(rows) * 1e-7).astype(np.float32)
+    c = rng.integers(0, 3, rows).astype(np.int32) * (rng.random(rows) < 1e-3)
+    host = torch.zeros((rows, 3), dtype=torch.int32)
+    host[:, 0] = torch.from_numpy(s).view(torch.int32)
+    host[:, 1] = torch.from_numpy(c.astype(np.int32))
+    host[:, 2] = torch.from_numpy(lo).view(torch.int32)
+    rows_in = host.to(DEV)
+    scratch = fa.scratch_buffer(rows, DEV)
+    report = fa.stats_buffer(1, DEV)
+    fa.fa_merge_gradient_stats(rows_in, rows, scratch, report)
+    h = fa.fa_read_report(report)
+    exact = math.fsum(s.astype(np.float64)) + math.fsum(lo.astype(np.float64))
+    got = float(h.sum_sq) + float(h.sum_sq_lo)
+    assert h.nonfinite == int(c.sum())
+    assert abs(got - exact) <= 1e-12 * exact
+
+
+def test_clip_decide_and_report_roundtrip(oracle_lib):
+    n = 256 * 4096
+    g, bits = _planted_grad(n, "bf16", 22, [], sigma=0.05)
+    rows = fa.fa_stats_rows(n, 256)
+    buf = fa.stats_buffer(rows, DEV)
+    scratch = fa.scratch_buffer(rows, DEV)
+    report = fa.stats_buffer(1, DEV)
+    fa.fa_analyze_gradient(g, 256, buf)
+    fa.fa_merge_gradient_stats(buf, rows, scratch, report)
+    skip, norm, coef = fa.fa_clip_decide(report, 4.0, 1.0)
+    s_or, c_or = oracle_lib.gradient_stats(bits, "bf16", 4.0)
+    o_skip, o_norm, o_coef = oracle_lib.clip_decision(s_or, c_or, 1.0)
+    assert skip == o_skip and abs(norm - o_norm) <= 1e-6 * o_norm
+    assert abs(coef - o_coef) <= 1e-6 * o_coef
+
+
+# ---- validation on the device -----------------------------------------------------
+
+def _state(n):
+    return [torch.randn(n, device=DEV) for _ in range(4)]
+
+
+def test_rejections_leave_inputs_untouched():
+    n = 4096
+    p, m, v, vm = _state(n)
+    g = torch.randn(n, device=DEV)
+    snap = [x.clone() for x in (p, m, v, vm, g)]
+    o = fa.options(amsgrad=True)
+    # overlapping state buffers
+    with pytest.raises(fa.FusedAdamWError) as e:
+        fa.fa_adamw_step_inplace(p, g, m, m, vm, 3, o, fa.control())
+    assert e.value.status == 5
+    big = torch.randn(2 * n, device=DEV)
+    with pytest.raises(fa.FusedAdamWError) as e:
+        fa.fa_adamw_step_inplace(big[:n], g, big[n // 2:n // 2 + n], v, vm, 3, o, fa.control())
+    assert e.value.status == 5
+    # gradient aliasing the parameters
+    with pytest.raises(fa.FusedAdamWError) as e:
+        fa.fa_adamw_step_inplace(p, p, m, v, vm, 3, o, fa.control())
+    assert e.value.status == 5
+    # host memory (pageable and pinned)
+    for host in (torch.randn(n), torch.randn(n).pin_memory()):
+        with pytest.raises((fa.FusedAdamWError, ValueError)):
+            fa.fa_adamw_step_inplace(p, host, m, v, vm, 3, o, fa.control())
+    # out of place: output aliasing an input
+    with pytest.raises(fa.FusedAdamWError) as e:
+        import ctypes
+        from amsgrad_optimizer_step_gb300 import _lib
+        tt, up = ctypes.c_uint64(), ctypes.c_int32()
+        st = _lib.load().fa_adamw_step(n, p.data_ptr(), g.data_ptr(), 0, m.data_ptr(),
+                                       v.data_ptr(), vm.data_ptr(), 3, ctypes.byref(o),
+                                       fa.control(), p.data_ptr(), m.data_ptr(),
+                                       v.data_ptr(), vm.data_ptr(), ctypes.byref(tt),
+                                       ctypes.byref(up), None)
+        _lib.check("fa_adamw_step", st)
+    assert e.value.status == 5
+    # misaligned FP32 pointer (2-byte offset)
+    import ctypes
+    from amsgrad_optimizer_step_gb300 import _lib
+    tt = ctypes.c_uint64(3)
+    up = ctypes.c_int32()
+    st = _lib.load().fa_adamw_step_inplace(n - 1, p.data_ptr() + 2, g.data_ptr(), 0, m.data_ptr(),
+                                           v.data_ptr(), vm.data_ptr(), ctypes.byref(tt),
+                                           ctypes.byref(o), fa.control(), 1.0, ctypes.byref(up),
+                                           None)
+    assert st == 7 and tt.value == 3
+    torch.cuda.synchronize()
+    for a, b in zip((p, m, v, vm, g), snap):
+        assert torch.equal(a, b)
+
+
+def test_analyze_rejects_plan_overflow():
+    n = 4_194_305 * 2
+    g = torch.zeros(n, dtype=torch.bfloat16, device=DEV)
+    buf = fa.stats_buffer(1, DEV)
+    with pytest.raises(fa.FusedAdamWError) as e:
+        fa.fa_analyze_gradient(g, 2, buf)
+    assert e.value.status == 8
+
+
+def test_host_pointers_rejected_by_the_library():
+    """The C ABI itself refuses host memory (pageable or pinned) with FA_ERR_POINTER."""
+    import ctypes
+    from amsgrad_optimizer_step_gb300 import _lib
+    n = 1024
+    p, m, v, _ = _state(n)
+    o = fa.options()
+    for host in (torch.randn(n), torch.randn(n).pin_memory()):
+        tt = ctypes.c_uint64(2)
+        up = ctypes.c_int32(5)
+        st = _lib.load().fa_adamw_step_inplace(n, p.data_ptr(), host.data_ptr(), 0, m.data_ptr(),
+                                               v.data_ptr(), None, ctypes.byref(tt),
+                                               ctypes.byref(o), fa.control(), 1.0,
+                                               ctypes.byref(up), None)
+        assert st == 6 and tt.value == 2 and up.value == 5
