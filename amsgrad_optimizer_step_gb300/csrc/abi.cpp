@@ -15,6 +15,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -31,6 +34,23 @@ int sm_count(int device) {
         return 0;
     if (device >= 0 && device < 64) cache[device] = n;
     return n;
+}
+
+int resident_ctas(const void *kernel, int device) {
+    // Immutable per (device, kernel): computed once, then looked up.
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({device, kernel});
+    if (it != cache.end()) return it->second;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        occ = 0;
+    }
+    if (occ < 1) occ = 1;
+    cache[{device, kernel}] = occ;
+    return occ;
 }
 
 }  // namespace fa

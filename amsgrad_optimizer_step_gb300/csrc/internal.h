@@ -59,4 +59,15 @@ cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaS
 // SM count of the current device (cached per device).
 int sm_count(int device);
 
+// Resident CTAs per SM of ``kernel`` at kThreads threads (cached per device and
+// kernel; >= 1), and the persistent grid for ``need`` CTAs of work.
+int resident_ctas(const void *kernel, int device);
+
+template <typename Kernel>
+inline int persistent_grid(Kernel kernel, int64_t need, int device) {
+    const int64_t cap = static_cast<int64_t>(sm_count(device)) *
+                        resident_ctas(reinterpret_cast<const void *>(kernel), device);
+    return static_cast<int>(need < cap ? need : cap);
+}
+
 }  // namespace fa

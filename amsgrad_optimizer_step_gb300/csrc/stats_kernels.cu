@@ -46,6 +46,9 @@ struct StatIO<FA_F32> {
     static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
         acc1(__ldcs(reinterpret_cast<const unsigned int *>(g) + i), s, c);
     }
+    static __device__ __forceinline__ void acc16(const uint4 &r, float &s, uint32_t &c) {
+        acc1(r.x, s, c); acc1(r.y, s, c); acc1(r.z, s, c); acc1(r.w, s, c);
+    }
 };
 
 template <>
@@ -68,6 +71,14 @@ struct StatIO<FA_BF16> {
     static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
         acc1(__ldcs(static_cast<const unsigned short *>(g) + i), s, c);
     }
+    static __device__ __forceinline__ void acc16(const uint4 &r, float &s, uint32_t &c) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc1(w[k] & 0xffffu, s, c);
+            acc1(w[k] >> 16, s, c);
+        }
+    }
 };
 
 template <>
@@ -89,6 +100,14 @@ struct StatIO<FA_F16> {
     }
     static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
         acc1(__ldcs(static_cast<const unsigned short *>(g) + i), s, c);
+    }
+    static __device__ __forceinline__ void acc16(const uint4 &r, float &s, uint32_t &c) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc1(w[k] & 0xffffu, s, c);
+            acc1(w[k] >> 16, s, c);
+        }
     }
 };
 
@@ -156,6 +175,122 @@ analyze_kernel(const __grid_constant__ AnalyzeArgs a) {
     }
 }
 
+// Squares of one 16-byte word, added unconditionally (no finiteness test).
+template <int GT>
+__device__ __forceinline__ void sq16(const uint4 &r, float &s) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (GT == FA_F32) {
+            const float x = __uint_as_float(w[k]);
+            s = fmaf(x, x, s);
+        } else if (GT == FA_BF16) {
+            const float lo = __uint_as_float(w[k] << 16);
+            const float hi = __uint_as_float(w[k] & 0xffff0000u);
+            s = fmaf(lo, lo, s);
+            s = fmaf(hi, hi, s);
+        } else {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            s = fmaf(f.x, f.x, s);
+            s = fmaf(f.y, f.y, s);
+        }
+    }
+}
+
+// Exact count of NaN / +-Inf patterns in one 16-byte word.
+template <int GT>
+__device__ __forceinline__ uint32_t count_nonfinite16(const uint4 &r) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    uint32_t c = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (GT == FA_F32) {
+            c += (w[k] & 0x7f800000u) == 0x7f800000u;
+        } else {
+            const uint32_t e = GT == FA_BF16 ? 0x7f80u : 0x7c00u;
+            c += (w[k] & e) == e;
+            c += ((w[k] >> 16) & e) == e;
+        }
+    }
+    return c;
+}
+
+// Fast path: every row start 16-byte aligned and a full row a whole number
+// CH of 512-byte warp chunks.  A warp takes 8/CH consecutive rows per
+// iteration and issues all their 16-byte loads (8 per lane, 4 KB per warp)
+// before any arithmetic.  Squares are summed without a finiteness test: a
+// row's FP32 sum of non-negative terms is finite exactly when none of its
+// values is NaN or +-Inf, unless a finite value's square overflows FP32.  So
+// the exact bit-pattern count runs only for rows whose sum came out
+// non-finite, from the words still held in registers.  The rare short row at
+// a segment's end takes the checked scalar loop.
+template <int GT, int CH>
+__global__ void __launch_bounds__(kThreads)
+analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
+    constexpr int R = 8 / CH;
+    constexpr int64_t kElemBytes = GT == FA_F32 ? 4 : 2;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    const char *gb = static_cast<const char *>(a.g);
+
+    for (int64_t r0 = warp * R; r0 < a.rows; r0 += nwarps * R) {
+        int k = a.nseg == 1 ? 0 : find_segment(a, r0);
+        uint32_t full = 0;
+        uint4 buf[R][CH];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int64_t r = r0 + j;
+            if (r < a.rows) {
+                while (k + 1 < a.nseg && a.row_start[k + 1] <= r) ++k;
+                const int64_t start = a.seg_start[k] + (r - a.row_start[k]) * a.row_len;
+                if (start + a.row_len <= a.seg_start[k + 1]) {
+                    full |= 1u << j;
+                    const uint4 *q = reinterpret_cast<const uint4 *>(gb + start * kElemBytes);
+#pragma unroll
+                    for (int ch = 0; ch < CH; ++ch) buf[j][ch] = __ldcs(q + ch * 32 + lane);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int64_t r = r0 + j;
+            float tot;
+            uint32_t cnt = 0;
+            if (full & (1u << j)) {
+                float sj = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < CH; ++ch) sq16<GT>(buf[j][ch], sj);
+                tot = warp_sum(sj);
+                if (!isfinite(tot)) {  // warp-uniform: the butterfly gives every lane the total
+                    uint32_t c = 0;
+#pragma unroll
+                    for (int ch = 0; ch < CH; ++ch) c += count_nonfinite16<GT>(buf[j][ch]);
+                    cnt = __reduce_add_sync(0xffffffffu, c);
+                }
+            } else if (r < a.rows) {
+                const int ks = a.nseg == 1 ? 0 : find_segment(a, r);
+                const int64_t start = a.seg_start[ks] + (r - a.row_start[ks]) * a.row_len;
+                const int64_t end = a.seg_start[ks + 1];
+                float sj = 0.f;
+                uint32_t c = 0;
+                for (int64_t i = start + lane; i < end; i += 32) StatIO<GT>::accs(a.g, i, sj, c);
+                tot = warp_sum(sj);
+                cnt = __reduce_add_sync(0xffffffffu, c);
+            } else {
+                continue;
+            }
+            if (lane == j) {
+                fa_stats rec;
+                rec.sum_sq = tot;
+                rec.nonfinite = cnt;
+                rec.sum_sq_lo = 0.f;
+                a.out[r] = rec;
+            }
+        }
+    }
+}
+
 // One CTA per group of kFanIn input records.
 __global__ void __launch_bounds__(kThreads)
 merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
@@ -202,15 +337,31 @@ cudaError_t launch_analyze_typed(const AnalyzeArgs &a, bool vec, cudaStream_t st
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return cudaErrorInvalidDevice;
-    const int64_t warps_needed = (a.rows + kRowsPerWarp - 1) / kRowsPerWarp;
-    const int64_t need = (warps_needed * 32 + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs (64 warps) per SM
-    const int grid = static_cast<int>(need < cap ? need : cap);
-    if (grid == 0) return cudaSuccess;
-    if (vec) analyze_kernel<GT, true><<<grid, kThreads, 0, stream>>>(a);
-    else analyze_kernel<GT, false><<<grid, kThreads, 0, stream>>>(a);
+    if (sm_count(dev) <= 0) return cudaErrorInvalidDevice;
+    const int64_t row_bytes = a.row_len * (GT == FA_F32 ? 4 : 2);
+    const int64_t ch = row_bytes % 512 == 0 ? row_bytes / 512 : 0;
+    auto ctas_for = [&](int64_t rows_per_warp) {
+        return (((a.rows + rows_per_warp - 1) / rows_per_warp) * 32 + kThreads - 1) / kThreads;
+    };
+    if (vec && (ch == 1 || ch == 2 || ch == 4 || ch == 8)) {
+        const int64_t need = ctas_for(8 / ch);
+        switch (ch) {
+            case 1: { auto k = analyze_fast_kernel<GT, 1>;
+                      k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
+            case 2: { auto k = analyze_fast_kernel<GT, 2>;
+                      k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
+            case 4: { auto k = analyze_fast_kernel<GT, 4>;
+                      k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
+            default: { auto k = analyze_fast_kernel<GT, 8>;
+                       k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
+        }
+    } else if (vec) {
+        auto k = analyze_kernel<GT, true>;
+        k<<<persistent_grid(k, ctas_for(kRowsPerWarp), dev), kThreads, 0, stream>>>(a);
+    } else {
+        auto k = analyze_kernel<GT, false>;
+        k<<<persistent_grid(k, ctas_for(kRowsPerWarp), dev), kThreads, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 

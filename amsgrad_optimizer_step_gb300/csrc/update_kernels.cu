@@ -213,34 +213,21 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return cudaErrorInvalidDevice;
+    if (sm_count(dev) <= 0) return cudaErrorInvalidDevice;
 
     if (vector_ok) {
         auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll>;
-        static int occupancy[64] = {0};  // resident CTAs per SM, by device (immutable property)
-        int occ = dev < 64 ? occupancy[dev] : 0;
-        if (occ == 0) {
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, 0);
-            if (err != cudaSuccess) return err;
-            if (occ < 1) occ = 1;
-            if (dev < 64) occupancy[dev] = occ;
-        }
         const int64_t per_cta = static_cast<int64_t>(kThreads) * kUnroll;
         int64_t need = (a.nvec + per_cta - 1) / per_cta;
-        const int64_t edge = a.head > (a.n - a.head - a.nvec * kVec)
-                                 ? a.head : (a.n - a.head - a.nvec * kVec);
-        need = need > 0 ? need : (edge > 0 ? 1 : 0);
-        const int64_t cap = static_cast<int64_t>(sms) * occ;
-        const int grid = static_cast<int>(need < cap ? need : cap);
+        if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
+        const int grid = persistent_grid(kern, need, dev);
         if (grid == 0) return cudaSuccess;
         kern<<<grid, kThreads, 0, stream>>>(a, c);
     } else {
-        const int64_t need = (a.n + kThreads - 1) / kThreads;
-        const int64_t cap = static_cast<int64_t>(sms) * 8;
-        const int grid = static_cast<int>(need < cap ? need : cap);
+        auto kern = update_scalar_kernel<GT, AMS, FIRST>;
+        const int grid = persistent_grid(kern, (a.n + kThreads - 1) / kThreads, dev);
         if (grid == 0) return cudaSuccess;
-        update_scalar_kernel<GT, AMS, FIRST><<<grid, kThreads, 0, stream>>>(a, c);
+        kern<<<grid, kThreads, 0, stream>>>(a, c);
     }
     return cudaGetLastError();
 }

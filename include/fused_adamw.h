@@ -78,9 +78,11 @@ typedef struct fa_step_control {
 
 /* 12-byte statistics record ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": a 12-byte
  * report).  Row records, intermediate merge records and the final report all
- * use it.  sum_sq + sum_sq_lo (added in FP64) is the sum of squares of the
- * STORED (still scaled) finite gradient values; nonfinite counts stored NaN
- * and +-Inf values, saturating at 2^32-1. */
+ * use it.  nonfinite counts stored NaN and +-Inf values exactly (saturating
+ * at 2^32-1).  When nonfinite == 0, sum_sq + sum_sq_lo (added in FP64) is the
+ * sum of squares of the STORED (still scaled) gradient values; when
+ * nonfinite > 0 the sum is unspecified (it may be Inf or NaN) -- the step is
+ * skipped then and the sum is never used. */
 typedef struct fa_stats {
     float sum_sq;
     uint32_t nonfinite;

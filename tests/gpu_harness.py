@@ -147,7 +147,7 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
                  full_grad_on_host: bool = True, step_check=True):
     """Runs every call of ``w`` (at size n) and checks each one.  Returns a summary."""
     lib = lib or oracle.lib()
-    ws = w if n == w.n else w.scaled(n, segments=None)
+    ws = w if n == w.n else w.scaled(n)
     if segments is not None and n != w.n:
         import dataclasses
         ws = dataclasses.replace(ws, segments=tuple(segments))
@@ -228,7 +228,9 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         # one step from identical state
         if step_check:
             zero = np.zeros(len(idx))
-            b4 = tuple(z if z is not None else zero for z in before)
+            # before the first update the moment buffers hold no state (never read)
+            b4 = (before[0], zero, zero, zero) if t_before == 0 else \
+                tuple(z if z is not None else zero for z in before)
             ref = oracle_one_step(gh, ws.grad_dtype, opts, ws.gradient_scale, coef_dev, st.t,
                                   b4, lib)
             gmul = (-1.0 if opts["maximize"] else 1.0) * coef_dev / ws.gradient_scale

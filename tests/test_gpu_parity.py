@@ -118,7 +118,7 @@ def test_misaligned_views(gdt, offsets):
     scalar head; mixed offsets -> all-scalar kernel.  Both must match the oracle."""
     n = 10_001
     w = dataclasses.replace(CONFIG2, grad_dtype=gdt, calls=3, skip_calls=(), amsgrad=True,
-                            inplace=True)
+                            inplace=True).scaled(n)
     import oracle
     lib = oracle.lib()
     idx = np.arange(n)
