@@ -23,7 +23,8 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
 __all__ = [
     "fa_abi_version", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
     "fa_adamw_step_inplace", "fa_bucket_step", "fa_stats_plan", "fa_stats_rows",
-    "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_read_report", "fa_clip_decision",
+    "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",
+    "fa_read_report", "fa_clip_decision",
     "fa_clip_decide", "fa_bucket_step_clipped", "options", "control", "stats_buffer",
     "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
 ]
@@ -247,6 +248,19 @@ def fa_merge_gradient_stats(rows_in: torch.Tensor, rows: int, scratch: Optional[
     check("fa_merge_gradient_stats", _L().fa_merge_gradient_stats(
         _ptr(rows_in), rows, _ptr(scratch), 0 if scratch is None else scratch.numel(),
         _ptr(report), _stream(stream)))
+
+
+def fa_merge_gradient_stats_static(rows_in: torch.Tensor, rows: int, report: torch.Tensor,
+                                   stream=None) -> None:
+    """Merge into ``report`` using the library's fixed scratch (allocates nothing).
+
+    For callers that cannot allocate device memory; calls on streams that are
+    not ordered with each other race on the shared scratch.
+    """
+    _stats_tensor("rows_in", rows_in)
+    _stats_tensor("report", report)
+    check("fa_merge_gradient_stats_static", _L().fa_merge_gradient_stats_static(
+        _ptr(rows_in), rows, _ptr(report), _stream(stream)))
 
 
 def fa_read_report(report: torch.Tensor, stream=None) -> FaStats:

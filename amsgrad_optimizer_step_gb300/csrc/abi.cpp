@@ -491,6 +491,40 @@ fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *
     return FA_OK;
 }
 
+fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
+                                         fa_stats *report, void *stream) {
+    int32_t kernels = 0;
+    int64_t need = 0;
+    fa_status st = fa_stats_plan(rows, &kernels, &need);
+    if (st != FA_OK) return st;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(rows_in, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(report, dev, 4)) != FA_OK) return st;
+    if (overlap({rows_in, static_cast<size_t>(rows) * 12}, {report, 12})) return FA_ERR_ALIAS;
+    float *scratch = nullptr;
+    int64_t capacity = 0;
+    if (fa::static_merge_scratch(dev, &scratch, &capacity) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    if (need > capacity) return FA_ERR_SIZE;
+
+    const fa_stats *in = rows_in;
+    int64_t count = rows;
+    fa_stats *next = reinterpret_cast<fa_stats *>(scratch);
+    for (int32_t level = 0; level < kernels; ++level) {
+        const int64_t out_count = (count + fa::kFanIn - 1) / fa::kFanIn;
+        fa_stats *out = out_count == 1 ? report : next;
+        cudaError_t err = fa::launch_merge(in, count, out, static_cast<cudaStream_t>(stream));
+        if (err != cudaSuccess) return FA_ERR_CUDA;
+        in = out;
+        count = out_count;
+        next = out + out_count;
+    }
+    return FA_OK;
+}
+
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream) {
     if (!report_host) return FA_ERR_NULL;
     int dev = 0;

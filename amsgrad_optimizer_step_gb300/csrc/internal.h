@@ -56,6 +56,11 @@ cudaError_t launch_analyze(const AnalyzeArgs &a, fa_dtype gdt, bool vector_ok,
 // One merge level: ceil(count / kFanIn) output records from count input records.
 cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream);
 
+// Device address and size of the library's fixed merge scratch on ``device``
+// (which must be the current device).  Looked up once per device.
+constexpr int64_t kStaticMergeScratchFloats = 12300;  // 3 * (4096 + 4): the largest plan
+cudaError_t static_merge_scratch(int device, float **ptr, int64_t *capacity_floats);
+
 // SM count of the current device (cached per device).
 int sm_count(int device);
 

@@ -12,6 +12,8 @@
 // warp shuffle tree) -- at 256 elements per row its relative error stays
 // below 1e-6.  Merges widen to FP64, add, and hand the FP64 total to the next
 // level as a (hi, lo) pair of floats, so later levels lose nothing.
+#include <mutex>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -382,6 +384,32 @@ cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaS
     if (grid <= 0) return cudaSuccess;
     merge_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(in, count, out);
     return cudaGetLastError();
+}
+
+// ---- fixed merge scratch for callers that cannot allocate ------------------------
+//
+// One file-scope device array, large enough for the biggest reduction plan
+// (4,194,304 rows -> 4096 + 4 intermediate 12-byte records = 12,300 floats,
+// 49,200 bytes).  Every GPU that loads this library holds it until the
+// process exits.  In host code the symbol is only a stand-in: its device
+// address comes from cudaGetSymbolAddress, looked up once per device.
+
+static __device__ __align__(256) float g_static_merge_scratch[kStaticMergeScratchFloats];
+
+cudaError_t static_merge_scratch(int device, float **ptr, int64_t *capacity_floats) {
+    static std::mutex mu;
+    static float *addr[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[device]) {
+        void *p = nullptr;
+        const cudaError_t err = cudaGetSymbolAddress(&p, g_static_merge_scratch);
+        if (err != cudaSuccess) return err;
+        addr[device] = static_cast<float *>(p);
+    }
+    *ptr = addr[device];
+    *capacity_floats = kStaticMergeScratchFloats;
+    return cudaSuccess;
 }
 
 }  // namespace fa

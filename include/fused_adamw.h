@@ -219,6 +219,33 @@ fa_status fa_analyze_gradient(const void *g, fa_dtype gdt, int64_t n, int32_t ro
 fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *scratch,
                                   int64_t scratch_elements, fa_stats *report, void *stream);
 
+/*
+ * fa_merge_gradient_stats without a caller-supplied scratch buffer.  The pages
+ * have no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory: for example a plugin whose host framework owns
+ * every device allocation and does not let extensions call cudaMalloc, or
+ * code on a latency-critical path where cudaMalloc/cudaFree, which may
+ * synchronise the device, are not allowed.  Inputs and output stay the
+ * caller's (rows_in and report, as in fa_merge_gradient_stats).
+ *
+ * The intermediate records go to one fixed scratch array inside the library
+ * (12,300 floats = 49,200 bytes: the largest reduction plan, 4,194,304 rows).
+ * Every GPU that loads the library holds that array until the process exits.
+ * rows outside 1..4,194,304 are rejected with FA_ERR_PLAN before anything is
+ * enqueued.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ * library routine is called.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array: the merge
+ * writes every scratch record before reading it, so leftovers from an
+ * earlier call never leak into a result, but calls whose kernels overlap on
+ * the GPU (different streams without ordering between them) race on the
+ * array and must be serialised by the caller.
+ */
+fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
+                                         fa_stats *report, void *stream);
+
 /* Copies the 12-byte device report to host memory and waits for the stream
  * ([TR-zh]: the report is read back before any update).  Synchronises. */
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream);
