@@ -36,20 +36,21 @@ int sm_count(int device) {
     return n;
 }
 
-int resident_ctas(const void *kernel, int device) {
-    // Immutable per (device, kernel): computed once, then looked up.
+int resident_ctas(const void *kernel, int device, int threads) {
+    // Immutable per (device, kernel, threads): computed once, then looked up.
     static std::mutex mu;
-    static std::map<std::pair<int, const void *>, int> cache;
+    static std::map<std::pair<std::pair<int, int>, const void *>, int> cache;
     std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find({device, kernel});
+    const auto key = std::make_pair(std::make_pair(device, threads), kernel);
+    auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0) != cudaSuccess) {
         cudaGetLastError();
         occ = 0;
     }
     if (occ < 1) occ = 1;
-    cache[{device, kernel}] = occ;
+    cache[key] = occ;
     return occ;
 }
 

@@ -64,14 +64,14 @@ cudaError_t static_merge_scratch(int device, float **ptr, int64_t *capacity_floa
 // SM count of the current device (cached per device).
 int sm_count(int device);
 
-// Resident CTAs per SM of ``kernel`` at kThreads threads (cached per device and
+// Resident CTAs per SM of ``kernel`` at ``threads`` threads (cached per device and
 // kernel; >= 1), and the persistent grid for ``need`` CTAs of work.
-int resident_ctas(const void *kernel, int device);
+int resident_ctas(const void *kernel, int device, int threads = kThreads);
 
 template <typename Kernel>
-inline int persistent_grid(Kernel kernel, int64_t need, int device) {
+inline int persistent_grid(Kernel kernel, int64_t need, int device, int threads = kThreads) {
     const int64_t cap = static_cast<int64_t>(sm_count(device)) *
-                        resident_ctas(reinterpret_cast<const void *>(kernel), device);
+                        resident_ctas(reinterpret_cast<const void *>(kernel), device, threads);
     return static_cast<int>(need < cap ? need : cap);
 }
 

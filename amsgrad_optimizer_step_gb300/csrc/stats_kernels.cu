@@ -217,78 +217,141 @@ __device__ __forceinline__ uint32_t count_nonfinite16(const uint4 &r) {
     return c;
 }
 
-// Fast path: every row start 16-byte aligned and a full row a whole number
-// CH of 512-byte warp chunks.  A warp takes 8/CH consecutive rows per
-// iteration and issues all their 16-byte loads (8 per lane, 4 KB per warp)
-// before any arithmetic.  Squares are summed without a finiteness test: a
-// row's FP32 sum of non-negative terms is finite exactly when none of its
-// values is NaN or +-Inf, unless a finite value's square overflows FP32.  So
-// the exact bit-pattern count runs only for rows whose sum came out
-// non-finite, from the words still held in registers.  The rare short row at
-// a segment's end takes the checked scalar loop.
-template <int GT, int CH>
+// Sums R rows' per-lane partials across the warp in one transposed butterfly:
+// at each of the first log2(R) levels a lane keeps half of its rows and
+// trades the other half with its partner, so R rows cost R-1 shuffles plus
+// the 5-log2(R) of a single butterfly.  Returns the total of row
+// (lane >> (5 - log2 R)) & (R - 1), which every lane of that group holds.
+template <int R>
+__device__ __forceinline__ float transpose_reduce(const float (&s)[R], int lane) {
+    float cur[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i] = s[i];
+    int off = 16;
+#pragma unroll
+    for (int h = R / 2; h >= 1; h >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? cur[i] : cur[i + h];
+            const float keep = upper ? cur[i + h] : cur[i];
+            cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        off >>= 1;
+    }
+#pragma unroll
+    for (; off >= 1; off >>= 1) cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], off);
+    return cur[0];
+}
+
+// Fast path: every row start 16-byte aligned and a full row exactly CH
+// 512-byte warp chunks (so the row length is a compile-time constant).  A
+// warp takes R = 8/CH consecutive rows per iteration and issues all their
+// 16-byte loads (8 per lane, 4 KB per warp) before any arithmetic; in a
+// single-segment buffer the rows of an iteration share one base address.
+// Squares are summed without a finiteness test: a row's FP32 sum of
+// non-negative terms is finite exactly when none of its values is NaN or
+// +-Inf (unless a finite value's square overflows FP32), so the exact
+// bit-pattern count runs only for rows whose sum came out non-finite, from
+// the words still held in registers.  Short rows at a segment's end take a
+// checked scalar loop.
+template <int GT, int CH, bool MULTI>
 __global__ void __launch_bounds__(kThreads)
 analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
     constexpr int R = 8 / CH;
+    constexpr int kLog2R = R == 8 ? 3 : R == 4 ? 2 : R == 2 ? 1 : 0;
     constexpr int64_t kElemBytes = GT == FA_F32 ? 4 : 2;
+    constexpr int64_t kRowElems = 512 * CH / kElemBytes;
     const int lane = threadIdx.x & 31;
+    const int my_row = (lane >> (5 - kLog2R)) & (R - 1);
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
     const char *gb = static_cast<const char *>(a.g);
+    const int64_t single_full_rows = MULTI ? 0 : (a.seg_start[1] - a.seg_start[0]) / kRowElems;
 
     for (int64_t r0 = warp * R; r0 < a.rows; r0 += nwarps * R) {
-        int k = a.nseg == 1 ? 0 : find_segment(a, r0);
-        uint32_t full = 0;
+        uint32_t full = 0, valid = 0;
         uint4 buf[R][CH];
+        if (!MULTI && r0 + R <= single_full_rows) {
+            const uint4 *q = reinterpret_cast<const uint4 *>(
+                                 gb + (a.seg_start[0] + r0 * kRowElems) * kElemBytes) + lane;
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const int64_t r = r0 + j;
-            if (r < a.rows) {
-                while (k + 1 < a.nseg && a.row_start[k + 1] <= r) ++k;
-                const int64_t start = a.seg_start[k] + (r - a.row_start[k]) * a.row_len;
-                if (start + a.row_len <= a.seg_start[k + 1]) {
-                    full |= 1u << j;
-                    const uint4 *q = reinterpret_cast<const uint4 *>(gb + start * kElemBytes);
+            for (int j = 0; j < R; ++j)
 #pragma unroll
-                    for (int ch = 0; ch < CH; ++ch) buf[j][ch] = __ldcs(q + ch * 32 + lane);
+                for (int ch = 0; ch < CH; ++ch) buf[j][ch] = __ldcs(q + (j * CH + ch) * 32);
+            full = valid = (1u << R) - 1;
+        } else {
+            int k = MULTI ? find_segment(a, r0) : 0;
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                const int64_t r = r0 + j;
+                if (r < a.rows) {
+                    valid |= 1u << j;
+                    if (MULTI)
+                        while (k + 1 < a.nseg && a.row_start[k + 1] <= r) ++k;
+                    const int64_t start = a.seg_start[k] + (r - a.row_start[k]) * kRowElems;
+                    if (start + kRowElems <= a.seg_start[k + 1]) {
+                        full |= 1u << j;
+                        const uint4 *q =
+                            reinterpret_cast<const uint4 *>(gb + start * kElemBytes) + lane;
+#pragma unroll
+                        for (int ch = 0; ch < CH; ++ch) buf[j][ch] = __ldcs(q + ch * 32);
+                    }
                 }
             }
         }
+        float s[R];
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-            const int64_t r = r0 + j;
-            float tot;
-            uint32_t cnt = 0;
+            s[j] = 0.f;
             if (full & (1u << j)) {
-                float sj = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < CH; ++ch) sq16<GT>(buf[j][ch], sj);
-                tot = warp_sum(sj);
-                if (!isfinite(tot)) {  // warp-uniform: the butterfly gives every lane the total
+                for (int ch = 0; ch < CH; ++ch) sq16<GT>(buf[j][ch], s[j]);
+            }
+        }
+        float tot = transpose_reduce<R>(s, lane);
+        uint32_t cnt = 0;
+
+        // rows whose FP32 sum is non-finite: exact count from the registers
+        const unsigned bad = __ballot_sync(0xffffffffu, ((full >> my_row) & 1u) && !isfinite(tot));
+        if (bad) {
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                if (bad & (1u << (j << (5 - kLog2R)))) {
                     uint32_t c = 0;
 #pragma unroll
                     for (int ch = 0; ch < CH; ++ch) c += count_nonfinite16<GT>(buf[j][ch]);
-                    cnt = __reduce_add_sync(0xffffffffu, c);
+                    c = __reduce_add_sync(0xffffffffu, c);
+                    if (my_row == j) cnt = c;
                 }
-            } else if (r < a.rows) {
-                const int ks = a.nseg == 1 ? 0 : find_segment(a, r);
-                const int64_t start = a.seg_start[ks] + (r - a.row_start[ks]) * a.row_len;
+            }
+        }
+        // short rows at a segment's end: checked scalar loop
+        const uint32_t partial = valid & ~full;
+        if (partial) {
+            for (int j = 0; j < R; ++j) {
+                if (!(partial & (1u << j))) continue;
+                const int64_t r = r0 + j;
+                const int ks = MULTI ? find_segment(a, r) : 0;
+                const int64_t start = a.seg_start[ks] + (r - a.row_start[ks]) * kRowElems;
                 const int64_t end = a.seg_start[ks + 1];
                 float sj = 0.f;
                 uint32_t c = 0;
                 for (int64_t i = start + lane; i < end; i += 32) StatIO<GT>::accs(a.g, i, sj, c);
-                tot = warp_sum(sj);
-                cnt = __reduce_add_sync(0xffffffffu, c);
-            } else {
-                continue;
+                sj = warp_sum(sj);
+                c = __reduce_add_sync(0xffffffffu, c);
+                if (my_row == j) {
+                    tot = sj;
+                    cnt = c;
+                }
             }
-            if (lane == j) {
-                fa_stats rec;
-                rec.sum_sq = tot;
-                rec.nonfinite = cnt;
-                rec.sum_sq_lo = 0.f;
-                a.out[r] = rec;
-            }
+        }
+        if ((lane & ((32 >> kLog2R) - 1)) == 0 && ((valid >> my_row) & 1u)) {
+            fa_stats rec;
+            rec.sum_sq = tot;
+            rec.nonfinite = cnt;
+            rec.sum_sq_lo = 0.f;
+            a.out[r0 + my_row] = rec;
         }
     }
 }
@@ -334,6 +397,13 @@ merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restric
     }
 }
 
+template <int GT, int CH, bool MULTI>
+cudaError_t launch_fast(const AnalyzeArgs &a, int64_t need, int dev, cudaStream_t stream) {
+    auto k = analyze_fast_kernel<GT, CH, MULTI>;
+    k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int GT>
 cudaError_t launch_analyze_typed(const AnalyzeArgs &a, bool vec, cudaStream_t stream) {
     int dev = 0;
@@ -347,15 +417,19 @@ cudaError_t launch_analyze_typed(const AnalyzeArgs &a, bool vec, cudaStream_t st
     };
     if (vec && (ch == 1 || ch == 2 || ch == 4 || ch == 8)) {
         const int64_t need = ctas_for(8 / ch);
+        if (a.nseg == 1) {
+            switch (ch) {
+                case 1: return launch_fast<GT, 1, false>(a, need, dev, stream);
+                case 2: return launch_fast<GT, 2, false>(a, need, dev, stream);
+                case 4: return launch_fast<GT, 4, false>(a, need, dev, stream);
+                default: return launch_fast<GT, 8, false>(a, need, dev, stream);
+            }
+        }
         switch (ch) {
-            case 1: { auto k = analyze_fast_kernel<GT, 1>;
-                      k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
-            case 2: { auto k = analyze_fast_kernel<GT, 2>;
-                      k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
-            case 4: { auto k = analyze_fast_kernel<GT, 4>;
-                      k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
-            default: { auto k = analyze_fast_kernel<GT, 8>;
-                       k<<<persistent_grid(k, need, dev), kThreads, 0, stream>>>(a); break; }
+            case 1: return launch_fast<GT, 1, true>(a, need, dev, stream);
+            case 2: return launch_fast<GT, 2, true>(a, need, dev, stream);
+            case 4: return launch_fast<GT, 4, true>(a, need, dev, stream);
+            default: return launch_fast<GT, 8, true>(a, need, dev, stream);
         }
     } else if (vec) {
         auto k = analyze_kernel<GT, true>;

@@ -23,10 +23,46 @@
 
 #include "internal.h"
 
+// Tuning knobs (compile-time): vectors per thread per iteration, threads per
+// CTA, and an L2 256-byte prefetch hint on the vector loads.
+#ifndef FA_UPDATE_UNROLL
+#define FA_UPDATE_UNROLL 2
+#endif
+#ifndef FA_UPDATE_THREADS
+#define FA_UPDATE_THREADS 512
+#endif
+#ifndef FA_UPDATE_L2_PREFETCH
+#define FA_UPDATE_L2_PREFETCH 0
+#endif
+
 namespace fa {
 namespace {
 
 constexpr int kVec = 8;  // elements per vector
+constexpr int kUThreads = FA_UPDATE_THREADS;
+
+// 16-byte evict-first loads of the vector body.
+__device__ __forceinline__ float4 ld16(const float4 *q) {
+#if FA_UPDATE_L2_PREFETCH
+    float4 r;
+    asm volatile("ld.global.cs.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(q));
+    return r;
+#else
+    return __ldcs(q);
+#endif
+}
+
+__device__ __forceinline__ uint4 ld16(const uint4 *q) {
+#if FA_UPDATE_L2_PREFETCH
+    uint4 r;
+    asm volatile("ld.global.cs.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(q));
+    return r;
+#else
+    return __ldcs(q);
+#endif
+}
 
 // ---- stored-gradient widening ------------------------------------------------
 
@@ -37,8 +73,8 @@ template <>
 struct GradIO<FA_F32> {
     static __device__ __forceinline__ void load8(const void *g, int64_t i, float (&x)[kVec]) {
         const float4 *q = reinterpret_cast<const float4 *>(static_cast<const float *>(g) + i);
-        float4 a = __ldcs(q);
-        float4 b = __ldcs(q + 1);
+        float4 a = ld16(q);
+        float4 b = ld16(q + 1);
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     }
@@ -51,7 +87,7 @@ struct GradIO<FA_F32> {
 template <>
 struct GradIO<FA_BF16> {
     static __device__ __forceinline__ void load8(const void *g, int64_t i, float (&x)[kVec]) {
-        uint4 r = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + i));
+        uint4 r = ld16(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + i));
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -68,7 +104,7 @@ struct GradIO<FA_BF16> {
 template <>
 struct GradIO<FA_F16> {
     static __device__ __forceinline__ void load8(const void *g, int64_t i, float (&x)[kVec]) {
-        uint4 r = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + i));
+        uint4 r = ld16(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + i));
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -117,8 +153,8 @@ __device__ __forceinline__ void adamw_element(const Coef &c, float x, float &p, 
 
 __device__ __forceinline__ void load8f(const float *base, int64_t i, float (&x)[kVec]) {
     const float4 *q = reinterpret_cast<const float4 *>(base + i);
-    float4 a = __ldcs(q);
-    float4 b = __ldcs(q + 1);
+    float4 a = ld16(q);
+    float4 b = ld16(q + 1);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
@@ -150,18 +186,18 @@ __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &
 // grid-stride iteration, spaced kThreads vectors apart so that a warp's
 // accesses to each stream are contiguous.
 template <int GT, bool AMS, bool FIRST, int UNROLL>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kUThreads)
 update_vec_kernel(const UpdateArgs a, const Coef c) {
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads * UNROLL;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kUThreads + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kUThreads * UNROLL;
 
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * UNROLL + threadIdx.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kUThreads * UNROLL + threadIdx.x;
          base < a.nvec; base += stride) {
         float x[UNROLL][kVec], p[UNROLL][kVec], m[UNROLL][kVec], v[UNROLL][kVec],
             vm[UNROLL][kVec];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t vi = base + static_cast<int64_t>(u) * kThreads;
+            const int64_t vi = base + static_cast<int64_t>(u) * kUThreads;
             if (vi < a.nvec) {
                 const int64_t e = a.head + vi * kVec;
                 GradIO<GT>::load8(a.g, e, x[u]);
@@ -175,7 +211,7 @@ update_vec_kernel(const UpdateArgs a, const Coef c) {
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t vi = base + static_cast<int64_t>(u) * kThreads;
+            const int64_t vi = base + static_cast<int64_t>(u) * kUThreads;
             if (vi < a.nvec) {
                 const int64_t e = a.head + vi * kVec;
 #pragma unroll
@@ -205,7 +241,7 @@ update_scalar_kernel(const UpdateArgs a, const Coef c) {
         scalar_element<GT, AMS, FIRST>(a, c, i);
 }
 
-constexpr int kUnroll = 2;
+constexpr int kUnroll = FA_UPDATE_UNROLL;
 
 template <int GT, bool AMS, bool FIRST>
 cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
@@ -217,12 +253,12 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
 
     if (vector_ok) {
         auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll>;
-        const int64_t per_cta = static_cast<int64_t>(kThreads) * kUnroll;
+        const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
         int64_t need = (a.nvec + per_cta - 1) / per_cta;
         if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
-        const int grid = persistent_grid(kern, need, dev);
+        const int grid = persistent_grid(kern, need, dev, kUThreads);
         if (grid == 0) return cudaSuccess;
-        kern<<<grid, kThreads, 0, stream>>>(a, c);
+        kern<<<grid, kUThreads, 0, stream>>>(a, c);
     } else {
         auto kern = update_scalar_kernel<GT, AMS, FIRST>;
         const int grid = persistent_grid(kern, (a.n + kThreads - 1) / kThreads, dev);

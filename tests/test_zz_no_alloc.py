@@ -14,6 +14,7 @@ run every other test first; it also passes on its own in a fresh process.
 """
 
 import ctypes
+import gc
 
 import numpy as np
 import pytest
@@ -57,6 +58,7 @@ def test_static_scratch_merge_matches_caller_scratch_merge(fa):
         want = fa.stats_buffer(1, DEV)
         fa.fa_merge_gradient_stats(recs, rows, scratch, want)
         got = fa.stats_buffer(1, DEV)
+        gc.collect()  # so that no earlier garbage is freed during the call
         torch.cuda.synchronize()
         allocated = torch.cuda.memory_allocated()
         st = lib.fa_merge_gradient_stats_static(ctypes.c_void_p(recs.data_ptr()), rows,
@@ -64,7 +66,7 @@ def test_static_scratch_merge_matches_caller_scratch_merge(fa):
                                                 ctypes.c_void_p(stream))
         assert st == 0, fa._lib.STATUS_NAMES.get(st, st)
         torch.cuda.synchronize()
-        assert torch.cuda.memory_allocated() == allocated
+        assert torch.cuda.memory_allocated() <= allocated  # nothing allocated
         s_want, c_want = _report(fa, want)
         s_got, c_got = _report(fa, got)
         assert c_got == c_want
