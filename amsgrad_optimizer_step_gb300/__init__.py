@@ -22,7 +22,8 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
 
 __all__ = [
     "fa_abi_version", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
-    "fa_adamw_step_inplace", "fa_bucket_step", "fa_stats_plan", "fa_stats_rows",
+    "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback", "fa_stats_plan",
+    "fa_stats_rows",
     "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",
     "fa_read_report", "fa_clip_decision",
     "fa_clip_decide", "fa_bucket_step_clipped", "options", "control", "stats_buffer",
@@ -205,6 +206,30 @@ def fa_bucket_step(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions, ctl: 
         seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
         ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, ctypes.byref(upd),
         _stream(stream)))
+    return tt.value, bool(upd.value)
+
+
+def fa_bucket_step_writeback(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                             ctl: FaStepControl, p_model: torch.Tensor, grad_mult: float = 1.0,
+                             stream=None) -> tuple[int, bool]:
+    """fa_bucket_step that also writes the BF16/FP16 model copy ``p_model``.
+
+    Returns (t, updated).
+    """
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _dense("p_model", p_model, n, (torch.float16, torch.bfloat16), p.device)
+    seg, nseg = _segments(seg_offsets)
+    tt, upd = ctypes.c_uint64(t), ctypes.c_int32()
+    check("fa_bucket_step_writeback", _L().fa_bucket_step_writeback(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, _ptr(p_model),
+        _TORCH_GRAD[p_model.dtype], ctypes.byref(upd), _stream(stream)))
     return tt.value, bool(upd.value)
 
 

@@ -177,7 +177,8 @@ int64_t vector_head(const void *const *ptrs, const size_t *esize, int count, int
 fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt, const float *m,
                          const float *v, const float *vmax, float *p_out, float *m_out,
                          float *v_out, float *vmax_out, const fa_options *o, uint64_t t_new,
-                         double scale, double grad_mult, void *stream) {
+                         double scale, double grad_mult, void *stream,
+                         void *p_model = nullptr, int model_dtype = fa::kNoModel) {
     Coef c;
     fa_status st = make_coef(o, t_new, scale, grad_mult, &c);
     if (st != FA_OK) return st;
@@ -192,15 +193,17 @@ fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt,
     a.m_out = m_out;
     a.v_out = v_out;
     a.vmax_out = o->amsgrad ? vmax_out : nullptr;
+    a.p_model = model_dtype == fa::kNoModel ? nullptr : p_model;
     a.n = n;
     const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g,
-                          a.p_out, a.m_out, a.v_out, a.vmax_out};
-    const size_t es[] = {4, 4, 4, 4, dtype_bytes(gdt), 4, 4, 4, 4};
-    const int64_t head = vector_head(ptrs, es, 9, n);
+                          a.p_out, a.m_out, a.v_out, a.vmax_out, a.p_model};
+    const size_t es[] = {4, 4, 4, 4, dtype_bytes(gdt), 4, 4, 4, 4, 2};
+    const int64_t head = vector_head(ptrs, es, 10, n);
     const bool vec = head >= 0;
     a.head = vec ? head : 0;
     a.nvec = vec ? (n - a.head) / 8 : 0;
     cudaError_t err = fa::launch_update(a, c, gdt, o->amsgrad != 0, first, vec,
+                                        a.p_model ? model_dtype : fa::kNoModel,
                                         static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -374,6 +377,43 @@ fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_tot
     if (st != FA_OK) return st;
     return fa_adamw_step_inplace(n_total, p, g, gdt, m, v, vmax, t, options, ctl, grad_mult,
                                  updated, stream);
+}
+
+fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                   float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                                   float *vmax, uint64_t *t, const fa_options *options,
+                                   fa_step_control ctl, double grad_mult, void *p_model,
+                                   fa_dtype model_dtype, int32_t *updated, void *stream) {
+    fa_status st;
+    if (!t || !updated) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (model_dtype != FA_F16 && model_dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (n_total < 0) return FA_ERR_SIZE;
+    if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (n_total == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
+        *updated = 0;
+        return FA_OK;
+    }
+    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(p_model, dev, 2)) != FA_OK) return st;
+    const size_t b = static_cast<size_t>(n_total) * 4;
+    const Range model{p_model, static_cast<size_t>(n_total) * 2};
+    const Range others[] = {{p, b}, {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b},
+                            {v, b}, {options->amsgrad ? vmax : nullptr, b}};
+    for (const Range &r : others)
+        if (overlap(model, r)) return FA_ERR_ALIAS;
+    st = enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, *t + 1,
+                        ctl.gradient_scale, grad_mult, stream, p_model, model_dtype);
+    if (st != FA_OK) return st;
+    *t += 1;
+    *updated = 1;
+    return FA_OK;
 }
 
 // ---- statistics ---------------------------------------------------------------

@@ -29,6 +29,7 @@ struct UpdateArgs {
     const float *p_in, *m_in, *v_in, *vmax_in;
     const void *g;
     float *p_out, *m_out, *v_out, *vmax_out;
+    void *p_model;  // low-precision copy of the updated p (nullptr: none)
     int64_t n;     // elements
     int64_t head;  // scalar elements before the 16-byte aligned vector body
     int64_t nvec;  // 8-element vectors in the body
@@ -36,8 +37,10 @@ struct UpdateArgs {
 
 // Enqueues one update kernel over a.n elements.  vector_ok: every pointer is
 // 16-byte aligned at element a.head.  Returns the CUDA launch status.
+// model_dtype: FA_F16 or FA_BF16 when a.p_model is set, else kNoModel.
+constexpr int kNoModel = -1;
 cudaError_t launch_update(const UpdateArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,
-                          bool first, bool vector_ok, cudaStream_t stream);
+                          bool first, bool vector_ok, int model_dtype, cudaStream_t stream);
 
 // Row-statistics launch over up to kMaxSegPerLaunch segments.
 struct AnalyzeArgs {

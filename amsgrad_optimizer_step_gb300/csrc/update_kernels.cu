@@ -165,7 +165,38 @@ __device__ __forceinline__ void store8f(float *base, int64_t i, const float (&x)
     __stcs(q + 1, make_float4(x[4], x[5], x[6], x[7]));
 }
 
-template <int GT, bool AMS, bool FIRST>
+// Low-precision model copy of the updated FP32 parameter: round to nearest,
+// ties to even ("训练与状态保存", section "FP32 主参数与混合参数存储": the FP32 master
+// is updated and the parameter is returned in its storage dtype).
+template <int MD>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if (MD == FA_BF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int MD>
+__device__ __forceinline__ void store8_model(void *base, int64_t i, const float (&x)[kVec]) {
+    uint4 w;
+    w.x = pack2<MD>(x[0], x[1]);
+    w.y = pack2<MD>(x[2], x[3]);
+    w.z = pack2<MD>(x[4], x[5]);
+    w.w = pack2<MD>(x[6], x[7]);
+    __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + i), w);
+}
+
+template <int MD>
+__device__ __forceinline__ void store1_model(void *base, int64_t i, float x) {
+    unsigned short h;
+    if (MD == FA_BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    else h = __half_as_ushort(__float2half_rn(x));
+    __stcs(static_cast<unsigned short *>(base) + i, h);
+}
+
+template <int GT, bool AMS, bool FIRST, int MD>
 __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &c, int64_t i) {
     float x = GradIO<GT>::load1(a.g, i);
     float p = __ldcs(a.p_in + i);
@@ -180,12 +211,13 @@ __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &
     __stcs(a.m_out + i, m);
     __stcs(a.v_out + i, v);
     if (AMS) __stcs(a.vmax_out + i, vm);
+    if (MD != kNoModel) store1_model<MD>(a.p_model, i, p);
 }
 
 // Vector body + scalar head/tail.  Each thread owns UNROLL vectors per
 // grid-stride iteration, spaced kThreads vectors apart so that a warp's
 // accesses to each stream are contiguous.
-template <int GT, bool AMS, bool FIRST, int UNROLL>
+template <int GT, bool AMS, bool FIRST, int UNROLL, int MD>
 __global__ void __launch_bounds__(kUThreads)
 update_vec_kernel(const UpdateArgs a, const Coef c) {
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kUThreads + threadIdx.x;
@@ -221,29 +253,30 @@ update_vec_kernel(const UpdateArgs a, const Coef c) {
                 store8f(a.m_out, e, m[u]);
                 store8f(a.v_out, e, v[u]);
                 if (AMS) store8f(a.vmax_out, e, vm[u]);
+                if (MD != kNoModel) store8_model<MD>(a.p_model, e, p[u]);
             }
         }
     }
 
     // Scalar head [0, head) and tail [head + 8*nvec, n).
-    if (tid < a.head) scalar_element<GT, AMS, FIRST>(a, c, tid);
+    if (tid < a.head) scalar_element<GT, AMS, FIRST, MD>(a, c, tid);
     const int64_t tail0 = a.head + a.nvec * kVec;
-    if (tid < a.n - tail0) scalar_element<GT, AMS, FIRST>(a, c, tail0 + tid);
+    if (tid < a.n - tail0) scalar_element<GT, AMS, FIRST, MD>(a, c, tail0 + tid);
 }
 
 // Every element one at a time (pointers not co-aligned to 16 bytes).
-template <int GT, bool AMS, bool FIRST>
+template <int GT, bool AMS, bool FIRST, int MD>
 __global__ void __launch_bounds__(kThreads)
 update_scalar_kernel(const UpdateArgs a, const Coef c) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < a.n;
          i += stride)
-        scalar_element<GT, AMS, FIRST>(a, c, i);
+        scalar_element<GT, AMS, FIRST, MD>(a, c, i);
 }
 
 constexpr int kUnroll = FA_UPDATE_UNROLL;
 
-template <int GT, bool AMS, bool FIRST>
+template <int GT, bool AMS, bool FIRST, int MD>
 cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
                          cudaStream_t stream) {
     int dev = 0;
@@ -252,7 +285,7 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
     if (sm_count(dev) <= 0) return cudaErrorInvalidDevice;
 
     if (vector_ok) {
-        auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll>;
+        auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD>;
         const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
         int64_t need = (a.nvec + per_cta - 1) / per_cta;
         if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
@@ -260,7 +293,7 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         if (grid == 0) return cudaSuccess;
         kern<<<grid, kUThreads, 0, stream>>>(a, c);
     } else {
-        auto kern = update_scalar_kernel<GT, AMS, FIRST>;
+        auto kern = update_scalar_kernel<GT, AMS, FIRST, MD>;
         const int grid = persistent_grid(kern, (a.n + kThreads - 1) / kThreads, dev);
         if (grid == 0) return cudaSuccess;
         kern<<<grid, kThreads, 0, stream>>>(a, c);
@@ -268,24 +301,38 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
     return cudaGetLastError();
 }
 
-template <int GT>
-cudaError_t launch_gt(const UpdateArgs &a, const Coef &c, bool ams, bool first, bool vec,
+template <int GT, int MD>
+cudaError_t launch_md(const UpdateArgs &a, const Coef &c, bool ams, bool first, bool vec,
                       cudaStream_t s) {
     if (ams)
-        return first ? launch_typed<GT, true, true>(a, c, vec, s)
-                     : launch_typed<GT, true, false>(a, c, vec, s);
-    return first ? launch_typed<GT, false, true>(a, c, vec, s)
-                 : launch_typed<GT, false, false>(a, c, vec, s);
+        return first ? launch_typed<GT, true, true, MD>(a, c, vec, s)
+                     : launch_typed<GT, true, false, MD>(a, c, vec, s);
+    return first ? launch_typed<GT, false, true, MD>(a, c, vec, s)
+                 : launch_typed<GT, false, false, MD>(a, c, vec, s);
+}
+
+template <int GT>
+cudaError_t launch_gt(const UpdateArgs &a, const Coef &c, bool ams, bool first, bool vec,
+                      int model_dtype, cudaStream_t s) {
+    switch (model_dtype) {
+        case kNoModel: return launch_md<GT, kNoModel>(a, c, ams, first, vec, s);
+        case FA_F16: return launch_md<GT, FA_F16>(a, c, ams, first, vec, s);
+        case FA_BF16: return launch_md<GT, FA_BF16>(a, c, ams, first, vec, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_update(const UpdateArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,
-                          bool first, bool vector_ok, cudaStream_t stream) {
+                          bool first, bool vector_ok, int model_dtype, cudaStream_t stream) {
     switch (gdt) {
-        case FA_F32: return launch_gt<FA_F32>(a, c, amsgrad, first, vector_ok, stream);
-        case FA_F16: return launch_gt<FA_F16>(a, c, amsgrad, first, vector_ok, stream);
-        case FA_BF16: return launch_gt<FA_BF16>(a, c, amsgrad, first, vector_ok, stream);
+        case FA_F32:
+            return launch_gt<FA_F32>(a, c, amsgrad, first, vector_ok, model_dtype, stream);
+        case FA_F16:
+            return launch_gt<FA_F16>(a, c, amsgrad, first, vector_ok, model_dtype, stream);
+        case FA_BF16:
+            return launch_gt<FA_BF16>(a, c, amsgrad, first, vector_ok, model_dtype, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--next-rows-steps", type=int, default=10)
     ap.add_argument("--n", type=int, default=0, help="override the parameter count (testing)")
     return ap.parse_args()
 
@@ -310,6 +311,45 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
 
+    # Next-row measurements on the same resident workload (update kernels only,
+    # CUDA events per launch): the plain update and the fused low-precision
+    # write-back (BF16 model copy, +2 B/param).
+    next_rows = None
+    if args.next_rows_steps > 0:
+        p_model = torch.empty(n, dtype=torch.bfloat16, device=dev)
+
+        def timed(fn, k):
+            for _ in range(2):
+                fn()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
+            torch.cuda.synchronize(dev)
+            for i in range(k):
+                ev[i].record(stream)
+                fn()
+            ev[k].record(stream)
+            torch.cuda.synchronize(dev)
+            return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(k))
+
+        def plain():
+            state["t"], _ = fa.fa_bucket_step(None, p, g, m, v, None, state["t"], opts, ctl, 1.0)
+
+        def writeback():
+            state["t"], _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, state["t"], opts,
+                                                        ctl, p_model, 1.0)
+
+        peak, peak_kind = measured_peaks()
+        rows_out = {}
+        for name, fn, bpp_k in (("update_only", plain, fa.bytes_per_param(2, False, False)),
+                                ("f1_writeback_bf16", writeback,
+                                 fa.bytes_per_param(2, False, False) + 2)):
+            ms = timed(fn, args.next_rows_steps)
+            gbs = bpp_k * n / (ms * 1e-3) / 1e9
+            rows_out[name] = {"ms": ms, "bytes_per_param": bpp_k, "achieved_gbs": gbs,
+                              "frac": gbs / peak, "peak_kind": peak_kind,
+                              "params_per_s": n / (ms * 1e-3)}
+        next_rows = rows_out
+        del p_model
+
     # End to end through the public C-ABI call, the gradient coming from pinned
     # host memory every step.  Two device gradient buffers: the copy of step
     # k+1's gradient (side stream) overlaps step k's compute; every copy and
@@ -396,6 +436,7 @@ def run_ours(args):
             "gpu_launches": timed_launches,
             "clocks": clock_info,
             "e2e": e2e,
+            "next_rows": next_rows,
         }
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)

@@ -176,6 +176,23 @@ fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_tot
                          fa_step_control ctl, double grad_mult, int32_t *updated,
                          void *stream);
 
+/*
+ * fa_bucket_step that also writes the low-precision model copy of the updated
+ * parameters in the same HBM pass ([TR-zh] "FP32 主参数与混合参数存储": the FP32
+ * master is updated in FP32 and the parameters are returned in their storage
+ * dtype; [FA-zh] "增加的实际能力": in the plain step that write-back is left to the
+ * caller).  p_model (device, n_total elements of model_dtype = FA_F16 or
+ * FA_BF16, 2-byte aligned, overlapping no other buffer) receives each updated
+ * FP32 p rounded to nearest, ties to even; +2 bytes per parameter instead of
+ * a separate 6-byte cast pass.  Skip / empty: nothing is written, p_model
+ * included.  FA_ERR_DTYPE for any other model_dtype.
+ */
+fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                   float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                                   float *vmax, uint64_t *t, const fa_options *options,
+                                   fa_step_control ctl, double grad_mult, void *p_model,
+                                   fa_dtype model_dtype, int32_t *updated, void *stream);
+
 /* ---- gradient statistics -------------------------------------------------- */
 
 /*

@@ -78,6 +78,8 @@ class OracleLib:
             ctypes.c_int64, P, ctypes.c_int, ctypes.POINTER(_Options), ctypes.c_double,
             ctypes.c_double, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, P, P, P, P]
         lib.oracle_adamw_update.restype = None
+        lib.oracle_model_copy.argtypes = [ctypes.c_int64, P, ctypes.c_int, P]
+        lib.oracle_model_copy.restype = None
         lib.oracle_gradient_stats.argtypes = [ctypes.c_int64, P, ctypes.c_int, ctypes.c_double,
                                               P, P]
         lib.oracle_gradient_stats.restype = None
@@ -116,6 +118,13 @@ class OracleLib:
                                       gradient_scale, clip_coef, t, int(have_state),
                                       int(round_fp32), p.ctypes.data, m.ctypes.data,
                                       v.ctypes.data, vmax.ctypes.data)
+
+    def model_copy(self, p: np.ndarray, dtype: str) -> np.ndarray:
+        """BF16/FP16 bit patterns of FP32 values, rounded to nearest, ties to even."""
+        p = np.ascontiguousarray(p, dtype=np.float32)
+        out = np.zeros(p.size, dtype=np.uint16)
+        self._lib.oracle_model_copy(p.size, p.ctypes.data, _DTYPE_CODE[dtype], out.ctypes.data)
+        return out
 
     # ---- statistics ---------------------------------------------------------
     def gradient_stats(self, g: np.ndarray, dtype: str, gradient_scale: float = 1.0):

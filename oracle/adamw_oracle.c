@@ -137,3 +137,72 @@ void oracle_adamw_update(int64_t n, const void *g, int gdtype,
         v[i] = store(v_new, round_fp32);
     }
 }
+
+/* ---- low-precision model copy ------------------------------------------------
+ *
+ * "训练与状态保存" (zh/docs/training), section "FP32 主参数与混合参数存储": the FP32
+ * master is updated in FP32 and the parameter is handed back in its storage
+ * dtype; "实验性融合 AdamW / AMSGrad", section "增加的实际能力": the low-precision
+ * write-back is the caller's job in the plain step.  The copy is the stored
+ * FP32 master value rounded to nearest, ties to even, in the target format.
+ *
+ * Written from the format definitions: a finite non-zero x with binary
+ * exponent e (2^e <= |x| < 2^(e+1)) has quantum 2^(e - (p - 1)) for p
+ * significant bits in the normal range and the fixed subnormal quantum
+ * below it; x / quantum is exact in FP64, rint() rounds it to the nearest
+ * integer with ties to even, and a result at or above 2^(emax+1) overflows
+ * to infinity.
+ */
+static double round_to_format(double x, int sig_bits, int emin, int emax)
+{
+    if (x == 0.0 || isnan(x) || isinf(x))
+        return x;
+    int e;
+    frexp(x, &e);          /* |x| = f * 2^e, 0.5 <= f < 1 */
+    e -= 1;                /* now 2^e <= |x| < 2^(e+1) */
+    int qexp = (e < emin ? emin : e) - (sig_bits - 1);
+    double q = ldexp(1.0, qexp);
+    double y = rint(x / q) * q;
+    if (fabs(y) >= ldexp(1.0, emax + 1))
+        return x > 0 ? INFINITY : -INFINITY;
+    return y;
+}
+
+/* BF16: 8 significant bits, exponents -126..127 (same range as FP32). */
+uint16_t oracle_to_bf16(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    if (isnan(x))
+        return (uint16_t)((b >> 16) | 0x40);            /* a quiet NaN */
+    double y = round_to_format((double)x, 8, -126, 127);
+    float yf = (float)y;                                 /* exact: y is a BF16 value */
+    memcpy(&b, &yf, 4);
+    return (uint16_t)(b >> 16);
+}
+
+/* IEEE binary16: 11 significant bits, exponents -14..15, subnormal quantum 2^-24. */
+uint16_t oracle_to_f16(float x)
+{
+    if (isnan(x))
+        return 0x7e00;
+    double y = round_to_format((double)x, 11, -14, 15);
+    uint16_t sign = signbit(y) ? 0x8000 : 0;
+    double a = fabs(y);
+    if (isinf(a))
+        return sign | 0x7c00;
+    if (a < ldexp(1.0, -14))                             /* subnormal or zero */
+        return sign | (uint16_t)(a / ldexp(1.0, -24));
+    int e;
+    double f = frexp(a, &e);                             /* a = f * 2^e, 0.5 <= f < 1 */
+    uint16_t expo = (uint16_t)(e - 1 + 15);
+    uint16_t frac = (uint16_t)((f * 2.0 - 1.0) * 1024.0);
+    return sign | (uint16_t)(expo << 10) | frac;
+}
+
+/* Model copies of n FP32 values: dtype ORACLE_BF16 or ORACLE_F16. */
+void oracle_model_copy(int64_t n, const float *p, int dtype, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = dtype == ORACLE_BF16 ? oracle_to_bf16(p[i]) : oracle_to_f16(p[i]);
+}

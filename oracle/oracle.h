@@ -19,6 +19,10 @@ void oracle_adamw_update(int64_t n, const void *g, int gdtype,
                          double clip_coef, uint64_t t, int have_state, int round_fp32,
                          double *p, double *m, double *v, double *vmax);
 
+uint16_t oracle_to_bf16(float x);
+uint16_t oracle_to_f16(float x);
+void oracle_model_copy(int64_t n, const float *p, int dtype, uint16_t *out);
+
 void oracle_gradient_stats(int64_t n, const void *g, int gdtype, double gradient_scale,
                            double *sum_sq, uint64_t *nonfinite);
 int64_t oracle_row_stats(int64_t n, const void *g, int gdtype, int64_t row_len,

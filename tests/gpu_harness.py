@@ -142,9 +142,38 @@ class DeviceState:
         return take(self.p), take(self.m), take(self.v), take(self.vmax)
 
 
+def ulp16(x, dtype):
+    """Spacing of the 16-bit format at |x| (subnormal spacing below the normal range)."""
+    sig, emin = (8, -126) if dtype == BF16 else (11, -14)
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.where(a > 0, np.floor(np.log2(np.where(a > 0, a, 1.0))), emin)
+    e = np.maximum(e, emin)
+    return np.ldexp(1.0, (e - (sig - 1)).astype(np.int64))
+
+
+def check_model_copy(model_bits, p_dev_f32, p_oracle_f32, dtype, lib, what):
+    """The device's low-precision copy is the round-to-nearest-even encoding of the
+    device's own FP32 parameters (bit-exact: the same decision in the same
+    precision), and a correct rounding of the oracle's own parameters up to the
+    trajectory tolerance: |copy - p| <= ulp/2 + 1e-5 * max(1, |p|)."""
+    want = lib.model_copy(p_dev_f32, dtype)
+    if not np.array_equal(model_bits, want):
+        i = int(np.argmax(model_bits != want))
+        raise AssertionError(f"{what}: model copy differs from the encoding of the device "
+                             f"parameter at {i}: {model_bits[i]:#06x} vs {want[i]:#06x}")
+    widened = widen_host(model_bits, dtype)
+    ref = p_oracle_f32.astype(np.float64)
+    lim = 0.5 * ulp16(ref, dtype) + 1e-5 * np.maximum(1.0, np.abs(ref))
+    err = np.abs(widened - ref)
+    if not np.all(err <= lim):
+        i = int(np.argmax(err - lim))
+        raise AssertionError(f"{what}: copy {widened[i]!r} is not a rounding of the oracle's "
+                             f"{ref[i]!r} (err {err[i]:.3e} > {lim[i]:.3e})")
+
+
 def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None = None,
                  guard: int = 0, segments=None, row_len: int = 0, lib=None,
-                 full_grad_on_host: bool = True, step_check=True):
+                 full_grad_on_host: bool = True, step_check=True, model_dtype=None):
     """Runs every call of ``w`` (at size n) and checks each one.  Returns a summary."""
     lib = lib or oracle.lib()
     ws = w if n == w.n else w.scaled(n)
@@ -161,6 +190,12 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
     p_host0 = ws.params_host(idx)
     assert np.array_equal(st.p[idx_t].cpu().numpy(), p_host0), "device/host inputs differ"
 
+    p_model = None
+    if model_dtype is not None:
+        full = torch.empty(n + 2 * guard, dtype=TORCH_DT[model_dtype], device=device)
+        full.view(torch.int16).fill_(0x7F7F)
+        p_model = full[guard:guard + n]
+        st._full["model"] = full
     if api == "clipped":
         rows = fa.fa_stats_rows(n, row_len, segs)
         rows_buf = fa.stats_buffer(rows, device)
@@ -174,6 +209,7 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         skip = call in ws.skip_calls
         ctl = fa.control(ws.gradient_scale, skip)
         before = st.snapshot(idx_t)
+        model_before = None if p_model is None else grad_bits_from_device(p_model[idx_t])
         t_before = st.t
         coef_dev = 1.0
         expect_skip = skip
@@ -204,6 +240,9 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         elif api == "inplace":
             t_new, updated = fa.fa_adamw_step_inplace(st.p, st.g, st.m, st.v, st.vmax, st.t,
                                                       fopts, ctl)
+        elif api == "bucket" and p_model is not None:
+            t_new, updated = fa.fa_bucket_step_writeback(segs, st.p, st.g, st.m, st.v, st.vmax,
+                                                         st.t, fopts, ctl, p_model)
         elif api == "bucket":
             t_new, updated = fa.fa_bucket_step(segs, st.p, st.g, st.m, st.v, st.vmax, st.t,
                                                fopts, ctl)
@@ -220,6 +259,9 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
             for a, b in zip(before, after):
                 if a is not None:
                     assert np.array_equal(a, b), "skipped call changed state"
+            if p_model is not None:
+                assert np.array_equal(grad_bits_from_device(p_model[idx_t]), model_before), \
+                    "skipped call wrote the model copy"
             summary["skips"] += 1
             traj.step(gh, ORACLE_DT[ws.grad_dtype], ws.gradient_scale, skip_update=True)
             continue
@@ -247,6 +289,10 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         gate(after[2], traj.state.v, 1e-5, f"call {call} trajectory v")
         if ws.amsgrad:
             gate(after[3], traj.state.vmax, 1e-5, f"call {call} trajectory vmax")
+        if p_model is not None:
+            check_model_copy(grad_bits_from_device(p_model[idx_t]),
+                             after[0].astype(np.float32), traj.p.astype(np.float32),
+                             model_dtype, lib, f"call {call} model copy")
     summary["t"] = st.t
     summary["state"] = st
     return summary

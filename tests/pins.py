@@ -331,6 +331,40 @@ def pin_widening(L):
 
 
 # ---------------------------------------------------------------------------
+# Low-precision model copy (round to nearest, ties to even)
+# ---------------------------------------------------------------------------
+
+def _tie_structured_f32():
+    """Every sign/exponent/high-mantissa pattern with low bits at and around the
+    BF16 and FP16 rounding points (exact ties, one below, one above)."""
+    hi = np.arange(1 << 16, dtype=np.uint32) << np.uint32(16)
+    lows = np.array([0x0000, 0x0001, 0x0FFF, 0x1000, 0x1001, 0x7FFF, 0x8000, 0x8001, 0xEFFF,
+                     0xF000, 0xFFFF], dtype=np.uint32)
+    bits = (hi[:, None] | lows[None, :]).ravel()
+    return bits.view(np.float32)
+
+
+def pin_model_copy_rounding(L):
+    import torch
+    x = _tie_structured_f32()
+    ok = ~np.isnan(x)
+    got = L.model_copy(x, "bf16")
+    want = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got[ok], want[ok]), "bf16 rounding differs from torch"
+    assert np.all((got[~ok] & 0x7F80) == 0x7F80) and np.all((got[~ok] & 0x7F) != 0)
+    rng = _rng(27)
+    y = np.concatenate([x[ok], (rng.standard_normal(200_000) * 10.0 ** rng.integers(-9, 6, 200_000)),
+                        np.array([65504, 65519.996, 65520, 65536, 6.1e-5, 6.0e-5, 2.98e-8,
+                                  2.9802322e-8, 5.96e-8, 1e-30, -0.0, 0.0, np.inf, -np.inf])
+                        ]).astype(np.float32)
+    with np.errstate(over="ignore"):
+        want16 = y.astype(np.float16).view(np.uint16)
+    got16 = L.model_copy(y, "f16")
+    assert np.array_equal(got16, want16), "f16 rounding differs from numpy"
+    assert L.model_copy(np.array([np.nan], np.float32), "f16")[0] & 0x7C00 == 0x7C00
+
+
+# ---------------------------------------------------------------------------
 # Statistics and the decision
 # ---------------------------------------------------------------------------
 

@@ -223,3 +223,21 @@ def test_byte_model_matches_pages():
     assert fa.bytes_per_param(4, False, True) == 20
     assert fa.bytes_per_param(2, False, True) == 18
     assert fa.bytes_per_param(2, True, True) == 22
+
+
+def test_writeback_validation_without_gpu(lib):
+    o = fa.options()
+    t = ctypes.c_uint64(4)
+    upd = ctypes.c_int32(9)
+    # model dtype must be FP16 or BF16: rejected before any pointer is looked at
+    st = lib.fa_bucket_step_writeback(None, 0, 16, None, None, 0, None, None, None,
+                                      ctypes.byref(t), ctypes.byref(o), fa.control(), 1.0,
+                                      None, 0, ctypes.byref(upd), None)
+    assert (st, t.value, upd.value) == (2, 4, 9)
+    # skip: nothing launched or written
+    st = lib.fa_bucket_step_writeback(None, 0, 16, None, None, 0, None, None, None,
+                                      ctypes.byref(t), ctypes.byref(o),
+                                      fa.control(skip_update=True), 1.0, None, 2,
+                                      ctypes.byref(upd), None)
+    assert (st, t.value, upd.value) == (0, 4, 0)
+    assert fa.bytes_per_param(2, False, False) + 2 == 28  # write-back adds one 16-bit store

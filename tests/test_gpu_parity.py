@@ -443,3 +443,75 @@ def test_host_pointers_rejected_by_the_library():
                                                ctypes.byref(o), fa.control(), 1.0,
                                                ctypes.byref(up), None)
         assert st == 6 and tt.value == 2 and up.value == 5
+
+
+# ---- fused low-precision write-back ------------------------------------------------
+
+@pytest.mark.parametrize("model_dtype", ["bf16", "f16"])
+def test_writeback_scaled_flat(model_dtype):
+    w = dataclasses.replace(CONFIG3, calls=6)
+    s = run_workload(w, 1_000_003, "bucket", DEV, guard=1024, model_dtype=model_dtype)
+    assert s["t"] == 6
+
+
+def test_writeback_scaled_decoder_bucket_with_skip():
+    off = small_decoder_offsets()
+    w = dataclasses.replace(CONFIG4_MAX, skip_calls=(3,), calls=5)
+    s = run_workload(w, int(off[-1]), "bucket", DEV, segments=off, guard=1024,
+                     model_dtype="f16")
+    assert s["t"] == 4 and s["skips"] == 1
+
+
+def test_writeback_full_size_sampled():
+    idx = sample_indices(CONFIG4.n, seed=6)
+    w = dataclasses.replace(CONFIG4, calls=3)
+    s = run_workload(w, w.n, "bucket", DEV, idx=idx, model_dtype="bf16")
+    assert s["t"] == 3
+
+
+@pytest.mark.parametrize("n", [1, 7, 9, 4097])
+@pytest.mark.parametrize("model_dtype", ["bf16", "f16"])
+def test_writeback_edge_sizes(n, model_dtype):
+    w = dataclasses.replace(CONFIG1, grad_dtype="bf16", calls=3, inplace=True)
+    run_workload(w, n, "bucket", DEV, guard=64, model_dtype=model_dtype)
+
+
+def test_writeback_misaligned_model_view(oracle_lib):
+    """A model copy starting 2 bytes off a 16-byte boundary takes the scalar kernel."""
+    n = 20_001
+    w = dataclasses.replace(CONFIG3, calls=2).scaled(n)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p)
+    m, v = torch.zeros(n, device=DEV), torch.zeros(n, device=DEV)
+    g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    full = torch.zeros(n + 8, dtype=torch.bfloat16, device=DEV)
+    model = full[1:1 + n]
+    t = 0
+    for call in (1, 2):
+        w.fill_grad_device(call, g)
+        t, _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, t, fa.options(**w.options()),
+                                           fa.control(), model)
+    torch.cuda.synchronize()
+    bits = model.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(bits, oracle_lib.model_copy(p.cpu().numpy(), "bf16"))
+
+
+def test_writeback_rejections():
+    n = 1024
+    p, m, v, _ = _state(n)
+    g = torch.randn(n, device=DEV)
+    model = torch.zeros(n, dtype=torch.bfloat16, device=DEV)
+    o = fa.options()
+    import ctypes
+    from amsgrad_optimizer_step_gb300 import _lib
+    tt, up = ctypes.c_uint64(1), ctypes.c_int32()
+    st = _lib.load().fa_bucket_step_writeback(None, 0, n, p.data_ptr(), g.data_ptr(), 0,
+                                              m.data_ptr(), v.data_ptr(), None, ctypes.byref(tt),
+                                              ctypes.byref(o), fa.control(), 1.0,
+                                              model.data_ptr(), 0, ctypes.byref(up), None)
+    assert st == 2  # FP32 is not a model-copy dtype
+    with pytest.raises(fa.FusedAdamWError) as e:
+        fa.fa_bucket_step_writeback(None, p, g, m, v, None, 1, o, fa.control(),
+                                    p.view(torch.bfloat16)[:n])
+    assert e.value.status == 5
+    assert not model.view(torch.int16).any()

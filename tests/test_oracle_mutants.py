@@ -44,6 +44,16 @@ MUTANTS = {
     "f16_exponent_bias": ("adamw_oracle.c", "expo - 25", "expo - 24"),
     "f16_subnormal_scale": ("adamw_oracle.c", "ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
     "bf16_shift": ("adamw_oracle.c", "(uint32_t)bits << 16", "(uint32_t)bits << 15"),
+    "model_copy_truncates": ("adamw_oracle.c", "double y = rint(x / q) * q;",
+                             "double y = trunc(x / q) * q;"),
+    "model_copy_ties_away": ("adamw_oracle.c", "double y = rint(x / q) * q;",
+                             "double y = round(x / q) * q;"),
+    "bf16_seven_bits": ("adamw_oracle.c", "round_to_format((double)x, 8, -126, 127)",
+                        "round_to_format((double)x, 7, -126, 127)"),
+    "f16_no_subnormal_floor": ("adamw_oracle.c", "int qexp = (e < emin ? emin : e) - (sig_bits - 1);",
+                               "int qexp = e - (sig_bits - 1);"),
+    "f16_no_overflow": ("adamw_oracle.c", "round_to_format((double)x, 11, -14, 15)",
+                        "round_to_format((double)x, 11, -14, 16)"),
     "stats_sum_not_squared": ("stats_oracle.c", "s += u * u;", "s += u;"),
     "stats_scale_ignored": ("stats_oracle.c", "double u = x / gradient_scale;", "double u = x;"),
     "stats_count_dropped": ("stats_oracle.c", "++c;\n            continue;\n        }\n        double u",
