@@ -347,8 +347,28 @@ def run_ours(args):
             rows_out[name] = {"ms": ms, "bytes_per_param": bpp_k, "achieved_gbs": gbs,
                               "frac": gbs / peak, "peak_kind": peak_kind,
                               "params_per_s": n / (ms * 1e-3)}
-        next_rows = rows_out
         del p_model
+
+        # f4: the torch.optim-style wrapper on the decoder-shaped 1.196e9-parameter
+        # model (199 FP32 tensors packed into one bucket), global clip 1.0: each
+        # step analyses, merges, reads back 12 bytes, decides and updates.
+        from amsgrad_optimizer_step_gb300.optim import FusedAdamW
+        from synthetic.configs import decoder_bucket_shapes
+        dparams = [torch.nn.Parameter(torch.zeros(shape, device=dev))
+                   for _, shape in decoder_bucket_shapes()]
+        dn = sum(x.numel() for x in dparams)
+        dopt = FusedAdamW(dparams, lr=1e-3, max_grad_norm=1.0)
+        dopt._buckets[0].grad.normal_(0.0, 1e-3)
+        ms = timed(dopt.step, args.next_rows_steps)
+        b4 = fa.bytes_per_param(4, False, False) + 4  # update + analysis read of the FP32 gradient
+        rows_out["f4_fused_adamw_decoder1.1B_clip"] = {
+            "ms": ms, "params": dn, "tensors": len(dparams), "row_len": dopt.row_len,
+            "bytes_per_param": b4, "achieved_gbs": b4 * dn / (ms * 1e-3) / 1e9,
+            "frac": b4 * dn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+            "params_per_s": dn / (ms * 1e-3), "skipped": dopt.last_report["skipped"]}
+        del dopt, dparams
+        torch.cuda.empty_cache()
+        next_rows = rows_out
 
     # End to end through the public C-ABI call, the gradient coming from pinned
     # host memory every step.  Two device gradient buffers: the copy of step

@@ -1,0 +1,231 @@
+"""The torch.optim-style FusedAdamW and its GradScaler, against the oracle."""
+
+import io
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from amsgrad_optimizer_step_gb300.optim import FusedAdamW, GradScaler
+from gpu_harness import gate
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+SHAPES = [(33, 17), (129,), (8, 1000), (5,), (64, 64)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from amsgrad_optimizer_step_gb300 import build
+    build.build()
+
+
+def _params(seed, dtype=torch.float32, shapes=SHAPES):
+    g = torch.Generator().manual_seed(seed)
+    return [torch.nn.Parameter((torch.randn(s, generator=g) * 0.02).to(dtype).to(DEV))
+            for s in shapes]
+
+
+def _grads(seed, step, shapes=SHAPES, scale=1.0):
+    g = torch.Generator().manual_seed(1000 * seed + step)
+    return [(torch.randn(s, generator=g) * 1e-2 * scale).to(torch.float32) for s in shapes]
+
+
+def _set_grads(params, grads):
+    for p, gr in zip(params, grads):
+        p.grad.copy_(gr.to(p.dtype).to(DEV))
+
+
+def _host(t):
+    return t.detach().float().cpu().numpy().reshape(-1)
+
+
+@pytest.mark.parametrize("amsgrad,maximize", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("clip", [None, 0.05])
+def test_matches_oracle_per_parameter(amsgrad, maximize, clip):
+    params = _params(1)
+    hp = dict(lr=2e-3, betas=(0.9, 0.99), eps=1e-6, weight_decay=0.01, amsgrad=amsgrad,
+              maximize=maximize)
+    opt = FusedAdamW(params, max_grad_norm=clip, **hp)
+    lib = oracle.lib()
+    oo = dict(lr=2e-3, beta1=0.9, beta2=0.99, eps=1e-6, weight_decay=0.01, amsgrad=amsgrad,
+              maximize=maximize)
+    refs = [oracle.OracleAdamW(_host(p), oo, lib_=lib) for p in params]
+    for step in range(1, 7):
+        grads = _grads(1, step)
+        _set_grads(params, grads)
+        opt.step()
+        coef = 1.0
+        if clip is not None:
+            allg = np.concatenate([g.numpy().reshape(-1) for g in grads])
+            s, c = lib.gradient_stats(allg, "f32")
+            _, norm, coef = lib.clip_decision(s, c, clip)
+            assert abs(opt.last_report["grad_norm"] - norm) <= 1e-5 * norm
+            assert coef < 1.0
+        for r, g in zip(refs, grads):
+            r.step(g.numpy().reshape(-1), "f32", clip_coef=coef)
+        torch.cuda.synchronize()
+        for p, r in zip(params, refs):
+            gate(_host(p), r.p, 1e-5, f"p step {step}")
+            st = opt.state[p]
+            gate(_host(st["exp_avg"]), r.state.m, 1e-5, "m")
+            gate(_host(st["exp_avg_sq"]), r.state.v, 1e-5, "v")
+            if amsgrad:
+                gate(_host(st["max_exp_avg_sq"]), r.state.vmax, 1e-5, "vmax")
+    assert float(opt.state_dict()["state"][0]["step"]) == 6
+
+
+def test_real_autograd_accumulates_into_the_bucket():
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(torch.nn.Linear(40, 64), torch.nn.Tanh(),
+                                torch.nn.Linear(64, 3)).to(DEV)
+    opt = FusedAdamW(model.parameters(), lr=1e-2, max_grad_norm=1.0)
+    bucket = opt._buckets[0]
+    lo, hi = bucket.grad.data_ptr(), bucket.grad.data_ptr() + bucket.grad.numel() * 4
+    x = torch.randn(16, 40, device=DEV)
+    y = torch.randn(16, 3, device=DEV)
+    losses = []
+    for _ in range(30):
+        opt.zero_grad()
+        loss = torch.nn.functional.mse_loss(model(x), y)
+        loss.backward()
+        for p in model.parameters():
+            assert lo <= p.grad.data_ptr() < hi, "gradient left the bucket"
+        opt.step()
+        losses.append(float(loss.detach()))
+    assert losses[-1] < 0.5 * losses[0]
+    assert opt.last_report["skipped"] is False and opt.last_report["grad_norm"] is not None
+
+
+def test_param_groups_share_one_global_clip():
+    a = _params(2, shapes=[(100,), (7, 9)])
+    b = _params(3, shapes=[(300,)])
+    opt = FusedAdamW([{"params": a, "lr": 1e-3}, {"params": b, "lr": 5e-3, "weight_decay": 0.1}],
+                     max_grad_norm=0.01)
+    lib = oracle.lib()
+    ga = _grads(2, 1, shapes=[(100,), (7, 9)])
+    gb = _grads(3, 1, shapes=[(300,)])
+    ra = [oracle.OracleAdamW(_host(p), dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-5,
+                                            weight_decay=1e-4, amsgrad=False, maximize=False),
+                             lib_=lib) for p in a]
+    rb = [oracle.OracleAdamW(_host(p), dict(lr=5e-3, beta1=0.9, beta2=0.999, eps=1e-5,
+                                            weight_decay=0.1, amsgrad=False, maximize=False),
+                             lib_=lib) for p in b]
+    _set_grads(a, ga)
+    _set_grads(b, gb)
+    opt.step()
+    allg = np.concatenate([g.numpy().reshape(-1) for g in ga + gb])
+    s, c = lib.gradient_stats(allg, "f32")
+    _, norm, coef = lib.clip_decision(s, c, 0.01)
+    for r, g, p in zip(ra + rb, ga + gb, a + b):
+        r.step(g.numpy().reshape(-1), "f32", clip_coef=coef)
+        gate(_host(p), r.p, 1e-6, "grouped p")
+
+
+def test_grad_scaler_skips_non_finite_and_backs_off():
+    params = _params(4)
+    opt = FusedAdamW(params, lr=1e-3)
+    scaler = GradScaler(init_scale=1024.0, growth_interval=2)
+    lib = oracle.lib()
+    oo = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=1e-4, amsgrad=False,
+              maximize=False)
+    refs = [oracle.OracleAdamW(_host(p), oo, lib_=lib) for p in params]
+    scales = []
+    for step in range(1, 7):
+        s = scaler.get_scale()
+        grads = _grads(4, step, scale=s)
+        if step == 3:
+            grads[2][1, 5] = float("inf")
+        before = [p.detach().clone() for p in params]
+        _set_grads(params, grads)
+        scaler.step(opt)
+        skipped = opt.last_report["skipped"]
+        assert skipped == (step == 3)
+        for r, g in zip(refs, grads):
+            r.step(g.numpy().reshape(-1), "f32", gradient_scale=s, skip_update=skipped)
+        torch.cuda.synchronize()
+        if skipped:
+            assert all(torch.equal(p, q) for p, q in zip(params, before))
+            assert opt.last_report["nonfinite"] == 1
+        for p, r in zip(params, refs):
+            gate(_host(p), r.p, 1e-5, f"scaled p step {step}")
+        scaler.update()
+        scales.append(scaler.get_scale())
+    assert scales[:3] == [1024.0, 2048.0, 1024.0]
+
+
+def _train(opt, params, steps, first=1):
+    for step in range(first, first + steps):
+        _set_grads(params, _grads(5, step))
+        opt.step()
+    torch.cuda.synchronize()
+
+
+def test_state_dict_round_trip_bitwise():
+    ref_params = _params(5)
+    ref = FusedAdamW(ref_params, amsgrad=True, max_grad_norm=0.5, hierarchical_stats=True)
+    _train(ref, ref_params, 10)
+
+    params = _params(5)
+    opt = FusedAdamW(params, amsgrad=True, max_grad_norm=0.5, hierarchical_stats=True)
+    _train(opt, params, 5)
+    buf = io.BytesIO()
+    torch.save({"model": [p.detach().cpu() for p in params], "opt": opt.state_dict()}, buf)
+    sd = opt.state_dict()
+    assert sd["fused_options"]["step_options_version"] == 2
+    buf.seek(0)
+    saved = torch.load(buf, weights_only=False)
+    fresh = _params(99)  # different initial values, overwritten by the checkpoint
+    with torch.no_grad():
+        for p, q in zip(fresh, saved["model"]):
+            p.copy_(q)
+    opt2 = FusedAdamW(fresh, amsgrad=True)
+    opt2.load_state_dict(saved["opt"])
+    assert opt2.max_grad_norm == 0.5 and opt2.hierarchical_stats
+    _train(opt2, fresh, 5, first=6)
+    for p, q in zip(fresh, ref_params):
+        assert torch.equal(p, q)
+    for p, q in zip(fresh, ref_params):
+        assert torch.equal(opt2.state[p]["exp_avg_sq"], ref.state[q]["exp_avg_sq"])
+
+
+def test_old_state_dict_turns_fused_modes_off():
+    params = _params(6)
+    opt = FusedAdamW(params, max_grad_norm=1.0, hierarchical_stats=True)
+    _train(opt, params, 2)
+    sd = opt.state_dict()
+    del sd["fused_options"]
+    opt2 = FusedAdamW(_params(6), max_grad_norm=1.0, hierarchical_stats=True)
+    opt2.load_state_dict(sd)
+    assert opt2.max_grad_norm is None and opt2.hierarchical_stats is False
+    sd1 = opt.state_dict()
+    sd1["fused_options"]["step_options_version"] = 1
+    opt3 = FusedAdamW(_params(6))
+    opt3.load_state_dict(sd1)
+    assert opt3.hierarchical_stats is False and opt3.max_grad_norm == 1.0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_low_precision_params_keep_fp32_masters(dtype):
+    params = _params(7, dtype=dtype)
+    masters0 = [_host(p) for p in params]
+    opt = FusedAdamW(params, lr=1e-3)
+    lib = oracle.lib()
+    oo = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=1e-4, amsgrad=False,
+              maximize=False)
+    refs = [oracle.OracleAdamW(m, oo, lib_=lib) for m in masters0]
+    name = "bf16" if dtype == torch.bfloat16 else "f16"
+    for step in range(1, 5):
+        grads = [g.to(dtype) for g in _grads(7, step)]
+        _set_grads(params, grads)
+        opt.step()
+        for r, g in zip(refs, grads):
+            bits = g.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+            r.step(bits, name)
+    torch.cuda.synchronize()
+    for p, r in zip(params, refs):
+        master = opt.state[p]["master_param"]
+        gate(_host(master), r.p, 1e-5, "master")
+        bits = p.detach().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
+        assert np.array_equal(bits, lib.model_copy(_host(master), name))
