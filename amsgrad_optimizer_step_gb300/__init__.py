@@ -22,7 +22,8 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
 
 __all__ = [
     "fa_abi_version", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
-    "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback", "fa_stats_plan",
+    "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback",
+    "fa_adamw_step_staged", "fa_stats_plan",
     "fa_stats_rows",
     "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",
     "fa_read_report", "fa_clip_decision",
@@ -230,6 +231,26 @@ def fa_bucket_step_writeback(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOpti
         seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
         ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, _ptr(p_model),
         _TORCH_GRAD[p_model.dtype], ctypes.byref(upd), _stream(stream)))
+    return tt.value, bool(upd.value)
+
+
+def fa_adamw_step_staged(p, g, m, v, vmax, t: int, opts: FaOptions, ctl: FaStepControl,
+                         delta: torch.Tensor, grad_mult: float = 1.0,
+                         stream=None) -> tuple[int, bool]:
+    """The 4/5-kernel staged comparison (benchmarks only).  Returns (t, updated)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    _dense("delta", delta, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    tt, upd = ctypes.c_uint64(t), ctypes.c_int32()
+    check("fa_adamw_step_staged", _L().fa_adamw_step_staged(
+        n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, _ptr(delta), ctypes.byref(upd),
+        _stream(stream)))
     return tt.value, bool(upd.value)
 
 

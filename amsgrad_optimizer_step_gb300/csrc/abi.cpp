@@ -416,6 +416,47 @@ fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int
     return FA_OK;
 }
 
+fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt, float *m,
+                               float *v, float *vmax, uint64_t *t, const fa_options *options,
+                               fa_step_control ctl, double grad_mult, float *delta,
+                               int32_t *updated, void *stream) {
+    fa_status st;
+    if (!t || !updated) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n < 0) return FA_ERR_SIZE;
+    if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
+    if (n == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
+        *updated = 0;
+        return FA_OK;
+    }
+    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(delta, dev, 4)) != FA_OK) return st;
+    const size_t b = static_cast<size_t>(n) * 4;
+    const Range others[] = {{p, b}, {g, static_cast<size_t>(n) * dtype_bytes(gdt)}, {m, b},
+                            {v, b}, {options->amsgrad ? vmax : nullptr, b}};
+    for (const Range &r : others)
+        if (overlap({delta, b}, r)) return FA_ERR_ALIAS;
+    // the stages move 16-byte vectors from the first element: every stream aligned
+    const void *ptrs[] = {p, m, v, options->amsgrad ? vmax : nullptr, delta};
+    for (const void *q : ptrs)
+        if (q && reinterpret_cast<uintptr_t>(q) % 16) return FA_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(g) % (gdt == FA_F32 ? 16 : 8)) return FA_ERR_ALIGN;
+    Coef c;
+    if ((st = make_coef(options, *t + 1, ctl.gradient_scale, grad_mult, &c)) != FA_OK) return st;
+    fa::StagedArgs a{p, m, v, options->amsgrad ? vmax : nullptr, delta, g, n};
+    if (fa::launch_staged(a, c, gdt, options->amsgrad != 0, *t == 0,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    *t += 1;
+    *updated = 1;
+    return FA_OK;
+}
+
 // ---- statistics ---------------------------------------------------------------
 
 fa_status fa_stats_plan(int64_t rows, int32_t *merge_kernels, int64_t *scratch_elements) {

@@ -42,6 +42,15 @@ constexpr int kNoModel = -1;
 cudaError_t launch_update(const UpdateArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,
                           bool first, bool vector_ok, int model_dtype, cudaStream_t stream);
 
+// The staged comparison: 4 kernels (5 with AMSGrad) through an FP32 delta buffer.
+struct StagedArgs {
+    float *p, *m, *v, *vmax, *delta;
+    const void *g;
+    int64_t n;
+};
+cudaError_t launch_staged(const StagedArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,
+                          bool first, cudaStream_t stream);
+
 // Row-statistics launch over up to kMaxSegPerLaunch segments.
 struct AnalyzeArgs {
     const void *g;

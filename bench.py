@@ -311,65 +311,6 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
 
-    # Next-row measurements on the same resident workload (update kernels only,
-    # CUDA events per launch): the plain update and the fused low-precision
-    # write-back (BF16 model copy, +2 B/param).
-    next_rows = None
-    if args.next_rows_steps > 0:
-        p_model = torch.empty(n, dtype=torch.bfloat16, device=dev)
-
-        def timed(fn, k):
-            for _ in range(2):
-                fn()
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
-            torch.cuda.synchronize(dev)
-            for i in range(k):
-                ev[i].record(stream)
-                fn()
-            ev[k].record(stream)
-            torch.cuda.synchronize(dev)
-            return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(k))
-
-        def plain():
-            state["t"], _ = fa.fa_bucket_step(None, p, g, m, v, None, state["t"], opts, ctl, 1.0)
-
-        def writeback():
-            state["t"], _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, state["t"], opts,
-                                                        ctl, p_model, 1.0)
-
-        peak, peak_kind = measured_peaks()
-        rows_out = {}
-        for name, fn, bpp_k in (("update_only", plain, fa.bytes_per_param(2, False, False)),
-                                ("f1_writeback_bf16", writeback,
-                                 fa.bytes_per_param(2, False, False) + 2)):
-            ms = timed(fn, args.next_rows_steps)
-            gbs = bpp_k * n / (ms * 1e-3) / 1e9
-            rows_out[name] = {"ms": ms, "bytes_per_param": bpp_k, "achieved_gbs": gbs,
-                              "frac": gbs / peak, "peak_kind": peak_kind,
-                              "params_per_s": n / (ms * 1e-3)}
-        del p_model
-
-        # f4: the torch.optim-style wrapper on the decoder-shaped 1.196e9-parameter
-        # model (199 FP32 tensors packed into one bucket), global clip 1.0: each
-        # step analyses, merges, reads back 12 bytes, decides and updates.
-        from amsgrad_optimizer_step_gb300.optim import FusedAdamW
-        from synthetic.configs import decoder_bucket_shapes
-        dparams = [torch.nn.Parameter(torch.zeros(shape, device=dev))
-                   for _, shape in decoder_bucket_shapes()]
-        dn = sum(x.numel() for x in dparams)
-        dopt = FusedAdamW(dparams, lr=1e-3, max_grad_norm=1.0)
-        dopt._buckets[0].grad.normal_(0.0, 1e-3)
-        ms = timed(dopt.step, args.next_rows_steps)
-        b4 = fa.bytes_per_param(4, False, False) + 4  # update + analysis read of the FP32 gradient
-        rows_out["f4_fused_adamw_decoder1.1B_clip"] = {
-            "ms": ms, "params": dn, "tensors": len(dparams), "row_len": dopt.row_len,
-            "bytes_per_param": b4, "achieved_gbs": b4 * dn / (ms * 1e-3) / 1e9,
-            "frac": b4 * dn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
-            "params_per_s": dn / (ms * 1e-3), "skipped": dopt.last_report["skipped"]}
-        del dopt, dparams
-        torch.cuda.empty_cache()
-        next_rows = rows_out
-
     # End to end through the public C-ABI call, the gradient coming from pinned
     # host memory every step.  Two device gradient buffers: the copy of step
     # k+1's gradient (side stream) overlaps step k's compute; every copy and
@@ -430,6 +371,94 @@ def run_ours(args):
                "what": "pinned-host BF16 gradient copied in every step (side stream, double "
                        "buffered), then the C-ABI statistics-guarded step (analyse, merge, "
                        "12-byte report read back, decide, update); wall clock"}
+
+    # Next-row measurements on the same resident workload (update kernels only,
+    # CUDA events per launch): the plain update and the fused low-precision
+    # write-back (BF16 model copy, +2 B/param).
+    next_rows = None
+    if args.next_rows_steps > 0:
+        p_model = torch.empty(n, dtype=torch.bfloat16, device=dev)
+
+        def timed(fn, k):
+            for _ in range(2):
+                fn()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
+            torch.cuda.synchronize(dev)
+            for i in range(k):
+                ev[i].record(stream)
+                fn()
+            ev[k].record(stream)
+            torch.cuda.synchronize(dev)
+            return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(k))
+
+        def plain():
+            state["t"], _ = fa.fa_bucket_step(None, p, g, m, v, None, state["t"], opts, ctl, 1.0)
+
+        def writeback():
+            state["t"], _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, state["t"], opts,
+                                                        ctl, p_model, 1.0)
+
+        peak, peak_kind = measured_peaks()
+        rows_out = {}
+        for name, fn, bpp_k in (("update_only", plain, fa.bytes_per_param(2, False, False)),
+                                ("f1_writeback_bf16", writeback,
+                                 fa.bytes_per_param(2, False, False) + 2)):
+            ms = timed(fn, args.next_rows_steps)
+            gbs = bpp_k * n / (ms * 1e-3) / 1e9
+            rows_out[name] = {"ms": ms, "bytes_per_param": bpp_k, "achieved_gbs": gbs,
+                              "frac": gbs / peak, "peak_kind": peak_kind,
+                              "params_per_s": n / (ms * 1e-3)}
+        del p_model
+
+        # f2: the pages' staged baseline against the fused update, on FP32
+        # gradients (the case their 48 -> 28 and 60 -> 36 B/param model is stated
+        # for), AdamW and AMSGrad, same resident state.
+        g32 = g.float()
+        delta = torch.empty_like(p)
+        vmax = torch.zeros_like(p)
+        for ams in (False, True):
+            o = fa.options(**dict(w.options(), amsgrad=ams))
+            vm = vmax if ams else None
+
+            def fused():
+                state["t"], _ = fa.fa_adamw_step_inplace(p, g32, m, v, vm, state["t"], o, ctl)
+
+            def staged():
+                state["t"], _ = fa.fa_adamw_step_staged(p, g32, m, v, vm, state["t"], o, ctl,
+                                                        delta)
+
+            tag = "amsgrad" if ams else "adamw"
+            fb = fa.bytes_per_param(4, ams, False)
+            sb = 60 if ams else 48
+            t_f = timed(fused, args.next_rows_steps)
+            t_s = timed(staged, args.next_rows_steps)
+            rows_out[f"f2_staged_vs_fused_f32_{tag}"] = {
+                "fused_ms": t_f, "staged_ms": t_s, "fused_bytes_per_param": fb,
+                "staged_bytes_per_param": sb, "fused_gbs": fb * n / (t_f * 1e-3) / 1e9,
+                "staged_gbs": sb * n / (t_s * 1e-3) / 1e9, "speedup": t_s / t_f,
+                "byte_model_ratio": sb / fb, "kernels": {"fused": 1, "staged": 5 if ams else 4}}
+        del g32, delta, vmax
+
+        # f4: the torch.optim-style wrapper on the decoder-shaped 1.196e9-parameter
+        # model (199 FP32 tensors packed into one bucket), global clip 1.0: each
+        # step analyses, merges, reads back 12 bytes, decides and updates.
+        from amsgrad_optimizer_step_gb300.optim import FusedAdamW
+        from synthetic.configs import decoder_bucket_shapes
+        dparams = [torch.nn.Parameter(torch.zeros(shape, device=dev))
+                   for _, shape in decoder_bucket_shapes()]
+        dn = sum(x.numel() for x in dparams)
+        dopt = FusedAdamW(dparams, lr=1e-3, max_grad_norm=1.0)
+        dopt._buckets[0].grad.normal_(0.0, 1e-3)
+        ms = timed(dopt.step, args.next_rows_steps)
+        b4 = fa.bytes_per_param(4, False, False) + 4  # update + analysis read of the FP32 gradient
+        rows_out["f4_fused_adamw_decoder1.1B_clip"] = {
+            "ms": ms, "params": dn, "tensors": len(dparams), "row_len": dopt.row_len,
+            "bytes_per_param": b4, "achieved_gbs": b4 * dn / (ms * 1e-3) / 1e9,
+            "frac": b4 * dn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+            "params_per_s": dn / (ms * 1e-3), "skipped": dopt.last_report["skipped"]}
+        del dopt, dparams
+        torch.cuda.empty_cache()
+        next_rows = rows_out
 
     if rank == 0:
         ms_step = total_ms / args.steps

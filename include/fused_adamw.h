@@ -193,6 +193,23 @@ fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int
                                    fa_step_control ctl, double grad_mult, void *p_model,
                                    fa_dtype model_dtype, int32_t *updated, void *stream);
 
+/*
+ * The staged comparison, for benchmarks only ([FA-ja] "割り当てとパフォーマンスのモデル";
+ * [FA-zh] "优化点与边界": an explicit staged baseline of 4 kernels, 5 with AMSGrad,
+ * with repeated gradient reads and a delta buffer: 48 and 60 bytes per
+ * parameter for FP32 gradients in steady state, against 28 and 36 fused).
+ * Stages: m; v; (vmax); delta = lr/bc1*m/(sqrt(v_used/bc2)+eps) into the
+ * caller's FP32 buffer ``delta`` (n elements, overlapping nothing); p.  Each
+ * stage evaluates the fused kernel's FP32 operations, so the results equal
+ * fa_adamw_step_inplace's bit for bit.  Arguments as fa_adamw_step_inplace;
+ * p, m, v, vmax and delta must be 16-byte aligned and g 16-byte (FP32) or
+ * 8-byte (FP16/BF16) aligned, else FA_ERR_ALIGN.
+ */
+fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt, float *m,
+                               float *v, float *vmax, uint64_t *t, const fa_options *options,
+                               fa_step_control ctl, double grad_mult, float *delta,
+                               int32_t *updated, void *stream);
+
 /* ---- gradient statistics -------------------------------------------------- */
 
 /*

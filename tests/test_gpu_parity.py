@@ -515,3 +515,42 @@ def test_writeback_rejections():
                                     p.view(torch.bfloat16)[:n])
     assert e.value.status == 5
     assert not model.view(torch.int16).any()
+
+
+# ---- staged comparison ---------------------------------------------------------------
+
+@pytest.mark.parametrize("gdt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("ams", [False, True])
+def test_staged_equals_fused_bitwise(gdt, ams):
+    """The 4/5-kernel staged baseline evaluates the fused kernel's FP32 operations
+    stage by stage: same results bit for bit, first step included."""
+    w, p0 = _fresh(70_001, gdt, 17, ams=ams)
+    o = fa.options(**dict(w.options(), maximize=True))
+    pa, pb = p0.clone(), p0.clone()
+    sa, sb = _zeros(w.n, 3), _zeros(w.n, 3)
+    if not ams:
+        sa[2] = sb[2] = None
+    delta = torch.empty(w.n, device=DEV)
+    ta = tb = 0
+    for call in range(1, 5):
+        g = _grads(w, call)
+        ta, _ = fa.fa_adamw_step_inplace(pa, g, *sa, ta, o, fa.control(2.0), grad_mult=0.75)
+        tb, _ = fa.fa_adamw_step_staged(pb, g, *sb, tb, o, fa.control(2.0), delta, grad_mult=0.75)
+    torch.cuda.synchronize()
+    assert ta == tb == 4
+    assert torch.equal(pa.view(torch.int32), pb.view(torch.int32))
+    for x, y in zip(sa, sb):
+        if x is not None:
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_staged_rejects_unaligned_views():
+    n = 4096
+    full = torch.zeros(n + 4, device=DEV)
+    p = full[1:1 + n]
+    m, v = torch.zeros(n, device=DEV), torch.zeros(n, device=DEV)
+    g = torch.zeros(n, device=DEV)
+    delta = torch.empty(n, device=DEV)
+    with pytest.raises(fa.FusedAdamWError) as e:
+        fa.fa_adamw_step_staged(p, g, m, v, None, 0, fa.options(), fa.control(), delta)
+    assert e.value.status == 7
