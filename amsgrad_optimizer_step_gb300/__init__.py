@@ -21,7 +21,7 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
                    FaStepReport, FusedAdamWError, check)
 
 __all__ = [
-    "fa_abi_version", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
+    "fa_abi_version", "fa_device_error", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
     "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback",
     "fa_adamw_step_staged", "fa_stats_plan",
     "fa_stats_rows",
@@ -92,6 +92,13 @@ def bytes_per_param(grad_bytes: int, amsgrad: bool, first_step: bool) -> int:
 
 def fa_abi_version() -> int:
     return _L().fa_abi_version()
+
+
+def fa_device_error(clear: bool = False) -> int:
+    """1 when an update kernel's bounded pipeline wait gave up on this device."""
+    v = ctypes.c_int32()
+    check("fa_device_error", _L().fa_device_error(ctypes.byref(v), int(bool(clear))))
+    return v.value
 
 
 def fa_options_default() -> FaOptions:

@@ -258,6 +258,17 @@ const char *fa_status_string(fa_status s) {
     return "unknown status";
 }
 
+fa_status fa_device_error(int32_t *flag, int32_t clear) {
+    if (!flag) return FA_ERR_NULL;
+    int v = 0;
+    if (fa::update_pipeline_error(&v, clear != 0) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    *flag = v;
+    return FA_OK;
+}
+
 fa_options fa_options_default(void) {
     fa_options o;
     o.lr = 1e-3;

@@ -37,6 +37,10 @@ struct UpdateArgs {
 
 // Enqueues one update kernel over a.n elements.  vector_ok: every pointer is
 // 16-byte aligned at element a.head.  Returns the CUDA launch status.
+// Reads (and optionally clears) the flag an update kernel sets when a bounded
+// wait in its shared-memory pipeline gives up.  Waits for the device.
+cudaError_t update_pipeline_error(int *flag, bool clear);
+
 // model_dtype: FA_F16 or FA_BF16 when a.p_model is set, else kNoModel.
 constexpr int kNoModel = -1;
 cudaError_t launch_update(const UpdateArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,

@@ -71,7 +71,7 @@ def update_kernel_traffic(n):
     summary scaled to ``n`` parameters; None once the kernel source has changed
     since the counters were taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "update_vec_kernel_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "update_kernel_traffic_flat256M_bf16.txt")
     try:
         vals = {}
         for line in open(path):
@@ -346,6 +346,15 @@ def run_ours(args):
                                                           opts, ctl, w.max_grad_norm, row_len,
                                                           rows_buf, scratch, report)
 
+        # the host-to-device link on its own (same buffer, same stream), for reading e2e
+        ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g_dev[1].copy_(g_host, non_blocking=True)
+        ev_a.record(stream)
+        g_dev[1].copy_(g_host, non_blocking=True)
+        ev_b.record(stream)
+        torch.cuda.synchronize(dev)
+        h2d_ms = ev_a.elapsed_time(ev_b)
+
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
@@ -368,6 +377,7 @@ def run_ours(args):
         e2e = {"value": world * n * args.e2e_steps / e2e_s, "unit": UNIT,
                "h2d_bytes_per_step": n * 2, "d2h_bytes_per_step": 12,
                "ms_per_step": e2e_s * 1e3 / args.e2e_steps, "steps": args.e2e_steps,
+               "h2d_copy_ms": h2d_ms, "h2d_gbs": n * 2 / (h2d_ms * 1e-3) / 1e9,
                "what": "pinned-host BF16 gradient copied in every step (side stream, double "
                        "buffered), then the C-ABI statistics-guarded step (analyse, merge, "
                        "12-byte report read back, decide, update); wall clock"}
@@ -475,7 +485,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_dict(w),
             "achieved_gbs_step": step_bytes / (ms_step * 1e-3) / 1e9,
-            "roofline": {"bound": "hbm", "kernel": "update_vec_kernel (fused AdamW, BF16 grad)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "update_tma_kernel (fused AdamW, BF16 grad, steady state)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "bytes_per_param": bpp, "traffic": update_kernel_traffic(n),

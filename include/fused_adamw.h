@@ -103,6 +103,14 @@ typedef struct fa_step_report {
 int32_t fa_abi_version(void);
 const char *fa_status_string(fa_status status);
 
+/* Large updates stage tiles through shared memory with TMA bulk copies; every
+ * wait in that pipeline is bounded (about a second), and a wait that gives up
+ * sets a device flag, drains its own copies and ends the kernel early (its
+ * outputs are then incomplete: discard them).  This reads the flag of the
+ * current device into *flag (0 = no wait ever gave up) and clears it when
+ * clear != 0.  Waits for the device; FA_ERR_CUDA if it cannot be read. */
+fa_status fa_device_error(int32_t *flag, int32_t clear);
+
 /* Defaults ([FA-ja] "この演算子を使用する理由": betas (0.9, 0.999), eps 1e-5,
  * weight_decay 1e-4, matching RUDA's AdamWConfig).  The pages state no default
  * learning rate; 1e-3 is used.  amsgrad = maximize = 0. */

@@ -554,3 +554,8 @@ def test_staged_rejects_unaligned_views():
     with pytest.raises(fa.FusedAdamWError) as e:
         fa.fa_adamw_step_staged(p, g, m, v, None, 0, fa.options(), fa.control(), delta)
     assert e.value.status == 7
+
+
+def test_update_pipeline_never_gave_up():
+    """After everything above, no bounded wait in the shared-memory pipeline gave up."""
+    assert fa.fa_device_error() == 0
