@@ -26,7 +26,9 @@ __all__ = [
     "fa_adamw_step_staged", "fa_stats_plan",
     "fa_stats_rows",
     "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",
-    "fa_read_report", "fa_clip_decision",
+    "fa_read_report", "fa_clip_decision", "fa_stats_chunk_scratch",
+    "fa_merge_gradient_stats_chunks", "fa_bucket_step_segment_scaled",
+    "fa_bucket_step_clipped_per_segment", "segment_rows",
     "fa_clip_decide", "fa_bucket_step_clipped", "options", "control", "stats_buffer",
     "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
 ]
@@ -314,6 +316,82 @@ def fa_merge_gradient_stats_static(rows_in: torch.Tensor, rows: int, report: tor
     _stats_tensor("report", report)
     check("fa_merge_gradient_stats_static", _L().fa_merge_gradient_stats_static(
         _ptr(rows_in), rows, _ptr(report), _stream(stream)))
+
+
+def fa_stats_chunk_scratch(chunk_rows: Sequence[int]) -> int:
+    arr = (ctypes.c_int64 * len(chunk_rows))(*[int(x) for x in chunk_rows])
+    e = ctypes.c_int64()
+    check("fa_stats_chunk_scratch",
+          _L().fa_stats_chunk_scratch(arr, len(chunk_rows) - 1, ctypes.byref(e)))
+    return e.value
+
+
+def segment_rows(seg_offsets: Sequence[int], row_len: int) -> list[int]:
+    """Row offsets of each segment's statistics rows (rows never span segments)."""
+    out = [0]
+    for a, b in zip(seg_offsets[:-1], seg_offsets[1:]):
+        out.append(out[-1] + (int(b) - int(a) + row_len - 1) // row_len)
+    return out
+
+
+def fa_merge_gradient_stats_chunks(rows_in: torch.Tensor, chunk_rows: Sequence[int],
+                                   scratch: torch.Tensor, chunk_reports: torch.Tensor,
+                                   stream=None) -> None:
+    _stats_tensor("rows_in", rows_in)
+    _stats_tensor("chunk_reports", chunk_reports)
+    arr = (ctypes.c_int64 * len(chunk_rows))(*[int(x) for x in chunk_rows])
+    check("fa_merge_gradient_stats_chunks", _L().fa_merge_gradient_stats_chunks(
+        _ptr(rows_in), arr, len(chunk_rows) - 1, _ptr(scratch), scratch.numel(),
+        _ptr(chunk_reports), _stream(stream)))
+
+
+def fa_bucket_step_segment_scaled(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                                  ctl: FaStepControl, seg_grad_mult: Sequence[float],
+                                  stream=None) -> tuple[int, bool]:
+    """Bucket update with one gradient multiplier per segment.  Returns (t, updated)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    seg, nseg = _segments(seg_offsets)
+    if len(seg_grad_mult) != nseg:
+        raise ValueError("one multiplier per segment")
+    mult = (ctypes.c_double * nseg)(*[float(x) for x in seg_grad_mult])
+    tt, upd = ctypes.c_uint64(t), ctypes.c_int32()
+    check("fa_bucket_step_segment_scaled", _L().fa_bucket_step_segment_scaled(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, mult, ctypes.byref(upd), _stream(stream)))
+    return tt.value, bool(upd.value)
+
+
+def fa_bucket_step_clipped_per_segment(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                                       ctl: FaStepControl, max_grad_norm: float, row_len: int,
+                                       rows_buf: torch.Tensor, scratch: torch.Tensor,
+                                       seg_reports: torch.Tensor, stream=None):
+    """Per-parameter clipped step.  Returns (t, report, segment norms, coefficients)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _stats_tensor("rows_buf", rows_buf)
+    _stats_tensor("seg_reports", seg_reports)
+    seg, nseg = _segments(seg_offsets)
+    norms = (ctypes.c_double * nseg)()
+    coefs = (ctypes.c_double * nseg)()
+    tt = ctypes.c_uint64(t)
+    rep = FaStepReport()
+    check("fa_bucket_step_clipped_per_segment", _L().fa_bucket_step_clipped_per_segment(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, max_grad_norm, row_len, _ptr(rows_buf),
+        rows_buf.shape[0], _ptr(scratch), scratch.numel(), _ptr(seg_reports), norms, coefs,
+        ctypes.byref(rep), _stream(stream)))
+    return tt.value, rep, list(norms), list(coefs)
 
 
 def fa_read_report(report: torch.Tensor, stream=None) -> FaStats:

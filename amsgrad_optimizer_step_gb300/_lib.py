@@ -71,6 +71,16 @@ SIGNATURES = {
     "fa_analyze_gradient": (c_i32, [P, c_i32, c_i64, c_i32, PI64, c_i32, P, c_i64, P]),
     "fa_merge_gradient_stats": (c_i32, [P, c_i64, P, c_i64, P, P]),
     "fa_merge_gradient_stats_static": (c_i32, [P, c_i64, P, P]),
+    "fa_stats_chunk_scratch": (c_i32, [PI64, c_i32, PI64]),
+    "fa_merge_gradient_stats_chunks": (c_i32, [P, PI64, c_i32, P, c_i64, P, P]),
+    "fa_bucket_step_segment_scaled": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
+                                              ctypes.POINTER(FaOptions), FaStepControl, PF64,
+                                              PI32, P]),
+    "fa_bucket_step_clipped_per_segment": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P,
+                                                   PU64, ctypes.POINTER(FaOptions),
+                                                   FaStepControl, c_f64, c_i32, P, c_i64, P,
+                                                   c_i64, P, PF64, PF64,
+                                                   ctypes.POINTER(FaStepReport), P]),
     "fa_read_report": (c_i32, [P, ctypes.POINTER(FaStats), P]),
     "fa_clip_decision": (c_i32, [c_f64, c_u64, c_f64, c_f64, PI32, PF64, PF64]),
     "fa_clip_decide": (c_i32, [P, c_f64, c_f64, PI32, PF64, PF64, P]),

@@ -18,6 +18,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -615,6 +616,210 @@ fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
         count = out_count;
         next = out + out_count;
     }
+    return FA_OK;
+}
+
+// ---- per-chunk (per-parameter) statistics and clipping ------------------------
+
+fa_status fa_stats_chunk_scratch(const int64_t *chunk_rows, int32_t nchunks,
+                                 int64_t *scratch_elements) {
+    if (!scratch_elements) return FA_ERR_NULL;
+    if (nchunks < 1) return FA_ERR_SEGMENTS;
+    if (!chunk_rows) return FA_ERR_NULL;
+    if (chunk_rows[0] != 0) return FA_ERR_SEGMENTS;
+    int64_t groups = 0;
+    for (int32_t k = 0; k < nchunks; ++k) {
+        const int64_t r = chunk_rows[k + 1] - chunk_rows[k];
+        if (r < 0) return FA_ERR_SEGMENTS;
+        groups += (r + fa::kFanIn - 1) / fa::kFanIn;
+    }
+    if (chunk_rows[nchunks] < 1 || chunk_rows[nchunks] > fa::kMaxRows) return FA_ERR_PLAN;
+    *scratch_elements = 3 * groups;
+    return FA_OK;
+}
+
+fa_status fa_merge_gradient_stats_chunks(const fa_stats *rows_in, const int64_t *chunk_rows,
+                                         int32_t nchunks, float *scratch,
+                                         int64_t scratch_elements, fa_stats *chunk_reports,
+                                         void *stream) {
+    int64_t need = 0;
+    fa_status st = fa_stats_chunk_scratch(chunk_rows, nchunks, &need);
+    if (st != FA_OK) return st;
+    if (scratch_elements < need || !scratch) return FA_ERR_SIZE;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(rows_in, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(chunk_reports, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(scratch, dev, 4)) != FA_OK) return st;
+    const int64_t rows = chunk_rows[nchunks];
+    const Range r[] = {{rows_in, static_cast<size_t>(rows) * 12},
+                       {scratch, static_cast<size_t>(need) * 4},
+                       {chunk_reports, static_cast<size_t>(nchunks) * 12}};
+    if (any_overlap(r, 3)) return FA_ERR_ALIAS;
+    fa_stats *partial = reinterpret_cast<fa_stats *>(scratch);
+    for (int32_t k0 = 0; k0 < nchunks; k0 += fa::kMaxSegPerLaunch) {
+        const int32_t cnt =
+            nchunks - k0 < fa::kMaxSegPerLaunch ? nchunks - k0 : fa::kMaxSegPerLaunch;
+        fa::ChunkMergeArgs a;
+        a.in = rows_in + chunk_rows[k0];
+        a.partial = partial;
+        a.out = chunk_reports + k0;
+        a.nchunks = cnt;
+        int64_t groups = 0;
+        for (int32_t j = 0; j <= cnt; ++j) {
+            a.row_start[j] = chunk_rows[k0 + j] - chunk_rows[k0];
+            a.group_start[j] = groups;
+            if (j < cnt)
+                groups += (chunk_rows[k0 + j + 1] - chunk_rows[k0 + j] + fa::kFanIn - 1) / fa::kFanIn;
+        }
+        if (fa::launch_merge_chunks(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return FA_ERR_CUDA;
+        partial += groups;
+    }
+    return FA_OK;
+}
+
+fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                        float *p, const void *g, fa_dtype gdt, float *m,
+                                        float *v, float *vmax, uint64_t *t,
+                                        const fa_options *options, fa_step_control ctl,
+                                        const double *seg_grad_mult, int32_t *updated,
+                                        void *stream) {
+    fa_status st;
+    if (!t || !updated) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n_total < 0) return FA_ERR_SIZE;
+    if (nseg < 1) return FA_ERR_SEGMENTS;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (!seg_grad_mult) return FA_ERR_NULL;
+    for (int32_t k = 0; k < nseg; ++k)
+        if (!is_finite(seg_grad_mult[k]) || seg_grad_mult[k] < 0) return FA_ERR_OPTION;
+    if (n_total == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
+        *updated = 0;
+        return FA_OK;
+    }
+    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    Coef c;
+    if ((st = make_coef(options, *t + 1, ctl.gradient_scale, 1.0, &c)) != FA_OK) return st;
+    const bool first = *t == 0;
+    const bool ams = options->amsgrad != 0;
+    const size_t gb = dtype_bytes(gdt);
+    for (int32_t k0 = 0; k0 < nseg; k0 += fa::kMaxSegPerLaunch) {
+        const int32_t cnt = nseg - k0 < fa::kMaxSegPerLaunch ? nseg - k0 : fa::kMaxSegPerLaunch;
+        const int64_t e0 = seg_offsets[k0], e1 = seg_offsets[k0 + cnt];
+        if (e1 == e0) continue;
+        fa::SegScaleArgs sa;
+        fa::UpdateArgs &a = sa.a;
+        a.p_in = p + e0;
+        a.m_in = first ? nullptr : m + e0;
+        a.v_in = first ? nullptr : v + e0;
+        a.vmax_in = (first || !ams) ? nullptr : vmax + e0;
+        a.g = static_cast<const char *>(g) + e0 * gb;
+        a.p_out = p + e0;
+        a.m_out = m + e0;
+        a.v_out = v + e0;
+        a.vmax_out = ams ? vmax + e0 : nullptr;
+        a.p_model = nullptr;
+        a.n = e1 - e0;
+        const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g};
+        const size_t es[] = {4, 4, 4, 4, gb};
+        const int64_t head = vector_head(ptrs, es, 5, a.n);
+        const bool vec = head >= 0;
+        a.head = vec ? head : 0;
+        a.nvec = vec ? (a.n - a.head) / 8 : 0;
+        sa.nseg = cnt;
+        for (int32_t j = 0; j <= cnt; ++j) sa.seg_start[j] = seg_offsets[k0 + j] - e0;
+        for (int32_t j = 0; j < cnt; ++j)
+            sa.gmul[j] = static_cast<float>((options->maximize ? -1.0 : 1.0) *
+                                            seg_grad_mult[k0 + j] / ctl.gradient_scale);
+        if (fa::launch_update_segment_scaled(sa, c, gdt, ams, first, vec,
+                                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    *t += 1;
+    *updated = 1;
+    return FA_OK;
+}
+
+fa_status fa_bucket_step_clipped_per_segment(
+    const int64_t *seg_offsets, int32_t nseg, int64_t n_total, float *p, const void *g,
+    fa_dtype gdt, float *m, float *v, float *vmax, uint64_t *t, const fa_options *options,
+    fa_step_control ctl, double max_grad_norm, int32_t row_len, fa_stats *rows_buf,
+    int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
+    double *seg_norms, double *seg_coefs, fa_step_report *out, void *stream) {
+    fa_status st;
+    if (!t || !out) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n_total < 0 || row_len <= 0) return FA_ERR_SIZE;
+    if (nseg < 1) return FA_ERR_SEGMENTS;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    fa_step_report rep{0, 0, 0, 0.0, 1.0};
+    if (n_total == 0 || ctl.skip_update) {
+        *out = rep;
+        return FA_OK;
+    }
+    std::vector<int64_t> chunk_rows(static_cast<size_t>(nseg) + 1, 0);
+    for (int32_t k = 0; k < nseg; ++k)
+        chunk_rows[k + 1] = chunk_rows[k] + (seg_offsets[k + 1] - seg_offsets[k] + row_len - 1) / row_len;
+    int64_t need = 0;
+    if ((st = fa_stats_chunk_scratch(chunk_rows.data(), nseg, &need)) != FA_OK) return st;
+    if (scratch_elements < need || rows_capacity < chunk_rows[nseg]) return FA_ERR_SIZE;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    if ((st = fa_analyze_gradient(g, gdt, n_total, row_len, seg_offsets, nseg, rows_buf,
+                                  rows_capacity, stream)) != FA_OK)
+        return st;
+    if ((st = fa_merge_gradient_stats_chunks(rows_buf, chunk_rows.data(), nseg, scratch,
+                                             scratch_elements, seg_reports, stream)) != FA_OK)
+        return st;
+    std::vector<fa_stats> host(static_cast<size_t>(nseg));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host.data(), seg_reports, host.size() * sizeof(fa_stats),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    std::vector<double> coef(static_cast<size_t>(nseg), 1.0);
+    double total = 0.0, min_coef = 1.0;
+    uint64_t bad = 0;
+    for (int32_t k = 0; k < nseg; ++k) {
+        const double sum = static_cast<double>(host[k].sum_sq) + static_cast<double>(host[k].sum_sq_lo);
+        int32_t skip = 0;
+        double norm = 0.0;
+        if ((st = fa_clip_decision(sum, host[k].nonfinite, ctl.gradient_scale, max_grad_norm, &skip,
+                                   &norm, &coef[k])) != FA_OK)
+            return st;
+        bad += host[k].nonfinite;
+        if (!skip) total += sum;
+        if (coef[k] < min_coef) min_coef = coef[k];
+        if (seg_norms) seg_norms[k] = norm;
+        if (seg_coefs) seg_coefs[k] = coef[k];
+    }
+    rep.nonfinite = bad;
+    rep.grad_norm = std::sqrt(total) / ctl.gradient_scale;
+    rep.clip_coef = min_coef;
+    if (bad > 0) {  // any non-finite value skips the whole step
+        rep.skipped_nonfinite = 1;
+        *out = rep;
+        return FA_OK;
+    }
+    int32_t updated = 0;
+    if ((st = fa_bucket_step_segment_scaled(seg_offsets, nseg, n_total, p, g, gdt, m, v, vmax, t,
+                                            options, ctl, coef.data(), &updated, stream)) != FA_OK)
+        return st;
+    rep.updated = updated;
+    *out = rep;
     return FA_OK;
 }
 

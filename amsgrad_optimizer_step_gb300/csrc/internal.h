@@ -69,6 +69,30 @@ struct AnalyzeArgs {
 cudaError_t launch_analyze(const AnalyzeArgs &a, fa_dtype gdt, bool vector_ok,
                            cudaStream_t stream);
 
+// Per-chunk merge of up to kMaxSegPerLaunch chunks: level A reduces groups of
+// at most kFanIn rows within a chunk into ``partial``, level B one chunk's
+// groups into out[k].
+struct ChunkMergeArgs {
+    const fa_stats *in;   // row records; chunk k holds [row_start[k], row_start[k+1])
+    fa_stats *partial;    // group_start[nchunks] level-A records
+    fa_stats *out;        // nchunks records
+    int32_t nchunks;
+    int64_t row_start[kMaxSegPerLaunch + 1];
+    int64_t group_start[kMaxSegPerLaunch + 1];
+};
+cudaError_t launch_merge_chunks(const ChunkMergeArgs &a, cudaStream_t stream);
+
+// The update with one gradient multiplier per segment (per-parameter clipping).
+struct SegScaleArgs {
+    UpdateArgs a;        // pointers of this launch's first element; a.n elements
+    int32_t nseg;
+    int64_t seg_start[kMaxSegPerLaunch + 1];  // relative to the launch's first element
+    float gmul[kMaxSegPerLaunch];             // (maximize ? -1 : 1) * multiplier / scale
+};
+cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, fa_dtype gdt,
+                                         bool amsgrad, bool first, bool vector_ok,
+                                         cudaStream_t stream);
+
 // One merge level: ceil(count / kFanIn) output records from count input records.
 cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream);
 

@@ -356,17 +356,15 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
     }
 }
 
-// One CTA per group of kFanIn input records.
-__global__ void __launch_bounds__(kThreads)
-merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
+// One CTA reduces records [lo, hi) into *out: FP64 sums per thread, warp
+// shuffles, then shared memory; the total leaves as an FP32 (hi, lo) pair.
+__device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int64_t lo,
+                                            int64_t hi, fa_stats *__restrict__ out) {
     __shared__ double s_sum[kThreads / 32];
     __shared__ unsigned long long s_cnt[kThreads / 32];
-    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kFanIn;
-    const int64_t g1 = g0 + kFanIn < count ? g0 + kFanIn : count;
-
     double s = 0.0;
     unsigned long long c = 0;
-    for (int64_t i = g0 + threadIdx.x; i < g1; i += kThreads) {
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
         const fa_stats r = in[i];
         s += static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
         c += r.nonfinite;
@@ -393,8 +391,44 @@ merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restric
         rec.sum_sq = static_cast<float>(ts);
         rec.sum_sq_lo = static_cast<float>(ts - static_cast<double>(rec.sum_sq));
         rec.nonfinite = tc > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(tc);
-        out[blockIdx.x] = rec;
+        *out = rec;
     }
+}
+
+// One CTA per group of kFanIn input records.
+__global__ void __launch_bounds__(kThreads)
+merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kFanIn;
+    const int64_t g1 = g0 + kFanIn < count ? g0 + kFanIn : count;
+    block_merge(in, g0, g1, out + blockIdx.x);
+}
+
+// Per-chunk merge, level A: one CTA per group of at most kFanIn records of one
+// chunk (groups never span two chunks).
+__device__ __forceinline__ int find_chunk(const ChunkMergeArgs &a, int64_t group) {
+    int lo = 0, hi = a.nchunks - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.group_start[mid] <= group) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kThreads)
+merge_chunks_a_kernel(const __grid_constant__ ChunkMergeArgs a) {
+    const int64_t b = blockIdx.x;
+    const int k = find_chunk(a, b);
+    const int64_t lo = a.row_start[k] + (b - a.group_start[k]) * kFanIn;
+    const int64_t hi = lo + kFanIn < a.row_start[k + 1] ? lo + kFanIn : a.row_start[k + 1];
+    block_merge(a.in, lo, hi, a.partial + b);
+}
+
+// Level B: one CTA per chunk over its level-A records (an empty chunk gives a
+// zero record).
+__global__ void __launch_bounds__(kThreads)
+merge_chunks_b_kernel(const __grid_constant__ ChunkMergeArgs a) {
+    const int k = blockIdx.x;
+    block_merge(a.partial, a.group_start[k], a.group_start[k + 1], a.out + k);
 }
 
 template <int GT, int CH, bool MULTI>
@@ -451,6 +485,17 @@ cudaError_t launch_analyze(const AnalyzeArgs &a, fa_dtype gdt, bool vector_ok,
         case FA_BF16: return launch_analyze_typed<FA_BF16>(a, vector_ok, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge_chunks(const ChunkMergeArgs &a, cudaStream_t stream) {
+    const int64_t groups = a.group_start[a.nchunks];
+    if (groups > 0) {
+        merge_chunks_a_kernel<<<static_cast<unsigned>(groups), kThreads, 0, stream>>>(a);
+        const cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    if (a.nchunks > 0) merge_chunks_b_kernel<<<a.nchunks, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream) {

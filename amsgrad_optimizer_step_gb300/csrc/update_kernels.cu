@@ -291,6 +291,39 @@ update_scalar_kernel(const UpdateArgs a, const Coef c) {
         scalar_element<GT, AMS, FIRST, MD>(a, c, i);
 }
 
+// ---- one gradient multiplier per segment -----------------------------------------
+//
+// Per-parameter clipping ("训练与状态保存", section "FP32 主参数与混合参数存储": clipping
+// follows a per-parameter rule, not a whole-model norm): the bucket update with
+// the gradient multiplier of the segment each element belongs to, from a
+// segment table in kernel parameters.  Register-staged 8-element vectors; a
+// vector inside one segment takes one lookup, a vector that straddles a
+// boundary looks up each element.
+__device__ __forceinline__ int find_seg_in(const SegScaleArgs &s, int64_t e, int lo, int hi) {
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.seg_start[mid] <= e) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int find_seg(const SegScaleArgs &s, int64_t e) {
+    int lo = 0, hi = s.nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.seg_start[mid] <= e) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int GT, bool AMS, bool FIRST>
+__device__ __forceinline__ void scalar_element_seg(const SegScaleArgs &s, const Coef &c,
+                                                   int64_t i) {
+    Coef cc = c;
+    cc.gmul = s.gmul[find_seg(s, i)];
+    scalar_element<GT, AMS, FIRST, kNoModel>(s.a, cc, i);
+}
+
 #if FA_UPDATE_TMA
 // ---- shared-memory staging with 1-D TMA bulk copies ---------------------------
 //
@@ -387,9 +420,12 @@ struct TmaLayout {
     static_assert(kStages >= 2, "at least two stages");
 };
 
-template <int GT, bool AMS, bool FIRST, int MD>
+// SEG: one gradient multiplier per segment from s's table (MD must be kNoModel);
+// otherwise s.nseg is 0 and c.gmul applies to every element.
+template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-update_tma_kernel(const UpdateArgs a, const Coef c, int64_t ntiles) {
+update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c, int64_t ntiles) {
+    const UpdateArgs &a = sa.a;
     using L = TmaLayout<GT, AMS, MD>;
     constexpr int S = L::kStages;
     constexpr uint32_t kLoadBytes =
@@ -445,6 +481,13 @@ update_tma_kernel(const UpdateArgs a, const Coef c, int64_t ntiles) {
         if (tid == 0) consumed[s] = issued[s];
 
         unsigned char *b = smem + s * L::kStage;
+        // segments of this tile's first and last element (warp-uniform searches)
+        int k_lo = 0, k_hi = 0;
+        if (SEG) {
+            const int64_t t0 = a.head + tile * L::kTile;
+            k_lo = find_seg(sa, t0);
+            k_hi = find_seg_in(sa, t0 + L::kTile - 1, k_lo, sa.nseg - 1);
+        }
 #pragma unroll
         for (int h = 0; h < L::kChunks; ++h) {
             const int j = h * 4 * kTmaThreads + 4 * tid;  // first element of this chunk
@@ -478,8 +521,25 @@ update_tma_kernel(const UpdateArgs a, const Coef c, int64_t ntiles) {
                     vm[0] = w4.x; vm[1] = w4.y; vm[2] = w4.z; vm[3] = w4.w;
                 }
             }
+            if (SEG) {
+                Coef cc = c;
+                if (k_lo == k_hi) {  // the whole tile lies in one segment
+                    cc.gmul = sa.gmul[k_lo];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) adamw_element<AMS, FIRST>(c, x[q], p[q], m[q], v[q], vm[q]);
+                    for (int q = 0; q < 4; ++q)
+                        adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
+                } else {
+                    const int64_t e = a.head + tile * L::kTile + j;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        cc.gmul = sa.gmul[find_seg_in(sa, e + q, k_lo, k_hi)];
+                        adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) adamw_element<AMS, FIRST>(c, x[q], p[q], m[q], v[q], vm[q]);
+            }
             *pp = make_float4(p[0], p[1], p[2], p[3]);
             *mp = make_float4(m[0], m[1], m[2], m[3]);
             *vp = make_float4(v[0], v[1], v[2], v[3]);
@@ -536,11 +596,126 @@ update_tma_kernel(const UpdateArgs a, const Coef c, int64_t ntiles) {
     // scalar head [0, head) and tail after the last full tile
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kTmaThreads + tid;
     const int64_t gsz = static_cast<int64_t>(gridDim.x) * kTmaThreads;
-    for (int64_t i = gtid; i < a.head; i += gsz) scalar_element<GT, AMS, FIRST, MD>(a, c, i);
     const int64_t tail0 = a.head + ntiles * L::kTile;
-    for (int64_t i = tail0 + gtid; i < a.n; i += gsz) scalar_element<GT, AMS, FIRST, MD>(a, c, i);
+    if (SEG) {
+        for (int64_t i = gtid; i < a.head; i += gsz) scalar_element_seg<GT, AMS, FIRST>(sa, c, i);
+        for (int64_t i = tail0 + gtid; i < a.n; i += gsz) scalar_element_seg<GT, AMS, FIRST>(sa, c, i);
+    } else {
+        for (int64_t i = gtid; i < a.head; i += gsz) scalar_element<GT, AMS, FIRST, MD>(a, c, i);
+        for (int64_t i = tail0 + gtid; i < a.n; i += gsz) scalar_element<GT, AMS, FIRST, MD>(a, c, i);
+    }
 }
 #endif  // FA_UPDATE_TMA
+
+#if FA_UPDATE_TMA
+// Steady steps of at least two tiles per SM take the TMA pipeline; the first
+// step (moments only written: 6 B in, 12 B out) measured faster through the
+// register kernel (3.0 vs 3.7 ms at 1.07e9), and so did small tensors.
+template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
+cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vector_ok, int dev,
+                                cudaStream_t stream, bool *launched) {
+    using L = TmaLayout<GT, AMS, MD>;
+    *launched = false;
+    const int64_t ntiles = (s.a.n - s.a.head) / L::kTile;
+    const int64_t sms = sm_count(dev);
+    if (FIRST || !vector_ok || ntiles < 2 * sms) return cudaSuccess;
+    auto kern = update_tma_kernel<GT, AMS, FIRST, MD, SEG>;
+    static bool configured[64] = {};
+    if (dev < 64 && !configured[dev]) {
+        const cudaError_t err =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+        if (err != cudaSuccess) return err;
+        configured[dev] = true;
+    }
+    const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
+    kern<<<grid, kTmaThreads, L::kSmem, stream>>>(s, c, ntiles);
+    *launched = true;
+    return cudaGetLastError();
+}
+#endif
+
+template <int GT, bool AMS, bool FIRST>
+__global__ void __launch_bounds__(kThreads)
+update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
+    const UpdateArgs &a = s.a;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t vi = tid; vi < a.nvec; vi += stride) {
+        const int64_t e = a.head + vi * kVec;
+        float x[kVec], p[kVec], m[kVec], v[kVec], vm[kVec];
+        GradIO<GT>::load8(a.g, e, x);
+        load8f(a.p_in, e, p);
+        if (!FIRST) {
+            load8f(a.m_in, e, m);
+            load8f(a.v_in, e, v);
+            if (AMS) load8f(a.vmax_in, e, vm);
+        }
+        const int k = find_seg(s, e);
+        Coef cc = c;
+        if (e + kVec <= s.seg_start[k + 1]) {
+            cc.gmul = s.gmul[k];
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) {
+                cc.gmul = s.gmul[find_seg(s, e + q)];
+                adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
+            }
+        }
+        store8f(a.p_out, e, p);
+        store8f(a.m_out, e, m);
+        store8f(a.v_out, e, v);
+        if (AMS) store8f(a.vmax_out, e, vm);
+    }
+    if (tid < a.head) scalar_element_seg<GT, AMS, FIRST>(s, c, tid);
+    const int64_t tail0 = a.head + a.nvec * kVec;
+    if (tid < a.n - tail0) scalar_element_seg<GT, AMS, FIRST>(s, c, tail0 + tid);
+}
+
+template <int GT, bool AMS, bool FIRST>
+__global__ void __launch_bounds__(kThreads)
+update_segscaled_scalar_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < s.a.n;
+         i += stride)
+        scalar_element_seg<GT, AMS, FIRST>(s, c, i);
+}
+
+template <int GT, bool AMS, bool FIRST>
+cudaError_t launch_seg_typed(const SegScaleArgs &s, const Coef &c, bool vec, cudaStream_t st) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+#if FA_UPDATE_TMA
+    bool launched = false;
+    err = launch_tma_if_large<GT, AMS, FIRST, kNoModel, true>(s, c, vec, dev, st, &launched);
+    if (err != cudaSuccess || launched) return err;
+#endif
+    if (vec) {
+        auto kern = update_segscaled_kernel<GT, AMS, FIRST>;
+        int64_t need = (s.a.nvec + kThreads - 1) / kThreads;
+        if (need == 0 && s.a.n > 0) need = 1;
+        const int grid = persistent_grid(kern, need, dev);
+        if (grid > 0) kern<<<grid, kThreads, 0, st>>>(s, c);
+    } else {
+        auto kern = update_segscaled_scalar_kernel<GT, AMS, FIRST>;
+        const int grid = persistent_grid(kern, (s.a.n + kThreads - 1) / kThreads, dev);
+        if (grid > 0) kern<<<grid, kThreads, 0, st>>>(s, c);
+    }
+    return cudaGetLastError();
+}
+
+template <int GT>
+cudaError_t launch_seg_gt(const SegScaleArgs &s, const Coef &c, bool ams, bool first, bool vec,
+                          cudaStream_t st) {
+    if (ams)
+        return first ? launch_seg_typed<GT, true, true>(s, c, vec, st)
+                     : launch_seg_typed<GT, true, false>(s, c, vec, st);
+    return first ? launch_seg_typed<GT, false, true>(s, c, vec, st)
+                 : launch_seg_typed<GT, false, false>(s, c, vec, st);
+}
+
 
 constexpr int kUnroll = FA_UPDATE_UNROLL;
 
@@ -554,24 +729,12 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
 
 #if FA_UPDATE_TMA
     {
-        using L = TmaLayout<GT, AMS, MD>;
-        const int64_t ntiles = (a.n - a.head) / L::kTile;
-        // steady steps only: the first step (moments not read; 6 B in, 12 B out)
-        // measured faster through the register kernel (3.0 vs 3.7 ms at 1.07e9)
-        if (!FIRST && vector_ok && ntiles >= 2 * static_cast<int64_t>(sm_count(dev))) {
-            auto kern = update_tma_kernel<GT, AMS, FIRST, MD>;
-            static bool configured[64] = {};
-            if (dev < 64 && !configured[dev]) {
-                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           L::kSmem);
-                if (err != cudaSuccess) return err;
-                configured[dev] = true;
-            }
-            const int64_t sms = sm_count(dev);
-            const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
-            kern<<<grid, kTmaThreads, L::kSmem, stream>>>(a, c, ntiles);
-            return cudaGetLastError();
-        }
+        SegScaleArgs s;
+        s.a = a;
+        s.nseg = 0;
+        bool launched = false;
+        err = launch_tma_if_large<GT, AMS, FIRST, MD, false>(s, c, vector_ok, dev, stream, &launched);
+        if (err != cudaSuccess || launched) return err;
     }
 #endif
     if (vector_ok) {
@@ -613,6 +776,17 @@ cudaError_t launch_gt(const UpdateArgs &a, const Coef &c, bool ams, bool first, 
 }
 
 }  // namespace
+
+cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, fa_dtype gdt,
+                                         bool amsgrad, bool first, bool vector_ok,
+                                         cudaStream_t stream) {
+    switch (gdt) {
+        case FA_F32: return launch_seg_gt<FA_F32>(s, c, amsgrad, first, vector_ok, stream);
+        case FA_F16: return launch_seg_gt<FA_F16>(s, c, amsgrad, first, vector_ok, stream);
+        case FA_BF16: return launch_seg_gt<FA_BF16>(s, c, amsgrad, first, vector_ok, stream);
+    }
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t update_pipeline_error(int *flag, bool clear) {
 #if FA_UPDATE_TMA

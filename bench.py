@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--next-rows-steps", type=int, default=10)
     ap.add_argument("--n", type=int, default=0, help="override the parameter count (testing)")
@@ -355,21 +355,44 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         h2d_ms = ev_a.elapsed_time(ev_b)
 
+        # per-step events on both streams (to tell a slowed copy from a slowed step)
+        cp_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                 for _ in range(args.e2e_steps)]
+        st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                 for _ in range(args.e2e_steps)]
+
+        def enqueue_copy_timed(b, k):
+            with torch.cuda.stream(copy_stream):
+                if used[b]:
+                    copy_stream.wait_event(released[b])
+                cp_ev[k][0].record(copy_stream)
+                g_dev[b].copy_(g_host, non_blocking=True)
+                cp_ev[k][1].record(copy_stream)
+                copied[b].record(copy_stream)
+
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
-        enqueue_copy(0)
+        host_step = []
+        enqueue_copy_timed(0, 0)
         for k in range(args.e2e_steps):
             b = k % 2
             if k + 1 < args.e2e_steps:
-                enqueue_copy((k + 1) % 2)
+                enqueue_copy_timed((k + 1) % 2, k + 1)
             stream.wait_event(copied[b])
+            st_ev[k][0].record(stream)
+            h1 = time.perf_counter()
             e2e_step(g_dev[b])
+            h2 = time.perf_counter()
+            st_ev[k][1].record(stream)
             released[b].record(stream)
             used[b] = True
+            host_step.append((h2 - h1) * 1e3)
         torch.cuda.synchronize(dev)
         e2e_s = time.perf_counter() - t0
+        copy_ms = statistics.median(e[0].elapsed_time(e[1]) for e in cp_ev)
+        step_ms = statistics.median(e[0].elapsed_time(e[1]) for e in st_ev)
         if world > 1:
             tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -378,6 +401,9 @@ def run_ours(args):
                "h2d_bytes_per_step": n * 2, "d2h_bytes_per_step": 12,
                "ms_per_step": e2e_s * 1e3 / args.e2e_steps, "steps": args.e2e_steps,
                "h2d_copy_ms": h2d_ms, "h2d_gbs": n * 2 / (h2d_ms * 1e-3) / 1e9,
+               "overlapped_copy_ms_median": copy_ms, "overlapped_step_ms_median": step_ms,
+               "host_step_ms_median": statistics.median(host_step),
+               "host_step_ms_max": max(host_step),
                "what": "pinned-host BF16 gradient copied in every step (side stream, double "
                        "buffered), then the C-ABI statistics-guarded step (analyse, merge, "
                        "12-byte report read back, decide, update); wall clock"}
@@ -467,6 +493,38 @@ def run_ours(args):
             "frac": b4 * dn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
             "params_per_s": dn / (ms * 1e-3), "skipped": dopt.last_report["skipped"]}
         del dopt, dparams
+        torch.cuda.empty_cache()
+
+        # f3: per-parameter clipping on the decoder-shaped bucket (199 segments,
+        # FP16 gradients, AMSGrad): segment-aligned analysis, one report per
+        # segment, 199 x 12 bytes read back, per-segment clip, update.
+        from synthetic.configs import CONFIG4, decoder_bucket_offsets
+        seg = [int(x) for x in decoder_bucket_offsets()]
+        sn = seg[-1]
+        sp = torch.empty(sn, device=dev)
+        CONFIG4.fill_params_device(sp)
+        sm, sv, svm = (torch.zeros(sn, device=dev) for _ in range(3))
+        sg = torch.empty(sn, dtype=torch.float16, device=dev)
+        CONFIG4.fill_grad_device(1, sg)
+        crow = fa.segment_rows(seg, 512)
+        srows = fa.stats_buffer(crow[-1], dev)
+        sscr = torch.empty(fa.fa_stats_chunk_scratch(crow), device=dev)
+        srep = fa.stats_buffer(len(seg) - 1, dev)
+        so = fa.options(**CONFIG4.options())
+        sstate = {"t": 0, "rep": None}
+
+        def per_segment():
+            sstate["t"], sstate["rep"], _, _ = fa.fa_bucket_step_clipped_per_segment(
+                seg, sp, sg, sm, sv, svm, sstate["t"], so, ctl, 0.01, 512, srows, sscr, srep)
+
+        ms = timed(per_segment, args.next_rows_steps)
+        b3 = fa.bytes_per_param(2, True, False) + 2  # AMSGrad update + analysis read of the FP16 gradient
+        rows_out["f3_per_segment_clip_decoder1.1B_f16_amsgrad"] = {
+            "ms": ms, "params": sn, "segments": len(seg) - 1, "row_len": 512,
+            "bytes_per_param": b3, "achieved_gbs": b3 * sn / (ms * 1e-3) / 1e9,
+            "frac": b3 * sn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+            "params_per_s": sn / (ms * 1e-3), "min_clip_coef": sstate["rep"].clip_coef}
+        del sp, sm, sv, svm, sg, srows, sscr, srep
         torch.cuda.empty_cache()
         next_rows = rows_out
 

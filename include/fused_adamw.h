@@ -288,6 +288,64 @@ fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *
 fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
                                          fa_stats *report, void *stream);
 
+/* ---- per-parameter statistics and clipping ---------------------------------- */
+
+/* Scratch (FP32 elements) for fa_merge_gradient_stats_chunks: 3 words for each
+ * group of at most 1024 rows within a chunk.  chunk_rows (host, nchunks+1
+ * entries) are row offsets, non-decreasing from 0; their total must be a
+ * valid plan size (FA_ERR_PLAN else).  Host only. */
+fa_status fa_stats_chunk_scratch(const int64_t *chunk_rows, int32_t nchunks,
+                                 int64_t *scratch_elements);
+
+/*
+ * One report per chunk of rows ([FA-ja] "ネイティブ PyTorch ストレージと階層統計":
+ * merge_gradient_stats_chunks; chunks here are the rows of one bucket segment,
+ * i.e. one parameter).  Rows [chunk_rows[k], chunk_rows[k+1]) of rows_in merge
+ * into chunk_reports[k] (device, nchunks records; an empty chunk gives a zero
+ * record): first groups of at most 1024 rows that never span two chunks, into
+ * the caller's scratch (fa_stats_chunk_scratch elements), then one merge per
+ * chunk.  FP64 inside each kernel; a fixed order, so results are reproducible.
+ */
+fa_status fa_merge_gradient_stats_chunks(const fa_stats *rows_in, const int64_t *chunk_rows,
+                                         int32_t nchunks, float *scratch,
+                                         int64_t scratch_elements, fa_stats *chunk_reports,
+                                         void *stream);
+
+/*
+ * fa_bucket_step with one gradient multiplier per segment ([TR-zh] "FP32 主参数与
+ * 混合参数存储": Fp32MasterOptimizer's clipping follows a per-parameter rule, not
+ * a whole-model norm).  seg_grad_mult (host, nseg doubles, finite, >= 0)
+ * multiplies the unscaled gradient of segment k's elements.  nseg >= 1.  One
+ * launch per 240 segments.  Other arguments and the skip/empty rule as
+ * fa_adamw_step_inplace.
+ */
+fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                        float *p, const void *g, fa_dtype gdt, float *m,
+                                        float *v, float *vmax, uint64_t *t,
+                                        const fa_options *options, fa_step_control ctl,
+                                        const double *seg_grad_mult, int32_t *updated,
+                                        void *stream);
+
+/*
+ * The statistics-guarded step with per-parameter clipping: analyse the bucket
+ * in segment-aligned rows, merge one report per segment into seg_reports
+ * (device, nseg records), read them back (nseg * 12 bytes; synchronises),
+ * skip the whole step when any value is non-finite, else clip each segment
+ * by its own norm (coef_k = max_grad_norm / norm_k when above it, 1 otherwise;
+ * max_grad_norm <= 0: no clipping) and update with those multipliers.
+ * seg_norms / seg_coefs (host, nseg doubles, may be NULL) receive each
+ * segment's unscaled norm and coefficient; out->grad_norm is the whole
+ * gradient's norm and out->clip_coef the smallest coefficient.  Scratch is
+ * fa_stats_chunk_scratch's size for the segment rows; other arguments as
+ * fa_bucket_step_clipped.
+ */
+fa_status fa_bucket_step_clipped_per_segment(
+    const int64_t *seg_offsets, int32_t nseg, int64_t n_total, float *p, const void *g,
+    fa_dtype gdt, float *m, float *v, float *vmax, uint64_t *t, const fa_options *options,
+    fa_step_control ctl, double max_grad_norm, int32_t row_len, fa_stats *rows_buf,
+    int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
+    double *seg_norms, double *seg_coefs, fa_step_report *out, void *stream);
+
 /* Copies the 12-byte device report to host memory and waits for the stream
  * ([TR-zh]: the report is read back before any update).  Synchronises. */
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream);

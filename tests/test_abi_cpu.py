@@ -241,3 +241,13 @@ def test_writeback_validation_without_gpu(lib):
                                       ctypes.byref(upd), None)
     assert (st, t.value, upd.value) == (0, 4, 0)
     assert fa.bytes_per_param(2, False, False) + 2 == 28  # write-back adds one 16-bit store
+
+
+def test_chunk_scratch_plan():
+    assert fa.fa_stats_chunk_scratch([0, 1024, 1025, 5000]) == 3 * (1 + 1 + 4)
+    assert fa.fa_stats_chunk_scratch([0, 0, 7, 7]) == 3
+    assert fa.segment_rows([0, 5, 5, 700, 1300], 256) == [0, 1, 1, 4, 7]
+    for bad, code in (([0, 5, 3], 10), ([1, 5], 10), ([0, 0], 8), ([0, 4_194_305], 8)):
+        with pytest.raises(fa.FusedAdamWError) as e:
+            fa.fa_stats_chunk_scratch(bad)
+        assert e.value.status == code

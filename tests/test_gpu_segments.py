@@ -1,0 +1,180 @@
+"""Per-parameter statistics and clipping (chunk merge, segment multipliers) vs the oracle.
+
+The oracle needs nothing new here: a segment's statistics and its clip decision
+are the pinned whole-gradient functions applied to that segment's slice, and a
+segment's update is the pinned update with that segment's coefficient.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import amsgrad_optimizer_step_gb300 as fa
+import oracle
+from gpu_harness import gate, grad_bits_from_device, TORCH_DT
+from synthetic.configs import CONFIG4, decoder_bucket_shapes
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from amsgrad_optimizer_step_gb300 import build
+    build.build()
+
+
+def _segments(seed, count, max_len, empty_every=0):
+    rng = np.random.default_rng(seed)
+    sizes = rng.integers(1, max_len, count)
+    if empty_every:
+        sizes[::empty_every] = 0
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+
+
+def _slice_stats(lib, bits, dtype, seg, scale=1.0):
+    out = []
+    for a, b in zip(seg[:-1], seg[1:]):
+        out.append(lib.gradient_stats(bits[a:b], dtype, scale))
+    return out
+
+
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+@pytest.mark.parametrize("row_len", [256, 100])
+def test_chunk_reports_match_oracle_per_segment(gdt, row_len, oracle_lib):
+    seg = _segments(31, 300, 5000, empty_every=37)   # > 240 segments: several launches
+    n = int(seg[-1])
+    w = dataclasses.replace(CONFIG4, grad_dtype=gdt, segments=None).scaled(n)
+    g = torch.empty(n, dtype=TORCH_DT[gdt], device=DEV)
+    w.fill_grad_device(1, g)
+    bad = [int(seg[5]) + 1, int(seg[200])]   # NaN/Inf planted in two segments
+    g[bad[0]] = float("inf")
+    g[bad[1]] = float("nan")
+    bits = grad_bits_from_device(g)
+    crow = fa.segment_rows(list(seg), row_len)
+    rows_buf = fa.stats_buffer(crow[-1], DEV)
+    fa.fa_analyze_gradient(g, row_len, rows_buf, list(seg))
+    scratch = torch.empty(max(1, fa.fa_stats_chunk_scratch(crow)), device=DEV)
+    reports = fa.stats_buffer(len(seg) - 1, DEV)
+    fa.fa_merge_gradient_stats_chunks(rows_buf, crow, scratch, reports)
+    torch.cuda.synchronize()
+    host = reports.cpu()
+    sums = host[:, 0].view(torch.float32).double().numpy() + host[:, 2].view(torch.float32).double().numpy()
+    counts = host[:, 1].numpy().astype(np.int64)
+    want = _slice_stats(oracle_lib, bits, gdt, seg)
+    for k, (s, c) in enumerate(want):
+        assert counts[k] == c, (k, counts[k], c)
+        if c == 0:
+            assert abs(sums[k] - s) <= 1e-5 * s + 1e-30, (k, sums[k], s)
+    assert counts.sum() == 2
+
+
+def _bucket(n, gdt, seed):
+    w = dataclasses.replace(CONFIG4, grad_dtype=gdt, amsgrad=True, seed=seed, segments=None).scaled(n)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p)
+    return w, p
+
+
+def test_uniform_multipliers_equal_the_bucket_step_bitwise():
+    seg = _segments(32, 50, 300_000)
+    n = int(seg[-1])
+    w, p0 = _bucket(n, "f16", 33)
+    o = fa.options(**w.options())
+    g = torch.empty(n, dtype=torch.float16, device=DEV)
+    pa, pb = p0.clone(), p0.clone()
+    sa = [torch.zeros(n, device=DEV) for _ in range(3)]
+    sb = [torch.zeros(n, device=DEV) for _ in range(3)]
+    ta = tb = 0
+    for call in range(1, 4):
+        w.fill_grad_device(call, g)
+        ta, _ = fa.fa_bucket_step(list(seg), pa, g, *sa, ta, o, fa.control(2.0), 0.75)
+        tb, _ = fa.fa_bucket_step_segment_scaled(list(seg), pb, g, *sb, tb, o, fa.control(2.0),
+                                                 [0.75] * (len(seg) - 1))
+    torch.cuda.synchronize()
+    assert ta == tb == 3
+    assert torch.equal(pa, pb) and all(torch.equal(x, y) for x, y in zip(sa, sb))
+
+
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_segment_multipliers_vs_oracle(gdt, oracle_lib):
+    seg = _segments(34, 260, 3000, empty_every=50)
+    n = int(seg[-1])
+    w, p = _bucket(n, gdt, 35)
+    opts = w.options()
+    o = fa.options(**opts)
+    m, v, vm = (torch.zeros(n, device=DEV) for _ in range(3))
+    g = torch.empty(n, dtype=TORCH_DT[gdt], device=DEV)
+    rng = np.random.default_rng(36)
+    refs = [oracle.OracleAdamW(w.params_host(np.arange(a, b)), opts, lib_=oracle_lib)
+            for a, b in zip(seg[:-1], seg[1:])]
+    t = 0
+    for call in range(1, 4):
+        mult = rng.uniform(0.1, 1.0, len(seg) - 1)
+        w.fill_grad_device(call, g)
+        t, _ = fa.fa_bucket_step_segment_scaled(list(seg), p, g, m, v, vm, t, o, fa.control(), mult)
+        bits = grad_bits_from_device(g)
+        for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
+            refs[k].step(bits[a:b], gdt, clip_coef=float(mult[k]))
+    torch.cuda.synchronize()
+    ph = p.cpu().numpy()
+    vh = vm.cpu().numpy()
+    for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
+        gate(ph[a:b], refs[k].p, 1e-5, f"segment {k} p")
+        gate(vh[a:b], refs[k].state.vmax, 1e-5, f"segment {k} vmax")
+
+
+def _scaled_decoder_offsets(scale=32, layers=3):
+    sizes = [int(np.prod([max(1, d // scale) for d in shape]))
+             for _, shape in decoder_bucket_shapes()[:1 + 9 * layers]]
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+
+
+def test_per_segment_clipped_step_vs_oracle(oracle_lib):
+    seg = _scaled_decoder_offsets()
+    n = int(seg[-1])
+    w = dataclasses.replace(CONFIG4, segments=None, calls=4, inf_call=3, grad_sigma=1e-2).scaled(n)
+    opts = w.options()
+    o = fa.options(**opts)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p)
+    m, v, vm = (torch.zeros(n, device=DEV) for _ in range(3))
+    g = torch.empty(n, dtype=torch.float16, device=DEV)
+    row_len = 256
+    crow = fa.segment_rows(list(seg), row_len)
+    rows_buf = fa.stats_buffer(crow[-1], DEV)
+    scratch = torch.empty(fa.fa_stats_chunk_scratch(crow), device=DEV)
+    reports = fa.stats_buffer(len(seg) - 1, DEV)
+    refs = [oracle.OracleAdamW(w.params_host(np.arange(a, b)), opts, lib_=oracle_lib)
+            for a, b in zip(seg[:-1], seg[1:])]
+    max_norm = 0.05
+    t = 0
+    for call in range(1, w.calls + 1):
+        w.fill_grad_device(call, g)
+        before = p.clone()
+        t, rep, norms, coefs = fa.fa_bucket_step_clipped_per_segment(
+            list(seg), p, g, m, v, vm, t, o, fa.control(), max_norm, row_len, rows_buf, scratch,
+            reports)
+        bits = grad_bits_from_device(g)
+        stats = _slice_stats(oracle_lib, bits, "f16", seg)
+        any_bad = any(c > 0 for _, c in stats)
+        assert bool(rep.skipped_nonfinite) == any_bad == (call == 3)
+        if any_bad:
+            torch.cuda.synchronize()
+            assert torch.equal(p, before) and rep.updated == 0
+            for r in refs:
+                r.step(np.zeros(0, np.uint16), "f16", skip_update=True)
+            continue
+        for k, ((s, c), (a, b)) in enumerate(zip(stats, zip(seg[:-1], seg[1:]))):
+            _, norm, coef = oracle_lib.clip_decision(s, c, max_norm)
+            assert abs(norms[k] - norm) <= 1e-5 * norm + 1e-30
+            assert abs(coefs[k] - coef) <= 1e-5 * coef
+            refs[k].step(bits[a:b], "f16", clip_coef=coef)
+        assert min(coefs) < 1.0 and max(coefs) <= 1.0
+    torch.cuda.synchronize()
+    assert t == 3
+    ph = p.cpu().numpy()
+    for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
+        gate(ph[a:b], refs[k].p, 1e-5, f"segment {k}")
