@@ -21,7 +21,7 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
                    FaStepReport, FusedAdamWError, check)
 
 __all__ = [
-    "fa_abi_version", "fa_device_error", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
+    "fa_abi_version", "fa_device_error", "fa_pipeline_selftest", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
     "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback",
     "fa_adamw_step_staged", "fa_stats_plan",
     "fa_stats_rows",
@@ -101,6 +101,20 @@ def fa_device_error(clear: bool = False) -> int:
     v = ctypes.c_int32()
     check("fa_device_error", _L().fa_device_error(ctypes.byref(v), int(bool(clear))))
     return v.value
+
+
+def fa_pipeline_selftest(p, g, m, v, stream=None) -> int:
+    """Runs the bounded-wait self-test on these buffers; returns the flag (1 expected)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    flag = ctypes.c_int32()
+    check("fa_pipeline_selftest", _L().fa_pipeline_selftest(
+        n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), ctypes.byref(flag),
+        _stream(stream)))
+    return flag.value
 
 
 def fa_options_default() -> FaOptions:

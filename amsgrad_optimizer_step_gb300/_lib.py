@@ -52,6 +52,7 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [c_i32]),
     "fa_options_default": (FaOptions, []),
     "fa_device_error": (c_i32, [PI32, c_i32]),
+    "fa_pipeline_selftest": (c_i32, [c_i64, P, P, c_i32, P, P, PI32, P]),
     "fa_step_coefficients": (c_i32, [ctypes.POINTER(FaOptions), c_u64, c_f64, c_f64,
                                      ctypes.POINTER(ctypes.c_float)]),
     "fa_adamw_step": (c_i32, [c_i64, P, P, c_i32, P, P, P, c_u64, ctypes.POINTER(FaOptions),

@@ -195,6 +195,7 @@ fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt,
     a.v_out = v_out;
     a.vmax_out = o->amsgrad ? vmax_out : nullptr;
     a.p_model = model_dtype == fa::kNoModel ? nullptr : p_model;
+    a.extra_tx = 0;
     a.n = n;
     const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g,
                           a.p_out, a.m_out, a.v_out, a.vmax_out, a.p_model};
@@ -267,6 +268,53 @@ fa_status fa_device_error(int32_t *flag, int32_t clear) {
         return FA_ERR_CUDA;
     }
     *flag = v;
+    return FA_OK;
+}
+
+fa_status fa_pipeline_selftest(int64_t n, float *p, const void *g, fa_dtype gdt, float *m,
+                               float *v, int32_t *flag, void *stream) {
+    if (!flag) return FA_ERR_NULL;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n < 1) return FA_ERR_SIZE;
+    fa_options o = fa_options_default();
+    int dev = 0;
+    fa_status st;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n, p, g, gdt, m, v, nullptr, &o, dev)) != FA_OK) return st;
+    Coef c;
+    if ((st = make_coef(&o, 2, 1.0, 1.0, &c)) != FA_OK) return st;
+    fa::UpdateArgs a;
+    a.p_in = p;
+    a.m_in = m;
+    a.v_in = v;
+    a.vmax_in = nullptr;
+    a.g = g;
+    a.p_out = p;
+    a.m_out = m;
+    a.v_out = v;
+    a.vmax_out = nullptr;
+    a.p_model = nullptr;
+    a.extra_tx = 16;  // a barrier that waits for 16 bytes nobody sends
+    a.n = n;
+    const void *ptrs[] = {p, m, v, g};
+    const size_t es[] = {4, 4, 4, dtype_bytes(gdt)};
+    const int64_t head = vector_head(ptrs, es, 4, n);
+    if (head < 0) return FA_ERR_ALIGN;
+    a.head = head;
+    a.nvec = (n - head) / 8;
+    int prior = 0;
+    if (fa::update_pipeline_error(&prior, true) != cudaSuccess) return FA_ERR_CUDA;
+    bool launched = false;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fa::launch_pipeline_selftest(a, c, gdt, &launched, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (!launched) return FA_ERR_SIZE;
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    int v_flag = 0;
+    if (fa::update_pipeline_error(&v_flag, true) != cudaSuccess) return FA_ERR_CUDA;
+    *flag = v_flag;
     return FA_OK;
 }
 
@@ -725,6 +773,7 @@ fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg
         a.v_out = v + e0;
         a.vmax_out = ams ? vmax + e0 : nullptr;
         a.p_model = nullptr;
+        a.extra_tx = 0;
         a.n = e1 - e0;
         const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g};
         const size_t es[] = {4, 4, 4, 4, gb};

@@ -30,6 +30,7 @@ struct UpdateArgs {
     const void *g;
     float *p_out, *m_out, *v_out, *vmax_out;
     void *p_model;  // low-precision copy of the updated p (nullptr: none)
+    uint32_t extra_tx;  // self-test only: bytes a pipeline barrier waits for but never gets
     int64_t n;     // elements
     int64_t head;  // scalar elements before the 16-byte aligned vector body
     int64_t nvec;  // 8-element vectors in the body
@@ -37,6 +38,12 @@ struct UpdateArgs {
 
 // Enqueues one update kernel over a.n elements.  vector_ok: every pointer is
 // 16-byte aligned at element a.head.  Returns the CUDA launch status.
+// Self-test of the pipeline's bounded waits: one steady update launched with
+// a.extra_tx > 0 on the TMA path, so every wait runs out; *launched is false
+// when the tensor is too small for that path.
+cudaError_t launch_pipeline_selftest(const UpdateArgs &a, const Coef &c, fa_dtype gdt,
+                                     bool *launched, cudaStream_t stream);
+
 // Reads (and optionally clears) the flag an update kernel sets when a bounded
 // wait in its shared-memory pipeline gives up.  Waits for the device.
 cudaError_t update_pipeline_error(int *flag, bool clear);

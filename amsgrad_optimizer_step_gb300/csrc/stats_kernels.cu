@@ -362,12 +362,24 @@ __device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int
                                             int64_t hi, fa_stats *__restrict__ out) {
     __shared__ double s_sum[kThreads / 32];
     __shared__ unsigned long long s_cnt[kThreads / 32];
+    constexpr int kU = kFanIn / kThreads;  // records per thread per pass, loaded together
     double s = 0.0;
     unsigned long long c = 0;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
-        const fa_stats r = in[i];
-        s += static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
-        c += r.nonfinite;
+    for (int64_t base = lo + threadIdx.x; base < hi; base += kThreads * kU) {
+        fa_stats r[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t i = base + static_cast<int64_t>(u) * kThreads;
+            if (i < hi) r[u] = in[i];
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t i = base + static_cast<int64_t>(u) * kThreads;
+            if (i < hi) {
+                s += static_cast<double>(r[u].sum_sq) + static_cast<double>(r[u].sum_sq_lo);
+                c += r[u].nonfinite;
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {

@@ -442,7 +442,7 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c, int64_t
     auto issue_loads = [&](int s, int64_t tile) {
         unsigned char *b = smem + s * L::kStage;
         const int64_t e = a.head + tile * L::kTile;
-        mbar_expect_tx(&bars[s], kLoadBytes);
+        mbar_expect_tx(&bars[s], kLoadBytes + a.extra_tx);
         bulk_load(b + L::kP, a.p_in + e, L::kTile * 4, &bars[s]);
         bulk_load(b + L::kG, static_cast<const char *>(a.g) + e * L::kGB, L::kTile * L::kGB,
                   &bars[s]);
@@ -786,6 +786,34 @@ cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, f
         case FA_BF16: return launch_seg_gt<FA_BF16>(s, c, amsgrad, first, vector_ok, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pipeline_selftest(const UpdateArgs &a, const Coef &c, fa_dtype gdt,
+                                     bool *launched, cudaStream_t stream) {
+    *launched = false;
+#if FA_UPDATE_TMA
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    SegScaleArgs s;
+    s.a = a;
+    s.nseg = 0;
+    switch (gdt) {
+        case FA_F32:
+            return launch_tma_if_large<FA_F32, false, false, kNoModel, false>(s, c, true, dev,
+                                                                             stream, launched);
+        case FA_F16:
+            return launch_tma_if_large<FA_F16, false, false, kNoModel, false>(s, c, true, dev,
+                                                                             stream, launched);
+        case FA_BF16:
+            return launch_tma_if_large<FA_BF16, false, false, kNoModel, false>(s, c, true, dev,
+                                                                              stream, launched);
+    }
+    return cudaErrorInvalidValue;
+#else
+    (void)a; (void)c; (void)gdt; (void)stream;
+    return cudaSuccess;
+#endif
 }
 
 cudaError_t update_pipeline_error(int *flag, bool clear) {

@@ -111,6 +111,18 @@ const char *fa_status_string(fa_status status);
  * clear != 0.  Waits for the device; FA_ERR_CUDA if it cannot be read. */
 fa_status fa_device_error(int32_t *flag, int32_t clear);
 
+/* Self-test of the bounded waits above, with no fault: one steady-state update
+ * of the n-element p, m, v (device, FP32) with gradient g, launched so that
+ * every shared-memory stage waits for 16 bytes that never arrive.  Each wait
+ * gives up after its limit (about a second), the kernel drains its own
+ * copies and returns without writing p, m or v; the call waits for it and
+ * stores the flag in *flag (1 when the waits gave up, as they must), then
+ * clears it.  n must be large enough for the shared-memory path (at least two
+ * tiles per SM; FA_ERR_SIZE else) and the pointers 16-byte co-aligned
+ * (FA_ERR_ALIGN else).  Not part of the update path. */
+fa_status fa_pipeline_selftest(int64_t n, float *p, const void *g, fa_dtype gdt, float *m,
+                               float *v, int32_t *flag, void *stream);
+
 /* Defaults ([FA-ja] "この演算子を使用する理由": betas (0.9, 0.999), eps 1e-5,
  * weight_decay 1e-4, matching RUDA's AdamWConfig).  The pages state no default
  * learning rate; 1e-3 is used.  amsgrad = maximize = 0. */
