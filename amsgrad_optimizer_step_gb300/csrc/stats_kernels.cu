@@ -10,8 +10,9 @@
 // Record layout (12 bytes): {sum_sq: f32, nonfinite: u32, sum_sq_lo: f32}.
 // A row's sum of squares is accumulated in FP32 (8 values per lane, then a
 // warp shuffle tree) -- at 256 elements per row its relative error stays
-// below 1e-6.  Merges widen to FP64, add, and hand the FP64 total to the next
-// level as a (hi, lo) pair of floats, so later levels lose nothing.
+// below 1e-6.  Merges add (hi, lo) pairs as double-float values with
+// error-free FP32 transformations and hand each total to the next level as a
+// (hi, lo) pair of floats, so later levels lose nothing.
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -356,14 +357,33 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
     }
 }
 
-// One CTA reduces records [lo, hi) into *out: FP64 sums per thread, warp
-// shuffles, then shared memory; the total leaves as an FP32 (hi, lo) pair.
+// Error-free addition (Knuth's TwoSum): s + e == a + b exactly, s = fl(a + b).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Adds (bh, bl) into the double-float (h, l).
+__device__ __forceinline__ void df_add(float &h, float &l, float bh, float bl) {
+    float s, e;
+    two_sum(h, bh, s, e);
+    e += l + bl;
+    two_sum(s, e, h, l);
+}
+
+// One CTA reduces records [lo, hi) into *out.  Sums travel as double-float
+// pairs (an FP32 value and its FP32 residual, combined with error-free
+// TwoSum) through the per-thread loop and the warp shuffles, which keeps
+// every operation on the FP32 units (GB300's FP64 rate is low); only the
+// per-warp partials are added in FP64.  The total leaves as an FP32 (hi, lo)
+// pair.
 __device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int64_t lo,
                                             int64_t hi, fa_stats *__restrict__ out) {
     __shared__ double s_sum[kThreads / 32];
     __shared__ unsigned long long s_cnt[kThreads / 32];
     constexpr int kU = kFanIn / kThreads;  // records per thread per pass, loaded together
-    double s = 0.0;
+    float sh = 0.f, sl = 0.f;
     unsigned long long c = 0;
     for (int64_t base = lo + threadIdx.x; base < hi; base += kThreads * kU) {
         fa_stats r[kU];
@@ -376,19 +396,21 @@ __device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int
         for (int u = 0; u < kU; ++u) {
             const int64_t i = base + static_cast<int64_t>(u) * kThreads;
             if (i < hi) {
-                s += static_cast<double>(r[u].sum_sq) + static_cast<double>(r[u].sum_sq_lo);
+                df_add(sh, sl, r[u].sum_sq, r[u].sum_sq_lo);
                 c += r[u].nonfinite;
             }
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
+        df_add(sh, sl, oh, ol);
         c += __shfl_xor_sync(0xffffffffu, c, o);
     }
     const int w = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) {
-        s_sum[w] = s;
+        s_sum[w] = static_cast<double>(sh) + static_cast<double>(sl);
         s_cnt[w] = c;
     }
     __syncthreads();

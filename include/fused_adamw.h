@@ -267,8 +267,9 @@ fa_status fa_analyze_gradient(const void *g, fa_dtype gdt, int64_t n, int32_t ro
  * the clip policy).  Reduces ``rows`` device records to one device report, in
  * fa_stats_plan's merge kernels.  ``scratch`` is caller-owned device memory of
  * at least fa_stats_plan's scratch_elements floats (may be NULL when that is
- * 0); its contents on entry do not matter.  Sums are carried in FP64 inside
- * each kernel and passed between levels as (sum_sq, sum_sq_lo) pairs.
+ * 0); its contents on entry do not matter.  Sums are carried as double-float
+ * values (an FP32 value and its FP32 residual, added with error-free
+ * transformations) and passed between levels as (sum_sq, sum_sq_lo) pairs.
  */
 fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *scratch,
                                   int64_t scratch_elements, fa_stats *report, void *stream);
@@ -316,7 +317,8 @@ fa_status fa_stats_chunk_scratch(const int64_t *chunk_rows, int32_t nchunks,
  * into chunk_reports[k] (device, nchunks records; an empty chunk gives a zero
  * record): first groups of at most 1024 rows that never span two chunks, into
  * the caller's scratch (fa_stats_chunk_scratch elements), then one merge per
- * chunk.  FP64 inside each kernel; a fixed order, so results are reproducible.
+ * chunk.  Double-float sums as in fa_merge_gradient_stats; a fixed order, so
+ * results are reproducible.
  */
 fa_status fa_merge_gradient_stats_chunks(const fa_stats *rows_in, const int64_t *chunk_rows,
                                          int32_t nchunks, float *scratch,
