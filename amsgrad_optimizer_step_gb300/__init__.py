@@ -29,7 +29,8 @@ __all__ = [
     "fa_read_report", "fa_clip_decision", "fa_stats_chunk_scratch",
     "fa_merge_gradient_stats_chunks", "fa_bucket_step_segment_scaled",
     "fa_bucket_step_clipped_per_segment", "segment_rows",
-    "fa_clip_decide", "fa_bucket_step_clipped", "options", "control", "stats_buffer",
+    "fa_clip_decide", "fa_bucket_step_clipped", "fa_bucket_step_gated",
+    "fa_bucket_step_clipped_gated", "options", "control", "stats_buffer",
     "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
 ]
 
@@ -275,6 +276,49 @@ def fa_adamw_step_staged(p, g, m, v, vmax, t: int, opts: FaOptions, ctl: FaStepC
         ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, _ptr(delta), ctypes.byref(upd),
         _stream(stream)))
     return tt.value, bool(upd.value)
+
+
+def fa_bucket_step_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                         ctl: FaStepControl, report: torch.Tensor, max_grad_norm: float,
+                         stream=None) -> None:
+    """Enqueues the update gated on the device report; the caller advances t."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _stats_tensor("report", report)
+    seg, nseg = _segments(seg_offsets)
+    check("fa_bucket_step_gated", _L().fa_bucket_step_gated(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
+        ctypes.byref(opts), ctl, _ptr(report), max_grad_norm, _stream(stream)))
+
+
+def fa_bucket_step_clipped_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                                 ctl: FaStepControl, max_grad_norm: float, row_len: int,
+                                 rows_buf: torch.Tensor, scratch: Optional[torch.Tensor],
+                                 report: torch.Tensor, stream=None) -> tuple[int, FaStepReport]:
+    """The statistics-guarded step with the update gated on the device.  Returns (t, report)."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _stats_tensor("rows_buf", rows_buf)
+    _stats_tensor("report", report)
+    seg, nseg = _segments(seg_offsets)
+    tt = ctypes.c_uint64(t)
+    rep = FaStepReport()
+    check("fa_bucket_step_clipped_gated", _L().fa_bucket_step_clipped_gated(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
+        ctypes.byref(tt), ctypes.byref(opts), ctl, max_grad_norm, row_len, _ptr(rows_buf),
+        rows_buf.shape[0], _ptr(scratch), 0 if scratch is None else scratch.numel(),
+        _ptr(report), ctypes.byref(rep), _stream(stream)))
+    return tt.value, rep
 
 
 # ---- statistics ------------------------------------------------------------------

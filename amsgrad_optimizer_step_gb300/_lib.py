@@ -67,6 +67,12 @@ SIGNATURES = {
     "fa_adamw_step_staged": (c_i32, [c_i64, P, P, c_i32, P, P, P, PU64,
                                      ctypes.POINTER(FaOptions), FaStepControl, c_f64, P, PI32,
                                      P]),
+    "fa_bucket_step_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, c_u64,
+                                     ctypes.POINTER(FaOptions), FaStepControl, P, c_f64, P]),
+    "fa_bucket_step_clipped_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
+                                             ctypes.POINTER(FaOptions), FaStepControl, c_f64,
+                                             c_i32, P, c_i64, P, c_i64, P,
+                                             ctypes.POINTER(FaStepReport), P]),
     "fa_stats_plan": (c_i32, [c_i64, PI32, PI64]),
     "fa_stats_rows": (c_i32, [c_i64, c_i32, PI64, c_i32, PI64]),
     "fa_analyze_gradient": (c_i32, [P, c_i32, c_i64, c_i32, PI64, c_i32, P, c_i64, P]),

@@ -179,7 +179,8 @@ fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt,
                          const float *v, const float *vmax, float *p_out, float *m_out,
                          float *v_out, float *vmax_out, const fa_options *o, uint64_t t_new,
                          double scale, double grad_mult, void *stream,
-                         void *p_model = nullptr, int model_dtype = fa::kNoModel) {
+                         void *p_model = nullptr, int model_dtype = fa::kNoModel,
+                         const fa_stats *gate = nullptr, double gate_max_norm = 0.0) {
     Coef c;
     fa_status st = make_coef(o, t_new, scale, grad_mult, &c);
     if (st != FA_OK) return st;
@@ -196,6 +197,10 @@ fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt,
     a.vmax_out = o->amsgrad ? vmax_out : nullptr;
     a.p_model = model_dtype == fa::kNoModel ? nullptr : p_model;
     a.extra_tx = 0;
+    a.gate = gate;
+    a.gate_scale = scale;
+    a.gate_max_norm = gate_max_norm;
+    a.gate_sign = o->maximize ? -1.0 : 1.0;
     a.n = n;
     const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g,
                           a.p_out, a.m_out, a.v_out, a.vmax_out, a.p_model};
@@ -295,6 +300,8 @@ fa_status fa_pipeline_selftest(int64_t n, float *p, const void *g, fa_dtype gdt,
     a.vmax_out = nullptr;
     a.p_model = nullptr;
     a.extra_tx = 16;  // a barrier that waits for 16 bytes nobody sends
+    a.gate = nullptr;
+    a.gate_scale = a.gate_max_norm = a.gate_sign = 0.0;
     a.n = n;
     const void *ptrs[] = {p, m, v, g};
     const size_t es[] = {4, 4, 4, dtype_bytes(gdt)};
@@ -514,6 +521,148 @@ fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt,
         return FA_ERR_CUDA;
     *t += 1;
     *updated = 1;
+    return FA_OK;
+}
+
+fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                               float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                               float *vmax, uint64_t t, const fa_options *options,
+                               fa_step_control ctl, const fa_stats *report_dev,
+                               double max_grad_norm, void *stream) {
+    fa_status st;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n_total < 0) return FA_ERR_SIZE;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (n_total == 0 || ctl.skip_update) return FA_OK;
+    if (t == UINT64_MAX) return FA_ERR_OPTION;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
+    const size_t b = static_cast<size_t>(n_total) * 4;
+    const Range rep{report_dev, 12};
+    const Range others[] = {{p, b}, {m, b}, {v, b}, {options->amsgrad ? vmax : nullptr, b}};
+    for (const Range &r : others)
+        if (overlap(rep, r)) return FA_ERR_ALIAS;
+    return enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, t + 1,
+                          ctl.gradient_scale, 1.0, stream, nullptr, fa::kNoModel, report_dev,
+                          max_grad_norm);
+}
+
+namespace {
+
+// Per host thread: a pinned staging record for report read-backs that must not
+// block the stream, and an event marking its arrival (per device).
+struct ReadbackSlot {
+    fa_stats *pinned = nullptr;
+    cudaEvent_t event[64] = {};
+};
+
+fa_status readback_slot(int dev, ReadbackSlot **out) {
+    thread_local ReadbackSlot slot;
+    if (dev < 0 || dev >= 64) return FA_ERR_POINTER;
+    if (!slot.pinned) {
+        void *ptr = nullptr;
+        if (cudaHostAlloc(&ptr, 64, cudaHostAllocPortable) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_CUDA;
+        }
+        slot.pinned = static_cast<fa_stats *>(ptr);
+    }
+    if (!slot.event[dev] &&
+        cudaEventCreateWithFlags(&slot.event[dev], cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    *out = &slot;
+    return FA_OK;
+}
+
+}  // namespace
+
+fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                       float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                                       float *vmax, uint64_t *t, const fa_options *options,
+                                       fa_step_control ctl, double max_grad_norm,
+                                       int32_t row_len, fa_stats *rows_buf,
+                                       int64_t rows_capacity, float *scratch,
+                                       int64_t scratch_elements, fa_stats *report_dev,
+                                       fa_step_report *out, void *stream) {
+    fa_status st;
+    if (!t || !out) return FA_ERR_NULL;
+    if ((st = check_options(options)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if (n_total < 0) return FA_ERR_SIZE;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    fa_step_report rep{0, 0, 0, 0.0, 1.0};
+    if (n_total == 0 || ctl.skip_update) {
+        *out = rep;
+        return FA_OK;
+    }
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    int64_t rows = 0;
+    if ((st = fa_stats_rows(n_total, row_len, seg_offsets, nseg, &rows)) != FA_OK) return st;
+    int32_t kernels = 0;
+    int64_t need = 0;
+    if ((st = fa_stats_plan(rows, &kernels, &need)) != FA_OK) return st;
+    if (rows_capacity < rows || scratch_elements < need) return FA_ERR_SIZE;
+    const size_t b = static_cast<size_t>(n_total) * 4;
+    const Range r[] = {{p, b}, {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b},
+                       {v, b}, {options->amsgrad ? vmax : nullptr, b},
+                       {rows_buf, static_cast<size_t>(rows) * 12},
+                       {scratch, static_cast<size_t>(need) * 4}, {report_dev, 12}};
+    if (any_overlap(r, 8)) return FA_ERR_ALIAS;
+    ReadbackSlot *slot = nullptr;
+    if ((st = readback_slot(dev, &slot)) != FA_OK) return st;
+
+    if ((st = fa_analyze_gradient(g, gdt, n_total, row_len, seg_offsets, nseg, rows_buf,
+                                  rows_capacity, stream)) != FA_OK)
+        return st;
+    if ((st = fa_merge_gradient_stats(rows_buf, rows, scratch, scratch_elements, report_dev,
+                                      stream)) != FA_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(slot->pinned, report_dev, sizeof(fa_stats), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaEventRecord(slot->event[dev], s) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    // the update follows in stream order and decides on the device
+    if ((st = enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, *t + 1,
+                             ctl.gradient_scale, 1.0, stream, nullptr, fa::kNoModel, report_dev,
+                             max_grad_norm)) != FA_OK)
+        return st;
+    // meanwhile the host reads the same report and takes the same decision
+    if (cudaEventSynchronize(slot->event[dev]) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    const fa_stats h = *slot->pinned;
+    int32_t skip = 0;
+    double norm = 0, coef = 1;
+    const double sum = static_cast<double>(h.sum_sq) + static_cast<double>(h.sum_sq_lo);
+    if ((st = fa_clip_decision(sum, h.nonfinite, ctl.gradient_scale, max_grad_norm, &skip, &norm,
+                               &coef)) != FA_OK)
+        return st;
+    rep.nonfinite = h.nonfinite;
+    rep.grad_norm = norm;
+    rep.clip_coef = coef;
+    if (skip) {
+        rep.skipped_nonfinite = 1;
+    } else {
+        *t += 1;
+        rep.updated = 1;
+    }
+    *out = rep;
     return FA_OK;
 }
 
@@ -774,6 +923,8 @@ fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg
         a.vmax_out = ams ? vmax + e0 : nullptr;
         a.p_model = nullptr;
         a.extra_tx = 0;
+        a.gate = nullptr;
+        a.gate_scale = a.gate_max_norm = a.gate_sign = 0.0;
         a.n = e1 - e0;
         const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g};
         const size_t es[] = {4, 4, 4, 4, gb};

@@ -31,6 +31,10 @@ struct UpdateArgs {
     float *p_out, *m_out, *v_out, *vmax_out;
     void *p_model;  // low-precision copy of the updated p (nullptr: none)
     uint32_t extra_tx;  // self-test only: bytes a pipeline barrier waits for but never gets
+    // Device-side decision (nullptr: none): skip when the report counts a
+    // non-finite value, else gmul = sign * coef / scale with the host's formula.
+    const fa_stats *gate;
+    double gate_scale, gate_max_norm, gate_sign;
     int64_t n;     // elements
     int64_t head;  // scalar elements before the 16-byte aligned vector body
     int64_t nvec;  // 8-element vectors in the body

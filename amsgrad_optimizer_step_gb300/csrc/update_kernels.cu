@@ -160,6 +160,20 @@ __device__ __forceinline__ void adamw_element(const Coef &c, float x, float &p, 
     v = v_new;
 }
 
+// The host's skip / clip decision, taken on the device from the same report
+// with the same FP64 operations in the same order (so the multiplier is
+// bit-identical): false = skip the update.
+__device__ __forceinline__ bool gate_decision(const UpdateArgs &a, float *gmul) {
+    const fa_stats r = *a.gate;
+    if (r.nonfinite > 0) return false;
+    const double sum = static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
+    const double norm = sqrt(sum) / a.gate_scale;
+    double coef = 1.0;
+    if (a.gate_max_norm > 0 && norm > a.gate_max_norm) coef = a.gate_max_norm / norm;
+    *gmul = static_cast<float>(a.gate_sign * coef / a.gate_scale);
+    return true;
+}
+
 __device__ __forceinline__ void load8f(const float *base, int64_t i, float (&x)[kVec]) {
     const float4 *q = reinterpret_cast<const float4 *>(base + i);
     float4 a = ld16(q);
@@ -236,7 +250,9 @@ __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &
 // accesses to each stream are contiguous.
 template <int GT, bool AMS, bool FIRST, int UNROLL, int MD>
 __global__ void __launch_bounds__(kUThreads)
-update_vec_kernel(const UpdateArgs a, const Coef c) {
+update_vec_kernel(const UpdateArgs a, const Coef c0) {
+    Coef c = c0;
+    if (a.gate && !gate_decision(a, &c.gmul)) return;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kUThreads + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kUThreads * UNROLL;
 
@@ -284,7 +300,9 @@ update_vec_kernel(const UpdateArgs a, const Coef c) {
 // Every element one at a time (pointers not co-aligned to 16 bytes).
 template <int GT, bool AMS, bool FIRST, int MD>
 __global__ void __launch_bounds__(kThreads)
-update_scalar_kernel(const UpdateArgs a, const Coef c) {
+update_scalar_kernel(const UpdateArgs a, const Coef c0) {
+    Coef c = c0;
+    if (a.gate && !gate_decision(a, &c.gmul)) return;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < a.n;
          i += stride)
@@ -424,8 +442,11 @@ struct TmaLayout {
 // otherwise s.nseg is 0 and c.gmul applies to every element.
 template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c, int64_t ntiles) {
+update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_t ntiles) {
     const UpdateArgs &a = sa.a;
+    Coef c = c0;
+    // a skipped step returns before any copy is issued (every thread decides alike)
+    if (a.gate && !gate_decision(a, &c.gmul)) return;
     using L = TmaLayout<GT, AMS, MD>;
     constexpr int S = L::kStages;
     constexpr uint32_t kLoadBytes =

@@ -254,16 +254,42 @@ def run_ours(args):
     launches = {"n": 0}
     merge_kernels, _ = fa.fa_stats_plan(rows)
 
+    rep_pinned = torch.empty((1, 3), dtype=torch.int32).pin_memory()
+    rep_arrived = torch.cuda.Event()
+
     def step(ev=None):
+        """analyse -> merge -> 12-byte report -> decision -> update.
+
+        One GPU: the update is gated on the device by the same report, so it
+        follows the merge without a host round trip; the host reads the report
+        (pinned copy) meanwhile and advances t unless the step was skipped.
+        Several ranks: every rank reads its report, the ranks exchange their
+        totals and take one decision on the host before updating."""
         if ev: ev[0].record(stream)
         fa.fa_analyze_gradient(g, row_len, rows_buf)
         fa.fa_merge_gradient_stats(rows_buf, rows, scratch, report)
         if ev: ev[1].record(stream)
+        launches["n"] += 1 + merge_kernels
+        if world == 1:
+            rep_pinned.copy_(report, non_blocking=True)
+            rep_arrived.record(stream)
+            if ev: ev[2].record(stream)
+            fa.fa_bucket_step_gated(None, p, g, m, v, None, state["t"], opts, ctl, report,
+                                    w.max_grad_norm)
+            launches["n"] += 1
+            if ev: ev[3].record(stream)
+            rep_arrived.synchronize()
+            h = rep_pinned[0]
+            sum_sq = float(h[0:1].view(torch.float32)) + float(h[2:3].view(torch.float32))
+            skip, norm, _ = fa.fa_clip_decision(sum_sq, int(h[1]), w.gradient_scale,
+                                                w.max_grad_norm)
+            if not skip:
+                state["t"] += 1
+            return norm
         rep = fa.fa_read_report(report)
         skip, norm, coef = sharded.global_clip_decision(rep, w.gradient_scale, w.max_grad_norm,
                                                         device=dev)
         if ev: ev[2].record(stream)
-        launches["n"] += 1 + merge_kernels
         if not skip:
             state["t"], _ = fa.fa_bucket_step(None, p, g, m, v, None, state["t"], opts, ctl, coef)
             launches["n"] += 1
@@ -342,9 +368,10 @@ def run_ours(args):
                     state["t"], _ = fa.fa_bucket_step(None, p, gb, m, v, None, state["t"], opts,
                                                       ctl, coef)
             else:
-                state["t"], _ = fa.fa_bucket_step_clipped(None, p, gb, m, v, None, state["t"],
-                                                          opts, ctl, w.max_grad_norm, row_len,
-                                                          rows_buf, scratch, report)
+                state["t"], _ = fa.fa_bucket_step_clipped_gated(None, p, gb, m, v, None,
+                                                                state["t"], opts, ctl,
+                                                                w.max_grad_norm, row_len,
+                                                                rows_buf, scratch, report)
 
         # the host-to-device link on its own (same buffer, same stream), for reading e2e
         ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -406,7 +433,8 @@ def run_ours(args):
                "host_step_ms_max": max(host_step),
                "what": "pinned-host BF16 gradient copied in every step (side stream, double "
                        "buffered), then the C-ABI statistics-guarded step (analyse, merge, "
-                       "12-byte report read back, decide, update); wall clock"}
+                       "12-byte report read back, update gated on the same decision); "
+                       "wall clock"}
 
     # Next-row measurements on the same resident workload (update kernels only,
     # CUDA events per launch): the plain update and the fused low-precision

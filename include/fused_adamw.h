@@ -19,9 +19,13 @@
  *     failure discard them.
  *   - Validation happens before anything is enqueued or written; on any
  *     error no output (host or device) is modified ([FA-ja] "低レベルの使用").
- *   - The library never allocates device memory and keeps no mutable global
- *     state: buffers (outputs, row statistics, scratch, report) belong to the
- *     caller.
+ *   - The library never allocates device memory: buffers (outputs, row
+ *     statistics, scratch, report) belong to the caller.  Its only state is
+ *     caches of device properties, a device flag for the update pipeline's
+ *     bounded waits (fa_device_error), one fixed merge scratch array
+ *     (fa_merge_gradient_stats_static) and, per host thread that calls
+ *     fa_bucket_step_clipped_gated, a 64-byte pinned host staging record and
+ *     one event per device, allocated on first use and kept until exit.
  *   - Parameters and moments are dense contiguous FP32; gradients are dense
  *     contiguous FP32, FP16 or BF16 of the same element count
  *     ([FA-zh] "增加的实际能力").  Strides, broadcasts and sparse gradients
@@ -229,6 +233,45 @@ fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt,
                                float *v, float *vmax, uint64_t *t, const fa_options *options,
                                fa_step_control ctl, double grad_mult, float *delta,
                                int32_t *updated, void *stream);
+
+/*
+ * fa_bucket_step whose skip / clip decision is taken on the device: the
+ * update kernel reads ``report_dev`` (as produced by fa_merge_gradient_stats,
+ * earlier on the same stream), skips when it counts a non-finite value, and
+ * otherwise multiplies the unscaled gradient by the same coefficient that
+ * fa_clip_decision computes on the host (max_grad_norm <= 0: no clip) --
+ * the same FP64 operations in the same order, so the results are
+ * bit-identical to reading the report back and calling fa_bucket_step.
+ * ``t`` is the completed step count; the update uses step t+1 and this call
+ * does not change any count: the caller reads the report and advances its
+ * count by one unless the report shows a non-finite value.  Nothing is
+ * launched for n_total == 0 or ctl.skip_update.
+ */
+fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                               float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                               float *vmax, uint64_t t, const fa_options *options,
+                               fa_step_control ctl, const fa_stats *report_dev,
+                               double max_grad_norm, void *stream);
+
+/*
+ * fa_bucket_step_clipped with the update gated on the device: the analysis
+ * and merge are enqueued, then the 12-byte report's copy into pinned host
+ * memory, then the gated update, so the update does not wait for the host.
+ * The host waits only for the report, takes the same decision from it
+ * ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": the report is read back and a
+ * non-finite gradient skips the whole step) and advances *t unless the step
+ * was skipped.  Returns once the report is read; the update may still run
+ * (FA_OK means enqueued).  Results are bit-identical to
+ * fa_bucket_step_clipped.  Arguments as fa_bucket_step_clipped.
+ */
+fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
+                                       float *p, const void *g, fa_dtype gdt, float *m, float *v,
+                                       float *vmax, uint64_t *t, const fa_options *options,
+                                       fa_step_control ctl, double max_grad_norm,
+                                       int32_t row_len, fa_stats *rows_buf,
+                                       int64_t rows_capacity, float *scratch,
+                                       int64_t scratch_elements, fa_stats *report_dev,
+                                       fa_step_report *out, void *stream);
 
 /* ---- gradient statistics -------------------------------------------------- */
 

@@ -559,3 +559,55 @@ def test_staged_rejects_unaligned_views():
 def test_update_pipeline_never_gave_up():
     """After everything above, no bounded wait in the shared-memory pipeline gave up."""
     assert fa.fa_device_error() == 0
+
+
+# ---- device-gated update ---------------------------------------------------------------
+
+@pytest.mark.parametrize("max_norm", [1.0, 0.0, 1e6])
+def test_gated_step_equals_host_decided_step_bitwise(max_norm):
+    """Same report, same FP64 decision on the device: bit-identical to reading the
+    report back first, including the skipped call with a planted +Inf."""
+    n = 256 * 5000 + 77
+    w = CONFIG5.scaled(n, calls=4, inf_call=2)
+    dev_state = []
+    for gated in (False, True):
+        p = torch.empty(n, device=DEV)
+        w.fill_params_device(p)
+        m, v = torch.empty_like(p), torch.empty_like(p)
+        g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+        rows = fa.fa_stats_rows(n, 256)
+        rb, sc, rep = fa.stats_buffer(rows, DEV), fa.scratch_buffer(rows, DEV), fa.stats_buffer(1, DEV)
+        t = 0
+        reports = []
+        for call in range(1, w.calls + 1):
+            w.fill_grad_device(call, g)
+            fn = fa.fa_bucket_step_clipped_gated if gated else fa.fa_bucket_step_clipped
+            t, r = fn(None, p, g, m, v, None, t, fa.options(**w.options()), fa.control(),
+                      max_norm, 256, rb, sc, rep)
+            reports.append((r.updated, r.skipped_nonfinite, r.nonfinite, repr(r.grad_norm),
+                            repr(r.clip_coef)))  # repr: a skipped step's norm is NaN
+        torch.cuda.synchronize()
+        dev_state.append((t, reports, p.clone(), m.clone(), v.clone()))
+    (ta, ra, *sa), (tb, rb_, *sb) = dev_state
+    assert ta == tb == 3 and ra == rb_
+    assert ra[1][1] == 1  # the +Inf call was skipped
+    for x, y in zip(sa, sb):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_gated_update_skips_on_non_finite_report():
+    n = 4_000_000
+    p = torch.randn(n, device=DEV)
+    m, v = torch.randn(n, device=DEV), torch.rand(n, device=DEV)
+    g = torch.randn(n, device=DEV).to(torch.bfloat16)
+    snap = [x.clone() for x in (p, m, v)]
+    report = torch.zeros((1, 3), dtype=torch.int32, device=DEV)
+    report[0, 1] = 2  # two non-finite values
+    fa.fa_bucket_step_gated(None, p, g, m, v, None, 4, fa.options(), fa.control(), report, 1.0)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip((p, m, v), snap))
+    report[0, 1] = 0
+    report[0, 0] = torch.tensor([4.0], dtype=torch.float32).view(torch.int32)
+    fa.fa_bucket_step_gated(None, p, g, m, v, None, 4, fa.options(), fa.control(), report, 1.0)
+    torch.cuda.synchronize()
+    assert not torch.equal(p, snap[0])
