@@ -315,8 +315,8 @@ update_scalar_kernel(const UpdateArgs a, const Coef c0) {
 // follows a per-parameter rule, not a whole-model norm): the bucket update with
 // the gradient multiplier of the segment each element belongs to, from a
 // segment table in kernel parameters.  Register-staged 8-element vectors; a
-// vector inside one segment takes one lookup, a vector that straddles a
-// boundary looks up each element.
+// thread's vectors only move forward, so its segment index follows by a forward
+// scan; a vector that straddles a boundary looks up each element.
 __device__ __forceinline__ int find_seg_in(const SegScaleArgs &s, int64_t e, int lo, int hi) {
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -491,6 +491,10 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
 
     bool failed = false;
     int64_t k = 0;
+    // segment of the current tile's first element: a CTA's tiles only move forward,
+    // so the index advances by a scan whose total length over the launch is at most
+    // the number of segments
+    int k_lo = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
         const int s = static_cast<int>(k % S);
         const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
@@ -502,12 +506,15 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
         if (tid == 0) consumed[s] = issued[s];
 
         unsigned char *b = smem + s * L::kStage;
-        // segments of this tile's first and last element (warp-uniform searches)
-        int k_lo = 0, k_hi = 0;
+        // segments of this tile's first and last element (warp-uniform scans)
+        int k_hi = 0;
+        float seg_gmul = 0.f;
         if (SEG) {
             const int64_t t0 = a.head + tile * L::kTile;
-            k_lo = find_seg(sa, t0);
-            k_hi = find_seg_in(sa, t0 + L::kTile - 1, k_lo, sa.nseg - 1);
+            while (k_lo + 1 < sa.nseg && sa.seg_start[k_lo + 1] <= t0) ++k_lo;
+            k_hi = k_lo;
+            while (k_hi + 1 < sa.nseg && sa.seg_start[k_hi + 1] < t0 + L::kTile) ++k_hi;
+            seg_gmul = sa.gmul[k_lo];
         }
 #pragma unroll
         for (int h = 0; h < L::kChunks; ++h) {
@@ -545,7 +552,7 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
             if (SEG) {
                 Coef cc = c;
                 if (k_lo == k_hi) {  // the whole tile lies in one segment
-                    cc.gmul = sa.gmul[k_lo];
+                    cc.gmul = seg_gmul;
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
@@ -661,6 +668,7 @@ update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
     const UpdateArgs &a = s.a;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    int k = 0;  // segment of e; e only grows, so a forward scan finds it
     for (int64_t vi = tid; vi < a.nvec; vi += stride) {
         const int64_t e = a.head + vi * kVec;
         float x[kVec], p[kVec], m[kVec], v[kVec], vm[kVec];
@@ -671,7 +679,7 @@ update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
             load8f(a.v_in, e, v);
             if (AMS) load8f(a.vmax_in, e, vm);
         }
-        const int k = find_seg(s, e);
+        while (k + 1 < s.nseg && s.seg_start[k + 1] <= e) ++k;
         Coef cc = c;
         if (e + kVec <= s.seg_start[k + 1]) {
             cc.gmul = s.gmul[k];
@@ -680,7 +688,7 @@ update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
         } else {
 #pragma unroll
             for (int q = 0; q < kVec; ++q) {
-                cc.gmul = s.gmul[find_seg(s, e + q)];
+                cc.gmul = s.gmul[find_seg_in(s, e + q, k, s.nseg - 1)];
                 adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
             }
         }

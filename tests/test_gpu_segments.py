@@ -126,6 +126,42 @@ def test_segment_multipliers_vs_oracle(gdt, oracle_lib):
         gate(vh[a:b], refs[k].state.vmax, 1e-5, f"segment {k} vmax")
 
 
+@pytest.mark.parametrize("gdt", ["f16", "bf16"])
+def test_segment_multipliers_mixed_sizes_vs_oracle(gdt, oracle_lib):
+    """Large segments between runs of tiny and empty ones, several million elements:
+    steady steps take the shared-memory pipeline, whose tiles span up to dozens of
+    segments and whose per-CTA segment index has to skip whole runs between tiles."""
+    rng = np.random.default_rng(37)
+    sizes = rng.integers(0, 3000, 230)
+    sizes[::11] = rng.integers(150_000, 450_000, len(sizes[::11]))
+    sizes[3::17] = 0
+    seg = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    n = int(seg[-1])
+    assert n > 2 * 152 * 4096
+    w, p = _bucket(n, gdt, 38)
+    opts = w.options()
+    o = fa.options(**opts)
+    m, v, vm = (torch.zeros(n, device=DEV) for _ in range(3))
+    g = torch.empty(n, dtype=TORCH_DT[gdt], device=DEV)
+    refs = [oracle.OracleAdamW(w.params_host(np.arange(a, b)), opts, lib_=oracle_lib)
+            for a, b in zip(seg[:-1], seg[1:])]
+    t = 0
+    for call in range(1, 4):
+        mult = rng.uniform(0.1, 1.0, len(seg) - 1)
+        w.fill_grad_device(call, g)
+        t, _ = fa.fa_bucket_step_segment_scaled(list(seg), p, g, m, v, vm, t, o, fa.control(), mult)
+        bits = grad_bits_from_device(g)
+        for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
+            refs[k].step(bits[a:b], gdt, clip_coef=float(mult[k]))
+    torch.cuda.synchronize()
+    assert t == 3
+    ph, mh, vh = p.cpu().numpy(), m.cpu().numpy(), vm.cpu().numpy()
+    for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
+        gate(ph[a:b], refs[k].p, 1e-5, f"segment {k} p")
+        gate(mh[a:b], refs[k].state.m, 1e-5, f"segment {k} m")
+        gate(vh[a:b], refs[k].state.vmax, 1e-5, f"segment {k} vmax")
+
+
 def _scaled_decoder_offsets(scale=32, layers=3):
     sizes = [int(np.prod([max(1, d // scale) for d in shape]))
              for _, shape in decoder_bucket_shapes()[:1 + 9 * layers]]
