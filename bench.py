@@ -182,15 +182,113 @@ def oracle_steps(w, sample: int, steps: int, warmup: int):
     return statistics.median(times[warmup:]), 1
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_rank(conn, w, lo, hi):
+    """One host core of the all-cores oracle run: it holds elements [lo, hi) of the
+    workload and runs the oracle's step on them, statistics first, then the update
+    with the decision the parent sends back."""
+    import numpy as np
+    import oracle
+    lib = oracle.lib()
+    idx = np.arange(lo, hi)
+    grads = [w.grad_host(c, idx) for c in (1, 2)]
+    o = oracle.OracleAdamW(w.params_host(idx), w.options(), storage="f32", lib_=lib)
+    conn.send("ready")
+    while True:
+        k = conn.recv()
+        if k is None:
+            break
+        g = grads[k % 2]
+        conn.send(lib.gradient_stats(g, "bf16", w.gradient_scale))
+        skip, coef = conn.recv()
+        o.step(g, "bf16", w.gradient_scale, skip_update=skip, clip_coef=coef)
+        conn.send(True)
+    conn.close()
+
+
+def oracle_steps_all_cores(w, per_core: int, steps: int, warmup: int, cores: int):
+    """The oracle on every host core, static contiguous chunks of ``per_core``
+    elements, one process each (spawned: this may run after CUDA is initialised).
+    A step is: every chunk's statistics, their sum and the decision in the parent,
+    every chunk's update.  Returns seconds per step (median)."""
+    import math
+    import multiprocessing as mp
+    import oracle
+    lib = oracle.lib()
+    ctx = mp.get_context("spawn")
+    pipes, procs = [], []
+    try:
+        for r in range(cores):
+            a, b = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_rank, args=(b, w, r * per_core, (r + 1) * per_core),
+                             daemon=True)
+            pr.start()
+            pipes.append(a)
+            procs.append(pr)
+        for a in pipes:
+            if not a.poll(300):
+                raise RuntimeError("an oracle worker did not start")
+            a.recv()
+        times = []
+        for k in range(warmup + steps):
+            t0 = time.perf_counter()
+            for a in pipes:
+                a.send(k)
+            parts = [a.recv() for a in pipes]
+            s = math.fsum(x[0] for x in parts)
+            c = sum(int(x[1]) for x in parts)
+            skip, _, coef = lib.clip_decision(s, c, w.max_grad_norm)
+            for a in pipes:
+                a.send((skip, coef))
+            for a in pipes:
+                a.recv()
+            times.append(time.perf_counter() - t0)
+        return statistics.median(times[warmup:])
+    finally:
+        for a in pipes:
+            try:
+                a.send(None)
+            except Exception:
+                pass
+        for pr in procs:
+            pr.join(timeout=10)
+            if pr.is_alive():
+                pr.kill()
+
+
 def cpu_baseline(w, target_s=12.0):
     sample = 1 << 22
-    sec, cores = oracle_steps(w, sample, steps=1, warmup=0)
-    steps = max(2, int(target_s / max(sec, 1e-3)))
-    sec, cores = oracle_steps(w, sample, steps=steps, warmup=1)
-    return {"value": sample / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{sample} elements of the {w.name} recipe (BF16 gradients, FP32 state), "
-                      f"{steps} full steps (global stats + decision + update), single-threaded "
-                      "FP64 C loop, median step"}
+    sec, _ = oracle_steps(w, sample, steps=1, warmup=0)
+    steps = max(2, int(0.4 * target_s / max(sec, 1e-3)))
+    sec, _ = oracle_steps(w, sample, steps=steps, warmup=1)
+    single = sample / sec
+    cores = host_cores()
+    per_core = 1 << 21
+    out = {"value": single, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "single_core_value": single,
+           "sample": f"{sample} elements of the {w.name} recipe (BF16 gradients, FP32 state), "
+                     f"{steps} full steps (global stats + decision + update), single-threaded "
+                     "FP64 C loop, median step"}
+    if cores > 1:
+        try:
+            msteps = max(2, int(0.4 * target_s / max(sec * per_core / sample, 1e-3)))
+            secm = oracle_steps_all_cores(w, per_core, msteps, 2, cores)
+        except Exception as e:  # the single-core figure stands alone
+            out["all_cores_error"] = str(e)[:200]
+            return out
+        out.update({"value": cores * per_core / secm, "cores": cores,
+                    "sample": f"{cores} x {per_core} elements of the {w.name} recipe (BF16 "
+                              f"gradients, FP32 state), one process per host core on a static "
+                              f"chunk, {msteps} full steps (chunk statistics, summed decision, "
+                              f"chunk updates), FP64 C loop, median step; single-threaded on "
+                              f"{sample} elements: {single:.4g} params/s"})
+    return out
 
 
 def run_reference(args):
@@ -198,8 +296,16 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = workload(args.n)
-    sample = 1 << 22
-    sec, cores = oracle_steps(w, sample, steps=args.steps, warmup=args.warmup)
+    cores = host_cores()
+    if cores > 1:
+        sample = cores * (1 << 21)
+        sec = oracle_steps_all_cores(w, 1 << 21, args.steps, args.warmup, cores)
+        what = (f"{cores} x {1 << 21} elements per step of the {w.name} recipe, one process "
+                "per host core on a static chunk")
+    else:
+        sample = 1 << 22
+        sec, cores = oracle_steps(w, sample, steps=args.steps, warmup=args.warmup)
+        what = f"{sample} elements per step of the {w.name} recipe, single-threaded"
     value = sample / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -207,7 +313,7 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{sample} elements per step of the {w.name} recipe"},
+                             "sample": what},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -332,6 +438,7 @@ def run_ours(args):
 
     stats_ms = [e[0].elapsed_time(e[1]) for e in evs]
     update_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_each = [e[0].elapsed_time(e[3]) for e in evs]
     if world > 1:
         tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -467,6 +574,10 @@ def run_ours(args):
         def plain():
             state["t"], _ = fa.fa_bucket_step(None, p, g, m, v, None, state["t"], opts, ctl, 1.0)
 
+        def first():
+            # t = 0: the first-step kernel (moments written, not read); t is not kept
+            fa.fa_bucket_step(None, p, g, m, v, None, 0, opts, ctl, 1.0)
+
         def writeback():
             state["t"], _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, state["t"], opts,
                                                         ctl, p_model, 1.0)
@@ -474,6 +585,7 @@ def run_ours(args):
         peak, peak_kind = measured_peaks()
         rows_out = {}
         for name, fn, bpp_k in (("update_only", plain, fa.bytes_per_param(2, False, False)),
+                                ("first_step", first, fa.bytes_per_param(2, False, True)),
                                 ("f1_writeback_bf16", writeback,
                                  fa.bytes_per_param(2, False, False) + 2)):
             ms = timed(fn, args.next_rows_steps)
@@ -511,6 +623,30 @@ def run_ours(args):
                 "staged_gbs": sb * n / (t_s * 1e-3) / 1e9, "speedup": t_s / t_f,
                 "byte_model_ratio": sb / fb, "kernels": {"fused": 1, "staged": 5 if ams else 4}}
         del g32, delta, vmax
+
+        # the 124,439,808-parameter in-place BF16 workload (AdamW, wd 0.01, 1 % of the
+        # gradients x100): its own buffers, steady steps
+        from synthetic.configs import CONFIG3
+        n3 = CONFIG3.n
+        p3 = torch.empty(n3, device=dev)
+        CONFIG3.fill_params_device(p3)
+        m3, v3 = torch.zeros_like(p3), torch.zeros_like(p3)
+        g3 = torch.empty(n3, dtype=torch.bfloat16, device=dev)
+        CONFIG3.fill_grad_device(1, g3)
+        o3 = fa.options(**CONFIG3.options())
+        s3 = {"t": 0}
+
+        def inplace3():
+            s3["t"], _ = fa.fa_adamw_step_inplace(p3, g3, m3, v3, None, s3["t"], o3, ctl)
+
+        ms = timed(inplace3, args.next_rows_steps)
+        b = fa.bytes_per_param(2, False, False)
+        rows_out["inplace_124M_bf16_adamw"] = {
+            "ms": ms, "params": n3, "bytes_per_param": b,
+            "achieved_gbs": b * n3 / (ms * 1e-3) / 1e9,
+            "frac": b * n3 / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+            "params_per_s": n3 / (ms * 1e-3)}
+        del p3, m3, v3, g3
 
         # f4: the torch.optim-style wrapper on the decoder-shaped 1.196e9-parameter
         # model (199 FP32 tensors packed into one bucket), global clip 1.0: each
@@ -561,6 +697,23 @@ def run_ours(args):
             "bytes_per_param": b3, "achieved_gbs": b3 * sn / (ms * 1e-3) / 1e9,
             "frac": b3 * sn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
             "params_per_s": sn / (ms * 1e-3), "min_clip_coef": sstate["rep"].clip_coef}
+        # the same bucket without statistics (AMSGrad, FP16 gradients, one launch over
+        # 199 tensors), maximize off and on
+        from synthetic.configs import CONFIG4_MAX
+        for tag, cfg in (("", CONFIG4), ("_maximize", CONFIG4_MAX)):
+            ob = fa.options(**cfg.options())
+
+            def bucket():
+                sstate["t"], _ = fa.fa_bucket_step(seg, sp, sg, sm, sv, svm, sstate["t"], ob,
+                                                   ctl, 1.0)
+
+            ms = timed(bucket, args.next_rows_steps)
+            b = fa.bytes_per_param(2, True, False)
+            rows_out["bucket_decoder1.1B_f16_amsgrad" + tag] = {
+                "ms": ms, "params": sn, "tensors": len(seg) - 1, "bytes_per_param": b,
+                "achieved_gbs": b * sn / (ms * 1e-3) / 1e9,
+                "frac": b * sn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+                "params_per_s": sn / (ms * 1e-3)}
         del sp, sm, sv, svm, sg, srows, sscr, srep
         torch.cuda.empty_cache()
         next_rows = rows_out
@@ -585,7 +738,10 @@ def run_ours(args):
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "bytes_per_param": bpp, "traffic": update_kernel_traffic(n),
-                         "kernel_ms_median": upd_ms, "kernel_ms_min": min(update_ms)},
+                         "kernel_ms_median": upd_ms, "kernel_ms_min": min(update_ms),
+                         "kernel_ms_max": max(update_ms)},
+            "step_ms": {"median": statistics.median(step_each), "min": min(step_each),
+                        "max": max(step_each), "samples": len(step_each)},
             "stats_path": {"ms_median": st_ms, "analyze_bytes": n * 2 + rows * 12,
                            "achieved_gbs": (n * 2 + rows * 12) / (st_ms * 1e-3) / 1e9},
             "gpu_launches": timed_launches,
