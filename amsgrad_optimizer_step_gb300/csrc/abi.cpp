@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -28,12 +29,15 @@
 namespace fa {
 
 int sm_count(int device) {
-    static int cache[64] = {0};  // immutable device property
-    if (device >= 0 && device < 64 && cache[device] > 0) return cache[device];
+    static std::atomic<int> cache[64] = {};  // immutable device property; any thread may fill it
+    if (device >= 0 && device < 64) {
+        const int c = cache[device].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return 0;
-    if (device >= 0 && device < 64) cache[device] = n;
+    if (device >= 0 && device < 64) cache[device].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -17,6 +17,8 @@
 // an iteration issued before any arithmetic.  Elements before the first
 // 16-byte boundary and after the last full vector go through the same
 // arithmetic one at a time.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -648,12 +650,13 @@ cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vecto
     const int64_t sms = sm_count(dev);
     if (FIRST || !vector_ok || ntiles < 2 * sms) return cudaSuccess;
     auto kern = update_tma_kernel<GT, AMS, FIRST, MD, SEG>;
-    static bool configured[64] = {};
-    if (dev < 64 && !configured[dev]) {
+    // the attribute is per device; setting it twice from racing threads is harmless
+    static std::atomic<bool> configured[64] = {};
+    if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         const cudaError_t err =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
         if (err != cudaSuccess) return err;
-        configured[dev] = true;
+        if (dev < 64) configured[dev].store(true, std::memory_order_release);
     }
     const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
     kern<<<grid, kTmaThreads, L::kSmem, stream>>>(s, c, ntiles);
