@@ -13,7 +13,7 @@ import torch
 
 import amsgrad_optimizer_step_gb300 as fa
 import oracle
-from gpu_harness import gate, grad_bits_from_device, TORCH_DT
+from gpu_harness import gate, grad_bits_from_device, oracle_one_step, TORCH_DT
 from synthetic.configs import CONFIG4, decoder_bucket_shapes
 
 pytestmark = pytest.mark.gpu
@@ -214,3 +214,74 @@ def test_per_segment_clipped_step_vs_oracle(oracle_lib):
     ph = p.cpu().numpy()
     for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
         gate(ph[a:b], refs[k].p, 1e-5, f"segment {k}")
+
+
+def test_per_segment_clipped_full_size_sampled(oracle_lib):
+    """The per-parameter clipped step on the whole 1,195,991,040-parameter decoder bucket
+    (199 segments, FP16 gradients, AMSGrad, rows of 512), in the launch configuration the
+    benchmark times. Every segment's report and clip coefficient is checked against the
+    oracle over that segment's full gradient. Sampled elements are checked one step from
+    identical state and along the trajectory. Call 3 carries +Inf and is skipped."""
+    w = dataclasses.replace(CONFIG4, calls=4, inf_call=3)
+    seg = np.asarray(w.segments, dtype=np.int64)
+    n = w.n
+    opts = w.options()
+    o = fa.options(**opts)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p)
+    m, v, vm = (torch.zeros(n, device=DEV) for _ in range(3))
+    g = torch.empty(n, dtype=torch.float16, device=DEV)
+    row_len = 512
+    crow = fa.segment_rows(list(seg), row_len)
+    rows_buf = fa.stats_buffer(crow[-1], DEV)
+    scratch = torch.empty(fa.fa_stats_chunk_scratch(crow), device=DEV)
+    reports = fa.stats_buffer(len(seg) - 1, DEV)
+    rng = np.random.default_rng(40)
+    ends = np.concatenate([seg[1:-1], seg[1:-1] - 1, [0, n - 1, w.inf_index()]])
+    idx = np.unique(np.concatenate([rng.integers(0, n, 40000), ends]))
+    idx_t = torch.as_tensor(idx, device=DEV)
+    kseg = np.searchsorted(seg, idx, side="right") - 1
+    groups = [np.nonzero(kseg == k)[0] for k in range(len(seg) - 1)]
+    assert all(len(gk) >= 2 for gk in groups)
+    refs = [oracle.OracleAdamW(w.params_host(idx[gk]), opts, lib_=oracle_lib) for gk in groups]
+    max_norm = 0.01
+    t = 0
+    for call in range(1, w.calls + 1):
+        w.fill_grad_device(call, g)
+        before = [x[idx_t].double().cpu().numpy() for x in (p, m, v, vm)]
+        t_before = t
+        t, rep, norms, coefs = fa.fa_bucket_step_clipped_per_segment(
+            list(seg), p, g, m, v, vm, t, o, fa.control(), max_norm, row_len, rows_buf,
+            scratch, reports)
+        torch.cuda.synchronize()
+        bits = grad_bits_from_device(g)
+        assert np.array_equal(bits[idx], w.grad_host(call, idx)), "device/host grads differ"
+        stats = _slice_stats(oracle_lib, bits, "f16", seg)
+        del bits
+        after = [x[idx_t].double().cpu().numpy() for x in (p, m, v, vm)]
+        bad = call == w.inf_call
+        assert bool(rep.skipped_nonfinite) == bad == any(c > 0 for _, c in stats)
+        if bad:
+            assert t == t_before and rep.updated == 0
+            for a, b in zip(before, after):
+                assert np.array_equal(a, b), "skipped call changed state"
+            for r in refs:
+                r.step(np.zeros(0, np.uint16), "f16", skip_update=True)
+            continue
+        assert t == t_before + 1 and rep.updated == 1
+        gh = w.grad_host(call, idx)
+        for k, ((s_k, c_k), gk) in enumerate(zip(stats, groups)):
+            _, norm, coef = oracle_lib.clip_decision(s_k, c_k, max_norm)
+            assert abs(norms[k] - norm) <= 1e-5 * norm + 1e-30, (call, k, norms[k], norm)
+            assert abs(coefs[k] - coef) <= 1e-5 * coef, (call, k, coefs[k], coef)
+            zero = np.zeros(len(gk))
+            b4 = (before[0][gk], zero, zero, zero) if t_before == 0 else \
+                tuple(b[gk] for b in before)
+            one = oracle_one_step(gh[gk], "f16", opts, 1.0, float(coefs[k]), t, b4, oracle_lib)
+            for j, name in enumerate(("p", "m", "v", "vmax")):
+                gate(after[j][gk], one[j], 1e-6, f"call {call} segment {k} one-step {name}")
+            refs[k].step(gh[gk], "f16", clip_coef=coef)
+            gate(after[0][gk], refs[k].p, 1e-5, f"call {call} segment {k} trajectory p")
+            gate(after[3][gk], refs[k].state.vmax, 1e-5, f"call {call} segment {k} trajectory vmax")
+        assert min(coefs) < 1.0
+    assert t == 3
