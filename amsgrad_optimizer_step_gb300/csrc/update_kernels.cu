@@ -495,11 +495,37 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
     int64_t k = 0;
     // segment of the current tile's first element: a CTA's tiles only move forward,
     // so the index advances by a scan whose total length over the launch is at most
-    // the number of segments
+    // the number of segments; the next segment's start and the current multiplier
+    // stay in registers, so a tile inside one segment reads no table entry
     int k_lo = 0;
+    int64_t next_start = INT64_MAX;
+    float seg_gmul = 0.f;
+    if (SEG) {
+        if (sa.nseg > 1) next_start = sa.seg_start[1];
+        seg_gmul = sa.gmul[0];
+    }
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
         const int s = static_cast<int>(k % S);
         const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
+        // segments of this tile's first and last element (warp-uniform scans), found
+        // before the wait so that they cost nothing between the tile's arrival and
+        // the refill that follows its update
+        int k_hi = 0;
+        if (SEG) {
+            const int64_t t0 = a.head + tile * L::kTile;
+            if (t0 >= next_start) {
+                do {
+                    ++k_lo;
+                    next_start = k_lo + 1 < sa.nseg ? sa.seg_start[k_lo + 1] : INT64_MAX;
+                } while (t0 >= next_start);
+                seg_gmul = sa.gmul[k_lo];
+            }
+            k_hi = k_lo;
+            if (t0 + L::kTile > next_start) {  // the tile reaches into later segments
+                k_hi = k_lo + 1;
+                while (k_hi + 1 < sa.nseg && sa.seg_start[k_hi + 1] < t0 + L::kTile) ++k_hi;
+            }
+        }
         uint32_t it = 0;
         while (!mbar_try_wait(&bars[s], parity)) {
             if (++it == kTmaSpinLimit) { failed = true; break; }
@@ -508,16 +534,6 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
         if (tid == 0) consumed[s] = issued[s];
 
         unsigned char *b = smem + s * L::kStage;
-        // segments of this tile's first and last element (warp-uniform scans)
-        int k_hi = 0;
-        float seg_gmul = 0.f;
-        if (SEG) {
-            const int64_t t0 = a.head + tile * L::kTile;
-            while (k_lo + 1 < sa.nseg && sa.seg_start[k_lo + 1] <= t0) ++k_lo;
-            k_hi = k_lo;
-            while (k_hi + 1 < sa.nseg && sa.seg_start[k_hi + 1] < t0 + L::kTile) ++k_hi;
-            seg_gmul = sa.gmul[k_lo];
-        }
 #pragma unroll
         for (int h = 0; h < L::kChunks; ++h) {
             const int j = h * 4 * kTmaThreads + 4 * tid;  // first element of this chunk
