@@ -21,7 +21,10 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
+# Host code without floating-point contraction: the FP64 coefficient arithmetic then
+# rounds the same on x86-64 and AArch64, and as the device's explicitly rounded copy.
+COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-ffp-contract=off",
+          "-I", INCLUDE, "-I", CSRC]
 
 
 def nvcc() -> str:
