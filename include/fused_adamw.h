@@ -291,8 +291,9 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
  * bit-identical to fa_bucket_step / fa_bucket_step_clipped.
  *
  * Device memory, 80 bytes, 8-byte aligned, owned by the caller.  Zero it once
- * for a fresh optimizer (t = 0, state None); after that only the library
- * writes it.  It may be read back at any time after the stream has passed the
+ * for a fresh optimizer (t = 0, state None); to resume from a checkpoint,
+ * write the saved t with every other field zero.  Apart from that only the
+ * library writes it.  It may be read back at any time after the stream has passed the
  * step, e.g. for logging without a synchronisation inside the step.
  */
 typedef struct fa_device_step {
