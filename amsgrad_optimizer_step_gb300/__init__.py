@@ -17,8 +17,8 @@ from typing import Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import (FA_BF16, FA_F16, FA_F32, FaDeviceStep, FaOptions, FaStats,  # noqa: F401
-                   FaStepControl, FaStepReport, FusedAdamWError, check)
+from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  # noqa: F401
+                   FaStepReport, FusedAdamWError, check)
 
 __all__ = [
     "fa_abi_version", "fa_device_error", "fa_pipeline_selftest", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
@@ -30,9 +30,7 @@ __all__ = [
     "fa_merge_gradient_stats_chunks", "fa_bucket_step_segment_scaled",
     "fa_bucket_step_clipped_per_segment", "segment_rows",
     "fa_clip_decide", "fa_bucket_step_clipped", "fa_bucket_step_gated",
-    "fa_bucket_step_clipped_gated", "fa_bucket_step_capturable",
-    "fa_bucket_step_clipped_capturable", "device_step_buffer", "read_device_step",
-    "options", "control", "stats_buffer",
+    "fa_bucket_step_clipped_gated", "options", "control", "stats_buffer",
     "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
 ]
 
@@ -321,75 +319,6 @@ def fa_bucket_step_clipped_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: Fa
         rows_buf.shape[0], _ptr(scratch), 0 if scratch is None else scratch.numel(),
         _ptr(report), ctypes.byref(rep), _stream(stream)))
     return tt.value, rep
-
-
-# ---- device-resident step count ----------------------------------------------------
-
-DEVICE_STEP_BYTES = ctypes.sizeof(FaDeviceStep)  # 80
-
-
-def device_step_buffer(device) -> torch.Tensor:
-    """A zeroed 80-byte device step record (t = 0, state None), as uint8 [80]."""
-    return torch.zeros(DEVICE_STEP_BYTES, dtype=torch.uint8, device=device)
-
-
-def _device_step_tensor(dstep: torch.Tensor) -> None:
-    if (not isinstance(dstep, torch.Tensor) or dstep.dtype != torch.uint8 or dstep.dim() != 1
-            or dstep.numel() != DEVICE_STEP_BYTES or not dstep.is_contiguous()):
-        raise ValueError("dstep: expected a contiguous uint8 [80] device step record")
-
-
-def read_device_step(dstep: torch.Tensor) -> FaDeviceStep:
-    """Copies the record to the host (waits for the stream that wrote it)."""
-    _device_step_tensor(dstep)
-    host = dstep.cpu().numpy().tobytes()
-    return FaDeviceStep.from_buffer_copy(host)
-
-
-def fa_bucket_step_capturable(seg_offsets, p, g, m, v, vmax, dstep: torch.Tensor,
-                              opts: FaOptions, ctl: FaStepControl,
-                              report: Optional[torch.Tensor] = None,
-                              max_grad_norm: float = 0.0, stream=None) -> None:
-    """Enqueues the decision and update kernels of a step whose count lives in ``dstep``
-    (no host synchronisation: capturable into a CUDA graph)."""
-    n = p.numel()
-    _dense("p", p, n, (torch.float32,))
-    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
-    _dense("m", m, n, (torch.float32,), p.device)
-    _dense("v", v, n, (torch.float32,), p.device)
-    if vmax is not None:
-        _dense("vmax", vmax, n, (torch.float32,), p.device)
-    _device_step_tensor(dstep)
-    if report is not None:
-        _stats_tensor("report", report)
-    seg, nseg = _segments(seg_offsets)
-    check("fa_bucket_step_capturable", _L().fa_bucket_step_capturable(
-        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
-        _ptr(dstep), ctypes.byref(opts), ctl, _ptr(report), max_grad_norm, _stream(stream)))
-
-
-def fa_bucket_step_clipped_capturable(seg_offsets, p, g, m, v, vmax, dstep: torch.Tensor,
-                                      opts: FaOptions, ctl: FaStepControl,
-                                      max_grad_norm: float, row_len: int,
-                                      rows_buf: torch.Tensor, scratch: Optional[torch.Tensor],
-                                      report: torch.Tensor, stream=None) -> None:
-    """Analysis, merge, decision and update, all enqueued, none waited for."""
-    n = p.numel()
-    _dense("p", p, n, (torch.float32,))
-    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
-    _dense("m", m, n, (torch.float32,), p.device)
-    _dense("v", v, n, (torch.float32,), p.device)
-    if vmax is not None:
-        _dense("vmax", vmax, n, (torch.float32,), p.device)
-    _device_step_tensor(dstep)
-    _stats_tensor("rows_buf", rows_buf)
-    _stats_tensor("report", report)
-    seg, nseg = _segments(seg_offsets)
-    check("fa_bucket_step_clipped_capturable", _L().fa_bucket_step_clipped_capturable(
-        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
-        _ptr(dstep), ctypes.byref(opts), ctl, max_grad_norm, row_len, _ptr(rows_buf),
-        rows_buf.shape[0], _ptr(scratch), 0 if scratch is None else scratch.numel(),
-        _ptr(report), _stream(stream)))
 
 
 # ---- statistics ------------------------------------------------------------------

@@ -35,13 +35,6 @@ class FaStats(ctypes.Structure):
                 ("sum_sq_lo", ctypes.c_float)]
 
 
-class FaDeviceStep(ctypes.Structure):
-    """Host image of the 80-byte device-resident step record."""
-    _fields_ = [("t", c_u64), ("skipped", ctypes.c_uint32), ("nonfinite", ctypes.c_uint32),
-                ("grad_norm", c_f64), ("clip_coef", c_f64),
-                ("reserved", ctypes.c_uint32 * 12)]
-
-
 class FaStepReport(ctypes.Structure):
     _fields_ = [("updated", c_i32), ("skipped_nonfinite", c_i32), ("nonfinite", c_u64),
                 ("grad_norm", c_f64), ("clip_coef", c_f64)]
@@ -80,12 +73,6 @@ SIGNATURES = {
                                              ctypes.POINTER(FaOptions), FaStepControl, c_f64,
                                              c_i32, P, c_i64, P, c_i64, P,
                                              ctypes.POINTER(FaStepReport), P]),
-    "fa_bucket_step_capturable": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, P,
-                                          ctypes.POINTER(FaOptions), FaStepControl, P, c_f64,
-                                          P]),
-    "fa_bucket_step_clipped_capturable": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, P,
-                                                  ctypes.POINTER(FaOptions), FaStepControl,
-                                                  c_f64, c_i32, P, c_i64, P, c_i64, P, P]),
     "fa_stats_plan": (c_i32, [c_i64, PI32, PI64]),
     "fa_stats_rows": (c_i32, [c_i64, c_i32, PI64, c_i32, PI64]),
     "fa_analyze_gradient": (c_i32, [P, c_i32, c_i64, c_i32, PI64, c_i32, P, c_i64, P]),

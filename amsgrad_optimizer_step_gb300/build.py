@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Host code without floating-point contraction: the FP64 coefficient arithmetic then
-# rounds the same on x86-64 and AArch64, and as the device's explicitly rounded copy.
+# rounds the same on x86-64 and AArch64 (whose compilers may otherwise fuse 1 - lr*wd).
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-ffp-contract=off",
           "-I", INCLUDE, "-I", CSRC]
 

@@ -228,53 +228,6 @@ fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt,
     return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// The decision kernel, then the first-step and the steady update kernels of a
-// device-resident step; all pointers already validated.
-fa_status enqueue_capturable(int64_t n, float *p, const void *g, fa_dtype gdt, float *m,
-                             float *v, float *vmax, const fa_options *o, double scale,
-                             fa_device_step *dstep, const fa_stats *report,
-                             double max_grad_norm, void *stream) {
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    fa::DecideArgs d;
-    d.report = report;
-    d.lr = o->lr;
-    d.beta1 = o->beta1;
-    d.beta2 = o->beta2;
-    d.eps = o->eps;
-    d.weight_decay = o->weight_decay;
-    d.sign = o->maximize ? -1.0 : 1.0;
-    d.scale = scale;
-    d.max_grad_norm = max_grad_norm;
-    if (fa::launch_device_step_decide(dstep, d, s) != cudaSuccess) return FA_ERR_CUDA;
-    for (const bool first : {true, false}) {
-        fa::UpdateArgs a;
-        a.p_in = p;
-        a.m_in = first ? nullptr : m;
-        a.v_in = first ? nullptr : v;
-        a.vmax_in = (first || !o->amsgrad) ? nullptr : vmax;
-        a.g = g;
-        a.p_out = p;
-        a.m_out = m;
-        a.v_out = v;
-        a.vmax_out = o->amsgrad ? vmax : nullptr;
-        a.p_model = nullptr;
-        a.extra_tx = 0;
-        a.gate = nullptr;
-        a.gate_scale = a.gate_max_norm = a.gate_sign = 0.0;
-        a.dstep = dstep;
-        a.n = n;
-        const void *ptrs[] = {p, m, v, a.vmax_out, g};
-        const size_t es[] = {4, 4, 4, 4, dtype_bytes(gdt)};
-        const int64_t head = vector_head(ptrs, es, 5, n);
-        const bool vec = head >= 0;
-        a.head = vec ? head : 0;
-        a.nvec = vec ? (n - a.head) / 8 : 0;
-        if (fa::launch_update_device_step(a, gdt, o->amsgrad != 0, first, vec, s) != cudaSuccess)
-            return FA_ERR_CUDA;
-    }
-    return FA_OK;
-}
-
 // Validates the in-place argument set; fills the ranges for alias checks.
 fa_status check_inplace(int64_t n, float *p, const void *g, fa_dtype gdt, float *m, float *v,
                         float *vmax, const fa_options *o, int dev) {
@@ -1193,84 +1146,6 @@ fa_status fa_bucket_step_clipped(const int64_t *seg_offsets, int32_t nseg, int64
     rep.updated = 1;
     *out = rep;
     return FA_OK;
-}
-
-fa_status fa_bucket_step_capturable(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                                    float *p, const void *g, fa_dtype gdt, float *m, float *v,
-                                    float *vmax, fa_device_step *dstep,
-                                    const fa_options *options, fa_step_control ctl,
-                                    const fa_stats *report_dev, double max_grad_norm,
-                                    void *stream) {
-    fa_status st;
-    if (!dstep) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n_total < 0) return FA_ERR_SIZE;
-    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
-    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
-    if (n_total == 0 || ctl.skip_update) return FA_OK;
-    int dev = 0;
-    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
-    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    if ((st = check_device_ptr(dstep, dev, 8)) != FA_OK) return st;
-    if (report_dev && (st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
-    const size_t b = static_cast<size_t>(n_total) * 4;
-    const Range r[] = {{dstep, sizeof(fa_device_step)}, {report_dev, 12}, {p, b},
-                       {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b}, {v, b},
-                       {options->amsgrad ? vmax : nullptr, b}};
-    if (any_overlap(r, 7)) return FA_ERR_ALIAS;
-    return enqueue_capturable(n_total, p, g, gdt, m, v, vmax, options, ctl.gradient_scale,
-                              dstep, report_dev, max_grad_norm, stream);
-}
-
-fa_status fa_bucket_step_clipped_capturable(const int64_t *seg_offsets, int32_t nseg,
-                                            int64_t n_total, float *p, const void *g,
-                                            fa_dtype gdt, float *m, float *v, float *vmax,
-                                            fa_device_step *dstep, const fa_options *options,
-                                            fa_step_control ctl, double max_grad_norm,
-                                            int32_t row_len, fa_stats *rows_buf,
-                                            int64_t rows_capacity, float *scratch,
-                                            int64_t scratch_elements, fa_stats *report_dev,
-                                            void *stream) {
-    fa_status st;
-    if (!dstep) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n_total < 0) return FA_ERR_SIZE;
-    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
-    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
-    if (n_total == 0 || ctl.skip_update) return FA_OK;
-    int dev = 0;
-    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
-    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    int64_t rows = 0;
-    if ((st = fa_stats_rows(n_total, row_len, seg_offsets, nseg, &rows)) != FA_OK) return st;
-    int32_t kernels = 0;
-    int64_t need = 0;
-    if ((st = fa_stats_plan(rows, &kernels, &need)) != FA_OK) return st;
-    if (rows_capacity < rows || scratch_elements < need) return FA_ERR_SIZE;
-    if ((st = check_device_ptr(dstep, dev, 8)) != FA_OK) return st;
-    if ((st = check_device_ptr(rows_buf, dev, 4)) != FA_OK) return st;
-    if ((st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
-    if (need > 0 && (st = check_device_ptr(scratch, dev, 4)) != FA_OK) return st;
-    const size_t b = static_cast<size_t>(n_total) * 4;
-    const Range r[] = {{dstep, sizeof(fa_device_step)}, {p, b},
-                       {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b}, {v, b},
-                       {options->amsgrad ? vmax : nullptr, b},
-                       {rows_buf, static_cast<size_t>(rows) * 12},
-                       {scratch, static_cast<size_t>(need) * 4}, {report_dev, 12}};
-    if (any_overlap(r, 9)) return FA_ERR_ALIAS;
-
-    if ((st = fa_analyze_gradient(g, gdt, n_total, row_len, seg_offsets, nseg, rows_buf,
-                                  rows_capacity, stream)) != FA_OK)
-        return st;
-    if ((st = fa_merge_gradient_stats(rows_buf, rows, scratch, scratch_elements, report_dev,
-                                      stream)) != FA_OK)
-        return st;
-    return enqueue_capturable(n_total, p, g, gdt, m, v, vmax, options, ctl.gradient_scale,
-                              dstep, report_dev, max_grad_norm, stream);
 }
 
 }  // extern "C"

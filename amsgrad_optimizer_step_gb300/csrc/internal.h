@@ -35,10 +35,6 @@ struct UpdateArgs {
     // non-finite value, else gmul = sign * coef / scale with the host's formula.
     const fa_stats *gate;
     double gate_scale, gate_max_norm, gate_sign;
-    // Device-resident step record, read only by the kernels that
-    // launch_update_device_step selects (they take their coefficients from it and
-    // return at once when it skips the update or selects the other kernel).
-    const fa_device_step *dstep = nullptr;
     int64_t n;     // elements
     int64_t head;  // scalar elements before the 16-byte aligned vector body
     int64_t nvec;  // 8-element vectors in the body
@@ -55,31 +51,6 @@ cudaError_t launch_pipeline_selftest(const UpdateArgs &a, const Coef &c, fa_dtyp
 // Reads (and optionally clears) the flag an update kernel sets when a bounded
 // wait in its shared-memory pipeline gives up.  Waits for the device.
 cudaError_t update_pipeline_error(int *flag, bool clear);
-
-// Layout of fa_device_step::reserved: the FP32 coefficients of the pending
-// update in Coef's field order, then a flag that is 1 when that update is the
-// first (moments not read).
-constexpr int kStepCoefWords = 9;
-constexpr int kStepFirstWord = 9;
-static_assert(sizeof(Coef) == 4 * kStepCoefWords, "Coef is nine FP32 words");
-static_assert(sizeof(fa_device_step) == 80, "fa_device_step is 80 bytes");
-
-// Inputs of the one-thread decision kernel: the report (nullptr: no
-// statistics) and the doubles of the host decision and coefficients.
-struct DecideArgs {
-    const fa_stats *report;
-    double lr, beta1, beta2, eps, weight_decay, sign, scale, max_grad_norm;
-};
-
-// Enqueues the first-step (first) or steady update kernel of a device-resident
-// step: the kernels take the coefficients from a.dstep and return at once when
-// the record skips the update or selects the other kernel.  No model copy.
-cudaError_t launch_update_device_step(const UpdateArgs &a, fa_dtype gdt, bool amsgrad,
-                                      bool first, bool vector_ok, cudaStream_t stream);
-
-// Enqueues the decision kernel that advances *dstep (see fa_bucket_step_capturable).
-cudaError_t launch_device_step_decide(fa_device_step *dstep, const DecideArgs &a,
-                                      cudaStream_t stream);
 
 // model_dtype: FA_F16 or FA_BF16 when a.p_model is set, else kNoModel.
 constexpr int kNoModel = -1;

@@ -176,25 +176,6 @@ __device__ __forceinline__ bool gate_decision(const UpdateArgs &a, float *gmul) 
     return true;
 }
 
-// The coefficients of a device-resident step (written by the decision kernel
-// earlier on the stream); false = this kernel has nothing to do.
-template <bool FIRST>
-__device__ __forceinline__ bool device_step_take(const fa_device_step *d, Coef *c) {
-    if (d->skipped) return false;
-    if ((d->reserved[kStepFirstWord] != 0) != FIRST) return false;
-    const float *w = reinterpret_cast<const float *>(d->reserved);
-    c->b1 = w[0];
-    c->omb1 = w[1];
-    c->b2 = w[2];
-    c->omb2 = w[3];
-    c->step_size = w[4];
-    c->rbc2 = w[5];
-    c->eps = w[6];
-    c->decay = w[7];
-    c->gmul = w[8];
-    return true;
-}
-
 __device__ __forceinline__ void load8f(const float *base, int64_t i, float (&x)[kVec]) {
     const float4 *q = reinterpret_cast<const float4 *>(base + i);
     float4 a = ld16(q);
@@ -269,12 +250,11 @@ __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &
 // Vector body + scalar head/tail.  Each thread owns UNROLL vectors per
 // grid-stride iteration, spaced kThreads vectors apart so that a warp's
 // accesses to each stream are contiguous.
-template <int GT, bool AMS, bool FIRST, int UNROLL, int MD, bool DS = false>
+template <int GT, bool AMS, bool FIRST, int UNROLL, int MD>
 __global__ void __launch_bounds__(kUThreads)
 update_vec_kernel(const UpdateArgs a, const Coef c0) {
     Coef c = c0;
     if (a.gate && !gate_decision(a, &c.gmul)) return;
-    if (DS && !device_step_take<FIRST>(a.dstep, &c)) return;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kUThreads + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kUThreads * UNROLL;
 
@@ -320,12 +300,11 @@ update_vec_kernel(const UpdateArgs a, const Coef c0) {
 }
 
 // Every element one at a time (pointers not co-aligned to 16 bytes).
-template <int GT, bool AMS, bool FIRST, int MD, bool DS = false>
+template <int GT, bool AMS, bool FIRST, int MD>
 __global__ void __launch_bounds__(kThreads)
 update_scalar_kernel(const UpdateArgs a, const Coef c0) {
     Coef c = c0;
     if (a.gate && !gate_decision(a, &c.gmul)) return;
-    if (DS && !device_step_take<FIRST>(a.dstep, &c)) return;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < a.n;
          i += stride)
@@ -431,26 +410,20 @@ __device__ __forceinline__ void fence_mbar_init() {
 //   16 B (FP32 AdamW; BF16 + copy)   4096 x 3   6.93 / 6.73 TB/s
 //   18-22 B (AMSGrad, copies)        3072 x 3   6.75-6.87 TB/s
 // Two stages, and some power-of-two tile/stage pairs, fell to 3.1-6.4 TB/s.
-template <int GT, bool AMS, int MD, bool DS = false>
+template <int GT, bool AMS, int MD>
 struct TmaLayout {
     static constexpr int kGB = GT == FA_F32 ? 4 : 2;
     static constexpr int kElemBytes = 12 + (AMS ? 4 : 0) + kGB + (MD != kNoModel ? 2 : 0);
     static constexpr int kQuantum = 4 * kTmaThreads;
-#if defined(FA_TMA_DS_TILE_OVERRIDE)
-    static constexpr int kTile = DS ? FA_TMA_DS_TILE_OVERRIDE : (kElemBytes == 16 ? 4096 : 3072);
-    static constexpr int kWantStages = DS ? FA_TMA_DS_STAGES_OVERRIDE : (kElemBytes <= 14 ? 4 : 3);
-#elif defined(FA_TMA_TILE_OVERRIDE)
+#ifdef FA_TMA_TILE_OVERRIDE
     static constexpr int kTile = FA_TMA_TILE_OVERRIDE;
+#else
+    static constexpr int kTile = kElemBytes == 16 ? 4096 : 3072;
+#endif
+#ifdef FA_TMA_STAGES_OVERRIDE
     static constexpr int kWantStages = FA_TMA_STAGES_OVERRIDE;
 #else
-    // Measured on GB300 (1.07e9 parameters): the pipeline is sensitive to the
-    // tile x stage pair, and the device-step kernels (DS) measured best on a
-    // table of their own for the AdamW layouts (14 B: 2048 x 6 at 4.06 ms against
-    // 4.32-4.45 ms with 3072 x 3-4; 16 B: 2048 x 4).
-    static constexpr int kTile = DS ? (kElemBytes <= 16 ? 2048 : 3072)
-                                    : (kElemBytes == 16 ? 4096 : 3072);
-    static constexpr int kWantStages = DS ? (kElemBytes <= 14 ? 6 : kElemBytes == 16 ? 4 : 3)
-                                          : (kElemBytes <= 14 ? 4 : 3);
+    static constexpr int kWantStages = kElemBytes <= 14 ? 4 : 3;
 #endif
     static_assert(kTile % kQuantum == 0, "tile must be a whole number of 4-element chunks");
     static constexpr int kChunks = kTile / kQuantum;  // 4-element chunks per thread
@@ -469,18 +442,14 @@ struct TmaLayout {
 
 // SEG: one gradient multiplier per segment from s's table (MD must be kNoModel);
 // otherwise s.nseg is 0 and c.gmul applies to every element.
-template <int GT, bool AMS, bool FIRST, int MD, bool SEG, bool DS = false>
+template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_t ntiles) {
     const UpdateArgs &a = sa.a;
     Coef c = c0;
     // a skipped step returns before any copy is issued (every thread decides alike)
     if (a.gate && !gate_decision(a, &c.gmul)) return;
-    if (DS && !device_step_take<FIRST>(a.dstep, &c)) return;
-    // CTA b takes tiles b, b + grid, b + 2*grid, ... (one contiguous block of tiles
-    // per CTA measured 0.5-1 % slower)
-    const int64_t t_begin = blockIdx.x, t_end = ntiles, t_step = gridDim.x;
-    using L = TmaLayout<GT, AMS, MD, DS>;
+    using L = TmaLayout<GT, AMS, MD>;
     constexpr int S = L::kStages;
     constexpr uint32_t kLoadBytes =
         L::kTile * (4 + L::kGB + (FIRST ? 0 : (AMS ? 12 : 8)));
@@ -517,8 +486,8 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-            const int64_t tile = t_begin + static_cast<int64_t>(s) * t_step;
-            if (tile < t_end) issue_loads(s, tile);
+            const int64_t tile = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (tile < ntiles) issue_loads(s, tile);
         }
     }
 
@@ -535,7 +504,7 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
         if (sa.nseg > 1) next_start = sa.seg_start[1];
         seg_gmul = sa.gmul[0];
     }
-    for (int64_t tile = t_begin; tile < t_end; tile += t_step, ++k) {
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
         const int s = static_cast<int>(k % S);
         const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
         // segments of this tile's first and last element (warp-uniform scans), found
@@ -643,8 +612,8 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
             // iteration to finish reading shared memory
             if (k >= 1) {
                 const int sp = static_cast<int>((k - 1) % S);
-                const int64_t next = tile + static_cast<int64_t>(S - 1) * t_step;
-                if (next < t_end) {
+                const int64_t next = tile + static_cast<int64_t>(S - 1) * gridDim.x;
+                if (next < ntiles) {
                     bulk_wait_read1();
                     issue_loads(sp, next);
                 }
@@ -688,15 +657,15 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
 // Steady steps of at least two tiles per SM take the TMA pipeline; the first
 // step (moments only written: 6 B in, 12 B out) measured faster through the
 // register kernel (3.0 vs 3.7 ms at 1.07e9), and so did small tensors.
-template <int GT, bool AMS, bool FIRST, int MD, bool SEG, bool DS = false>
+template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
 cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vector_ok, int dev,
                                 cudaStream_t stream, bool *launched) {
-    using L = TmaLayout<GT, AMS, MD, DS>;
+    using L = TmaLayout<GT, AMS, MD>;
     *launched = false;
     const int64_t ntiles = (s.a.n - s.a.head) / L::kTile;
     const int64_t sms = sm_count(dev);
     if (FIRST || !vector_ok || ntiles < 2 * sms) return cudaSuccess;
-    auto kern = update_tma_kernel<GT, AMS, FIRST, MD, SEG, DS>;
+    auto kern = update_tma_kernel<GT, AMS, FIRST, MD, SEG>;
     // the attribute is per device; setting it twice from racing threads is harmless
     static std::atomic<bool> configured[64] = {};
     if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
@@ -798,7 +767,7 @@ cudaError_t launch_seg_gt(const SegScaleArgs &s, const Coef &c, bool ams, bool f
 
 constexpr int kUnroll = FA_UPDATE_UNROLL;
 
-template <int GT, bool AMS, bool FIRST, int MD, bool DS = false>
+template <int GT, bool AMS, bool FIRST, int MD>
 cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
                          cudaStream_t stream) {
     int dev = 0;
@@ -812,13 +781,12 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         s.a = a;
         s.nseg = 0;
         bool launched = false;
-        err = launch_tma_if_large<GT, AMS, FIRST, MD, false, DS>(s, c, vector_ok, dev, stream,
-                                                                 &launched);
+        err = launch_tma_if_large<GT, AMS, FIRST, MD, false>(s, c, vector_ok, dev, stream, &launched);
         if (err != cudaSuccess || launched) return err;
     }
 #endif
     if (vector_ok) {
-        auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD, DS>;
+        auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD>;
         const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
         int64_t need = (a.nvec + per_cta - 1) / per_cta;
         if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
@@ -826,22 +794,12 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         if (grid == 0) return cudaSuccess;
         kern<<<grid, kUThreads, 0, stream>>>(a, c);
     } else {
-        auto kern = update_scalar_kernel<GT, AMS, FIRST, MD, DS>;
+        auto kern = update_scalar_kernel<GT, AMS, FIRST, MD>;
         const int grid = persistent_grid(kern, (a.n + kThreads - 1) / kThreads, dev);
         if (grid == 0) return cudaSuccess;
         kern<<<grid, kThreads, 0, stream>>>(a, c);
     }
     return cudaGetLastError();
-}
-
-template <int GT>
-cudaError_t launch_ds_gt(const UpdateArgs &a, bool ams, bool first, bool vec, cudaStream_t s) {
-    const Coef c{};  // the kernels take the record's coefficients
-    if (ams)
-        return first ? launch_typed<GT, true, true, kNoModel, true>(a, c, vec, s)
-                     : launch_typed<GT, true, false, kNoModel, true>(a, c, vec, s);
-    return first ? launch_typed<GT, false, true, kNoModel, true>(a, c, vec, s)
-                 : launch_typed<GT, false, false, kNoModel, true>(a, c, vec, s);
 }
 
 template <int GT, int MD>
@@ -917,17 +875,6 @@ cudaError_t update_pipeline_error(int *flag, bool clear) {
     *flag = 0;
     return cudaSuccess;
 #endif
-}
-
-cudaError_t launch_update_device_step(const UpdateArgs &a, fa_dtype gdt, bool amsgrad,
-                                      bool first, bool vector_ok, cudaStream_t stream) {
-    if (!a.dstep) return cudaErrorInvalidValue;
-    switch (gdt) {
-        case FA_F32: return launch_ds_gt<FA_F32>(a, amsgrad, first, vector_ok, stream);
-        case FA_F16: return launch_ds_gt<FA_F16>(a, amsgrad, first, vector_ok, stream);
-        case FA_BF16: return launch_ds_gt<FA_BF16>(a, amsgrad, first, vector_ok, stream);
-    }
-    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_update(const UpdateArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,

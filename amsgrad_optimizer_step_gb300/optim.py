@@ -27,12 +27,9 @@ from typing import Optional
 
 import torch
 
-from collections.abc import Mapping
-
-from . import (FaDeviceStep, device_step_buffer, fa_analyze_gradient, fa_bucket_step,
-               fa_bucket_step_capturable, fa_bucket_step_writeback, fa_merge_gradient_stats,
-               fa_read_report, fa_stats_rows, options, control, read_device_step,
-               scratch_buffer, stats_buffer)
+from . import (fa_analyze_gradient, fa_bucket_step, fa_bucket_step_writeback,
+               fa_merge_gradient_stats, fa_read_report, fa_stats_rows, options,
+               control, scratch_buffer, stats_buffer)
 from . import sharded
 
 MAX_ROWS = 4_194_304
@@ -103,32 +100,6 @@ class _Bucket:
                     p.grad = mine
 
 
-class _DeviceReport(Mapping):
-    """The last step's report of a capturable optimizer, read from the device record
-    at every access (each read waits for the stream; after a graph replay it shows
-    the replayed step)."""
-
-    def __init__(self, record: torch.Tensor, found_inf: bool):
-        self._record = record
-        self._found_inf = found_inf
-
-    def _load(self) -> dict:
-        if self._found_inf:
-            return {"skipped": True, "nonfinite": 0, "grad_norm": None, "clip_coef": 1.0}
-        d = read_device_step(self._record)
-        return {"skipped": bool(d.skipped), "nonfinite": int(d.nonfinite),
-                "grad_norm": float(d.grad_norm), "clip_coef": float(d.clip_coef)}
-
-    def __getitem__(self, key):
-        return self._load()[key]
-
-    def __iter__(self):
-        return iter(self._load())
-
-    def __len__(self):
-        return len(self._load())
-
-
 class FusedAdamW(torch.optim.Optimizer):
     """AdamW / AMSGrad on GB300 through the fused step.
 
@@ -138,21 +109,12 @@ class FusedAdamW(torch.optim.Optimizer):
     ``GradScaler`` asks for it, the step first analyses every group's gradient,
     merges the statistics (fan-in 1024) and reads back the 12-byte report: a
     non-finite value skips the step, and the global norm sets the clip.
-
-    ``capturable=True`` keeps every group's step count and the skip / clip decision
-    on the device (the library's device step record): ``step()`` then enqueues
-    its kernels without reading anything back, so it can be captured into a CUDA
-    graph together with the forward and backward passes.  The results are
-    bit-identical to the default mode.  ``last_report`` is read from the device
-    when first accessed.  Capturable mode needs float32 parameters, and a
-    captured step keeps the gradient_scale it was captured with.
     """
 
     def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-5,
                  weight_decay: float = 1e-4, amsgrad: bool = False, maximize: bool = False,
                  fused_step: bool = True, max_grad_norm: Optional[float] = None,
-                 hierarchical_stats: bool = False, row_len: Optional[int] = None,
-                 capturable: bool = False):
+                 hierarchical_stats: bool = False, row_len: Optional[int] = None):
         if not fused_step:
             raise ValueError("FusedAdamW implements the fused step only (fused_step=True)")
         if max_grad_norm is not None and not max_grad_norm > 0:
@@ -166,14 +128,7 @@ class FusedAdamW(torch.optim.Optimizer):
         self._buckets = [_Bucket(list(g["params"]), g["amsgrad"]) for g in self.param_groups]
         self.row_len = row_len if row_len is not None else self._auto_row_len()
         self._stats = None
-        self.last_report: Mapping = {}
-        self.capturable = bool(capturable)
-        self._records = None
-        if self.capturable:
-            if any(b.master_separate for b in self._buckets):
-                raise ValueError("capturable=True needs float32 parameters (the device-step "
-                                 "update writes no low-precision model copy)")
-            self._records = [device_step_buffer(b.master.device) for b in self._buckets]
+        self.last_report: dict = {}
         self._bind_state()
 
     # ---- state -------------------------------------------------------------------
@@ -190,21 +145,9 @@ class FusedAdamW(torch.optim.Optimizer):
                 self.state[p] = st
 
     def _sync_steps(self) -> None:
-        if self.capturable:  # the counts live on the device
-            for b, rec in zip(self._buckets, self._records):
-                b.t = int(read_device_step(rec).t)
         for b in self._buckets:
             for p in b.params:
                 self.state[p]["step"] = torch.tensor(float(b.t))
-
-    def _write_records(self) -> None:
-        """A fresh device record holding each group's count (after a restore)."""
-        for b, rec in zip(self._buckets, self._records):
-            img = FaDeviceStep()
-            img.t = b.t
-            img.clip_coef = 1.0
-            host = torch.frombuffer(bytearray(bytes(img)), dtype=torch.uint8)
-            rec.copy_(host)
 
     def state_dict(self):
         self._sync_steps()
@@ -255,8 +198,6 @@ class FusedAdamW(torch.optim.Optimizer):
                 if len(steps) > 1:
                     raise ValueError("parameters of one group have different step counts")
                 b.t = steps.pop() if steps else 0
-        if self.capturable:
-            self._write_records()
         self._bind_state()
 
     def zero_grad(self, set_to_none: bool = False) -> None:
@@ -288,8 +229,8 @@ class FusedAdamW(torch.optim.Optimizer):
     def _rows(self, b: _Bucket) -> int:
         return fa_stats_rows(b.n, self.row_len, b.segments)
 
-    def _enqueue_statistics(self) -> torch.Tensor:
-        """Analyses every group and merges into the one 12-byte device report."""
+    def statistics(self, gradient_scale: float = 1.0):
+        """Analyse every group, merge, read back: (skip, global norm, clip coefficient)."""
         total, rows_buf, scratch, report = self._stats_buffers()
         off = 0
         for b in self._buckets:
@@ -297,11 +238,7 @@ class FusedAdamW(torch.optim.Optimizer):
             fa_analyze_gradient(b.grad, self.row_len, rows_buf[off:off + r], b.segments)
             off += r
         fa_merge_gradient_stats(rows_buf, total, scratch, report)
-        return report
-
-    def statistics(self, gradient_scale: float = 1.0):
-        """Analyse every group, merge, read back: (skip, global norm, clip coefficient)."""
-        rep = fa_read_report(self._enqueue_statistics())
+        rep = fa_read_report(report)
         skip, norm, coef = sharded.global_clip_decision(
             rep, gradient_scale, self.max_grad_norm if self.max_grad_norm else 0.0)
         return skip, norm, coef, int(rep.nonfinite)
@@ -315,9 +252,6 @@ class FusedAdamW(torch.optim.Optimizer):
                 loss = closure()
         for b in self._buckets:
             b.gather_grads()
-        if self.capturable:
-            self._step_on_device(gradient_scale, found_inf, check_finite)
-            return loss
         report = {"skipped": bool(found_inf), "nonfinite": 0, "grad_norm": None, "clip_coef": 1.0}
         if not found_inf and (self.max_grad_norm is not None or self.hierarchical_stats
                               or check_finite):
@@ -338,23 +272,6 @@ class FusedAdamW(torch.optim.Optimizer):
                                             b.t, o, ctl, report["clip_coef"])
         self.last_report = report
         return loss
-
-    def _step_on_device(self, gradient_scale: float, found_inf: bool,
-                        check_finite: bool) -> None:
-        """Statistics, decision and update, all enqueued; nothing is read back."""
-        self.last_report = _DeviceReport(self._records[0], bool(found_inf))
-        if found_inf:
-            return
-        report = None
-        if self.max_grad_norm is not None or self.hierarchical_stats or check_finite:
-            report = self._enqueue_statistics()
-        ctl = control(gradient_scale)
-        for group, b, rec in zip(self.param_groups, self._buckets, self._records):
-            o = options(lr=group["lr"], beta1=group["betas"][0], beta2=group["betas"][1],
-                        eps=group["eps"], weight_decay=group["weight_decay"],
-                        amsgrad=group["amsgrad"], maximize=group["maximize"])
-            fa_bucket_step_capturable(b.segments, b.master, b.grad, b.m, b.v, b.vmax, rec, o,
-                                      ctl, report, self.max_grad_norm or 0.0)
 
 
 class GradScaler:

@@ -21,7 +21,6 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
-import dataclasses
 import json
 import os
 import statistics
@@ -595,75 +594,6 @@ def run_ours(args):
                               "frac": gbs / peak, "peak_kind": peak_kind,
                               "params_per_s": n / (ms * 1e-3)}
         del p_model
-
-        # CUDA-graph replay of the statistics-guarded step with the step count on the
-        # device, against the host-synchronised step (analysis, merge, 12-byte read-back,
-        # host decision, update): on this workload, and on a 65,536-parameter FP32 one
-        # whose step is bound by launches and the host round trip.
-        def graph_vs_host(wk, gk, pk, mk, vk, rows_k, scr_k, rep_k, steps):
-            ok = fa.options(**wk.options())
-            ck = fa.control(wk.gradient_scale)
-            dk = fa.device_step_buffer(dev)
-            hk = {"t": 0}
-
-            def host_step():
-                hk["t"], _ = fa.fa_bucket_step_clipped(None, pk, gk, mk, vk, None, hk["t"], ok,
-                                                       ck, 1.0, wk.row_len, rows_k, scr_k,
-                                                       rep_k)
-
-            def capturable_step():
-                fa.fa_bucket_step_clipped_capturable(None, pk, gk, mk, vk, None, dk, ok, ck,
-                                                     1.0, wk.row_len, rows_k, scr_k, rep_k)
-
-            side = torch.cuda.Stream(dev)
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
-                for _ in range(2):
-                    capturable_step()
-            stream.wait_stream(side)
-            torch.cuda.synchronize(dev)
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                capturable_step()
-            torch.cuda.synchronize(dev)
-
-            def run(fn):
-                for _ in range(3):
-                    fn()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                torch.cuda.synchronize(dev)
-                t0 = time.perf_counter()
-                e0.record(stream)
-                for _ in range(steps):
-                    fn()
-                e1.record(stream)
-                torch.cuda.synchronize(dev)
-                wall = (time.perf_counter() - t0) / steps
-                return e0.elapsed_time(e1) / steps, wall * 1e3
-
-            host_ms, host_wall = run(host_step)
-            graph_ms, graph_wall = run(graph.replay)
-            del graph
-            return {"params": wk.n, "host_sync_step_ms": host_ms,
-                    "host_sync_step_wall_ms": host_wall, "graph_replay_step_ms": graph_ms,
-                    "graph_replay_step_wall_ms": graph_wall, "speedup": host_ms / graph_ms,
-                    "kernels_per_graph_step": 1 + fa.fa_stats_plan(rows_k.shape[0])[0] + 3}
-
-        rows_out["graph_step_flat1G_bf16_stats_clip"] = graph_vs_host(
-            w, g, p, m, v, rows_buf, scratch, report, args.next_rows_steps)
-        from synthetic.configs import CONFIG1
-        w1 = dataclasses.replace(CONFIG1, row_len=256, max_grad_norm=1.0)
-        p1 = torch.empty(w1.n, device=dev)
-        w1.fill_params_device(p1)
-        m1, v1 = torch.zeros_like(p1), torch.zeros_like(p1)
-        g1 = torch.empty(w1.n, device=dev)
-        w1.fill_grad_device(1, g1)
-        r1 = fa.stats_buffer(fa.fa_stats_rows(w1.n, 256), dev)
-        rows_out["graph_step_flat65536_f32_stats_clip"] = graph_vs_host(
-            w1, g1, p1, m1, v1, r1, fa.scratch_buffer(r1.shape[0], dev), fa.stats_buffer(1, dev),
-            200)
-        del p1, m1, v1, g1, r1
 
         # f2: the pages' staged baseline against the fused update, on FP32
         # gradients (the case their 48 -> 28 and 60 -> 36 B/param model is stated

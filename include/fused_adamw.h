@@ -26,8 +26,6 @@
  *     (fa_merge_gradient_stats_static) and, per host thread that calls
  *     fa_bucket_step_clipped_gated, a 64-byte pinned host staging record and
  *     one event per device, allocated on first use and kept until exit.
- *     Optimizer state that must live on the device (fa_device_step) is the
- *     caller's too.
  *   - Parameters and moments are dense contiguous FP32; gradients are dense
  *     contiguous FP32, FP16 or BF16 of the same element count
  *     ([FA-zh] "增加的实际能力").  Strides, broadcasts and sparse gradients
@@ -274,79 +272,6 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
                                        int64_t rows_capacity, float *scratch,
                                        int64_t scratch_elements, fa_stats *report_dev,
                                        fa_step_report *out, void *stream);
-
-/* ---- steps with a device-resident step count (CUDA-graph capturable) ------- */
-
-/*
- * The pages have no counterpart for this record or the two calls below.  They
- * keep the step count and the skip / clip decision on the device so that a
- * whole step enqueues no host synchronisation and takes no host-side value
- * that changes from step to step.  One captured CUDA graph can then be
- * replayed for every step: statistics, decision, update.  The arithmetic is
- * the same as the host-decided path's: the skip and clip decision of
- * fa_clip_decision ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练") and the bias
- * correction and FP32 coefficients of the fused update ([FA-ja]
- * "低レベルの使用"), evaluated in FP64 on the device with the host's operations
- * in the host's order and no contraction.  The results are therefore
- * bit-identical to fa_bucket_step / fa_bucket_step_clipped.
- *
- * Device memory, 80 bytes, 8-byte aligned, owned by the caller.  Zero it once
- * for a fresh optimizer (t = 0, state None); to resume from a checkpoint,
- * write the saved t with every other field zero.  Apart from that only the
- * library writes it.  It may be read back at any time after the stream has passed the
- * step, e.g. for logging without a synchronisation inside the step.
- */
-typedef struct fa_device_step {
-    uint64_t t;            /* steps taken; 0 before the first update                 */
-    uint32_t skipped;      /* 1 when the last call skipped its update                */
-    uint32_t nonfinite;    /* the last report's non-finite count (0 without report)  */
-    double grad_norm;      /* the last report's L2 norm after unscaling (0 without)  */
-    double clip_coef;      /* the clip coefficient of the last call (1 without clip) */
-    uint32_t reserved[12]; /* the library's own: the pending update's coefficients   */
-} fa_device_step;
-
-/*
- * fa_bucket_step with the step count in ``dstep``.  Enqueues three kernels:
- * a one-thread decision kernel, then the first-step and the steady update
- * kernels, each of which returns at once unless the decision selected it.
- * With ``report_dev`` (as produced by fa_merge_gradient_stats earlier on the
- * stream) the decision skips the update when the report counts a non-finite
- * value and otherwise clips by max_grad_norm (<= 0: no clip); without it
- * (NULL) every call updates, unclipped.  A skipped call leaves p, m, v, vmax
- * and dstep->t unchanged.  Nothing is enqueued for n_total == 0 or
- * ctl.skip_update (a graph captured with skip_update set does nothing).
- * dstep must not overlap any other buffer (FA_ERR_ALIAS).
- *
- * Graph capture: nothing here synchronises or reads device memory on the
- * host.  While ``stream`` is capturing, its device is not checked (CUDA
- * cannot report it then).  The first call for a given shape configures
- * kernel attributes and caches occupancy figures: make one call outside the
- * capture first (on buffers of the same sizes and dtypes), as usual before
- * capturing.
- */
-fa_status fa_bucket_step_capturable(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                                    float *p, const void *g, fa_dtype gdt, float *m, float *v,
-                                    float *vmax, fa_device_step *dstep,
-                                    const fa_options *options, fa_step_control ctl,
-                                    const fa_stats *report_dev, double max_grad_norm,
-                                    void *stream);
-
-/*
- * The whole statistics-guarded step without a host synchronisation: the
- * analysis, the merge into ``report_dev``, then fa_bucket_step_capturable
- * gated on that report.  Arguments as fa_bucket_step_clipped, with dstep in
- * place of t and no host report (read dstep after the stream has passed the
- * step).  Bit-identical to fa_bucket_step_clipped.
- */
-fa_status fa_bucket_step_clipped_capturable(const int64_t *seg_offsets, int32_t nseg,
-                                            int64_t n_total, float *p, const void *g,
-                                            fa_dtype gdt, float *m, float *v, float *vmax,
-                                            fa_device_step *dstep, const fa_options *options,
-                                            fa_step_control ctl, double max_grad_norm,
-                                            int32_t row_len, fa_stats *rows_buf,
-                                            int64_t rows_capacity, float *scratch,
-                                            int64_t scratch_elements, fa_stats *report_dev,
-                                            void *stream);
 
 /* ---- gradient statistics -------------------------------------------------- */
 

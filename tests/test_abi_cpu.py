@@ -251,40 +251,3 @@ def test_chunk_scratch_plan():
         with pytest.raises(fa.FusedAdamWError) as e:
             fa.fa_stats_chunk_scratch(bad)
         assert e.value.status == code
-
-
-def test_device_step_record_layout():
-    """The host image of fa_device_step matches the header's 80-byte layout."""
-    from amsgrad_optimizer_step_gb300 import FaDeviceStep
-    assert ctypes.sizeof(FaDeviceStep) == 80
-    offs = {name: getattr(FaDeviceStep, name).offset
-            for name in ("t", "skipped", "nonfinite", "grad_norm", "clip_coef", "reserved")}
-    assert offs == {"t": 0, "skipped": 8, "nonfinite": 12, "grad_norm": 16, "clip_coef": 24,
-                    "reserved": 32}
-
-
-def test_capturable_validation_without_gpu(lib):
-    """Validation of the device-resident step runs before any CUDA call: a missing
-    record, bad options, a NaN clip bound or a bad segment table are rejected; an empty
-    bucket or skip_update returns FA_OK with nothing enqueued."""
-    o = fa.options()
-    fake = ctypes.c_void_p(0x1000)
-    seg = (ctypes.c_int64 * 2)(0, 5)
-
-    def call(n=10, dstep=fake, opts=o, ctl=fa.control(), max_norm=1.0, segs=None, nseg=0):
-        return lib.fa_bucket_step_capturable(segs, nseg, n, None, None, 0, None, None, None,
-                                             dstep, ctypes.byref(opts), ctl, None, max_norm,
-                                             None)
-
-    assert call(dstep=None) == 1
-    bad = fa.options(beta1=1.0)
-    assert call(opts=bad) == 4
-    assert call(max_norm=float("nan")) == 4
-    assert call(ctl=fa.control(gradient_scale=0.0)) == 4
-    assert call(segs=seg, nseg=1, n=10) == 10
-    assert call(n=0) == 0
-    assert call(ctl=fa.control(skip_update=True)) == 0
-    st = lib.fa_bucket_step_clipped_capturable(None, 0, 0, None, None, 0, None, None, None,
-                                               fake, ctypes.byref(o), fa.control(), 1.0, 256,
-                                               None, 0, None, 0, None, None)
-    assert st == 0

@@ -229,88 +229,3 @@ def test_low_precision_params_keep_fp32_masters(dtype):
         gate(_host(master), r.p, 1e-5, "master")
         bits = p.detach().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
         assert np.array_equal(bits, lib.model_copy(_host(master), name))
-
-
-def _same_state(a_params, a_opt, b_params, b_opt):
-    for p, q in zip(a_params, b_params):
-        assert torch.equal(p, q)
-        for key in ("exp_avg", "exp_avg_sq", "max_exp_avg_sq"):
-            if key in a_opt.state[p]:
-                assert torch.equal(a_opt.state[p][key], b_opt.state[q][key]), key
-
-
-@pytest.mark.parametrize("clip,amsgrad", [(0.05, True), (None, False)])
-def test_capturable_mode_matches_default_bitwise(clip, amsgrad):
-    pa, pb = _params(8), _params(8)
-    kw = dict(lr=2e-3, weight_decay=0.01, amsgrad=amsgrad, max_grad_norm=clip)
-    a = FusedAdamW(pa, **kw)
-    b = FusedAdamW(pb, capturable=True, **kw)
-    for step in range(1, 7):
-        grads = _grads(8, step)
-        if step == 4 and clip is not None:
-            grads[0][3, 2] = float("nan")
-        _set_grads(pa, grads)
-        _set_grads(pb, grads)
-        a.step()
-        b.step()
-        torch.cuda.synchronize()
-        assert b.last_report["skipped"] == a.last_report["skipped"] == (step == 4 and clip is not None)
-        assert b.last_report["clip_coef"] == a.last_report["clip_coef"]
-        if clip is not None and not a.last_report["skipped"]:
-            assert b.last_report["grad_norm"] == a.last_report["grad_norm"]
-        _same_state(pa, a, pb, b)
-    assert float(b.state_dict()["state"][0]["step"]) == float(a.state_dict()["state"][0]["step"])
-
-
-def test_capturable_step_replayed_from_a_cuda_graph():
-    """opt.step() captured once, replayed for every step with fresh gradients copied into
-    the bucket; equal bit for bit to the default mode, a NaN step skipped inside a replay."""
-    kw = dict(lr=1e-3, amsgrad=True, max_grad_norm=0.05)
-    warm_params = _params(9)
-    warm = FusedAdamW(warm_params, capturable=True, **kw)  # kernel attributes, occupancy caches
-    _set_grads(warm_params, _grads(9, 1))
-    warm.step()
-    torch.cuda.synchronize()
-
-    pa, pb = _params(10), _params(10)
-    a = FusedAdamW(pa, **kw)
-    b = FusedAdamW(pb, capturable=True, **kw)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        b.step()
-    for step in range(1, 7):
-        grads = _grads(10, step)
-        if step == 3:
-            grads[0][5, 5] = float("inf")
-        _set_grads(pa, grads)
-        _set_grads(pb, grads)
-        a.step()
-        graph.replay()
-        torch.cuda.synchronize()
-        _same_state(pa, a, pb, b)
-    assert float(b.state_dict()["state"][0]["step"]) == 5
-
-
-def test_capturable_state_dict_round_trip_bitwise():
-    kw = dict(lr=1e-3, amsgrad=True, max_grad_norm=0.5)
-    ref_params = _params(11)
-    ref = FusedAdamW(ref_params, capturable=True, **kw)
-    _train(ref, ref_params, 8)
-    params = _params(11)
-    opt = FusedAdamW(params, capturable=True, **kw)
-    _train(opt, params, 4)
-    sd = opt.state_dict()
-    assert float(sd["state"][0]["step"]) == 4
-    fresh = _params(11)
-    with torch.no_grad():
-        for p, q in zip(fresh, params):
-            p.copy_(q)
-    opt2 = FusedAdamW(fresh, capturable=True, **kw)
-    opt2.load_state_dict(sd)
-    _train(opt2, fresh, 4, first=5)
-    _same_state(ref_params, ref, fresh, opt2)
-
-
-def test_capturable_mode_needs_float32_parameters():
-    with pytest.raises(ValueError, match="float32"):
-        FusedAdamW(_params(12, dtype=torch.bfloat16), capturable=True)
