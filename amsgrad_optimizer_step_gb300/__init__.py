@@ -21,7 +21,7 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
                    FaStepReport, FusedAdamWError, check)
 
 __all__ = [
-    "fa_abi_version", "fa_device_error", "fa_pipeline_selftest", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
+    "fa_abi_version", "fa_device_error", "fa_bounds_check_report", "fa_pipeline_selftest", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
     "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback",
     "fa_adamw_step_staged", "fa_stats_plan",
     "fa_stats_rows",
@@ -102,6 +102,15 @@ def fa_device_error(clear: bool = False) -> int:
     v = ctypes.c_int32()
     check("fa_device_error", _L().fa_device_error(ctypes.byref(v), int(bool(clear))))
     return v.value
+
+
+def fa_bounds_check_report(clear: bool = False) -> tuple[bool, int]:
+    """(checked build?, out-of-range accesses counted and skipped since the last clear)."""
+    en = ctypes.c_int32()
+    n = ctypes.c_uint64()
+    check("fa_bounds_check_report",
+          _L().fa_bounds_check_report(ctypes.byref(en), ctypes.byref(n), int(bool(clear))))
+    return bool(en.value), int(n.value)
 
 
 def fa_pipeline_selftest(p, g, m, v, stream=None) -> int:

@@ -6,6 +6,7 @@ fallback of any kind.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -52,6 +53,7 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [c_i32]),
     "fa_options_default": (FaOptions, []),
     "fa_device_error": (c_i32, [PI32, c_i32]),
+    "fa_bounds_check_report": (c_i32, [PI32, PU64, c_i32]),
     "fa_pipeline_selftest": (c_i32, [c_i64, P, P, c_i32, P, P, PI32, P]),
     "fa_step_coefficients": (c_i32, [ctypes.POINTER(FaOptions), c_u64, c_f64, c_f64,
                                      ctypes.POINTER(ctypes.c_float)]),
@@ -97,13 +99,11 @@ SIGNATURES = {
 }
 
 _LIB = None
+_OVERRIDE = None  # a library variant used in place of the normal one (see ``using``)
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """The loaded library; raises if it has not been built."""
-    global _LIB
-    if _LIB is not None:
-        return _LIB
+def open_library(path: str) -> ctypes.CDLL:
+    """Loads a build of the library at ``path`` with every signature declared."""
     if not os.path.exists(path):
         raise RuntimeError(
             f"{os.path.basename(path)} is not built: run amsgrad_optimizer_step_gb300.build.build() "
@@ -113,8 +113,29 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _LIB = lib
     return lib
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _OVERRIDE is not None:
+        return _OVERRIDE
+    if _LIB is None:
+        _LIB = open_library(path)
+    return _LIB
+
+
+@contextlib.contextmanager
+def using(lib: ctypes.CDLL):
+    """Routes every binding call through ``lib`` (e.g. the bounds-checked build)."""
+    global _OVERRIDE
+    prev = _OVERRIDE
+    _OVERRIDE = lib
+    try:
+        yield lib
+    finally:
+        _OVERRIDE = prev
 
 
 class FusedAdamWError(RuntimeError):

@@ -20,6 +20,14 @@ LIB_NAME = "libfused_adamw.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 BUILD_DIR = os.path.join(PKG, "_build")
 
+# Build variants: the normal library, and the bounds-checked test variant whose
+# kernels count and skip any access outside their arrays (-DFA_BOUNDS_CHECK=1).
+VARIANTS = {
+    "normal": (LIB_PATH, BUILD_DIR, []),
+    "checked": (os.path.join(PKG, "libfused_adamw_checked.so"),
+                os.path.join(PKG, "_build_checked"), ["-DFA_BOUNDS_CHECK=1"]),
+}
+
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Host code without floating-point contraction: the FP64 coefficient arithmetic then
 # rounds the same on x86-64 and AArch64 (whose compilers may otherwise fuse 1 - lr*wd).
@@ -45,23 +53,25 @@ def _deps() -> list[str]:
     return sources() + hdrs + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          variant: str = "normal") -> str:
     """Compile and link the library if any source is newer; returns its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    lib_path, build_dir, defines = VARIANTS[variant]
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + defines
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *COMMON, *extra, "-c", src, "-o", obj]
         if src.endswith(".cpp"):
             cmd[1:1] = ["-x", "cu"]
@@ -74,16 +84,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=8) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                variant="checked" if "--checked" in sys.argv else "normal"))

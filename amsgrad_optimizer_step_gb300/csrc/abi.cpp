@@ -289,6 +289,26 @@ fa_status fa_device_error(int32_t *flag, int32_t clear) {
     return FA_OK;
 }
 
+fa_status fa_bounds_check_report(int32_t *enabled, uint64_t *violations, int32_t clear) {
+    if (!enabled) return FA_ERR_NULL;
+    *enabled = FA_BOUNDS_CHECK;
+    if (!violations) return FA_OK;
+#if FA_BOUNDS_CHECK
+    unsigned long long a = 0, b = 0, c = 0;
+    if (fa::update_bounds_violations(&a, clear != 0) != cudaSuccess ||
+        fa::stats_bounds_violations(&b, clear != 0) != cudaSuccess ||
+        fa::staged_bounds_violations(&c, clear != 0) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    *violations = a + b + c;
+#else
+    (void)clear;
+    *violations = 0;
+#endif
+    return FA_OK;
+}
+
 fa_status fa_pipeline_selftest(int64_t n, float *p, const void *g, fa_dtype gdt, float *m,
                                float *v, int32_t *flag, void *stream) {
     if (!flag) return FA_ERR_NULL;
@@ -744,6 +764,7 @@ fa_status fa_analyze_gradient(const void *g, fa_dtype gdt, int64_t n, int32_t ro
         const int32_t cnt = ns - k0 < fa::kMaxSegPerLaunch ? ns - k0 : fa::kMaxSegPerLaunch;
         fa::AnalyzeArgs a;
         a.g = g;
+        a.n = n;
         a.out = rows_out + row_base;
         a.row_len = row_len;
         a.nseg = cnt;

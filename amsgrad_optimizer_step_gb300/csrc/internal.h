@@ -7,6 +7,32 @@
 
 #include "fused_adamw.h"
 
+// Bounds-checked build (-DFA_BOUNDS_CHECK=1, a test variant of the library): every
+// kernel checks the element range it is about to touch against the length of its
+// array; an access outside it is counted in the translation unit's device counter
+// and skipped, never performed.  The normal build compiles the checks out.
+#ifndef FA_BOUNDS_CHECK
+#define FA_BOUNDS_CHECK 0
+#endif
+
+#if defined(__CUDACC__)
+#if FA_BOUNDS_CHECK
+#define FA_BOUNDS_COUNTER(counter)                                                     \
+    static __device__ unsigned long long counter;                                     \
+    __device__ __forceinline__ bool fa_in_bounds(int64_t first, int64_t count,          \
+                                                 int64_t n) {                          \
+        if (first >= 0 && count >= 0 && first + count <= n) return true;              \
+        atomicAdd(&counter, 1ull);                                                     \
+        return false;                                                                  \
+    }
+#else
+#define FA_BOUNDS_COUNTER(counter)                                                     \
+    __device__ __forceinline__ constexpr bool fa_in_bounds(int64_t, int64_t, int64_t) { \
+        return true;                                                                   \
+    }
+#endif
+#endif
+
 namespace fa {
 
 constexpr int kThreads = 256;            // threads per CTA for every kernel here
@@ -52,6 +78,13 @@ cudaError_t launch_pipeline_selftest(const UpdateArgs &a, const Coef &c, fa_dtyp
 // wait in its shared-memory pipeline gives up.  Waits for the device.
 cudaError_t update_pipeline_error(int *flag, bool clear);
 
+// Out-of-range accesses counted (and skipped) by each file's kernels in the
+// bounds-checked build since the last clear; always 0 in the normal build.
+// Wait for the device.
+cudaError_t update_bounds_violations(unsigned long long *count, bool clear);
+cudaError_t stats_bounds_violations(unsigned long long *count, bool clear);
+cudaError_t staged_bounds_violations(unsigned long long *count, bool clear);
+
 // model_dtype: FA_F16 or FA_BF16 when a.p_model is set, else kNoModel.
 constexpr int kNoModel = -1;
 cudaError_t launch_update(const UpdateArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,
@@ -69,6 +102,7 @@ cudaError_t launch_staged(const StagedArgs &a, const Coef &c, fa_dtype gdt, bool
 // Row-statistics launch over up to kMaxSegPerLaunch segments.
 struct AnalyzeArgs {
     const void *g;
+    int64_t n;            // elements of g (bounds-checked build)
     fa_stats *out;        // first row record of this launch
     int64_t row_len;
     int64_t rows;         // rows in this launch

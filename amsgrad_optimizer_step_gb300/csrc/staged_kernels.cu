@@ -24,6 +24,8 @@
 namespace fa {
 namespace {
 
+FA_BOUNDS_COUNTER(g_staged_oob)
+
 template <int GT>
 __device__ __forceinline__ float grad1(const void *g, int64_t i) {
     if (GT == FA_F32) return __ldcs(static_cast<const float *>(g) + i);
@@ -50,8 +52,10 @@ __device__ __forceinline__ void grid_stride_vec4(int64_t n, FV body_vec, FS body
     const int64_t nv = n / 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (int64_t q = first; q < nv; q += stride) body_vec(4 * q);
-    for (int64_t i = 4 * nv + first; i < n; i += stride) body_scalar(i);
+    for (int64_t q = first; q < nv; q += stride)
+        if (fa_in_bounds(4 * q, 4, n)) body_vec(4 * q);
+    for (int64_t i = 4 * nv + first; i < n; i += stride)
+        if (fa_in_bounds(i, 1, n)) body_scalar(i);
 }
 
 // Stage 1: m = beta1*m + (1-beta1)*g   (first step: m = (1-beta1)*g, m not read)
@@ -173,6 +177,19 @@ cudaError_t launch_staged_gt(const StagedArgs &a, const Coef &c, bool ams, bool 
 }
 
 }  // namespace
+
+cudaError_t staged_bounds_violations(unsigned long long *count, bool clear) {
+#if FA_BOUNDS_CHECK
+    cudaError_t err = cudaMemcpyFromSymbol(count, g_staged_oob, sizeof(*count));
+    if (err != cudaSuccess || !clear) return err;
+    const unsigned long long zero = 0;
+    return cudaMemcpyToSymbol(g_staged_oob, &zero, sizeof(zero));
+#else
+    (void)clear;
+    *count = 0;
+    return cudaSuccess;
+#endif
+}
 
 cudaError_t launch_staged(const StagedArgs &a, const Coef &c, fa_dtype gdt, bool amsgrad,
                           bool first, cudaStream_t stream) {

@@ -27,6 +27,8 @@ namespace {
 constexpr int kVec = 8;
 constexpr int kRowsPerWarp = 4;  // rows a warp analyses concurrently
 
+FA_BOUNDS_COUNTER(g_stats_oob)
+
 // Widened value and whether the stored pattern is NaN or +-Inf (exponent all ones).
 template <int GT>
 struct StatIO;
@@ -154,10 +156,11 @@ analyze_kernel(const __grid_constant__ AnalyzeArgs a) {
                 const int64_t end = start + a.row_len < seg_end ? start + a.row_len : seg_end;
                 for (int64_t i = start + lane * kVec; i < end; i += 32 * kVec) {
                     if (VEC && i + kVec <= end) {
-                        StatIO<GT>::acc8(a.g, i, s[j], c[j]);
+                        if (fa_in_bounds(i, kVec, a.n)) StatIO<GT>::acc8(a.g, i, s[j], c[j]);
                     } else {
                         const int64_t e = i + kVec < end ? i + kVec : end;
-                        for (int64_t q = i; q < e; ++q) StatIO<GT>::accs(a.g, q, s[j], c[j]);
+                        for (int64_t q = i; q < e; ++q)
+                            if (fa_in_bounds(q, 1, a.n)) StatIO<GT>::accs(a.g, q, s[j], c[j]);
                     }
                 }
             }
@@ -167,7 +170,7 @@ analyze_kernel(const __grid_constant__ AnalyzeArgs a) {
             const float tot = warp_sum(s[j]);
             const uint32_t cnt = __reduce_add_sync(0xffffffffu, c[j]);
             const int64_t r = r0 + j;
-            if (lane == j && r < a.rows) {
+            if (lane == j && r < a.rows && fa_in_bounds(r, 1, a.rows)) {
                 fa_stats rec;
                 rec.sum_sq = tot;
                 rec.nonfinite = cnt;
@@ -273,7 +276,8 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
     for (int64_t r0 = warp * R; r0 < a.rows; r0 += nwarps * R) {
         uint32_t full = 0, valid = 0;
         uint4 buf[R][CH];
-        if (!MULTI && r0 + R <= single_full_rows) {
+        if (!MULTI && r0 + R <= single_full_rows &&
+            fa_in_bounds(a.seg_start[0] + r0 * kRowElems, R * kRowElems, a.n)) {
             const uint4 *q = reinterpret_cast<const uint4 *>(
                                  gb + (a.seg_start[0] + r0 * kRowElems) * kElemBytes) + lane;
 #pragma unroll
@@ -291,7 +295,8 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
                     if (MULTI)
                         while (k + 1 < a.nseg && a.row_start[k + 1] <= r) ++k;
                     const int64_t start = a.seg_start[k] + (r - a.row_start[k]) * kRowElems;
-                    if (start + kRowElems <= a.seg_start[k + 1]) {
+                    if (start + kRowElems <= a.seg_start[k + 1] &&
+                        fa_in_bounds(start, kRowElems, a.n)) {
                         full |= 1u << j;
                         const uint4 *q =
                             reinterpret_cast<const uint4 *>(gb + start * kElemBytes) + lane;
@@ -338,7 +343,8 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
                 const int64_t end = a.seg_start[ks + 1];
                 float sj = 0.f;
                 uint32_t c = 0;
-                for (int64_t i = start + lane; i < end; i += 32) StatIO<GT>::accs(a.g, i, sj, c);
+                for (int64_t i = start + lane; i < end; i += 32)
+                    if (fa_in_bounds(i, 1, a.n)) StatIO<GT>::accs(a.g, i, sj, c);
                 sj = warp_sum(sj);
                 c = __reduce_add_sync(0xffffffffu, c);
                 if (my_row == j) {
@@ -347,7 +353,8 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
                 }
             }
         }
-        if ((lane & ((32 >> kLog2R) - 1)) == 0 && ((valid >> my_row) & 1u)) {
+        if ((lane & ((32 >> kLog2R) - 1)) == 0 && ((valid >> my_row) & 1u) &&
+            fa_in_bounds(r0 + my_row, 1, a.rows)) {
             fa_stats rec;
             rec.sum_sq = tot;
             rec.nonfinite = cnt;
@@ -379,12 +386,14 @@ __device__ __forceinline__ void df_add(float &h, float &l, float bh, float bl) {
 // per-warp partials are added in FP64.  The total leaves as an FP32 (hi, lo)
 // pair.
 __device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int64_t lo,
-                                            int64_t hi, fa_stats *__restrict__ out) {
+                                            int64_t hi, int64_t in_count,
+                                            fa_stats *__restrict__ out) {
     __shared__ double s_sum[kThreads / 32];
     __shared__ unsigned long long s_cnt[kThreads / 32];
     constexpr int kU = kFanIn / kThreads;  // records per thread per pass, loaded together
     float sh = 0.f, sl = 0.f;
     unsigned long long c = 0;
+    if (!fa_in_bounds(lo, hi - lo, in_count)) hi = lo;  // (bounds-checked build only)
     for (int64_t base = lo + threadIdx.x; base < hi; base += kThreads * kU) {
         fa_stats r[kU];
 #pragma unroll
@@ -434,7 +443,7 @@ __global__ void __launch_bounds__(kThreads)
 merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
     const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kFanIn;
     const int64_t g1 = g0 + kFanIn < count ? g0 + kFanIn : count;
-    block_merge(in, g0, g1, out + blockIdx.x);
+    block_merge(in, g0, g1, count, out + blockIdx.x);
 }
 
 // Per-chunk merge, level A: one CTA per group of at most kFanIn records of one
@@ -454,7 +463,7 @@ merge_chunks_a_kernel(const __grid_constant__ ChunkMergeArgs a) {
     const int k = find_chunk(a, b);
     const int64_t lo = a.row_start[k] + (b - a.group_start[k]) * kFanIn;
     const int64_t hi = lo + kFanIn < a.row_start[k + 1] ? lo + kFanIn : a.row_start[k + 1];
-    block_merge(a.in, lo, hi, a.partial + b);
+    block_merge(a.in, lo, hi, a.row_start[a.nchunks], a.partial + b);
 }
 
 // Level B: one CTA per chunk over its level-A records (an empty chunk gives a
@@ -462,7 +471,8 @@ merge_chunks_a_kernel(const __grid_constant__ ChunkMergeArgs a) {
 __global__ void __launch_bounds__(kThreads)
 merge_chunks_b_kernel(const __grid_constant__ ChunkMergeArgs a) {
     const int k = blockIdx.x;
-    block_merge(a.partial, a.group_start[k], a.group_start[k + 1], a.out + k);
+    block_merge(a.partial, a.group_start[k], a.group_start[k + 1], a.group_start[a.nchunks],
+                a.out + k);
 }
 
 template <int GT, int CH, bool MULTI>
@@ -519,6 +529,19 @@ cudaError_t launch_analyze(const AnalyzeArgs &a, fa_dtype gdt, bool vector_ok,
         case FA_BF16: return launch_analyze_typed<FA_BF16>(a, vector_ok, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t stats_bounds_violations(unsigned long long *count, bool clear) {
+#if FA_BOUNDS_CHECK
+    cudaError_t err = cudaMemcpyFromSymbol(count, g_stats_oob, sizeof(*count));
+    if (err != cudaSuccess || !clear) return err;
+    const unsigned long long zero = 0;
+    return cudaMemcpyToSymbol(g_stats_oob, &zero, sizeof(zero));
+#else
+    (void)clear;
+    *count = 0;
+    return cudaSuccess;
+#endif
 }
 
 cudaError_t launch_merge_chunks(const ChunkMergeArgs &a, cudaStream_t stream) {

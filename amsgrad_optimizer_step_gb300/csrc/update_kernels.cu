@@ -52,6 +52,8 @@ namespace {
 constexpr int kVec = 8;  // elements per vector
 constexpr int kUThreads = FA_UPDATE_THREADS;
 
+FA_BOUNDS_COUNTER(g_update_oob)
+
 // 16-byte evict-first loads of the vector body.
 __device__ __forceinline__ float4 ld16(const float4 *q) {
 #if FA_UPDATE_L2_PREFETCH
@@ -231,6 +233,7 @@ __device__ __forceinline__ void store1_model(void *base, int64_t i, float x) {
 
 template <int GT, bool AMS, bool FIRST, int MD>
 __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &c, int64_t i) {
+    if (!fa_in_bounds(i, 1, a.n)) return;
     float x = GradIO<GT>::load1(a.g, i);
     float p = __ldcs(a.p_in + i);
     float m = 0.f, v = 0.f, vm = 0.f;
@@ -262,10 +265,12 @@ update_vec_kernel(const UpdateArgs a, const Coef c0) {
          base < a.nvec; base += stride) {
         float x[UNROLL][kVec], p[UNROLL][kVec], m[UNROLL][kVec], v[UNROLL][kVec],
             vm[UNROLL][kVec];
+        bool ok[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t vi = base + static_cast<int64_t>(u) * kUThreads;
-            if (vi < a.nvec) {
+            ok[u] = vi < a.nvec && fa_in_bounds(a.head + vi * kVec, kVec, a.n);
+            if (ok[u]) {
                 const int64_t e = a.head + vi * kVec;
                 GradIO<GT>::load8(a.g, e, x[u]);
                 load8f(a.p_in, e, p[u]);
@@ -279,7 +284,7 @@ update_vec_kernel(const UpdateArgs a, const Coef c0) {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t vi = base + static_cast<int64_t>(u) * kUThreads;
-            if (vi < a.nvec) {
+            if (ok[u]) {
                 const int64_t e = a.head + vi * kVec;
 #pragma unroll
                 for (int k = 0; k < kVec; ++k)
@@ -465,6 +470,9 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
     auto issue_loads = [&](int s, int64_t tile) {
         unsigned char *b = smem + s * L::kStage;
         const int64_t e = a.head + tile * L::kTile;
+        // (a tile out of range is skipped; its wait then runs out and the
+        // pipeline's error flag is raised as well)
+        if (!fa_in_bounds(e, L::kTile, a.n)) return;
         mbar_expect_tx(&bars[s], kLoadBytes + a.extra_tx);
         bulk_load(b + L::kP, a.p_in + e, L::kTile * 4, &bars[s]);
         bulk_load(b + L::kG, static_cast<const char *>(a.g) + e * L::kGB, L::kTile * L::kGB,
@@ -601,12 +609,15 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
         __syncthreads();
         if (tid == 0) {
             const int64_t e = a.head + tile * L::kTile;
-            bulk_store(a.p_out + e, b + L::kP, L::kTile * 4);
-            bulk_store(a.m_out + e, b + L::kM, L::kTile * 4);
-            bulk_store(a.v_out + e, b + L::kV, L::kTile * 4);
-            if (AMS) bulk_store(a.vmax_out + e, b + L::kVM, L::kTile * 4);
-            if (MD != kNoModel)
-                bulk_store(static_cast<uint16_t *>(a.p_model) + e, b + L::kModel, L::kTile * 2);
+            if (fa_in_bounds(e, L::kTile, a.n)) {
+                bulk_store(a.p_out + e, b + L::kP, L::kTile * 4);
+                bulk_store(a.m_out + e, b + L::kM, L::kTile * 4);
+                bulk_store(a.v_out + e, b + L::kV, L::kTile * 4);
+                if (AMS) bulk_store(a.vmax_out + e, b + L::kVM, L::kTile * 4);
+                if (MD != kNoModel)
+                    bulk_store(static_cast<uint16_t *>(a.p_model) + e, b + L::kModel,
+                               L::kTile * 2);
+            }
             bulk_commit();
             // refill the stage used one iteration ago: its stores had a whole
             // iteration to finish reading shared memory
@@ -690,6 +701,7 @@ update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
     int k = 0;  // segment of e; e only grows, so a forward scan finds it
     for (int64_t vi = tid; vi < a.nvec; vi += stride) {
         const int64_t e = a.head + vi * kVec;
+        if (!fa_in_bounds(e, kVec, a.n)) continue;
         float x[kVec], p[kVec], m[kVec], v[kVec], vm[kVec];
         GradIO<GT>::load8(a.g, e, x);
         load8f(a.p_in, e, p);
@@ -860,6 +872,19 @@ cudaError_t launch_pipeline_selftest(const UpdateArgs &a, const Coef &c, fa_dtyp
     return cudaErrorInvalidValue;
 #else
     (void)a; (void)c; (void)gdt; (void)stream;
+    return cudaSuccess;
+#endif
+}
+
+cudaError_t update_bounds_violations(unsigned long long *count, bool clear) {
+#if FA_BOUNDS_CHECK
+    cudaError_t err = cudaMemcpyFromSymbol(count, g_update_oob, sizeof(*count));
+    if (err != cudaSuccess || !clear) return err;
+    const unsigned long long zero = 0;
+    return cudaMemcpyToSymbol(g_update_oob, &zero, sizeof(zero));
+#else
+    (void)clear;
+    *count = 0;
     return cudaSuccess;
 #endif
 }

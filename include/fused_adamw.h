@@ -115,6 +115,17 @@ const char *fa_status_string(fa_status status);
  * clear != 0.  Waits for the device; FA_ERR_CUDA if it cannot be read. */
 fa_status fa_device_error(int32_t *flag, int32_t clear);
 
+/* Bounds-checked build (a test variant of the library compiled with
+ * -DFA_BOUNDS_CHECK=1; the pages have no counterpart): every kernel checks the
+ * element range it is about to touch against its array's length, and counts
+ * and skips an access outside it instead of performing it.  *enabled is 1 in
+ * that build and 0 in the normal one.  When violations is not NULL it receives
+ * the number of out-of-range accesses on the current device since the last
+ * clear (always 0 in the normal build, which touches no device for this);
+ * clear != 0 resets the count.  Waits for the device in the checked build;
+ * FA_ERR_CUDA if the count cannot be read. */
+fa_status fa_bounds_check_report(int32_t *enabled, uint64_t *violations, int32_t clear);
+
 /* Self-test of the bounded waits above, with no fault: one steady-state update
  * of the n-element p, m, v (device, FP32) with gradient g, launched so that
  * every shared-memory stage waits for 16 bytes that never arrive.  Each wait
