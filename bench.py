@@ -182,6 +182,46 @@ def oracle_steps(w, sample: int, steps: int, warmup: int):
     return statistics.median(times[warmup:]), 1
 
 
+def host_info() -> dict:
+    """CPU model, core count and architecture of the host."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return {"cpu": model or platform.processor() or "unknown", "cores": host_cores(),
+            "machine": platform.machine()}
+
+
+def gpu_info(dev) -> dict:
+    import torch
+    prop = torch.cuda.get_device_properties(dev)
+    driver = None
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(dev.index or 0)], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        driver = out.splitlines()[0] if out else None
+    except Exception:
+        pass
+    return {"name": prop.name, "sms": prop.multi_processor_count,
+            "memory_gib": round(prop.total_memory / 2 ** 30, 1), "driver": driver,
+            "cuda_runtime": torch.version.cuda, "torch": torch.__version__}
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -314,6 +354,7 @@ def run_reference(args):
             "config": config_dict(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": what},
+            "host": host_info(),
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -746,6 +787,8 @@ def run_ours(args):
                            "achieved_gbs": (n * 2 + rows * 12) / (st_ms * 1e-3) / 1e9},
             "gpu_launches": timed_launches,
             "clocks": clock_info,
+            "host": host_info(),
+            "gpu": gpu_info(dev),
             "e2e": e2e,
             "next_rows": next_rows,
         }
