@@ -147,6 +147,71 @@ def test_misaligned_views(gdt, offsets):
     gate(views["vmax"].cpu().numpy(), traj.state.vmax, 1e-6, "vmax")
 
 
+# ---- degenerate hyper-parameters ------------------------------------------------
+
+DEGENERATE = {
+    "lr0": dict(lr=0.0),
+    "wd0": dict(weight_decay=0.0),
+    "beta1_0": dict(beta1=0.0),
+    "beta2_0": dict(beta2=0.0),
+    "betas_0": dict(beta1=0.0, beta2=0.0),
+    # seed 4: no gradient value is exactly zero at these sizes (with eps 0 a zero
+    # gradient on the first step gives 0/0 on both sides)
+    "eps0": dict(eps=0.0, seed=4),
+}
+
+
+@pytest.mark.parametrize("n", [4097, 1_000_003])
+@pytest.mark.parametrize("name", sorted(DEGENERATE))
+def test_degenerate_options_vs_oracle(name, n):
+    """Boundary values of the options: lr 0 (p must stay bit-identical), no decay,
+    beta1 or beta2 = 0 (bias corrections exactly 1), eps 0 (no zero gradient present)."""
+    w = dataclasses.replace(CONFIG2, calls=4, skip_calls=(), amsgrad=True, inplace=True,
+                            **DEGENERATE[name]).scaled(n)
+    if name == "eps0":
+        for call in range(1, w.calls + 1):
+            assert not (widen(w, call) == 0).any(), "a zero gradient would make 0/0 here"
+    p0 = None
+    if name == "lr0":
+        p0 = torch.empty(n, device=DEV)
+        w.fill_params_device(p0)
+    s = run_workload(w, n, "inplace", DEV, guard=64)
+    assert s["t"] == 4
+    if p0 is not None:
+        assert torch.equal(s["state"].p, p0)
+
+
+def widen(w, call):
+    from gpu_harness import widen_host
+    return widen_host(w.grad_host(call, np.arange(w.n)), w.grad_dtype)
+
+
+@pytest.mark.parametrize("t", [1_000, 1_000_000, 100_000_000])
+def test_large_step_count_vs_oracle(t, oracle_lib):
+    """Far into training beta^t underflows and the bias corrections are exactly 1."""
+    from gpu_harness import gate, oracle_one_step
+    n = 100_003
+    w = dataclasses.replace(CONFIG2, amsgrad=True, skip_calls=()).scaled(n)
+    opts = w.options()
+    p, m, v, vm = (torch.empty(n, device=DEV) for _ in range(4))
+    w.fill_params_device(p)
+    rng = np.random.default_rng(11)
+    for x in (m, v, vm):
+        x.copy_(torch.from_numpy(rng.random(n, dtype=np.float32) * 1e-4))
+    vm.copy_(torch.maximum(vm, v))
+    g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    w.fill_grad_device(1, g)
+    before = [x.double().cpu().numpy() for x in (p, m, v, vm)]
+    t_new, upd = fa.fa_adamw_step_inplace(p, g, m, v, vm, t, fa.options(**opts),
+                                          fa.control(w.gradient_scale))
+    torch.cuda.synchronize()
+    assert t_new == t + 1 and upd
+    ref = oracle_one_step(w.grad_host(1, np.arange(n)), w.grad_dtype, opts, w.gradient_scale,
+                          1.0, t + 1, before, oracle_lib)
+    for dev_x, ref_x, nm in zip((p, m, v, vm), ref, "p m v vmax".split()):
+        gate(dev_x.cpu().numpy(), ref_x, 1e-6, f"t={t} {nm}")
+
+
 # ---- bitwise invariants ---------------------------------------------------------
 
 def _fresh(n, gdt, seed, ams=True):
@@ -593,6 +658,41 @@ def test_gated_step_equals_host_decided_step_bitwise(max_norm):
     assert ra[1][1] == 1  # the +Inf call was skipped
     for x, y in zip(sa, sb):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_gated_step_full_size_bitwise():
+    """The benchmark's launch configuration: the 1,073,741,824-parameter workload, rows of
+    256, the update gated on the device report, five calls with the +Inf in call 3;
+    bit-identical at every call to the host-decided step (itself checked against the
+    oracle at this size in test_config5_full_size_sampled)."""
+    w = CONFIG5
+    n = w.n
+    g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    states = []
+    for _ in range(2):
+        p = torch.empty(n, device=DEV)
+        w.fill_params_device(p)
+        rows = fa.fa_stats_rows(n, w.row_len)
+        states.append({"p": p, "m": torch.empty_like(p), "v": torch.empty_like(p), "t": 0,
+                       "rows": fa.stats_buffer(rows, DEV), "scr": fa.scratch_buffer(rows, DEV),
+                       "rep": fa.stats_buffer(1, DEV)})
+    o = fa.options(**w.options())
+    for call in range(1, w.calls + 1):
+        w.fill_grad_device(call, g)
+        reps = []
+        for s_, fn in zip(states, (fa.fa_bucket_step_clipped, fa.fa_bucket_step_clipped_gated)):
+            s_["t"], r = fn(None, s_["p"], g, s_["m"], s_["v"], None, s_["t"], o, fa.control(),
+                            w.max_grad_norm, w.row_len, s_["rows"], s_["scr"], s_["rep"])
+            reps.append((r.updated, r.skipped_nonfinite, r.nonfinite, repr(r.grad_norm),
+                         repr(r.clip_coef)))
+        torch.cuda.synchronize()
+        assert reps[0] == reps[1], (call, reps)
+        assert reps[0][1] == (call == w.inf_call)
+        a, b = states
+        assert a["t"] == b["t"]
+        for k in ("p", "m", "v"):
+            assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), (call, k)
+    assert states[0]["t"] == 4
 
 
 def test_gated_update_skips_on_non_finite_report():
