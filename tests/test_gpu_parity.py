@@ -212,6 +212,48 @@ def test_large_step_count_vs_oracle(t, oracle_lib):
         gate(dev_x.cpu().numpy(), ref_x, 1e-6, f"t={t} {nm}")
 
 
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_non_finite_gradients_propagate_like_the_oracle(gdt, oracle_lib):
+    """A plain step takes no finiteness decision: NaN and +-Inf in the gradient follow
+    IEEE arithmetic, and the AMSGrad max keeps a NaN once it has one.  Special values must
+    sit exactly where the oracle has them; everything else within the usual tolerance."""
+    import oracle
+    n = 1_000_003  # steady steps take the shared-memory pipeline
+    w = dataclasses.replace(CONFIG2, grad_dtype=gdt, calls=3, skip_calls=(), amsgrad=True,
+                            inplace=True, gradient_scale=1.0, grad_premul=1.0).scaled(n)
+    opts = w.options()
+    idx = np.arange(n)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p)
+    m, v, vm = (torch.zeros(n, device=DEV) for _ in range(3))
+    g = torch.empty(n, dtype={"f32": torch.float32, "bf16": torch.bfloat16}[gdt], device=DEV)
+    ref = oracle.OracleAdamW(w.params_host(idx), opts, lib_=oracle_lib)
+    planted = {1: {5: float("nan"), 77_777: float("inf")},
+               2: {5: 1.0, 123_456: float("-inf"), 999_999: float("nan")},
+               3: {}}
+    t = 0
+    for call in range(1, w.calls + 1):
+        w.fill_grad_device(call, g)
+        for i, x in planted[call].items():
+            g[i] = x
+        from gpu_harness import grad_bits_from_device
+        bits = grad_bits_from_device(g)
+        t, _ = fa.fa_adamw_step_inplace(p, g, m, v, vm, t, fa.options(**opts), fa.control())
+        ref.step(bits, gdt)
+        torch.cuda.synchronize()
+        for dev_x, ref_x, nm in ((p, ref.p, "p"), (m, ref.state.m, "m"), (v, ref.state.v, "v"),
+                                 (vm, ref.state.vmax, "vmax")):
+            d = dev_x.cpu().numpy().astype(np.float64)
+            r = np.asarray(ref_x, np.float64)
+            assert np.array_equal(np.isnan(d), np.isnan(r)), f"call {call} {nm}: NaN positions"
+            assert np.array_equal(np.isposinf(d), np.isposinf(r)), f"call {call} {nm}: +Inf"
+            assert np.array_equal(np.isneginf(d), np.isneginf(r)), f"call {call} {nm}: -Inf"
+            fin = np.isfinite(r)
+            from gpu_harness import gate
+            gate(d[fin], r[fin], 1e-5, f"call {call} {nm} (finite elements)")
+    assert np.isnan(vm[5].item()), "the AMSGrad max keeps the NaN of call 1"
+
+
 # ---- bitwise invariants ---------------------------------------------------------
 
 def _fresh(n, gdt, seed, ams=True):
