@@ -245,6 +245,16 @@ fa_status check_inplace(int64_t n, float *p, const void *g, fa_dtype gdt, float 
     return FA_OK;
 }
 
+// The first checks of every step entry point, in this order: options, control,
+// gradient dtype, element count.
+fa_status check_step_args(const fa_options *o, fa_step_control ctl, fa_dtype gdt, int64_t n) {
+    fa_status st;
+    if ((st = check_options(o)) != FA_OK) return st;
+    if ((st = check_control(ctl)) != FA_OK) return st;
+    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    return n < 0 ? FA_ERR_SIZE : FA_OK;
+}
+
 fa_status check_segments(const int64_t *seg, int32_t nseg, int64_t n) {
     if (nseg < 0) return FA_ERR_SEGMENTS;
     if (nseg == 0) return FA_OK;
@@ -391,10 +401,7 @@ fa_status fa_adamw_step(int64_t n, const float *p, const void *g, fa_dtype gdt, 
                         int32_t *updated, void *stream) {
     fa_status st;
     if (!t_out || !updated) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n < 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n)) != FA_OK) return st;
     if (n == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
         *t_out = t_in;
         *updated = 0;
@@ -447,10 +454,7 @@ fa_status fa_adamw_step_inplace(int64_t n, float *p, const void *g, fa_dtype gdt
                                 double grad_mult, int32_t *updated, void *stream) {
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n < 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n)) != FA_OK) return st;
     if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
     if (n == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
         *updated = 0;
@@ -486,11 +490,8 @@ fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int
                                    fa_dtype model_dtype, int32_t *updated, void *stream) {
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
     if (model_dtype != FA_F16 && model_dtype != FA_BF16) return FA_ERR_DTYPE;
-    if (n_total < 0) return FA_ERR_SIZE;
     if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
     if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
     if (n_total == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
@@ -522,10 +523,7 @@ fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt,
                                int32_t *updated, void *stream) {
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n < 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n)) != FA_OK) return st;
     if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
     if (n == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
         *updated = 0;
@@ -563,10 +561,7 @@ fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t
                                fa_step_control ctl, const fa_stats *report_dev,
                                double max_grad_norm, void *stream) {
     fa_status st;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n_total < 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
     if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
     if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
     if (n_total == 0 || ctl.skip_update) return FA_OK;
@@ -626,10 +621,7 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
                                        fa_step_report *out, void *stream) {
     fa_status st;
     if (!t || !out) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n_total < 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
     if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
     if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
     if (*t == UINT64_MAX) return FA_ERR_OPTION;
@@ -918,10 +910,7 @@ fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg
                                         void *stream) {
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n_total < 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
     if (nseg < 1) return FA_ERR_SEGMENTS;
     if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
     if (!seg_grad_mult) return FA_ERR_NULL;
@@ -988,10 +977,8 @@ fa_status fa_bucket_step_clipped_per_segment(
     double *seg_norms, double *seg_coefs, fa_step_report *out, void *stream) {
     fa_status st;
     if (!t || !out) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n_total < 0 || row_len <= 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
+    if (row_len <= 0) return FA_ERR_SIZE;
     if (nseg < 1) return FA_ERR_SEGMENTS;
     if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
     if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
@@ -1110,10 +1097,7 @@ fa_status fa_bucket_step_clipped(const int64_t *seg_offsets, int32_t nseg, int64
                                  fa_step_report *out, void *stream) {
     fa_status st;
     if (!t || !out) return FA_ERR_NULL;
-    if ((st = check_options(options)) != FA_OK) return st;
-    if ((st = check_control(ctl)) != FA_OK) return st;
-    if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
-    if (n_total < 0) return FA_ERR_SIZE;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
     if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
     if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
     if (*t == UINT64_MAX) return FA_ERR_OPTION;
