@@ -597,7 +597,7 @@ def run_ours(args):
     # CUDA events per launch): the plain update and the fused low-precision
     # write-back (BF16 model copy, +2 B/param).
     next_rows = None
-    if args.next_rows_steps > 0:
+    if args.next_rows_steps > 0 and world == 1:  # the single-GPU rows, at N = 1 only
         p_model = torch.empty(n, dtype=torch.bfloat16, device=dev)
 
         def timed(fn, k):
@@ -792,7 +792,7 @@ def run_ours(args):
             "e2e": e2e,
             "next_rows": next_rows,
         }
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:  # rank 0 at N = 1 only
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
     if world > 1:
