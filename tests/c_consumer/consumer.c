@@ -1,0 +1,123 @@
+/*
+ * A plain C program that uses the library through include/fused_adamw.h only:
+ * device buffers from the CUDA runtime, three statistics-guarded steps of the
+ * fused AdamW update (analysis, merge, report, skip/clip decision, update) on
+ * n FP32 parameters with FP32 gradients, the second call carrying a +Inf, then
+ * the final p, m, v and the three step reports written to a binary file.
+ *
+ * Inputs are integer hashes scaled by powers of two, exact in FP32, so the test
+ * that runs this program can rebuild them bit for bit.
+ *
+ *   consumer <n> <output file>
+ */
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <cuda_runtime.h>
+
+#include "fused_adamw.h"
+
+static uint32_t mix(uint32_t x) {
+    x ^= x >> 16;
+    x *= 0x7feb352du;
+    x ^= x >> 15;
+    x *= 0x846ca68bu;
+    x ^= x >> 16;
+    return x;
+}
+
+/* a value in [-scale, scale) with 16 significant bits: exact in FP32 */
+static float sample(uint32_t stream, uint32_t i, float scale) {
+    const int32_t u = (int32_t)(mix(mix(stream) ^ i) >> 16) - 32768;
+    return (float)u / 32768.0f * scale;
+}
+
+#define CHECK_CUDA(x)                                                          \
+    do {                                                                       \
+        cudaError_t e_ = (x);                                                  \
+        if (e_ != cudaSuccess) {                                               \
+            fprintf(stderr, "%s: %s\n", #x, cudaGetErrorString(e_));           \
+            return 2;                                                          \
+        }                                                                      \
+    } while (0)
+
+#define CHECK_FA(x)                                                            \
+    do {                                                                       \
+        fa_status s_ = (x);                                                    \
+        if (s_ != FA_OK) {                                                     \
+            fprintf(stderr, "%s: %s\n", #x, fa_status_string(s_));             \
+            return 3;                                                          \
+        }                                                                      \
+    } while (0)
+
+int main(int argc, char **argv) {
+    if (argc != 3) {
+        fprintf(stderr, "usage: consumer <n> <output file>\n");
+        return 1;
+    }
+    const int64_t n = atoll(argv[1]);
+    if (n < 2) return 1;
+    const int32_t row_len = 256;
+    if (fa_abi_version() != FA_ABI_VERSION) return 4;
+
+    int64_t rows = 0, scratch_elems = 0;
+    int32_t merge_kernels = 0;
+    CHECK_FA(fa_stats_rows(n, row_len, NULL, 0, &rows));
+    CHECK_FA(fa_stats_plan(rows, &merge_kernels, &scratch_elems));
+
+    float *h = (float *)malloc((size_t)n * sizeof(float));
+    float *p, *g, *m, *v, *scratch = NULL;
+    fa_stats *rows_buf, *report;
+    CHECK_CUDA(cudaMalloc((void **)&p, (size_t)n * 4));
+    CHECK_CUDA(cudaMalloc((void **)&g, (size_t)n * 4));
+    CHECK_CUDA(cudaMalloc((void **)&m, (size_t)n * 4));
+    CHECK_CUDA(cudaMalloc((void **)&v, (size_t)n * 4));
+    CHECK_CUDA(cudaMalloc((void **)&rows_buf, (size_t)rows * sizeof(fa_stats)));
+    CHECK_CUDA(cudaMalloc((void **)&report, sizeof(fa_stats)));
+    if (scratch_elems > 0) CHECK_CUDA(cudaMalloc((void **)&scratch, (size_t)scratch_elems * 4));
+    cudaStream_t stream;
+    CHECK_CUDA(cudaStreamCreate(&stream));
+
+    for (int64_t i = 0; i < n; ++i) h[i] = sample(1u, (uint32_t)i, 0.03125f);
+    CHECK_CUDA(cudaMemcpy(p, h, (size_t)n * 4, cudaMemcpyHostToDevice));
+
+    fa_options o = fa_options_default();
+    o.lr = 1e-3;
+    o.amsgrad = 0;
+    fa_step_control ctl;
+    ctl.gradient_scale = 4.0;
+    ctl.skip_update = 0;
+    uint64_t t = 0;
+    fa_step_report reps[3];
+    for (int call = 1; call <= 3; ++call) {
+        for (int64_t i = 0; i < n; ++i) h[i] = sample(100u + (uint32_t)call, (uint32_t)i, 0.0625f);
+        if (call == 2) h[n / 2] = 1.0f / 0.0f; /* +Inf: this step is skipped */
+        CHECK_CUDA(cudaMemcpy(g, h, (size_t)n * 4, cudaMemcpyHostToDevice));
+        CHECK_FA(fa_bucket_step_clipped(NULL, 0, n, p, g, FA_F32, m, v, NULL, &t, &o, ctl,
+                                        0.5, row_len, rows_buf, rows, scratch, scratch_elems,
+                                        report, &reps[call - 1], stream));
+    }
+    CHECK_CUDA(cudaStreamSynchronize(stream));
+
+    FILE *f = fopen(argv[2], "wb");
+    if (!f) return 5;
+    fwrite(&t, sizeof t, 1, f);
+    fwrite(reps, sizeof reps, 1, f);
+    float *bufs[3] = {p, m, v};
+    for (int k = 0; k < 3; ++k) {
+        CHECK_CUDA(cudaMemcpy(h, bufs[k], (size_t)n * 4, cudaMemcpyDeviceToHost));
+        fwrite(h, 4, (size_t)n, f);
+    }
+    fclose(f);
+    cudaFree(p);
+    cudaFree(g);
+    cudaFree(m);
+    cudaFree(v);
+    cudaFree(rows_buf);
+    cudaFree(report);
+    cudaFree(scratch);
+    cudaStreamDestroy(stream);
+    free(h);
+    return 0;
+}
