@@ -46,7 +46,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--next-rows-steps", type=int, default=10)
-    ap.add_argument("--n", type=int, default=0, help="override the parameter count (testing)")
+    # (under torchrun spell it --params: torchrun's own parser takes --n for one of its flags)
+    ap.add_argument("--params", "--n", dest="n", type=int, default=0,
+                    help="override the parameter count (testing)")
     return ap.parse_args()
 
 
@@ -63,7 +65,8 @@ def config_dict(w):
             "optimizer": "adamw", "lr": w.lr, "betas": [w.beta1, w.beta2], "eps": w.eps,
             "weight_decay": w.weight_decay, "row_len": w.row_len, "merge_fan_in": 1024,
             "max_grad_norm": w.max_grad_norm, "gradient_scale": w.gradient_scale,
-            "l2_policy": "inputs larger than L2 (about 30 GB moved per step), no flush"}
+            "l2_policy": f"inputs larger than L2 (about {28 * w.n / 1e9:.0f} GB moved per step), "
+                         "no flush"}
 
 
 def update_kernel_traffic(n):
