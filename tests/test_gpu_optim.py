@@ -229,3 +229,50 @@ def test_low_precision_params_keep_fp32_masters(dtype):
         gate(_host(master), r.p, 1e-5, "master")
         bits = p.detach().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
         assert np.array_equal(bits, lib.model_copy(_host(master), name))
+
+
+def test_empty_and_gradless_parameters():
+    """A zero-element parameter and one that never receives a gradient share a bucket
+    with ordinary ones: the empty one is carried along untouched, the gradless one is
+    updated with a zero gradient (decay only, as the oracle does), the rest as usual."""
+    shapes = [(0,), (17,), (3, 5)]
+    params = _params(13, shapes=shapes)
+    opt = FusedAdamW(params, lr=1e-2, weight_decay=0.1, max_grad_norm=1.0)
+    lib = oracle.lib()
+    oo = dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=0.1, amsgrad=False,
+              maximize=False)
+    refs = [oracle.OracleAdamW(_host(p), oo, lib_=lib) for p in params]
+    for step in range(1, 4):
+        g17 = (torch.randn(17, generator=torch.Generator().manual_seed(step)) * 1e-2)
+        params[0].grad = None
+        params[1].grad = g17.to(DEV)        # a new tensor: gathered into the bucket
+        params[2].grad = None               # never receives a gradient
+        opt.step()
+        grads = [np.zeros(0, np.float32), g17.numpy(), np.zeros(15, np.float32)]
+        allg = np.concatenate(grads)
+        s, c = lib.gradient_stats(allg, "f32")
+        _, norm, coef = lib.clip_decision(s, c, 1.0)
+        for r, g in zip(refs, grads):
+            r.step(g, "f32", clip_coef=coef)
+    torch.cuda.synchronize()
+    assert params[0].numel() == 0
+    for p, r in zip(params[1:], refs[1:]):
+        gate(_host(p), r.p, 1e-5, "p")
+    assert float(opt.state_dict()["state"][1]["step"]) == 3
+
+
+def test_replaced_gradients_are_gathered_into_the_bucket():
+    params = _params(14)
+    ref_params = _params(14)
+    opt = FusedAdamW(params, lr=1e-3)
+    ref = FusedAdamW(ref_params, lr=1e-3)
+    for step in range(1, 4):
+        grads = _grads(14, step)
+        for p, g in zip(params, grads):      # new tensors, not views of the bucket
+            p.grad = g.to(DEV).clone()
+        _set_grads(ref_params, grads)        # written into the bucket views
+        opt.step()
+        ref.step()
+    torch.cuda.synchronize()
+    for p, q in zip(params, ref_params):
+        assert torch.equal(p, q)
