@@ -26,6 +26,13 @@
  *     (fa_merge_gradient_stats_static) and, per host thread that calls
  *     fa_bucket_step_clipped_gated, a 64-byte pinned host staging record and
  *     one event per device, allocated on first use and kept until exit.
+ *   - A stream that is being captured into a CUDA graph is accepted without
+ *     the device check (CUDA cannot report a capturing stream's device).  The
+ *     statistics calls may be captured.  The update calls take the step count
+ *     and the coefficients from the host at every call, so a captured update
+ *     would replay one fixed step: do not capture them ([FA-ja]
+ *     "サポートされている契約": graph replay with a device step counter is not
+ *     supported).
  *   - Parameters and moments are dense contiguous FP32; gradients are dense
  *     contiguous FP32, FP16 or BF16 of the same element count
  *     ([FA-zh] "增加的实际能力").  Strides, broadcasts and sparse gradients
