@@ -27,8 +27,9 @@
  *     fa_bucket_step_clipped_gated, a 64-byte pinned host staging record and
  *     one event per device, allocated on first use and kept until exit.
  *   - A stream that is being captured into a CUDA graph is accepted without
- *     the device check (CUDA cannot report a capturing stream's device).  The
- *     statistics calls may be captured.  The update calls take the step count
+ *     the device check (CUDA cannot report a capturing stream's device).
+ *     fa_analyze_gradient and fa_merge_gradient_stats (and the chunk merge) may
+ *     be captured and replayed.  The update calls take the step count
  *     and the coefficients from the host at every call, so a captured update
  *     would replay one fixed step: do not capture them ([FA-ja]
  *     "サポートされている契約": graph replay with a device step counter is not

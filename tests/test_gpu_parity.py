@@ -455,6 +455,33 @@ def test_merge_matches_exact_sum(rows):
     assert abs(got - exact) <= 1e-12 * exact
 
 
+def test_statistics_capture_into_a_cuda_graph():
+    """Analysis and merge captured once into a CUDA graph and replayed on new gradients
+    give the same report, bit for bit, as the direct calls."""
+    n = 256 * 5000 + 77
+    w = CONFIG5.scaled(n, calls=3)
+    g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    rows = fa.fa_stats_rows(n, 256)
+    rb, sc, rep = fa.stats_buffer(rows, DEV), fa.scratch_buffer(rows, DEV), fa.stats_buffer(1, DEV)
+    rb2, sc2, rep2 = (fa.stats_buffer(rows, DEV), fa.scratch_buffer(rows, DEV),
+                      fa.stats_buffer(1, DEV))
+    w.fill_grad_device(1, g)
+    fa.fa_analyze_gradient(g, 256, rb)  # first use outside the capture
+    fa.fa_merge_gradient_stats(rb, rows, sc, rep)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fa.fa_analyze_gradient(g, 256, rb)
+        fa.fa_merge_gradient_stats(rb, rows, sc, rep)
+    for call in range(1, w.calls + 1):
+        w.fill_grad_device(call, g)
+        graph.replay()
+        fa.fa_analyze_gradient(g, 256, rb2)
+        fa.fa_merge_gradient_stats(rb2, rows, sc2, rep2)
+        torch.cuda.synchronize()
+        assert torch.equal(rep, rep2) and torch.equal(rb, rb2), call
+
+
 def test_clip_decide_and_report_roundtrip(oracle_lib):
     n = 256 * 4096
     g, bits = _planted_grad(n, "bf16", 22, [], sigma=0.05)
