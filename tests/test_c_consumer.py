@@ -11,7 +11,6 @@ import os
 import shutil
 import struct
 import subprocess
-import tempfile
 
 import numpy as np
 import pytest
@@ -65,24 +64,23 @@ def _sample(stream, n, scale):
 
 
 @pytest.mark.gpu
-def test_consumer_runs_and_matches_the_oracle(oracle_lib):
+def test_consumer_runs_and_matches_the_oracle(oracle_lib, tmp_path):
     import oracle
     from amsgrad_optimizer_step_gb300 import build
     lib_path = build.build()
     pkg = os.path.dirname(lib_path)
     n = 100_003
-    with tempfile.TemporaryDirectory() as tmp:
-        exe = os.path.join(tmp, "consumer")
-        r = subprocess.run([_gcc(), "-std=c11", "-O2", SRC, "-I", INCLUDE,
-                            "-I", os.path.join(CUDA, "include"), "-L", pkg, "-lfused_adamw",
-                            "-L", os.path.join(CUDA, "lib64"), "-lcudart",
-                            f"-Wl,-rpath,{pkg}:{os.path.join(CUDA, 'lib64')}", "-o", exe],
-                           capture_output=True, text=True)
-        assert r.returncode == 0, r.stderr
-        out = os.path.join(tmp, "out.bin")
-        r = subprocess.run([exe, str(n), out], capture_output=True, text=True, timeout=120)
-        assert r.returncode == 0, r.stderr
-        raw = open(out, "rb").read()
+    exe = str(tmp_path / "consumer")
+    r = subprocess.run([_gcc(), "-std=c11", "-O2", SRC, "-I", INCLUDE,
+                        "-I", os.path.join(CUDA, "include"), "-L", pkg, "-lfused_adamw",
+                        "-L", os.path.join(CUDA, "lib64"), "-lcudart",
+                        f"-Wl,-rpath,{pkg}:{os.path.join(CUDA, 'lib64')}", "-o", exe],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = str(tmp_path / "out.bin")
+    r = subprocess.run([exe, str(n), out], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    raw = open(out, "rb").read()
     t = struct.unpack_from("<Q", raw, 0)[0]
     reps = [struct.unpack_from("<iiQdd", raw, 8 + 32 * k) for k in range(3)]
     arrays = np.frombuffer(raw, dtype=np.float32, offset=8 + 96).reshape(3, n)
