@@ -63,7 +63,7 @@ CASES = [
     ("per-segment reports", lambda lib: S.test_chunk_reports_match_oracle_per_segment(
         "bf16", 100, lib)),
     ("per-segment multipliers, shared-memory pipeline",
-     lambda lib: S.test_segment_multipliers_mixed_sizes_vs_oracle("f16", lib)),
+     lambda lib: S.test_segment_multipliers_mixed_sizes_vs_oracle("f16", False, lib)),
 ]
 
 

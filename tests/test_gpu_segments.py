@@ -126,8 +126,8 @@ def test_segment_multipliers_vs_oracle(gdt, oracle_lib):
         gate(vh[a:b], refs[k].state.vmax, 1e-5, f"segment {k} vmax")
 
 
-@pytest.mark.parametrize("gdt", ["f16", "bf16"])
-def test_segment_multipliers_mixed_sizes_vs_oracle(gdt, oracle_lib):
+@pytest.mark.parametrize("gdt,maximize", [("f16", False), ("bf16", False), ("f32", True)])
+def test_segment_multipliers_mixed_sizes_vs_oracle(gdt, maximize, oracle_lib):
     """Large segments between runs of tiny and empty ones, several million elements:
     steady steps take the shared-memory pipeline, whose tiles span up to dozens of
     segments and whose per-CTA segment index has to skip whole runs between tiles."""
@@ -139,6 +139,7 @@ def test_segment_multipliers_mixed_sizes_vs_oracle(gdt, oracle_lib):
     n = int(seg[-1])
     assert n > 2 * 152 * 4096
     w, p = _bucket(n, gdt, 38)
+    w = dataclasses.replace(w, maximize=maximize)
     opts = w.options()
     o = fa.options(**opts)
     m, v, vm = (torch.zeros(n, device=DEV) for _ in range(3))
