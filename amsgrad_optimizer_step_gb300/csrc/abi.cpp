@@ -22,6 +22,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "fused_adamw.h"
 #include "internal.h"
@@ -100,6 +101,15 @@ bool valid_dtype(fa_dtype d) { return d == FA_F32 || d == FA_F16 || d == FA_BF16
 size_t dtype_bytes(fa_dtype d) { return d == FA_F32 ? 4 : 2; }
 
 // Device of the stream (current device for the legacy default stream).
+// Host-side trace ranges (NVTX): a profiler attached to the process shows each
+// entry point's span around the kernels it enqueues; without one they cost nothing.
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
+
 fa_status stream_device(void *stream, int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess) {
         cudaGetLastError();
@@ -399,6 +409,7 @@ fa_status fa_adamw_step(int64_t n, const float *p, const void *g, fa_dtype gdt, 
                         const fa_options *options, fa_step_control ctl, float *p_out,
                         float *m_out, float *v_out, float *vmax_out, uint64_t *t_out,
                         int32_t *updated, void *stream) {
+    TraceRange trace("fa_adamw_step");
     fa_status st;
     if (!t_out || !updated) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n)) != FA_OK) return st;
@@ -452,6 +463,7 @@ fa_status fa_adamw_step_inplace(int64_t n, float *p, const void *g, fa_dtype gdt
                                 float *v, float *vmax, uint64_t *t,
                                 const fa_options *options, fa_step_control ctl,
                                 double grad_mult, int32_t *updated, void *stream) {
+    TraceRange trace("fa_adamw_step_inplace");
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n)) != FA_OK) return st;
@@ -476,6 +488,7 @@ fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_tot
                          const void *g, fa_dtype gdt, float *m, float *v, float *vmax,
                          uint64_t *t, const fa_options *options, fa_step_control ctl,
                          double grad_mult, int32_t *updated, void *stream) {
+    TraceRange trace("fa_bucket_step");
     if (n_total < 0) return FA_ERR_SIZE;
     fa_status st = check_segments(seg_offsets, nseg, n_total);
     if (st != FA_OK) return st;
@@ -488,6 +501,7 @@ fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int
                                    float *vmax, uint64_t *t, const fa_options *options,
                                    fa_step_control ctl, double grad_mult, void *p_model,
                                    fa_dtype model_dtype, int32_t *updated, void *stream) {
+    TraceRange trace("fa_bucket_step_writeback");
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
@@ -521,6 +535,7 @@ fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt,
                                float *v, float *vmax, uint64_t *t, const fa_options *options,
                                fa_step_control ctl, double grad_mult, float *delta,
                                int32_t *updated, void *stream) {
+    TraceRange trace("fa_adamw_step_staged");
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n)) != FA_OK) return st;
@@ -560,6 +575,7 @@ fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t
                                float *vmax, uint64_t t, const fa_options *options,
                                fa_step_control ctl, const fa_stats *report_dev,
                                double max_grad_norm, void *stream) {
+    TraceRange trace("fa_bucket_step_gated");
     fa_status st;
     if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
     if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
@@ -619,6 +635,7 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
                                        int64_t rows_capacity, float *scratch,
                                        int64_t scratch_elements, fa_stats *report_dev,
                                        fa_step_report *out, void *stream) {
+    TraceRange trace("fa_bucket_step_clipped_gated");
     fa_status st;
     if (!t || !out) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
@@ -729,6 +746,7 @@ fa_status fa_stats_rows(int64_t n, int32_t row_len, const int64_t *seg_offsets, 
 fa_status fa_analyze_gradient(const void *g, fa_dtype gdt, int64_t n, int32_t row_len,
                               const int64_t *seg_offsets, int32_t nseg, fa_stats *rows_out,
                               int64_t rows_capacity, void *stream) {
+    TraceRange trace("fa_analyze_gradient");
     if (!valid_dtype(gdt)) return FA_ERR_DTYPE;
     int64_t rows = 0;
     fa_status st = fa_stats_rows(n, row_len, seg_offsets, nseg, &rows);
@@ -778,6 +796,7 @@ fa_status fa_analyze_gradient(const void *g, fa_dtype gdt, int64_t n, int32_t ro
 
 fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *scratch,
                                   int64_t scratch_elements, fa_stats *report, void *stream) {
+    TraceRange trace("fa_merge_gradient_stats");
     int32_t kernels = 0;
     int64_t need = 0;
     fa_status st = fa_stats_plan(rows, &kernels, &need);
@@ -810,6 +829,7 @@ fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *
 
 fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
                                          fa_stats *report, void *stream) {
+    TraceRange trace("fa_merge_gradient_stats_static");
     int32_t kernels = 0;
     int64_t need = 0;
     fa_status st = fa_stats_plan(rows, &kernels, &need);
@@ -865,6 +885,7 @@ fa_status fa_merge_gradient_stats_chunks(const fa_stats *rows_in, const int64_t 
                                          int32_t nchunks, float *scratch,
                                          int64_t scratch_elements, fa_stats *chunk_reports,
                                          void *stream) {
+    TraceRange trace("fa_merge_gradient_stats_chunks");
     int64_t need = 0;
     fa_status st = fa_stats_chunk_scratch(chunk_rows, nchunks, &need);
     if (st != FA_OK) return st;
@@ -908,6 +929,7 @@ fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg
                                         const fa_options *options, fa_step_control ctl,
                                         const double *seg_grad_mult, int32_t *updated,
                                         void *stream) {
+    TraceRange trace("fa_bucket_step_segment_scaled");
     fa_status st;
     if (!t || !updated) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
@@ -975,6 +997,7 @@ fa_status fa_bucket_step_clipped_per_segment(
     fa_step_control ctl, double max_grad_norm, int32_t row_len, fa_stats *rows_buf,
     int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
     double *seg_norms, double *seg_coefs, fa_step_report *out, void *stream) {
+    TraceRange trace("fa_bucket_step_clipped_per_segment");
     fa_status st;
     if (!t || !out) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
@@ -1045,6 +1068,7 @@ fa_status fa_bucket_step_clipped_per_segment(
 }
 
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream) {
+    TraceRange trace("fa_read_report");
     if (!report_host) return FA_ERR_NULL;
     int dev = 0;
     fa_status st = stream_device(stream, &dev);
@@ -1095,6 +1119,7 @@ fa_status fa_bucket_step_clipped(const int64_t *seg_offsets, int32_t nseg, int64
                                  fa_stats *rows_buf, int64_t rows_capacity, float *scratch,
                                  int64_t scratch_elements, fa_stats *report_dev,
                                  fa_step_report *out, void *stream) {
+    TraceRange trace("fa_bucket_step_clipped");
     fa_status st;
     if (!t || !out) return FA_ERR_NULL;
     if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
