@@ -147,6 +147,18 @@ def test_misaligned_views(gdt, offsets):
     gate(views["vmax"].cpu().numpy(), traj.state.vmax, 1e-6, "vmax")
 
 
+def test_more_than_2_31_elements_sampled():
+    """A bucket of 2^31 + 777 parameters (8.6 GB per FP32 array): every element offset in
+    the kernels is 64-bit; sampled elements on both sides of 2^31, at the ragged end and
+    at random match the oracle, first step and steady steps."""
+    n = 2 ** 31 + 777
+    w = dataclasses.replace(CONFIG3, calls=3, inplace=True, outlier_per_10000=0)
+    edges = [2 ** 31 - 9, 2 ** 31 - 1, 2 ** 31, 2 ** 31 + 1, 2 ** 31 + 8, 2 ** 30 * 3 // 2]
+    idx = sample_indices(n, k=20000, seed=31, extra=edges)
+    s = run_workload(w, n, "inplace", DEV, idx=idx, step_check=True)
+    assert s["t"] == 3
+
+
 # ---- degenerate hyper-parameters ------------------------------------------------
 
 DEGENERATE = {
