@@ -149,14 +149,19 @@ def test_misaligned_views(gdt, offsets):
 
 def test_more_than_2_31_elements_sampled():
     """A bucket of 2^31 + 777 parameters (8.6 GB per FP32 array): every element offset in
-    the kernels is 64-bit; sampled elements on both sides of 2^31, at the ragged end and
-    at random match the oracle, first step and steady steps."""
+    the kernels is 64-bit; the norm matches the oracle's over the whole gradient, and
+    sampled elements on both sides of 2^31, at the ragged end and at random match it too,
+    first step and steady steps."""
     n = 2 ** 31 + 777
-    w = dataclasses.replace(CONFIG3, calls=3, inplace=True, outlier_per_10000=0)
+    w = dataclasses.replace(CONFIG3, calls=3, inplace=True, outlier_per_10000=0,
+                            max_grad_norm=1.0, row_len=1024)
     edges = [2 ** 31 - 9, 2 ** 31 - 1, 2 ** 31, 2 ** 31 + 1, 2 ** 31 + 8, 2 ** 30 * 3 // 2]
     idx = sample_indices(n, k=20000, seed=31, extra=edges)
-    s = run_workload(w, n, "inplace", DEV, idx=idx, step_check=True)
-    assert s["t"] == 3
+    # the whole statistics-guarded step: analysis in rows of 1024 (2,097,153 rows), the
+    # merge, the norm against the oracle's sum over all 2^31 + 777 values, the clipped update
+    s = run_workload(w, n, "clipped", DEV, idx=idx, row_len=1024, full_grad_on_host=False)
+    assert s["t"] == 3 and s["updates"] == 3
+    assert all(r[1] > 1.0 for r in s["reports"])  # the clip is active
 
 
 # ---- degenerate hyper-parameters ------------------------------------------------
