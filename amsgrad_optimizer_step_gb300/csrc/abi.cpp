@@ -1,6 +1,7 @@
 // C-ABI host layer: validation, FP64 host coefficients, the statistics plan,
 // the skip / clip decision, and kernel launches.  Everything that touches the
-// device goes through the kernels in update_kernels.cu and stats_kernels.cu.
+// device goes through the kernels in update_kernels.cu, stats_kernels.cu and
+// staged_kernels.cu (the staged comparison).
 //
 // Contract sources (RUDA documentation pages):
 //   "実験的なデバイス上の融合 AdamW / AMSGrad" (ja/docs/fused-adamw): "この演算子を使用する
@@ -12,10 +13,10 @@
 //     tensor or skip_update launches nothing and does not advance the step).
 //   "训练与状态保存" (zh/docs/training): "在 ruda:0 上进行原生 PyTorch 训练" (12-byte
 //     report read back first, non-finite skip, global clip after unscale).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>

@@ -9,14 +9,20 @@
 // moments, FP32/FP16/BF16 gradients, the first update initialises the moments
 // inside the kernel without reading them).
 //
-// Design: one HBM pass per parameter.  The kernel is bandwidth bound (about
-// 0.7 flop per byte), so it is built for bytes in flight: persistent CTAs,
-// grid-stride over 8-element vectors, every stream moved with 16-byte
-// evict-first loads and stores (p, m, v, vmax as two float4; a BF16/FP16
-// gradient as one 16-byte word, an FP32 gradient as two float4), all loads of
-// an iteration issued before any arithmetic.  Elements before the first
-// 16-byte boundary and after the last full vector go through the same
-// arithmetic one at a time.
+// Design: one HBM pass per parameter.  The update is bandwidth bound (about
+// 0.7 flop per byte), so it is built for bytes in flight.  Two kernels share the
+// element arithmetic:
+//   - steady steps of large tensors: update_tma_kernel, one CTA per SM staging
+//     tiles of every stream through shared memory with 1-D TMA bulk copies and
+//     mbarriers, several stages in flight, bounded waits (further below);
+//   - first steps, small tensors: update_vec_kernel, persistent CTAs grid-striding
+//     over 8-element vectors, every stream moved with 16-byte evict-first loads
+//     and stores (p, m, v, vmax as two float4; a BF16/FP16 gradient as one 16-byte
+//     word, an FP32 gradient as two float4), all loads of an iteration issued
+//     before any arithmetic;
+//   - views not co-aligned to 16 bytes: update_scalar_kernel.
+// Elements before the first 16-byte boundary and after the last full vector or
+// tile go through the same arithmetic one at a time.
 #include <atomic>
 
 #include <cuda_bf16.h>
