@@ -53,8 +53,28 @@ def _deps() -> list[str]:
     return sources() + hdrs + [os.path.abspath(__file__)]
 
 
+# ELF e_machine of a shared object built for this host (x86-64: 62, AArch64: 183).
+_ELF_MACHINE = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}
+
+
+def _built_for_this_host(path: str) -> bool:
+    """False for a library built for another architecture (e.g. copied from an x86
+    host to an AArch64 one), which must be rebuilt rather than loaded."""
+    import platform
+    want = _ELF_MACHINE.get(platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    machine = int.from_bytes(head[18:20], "little" if head[5] == 1 else "big")
+    return want is None or machine == want
+
+
 def up_to_date(lib_path: str = LIB_PATH) -> bool:
-    if not os.path.exists(lib_path):
+    if not os.path.exists(lib_path) or not _built_for_this_host(lib_path):
         return False
     t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(d) <= t for d in _deps())

@@ -46,11 +46,27 @@ class _Options(ctypes.Structure):
                 ("maximize", ctypes.c_int32)]
 
 
+def _native(path: str) -> bool:
+    """True when the shared object at ``path`` was built for this machine (its ELF
+    e_machine matches), so that one copied from another architecture is rebuilt."""
+    import platform
+    want = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}.get(
+        platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return want is None or int.from_bytes(head[18:20], "little") == want
+
+
 def build(src_dir: str = HERE, out_path: Optional[str] = None, force: bool = False) -> str:
     """Compile the oracle C sources into a shared library; returns its path."""
     out_path = out_path or os.path.join(src_dir, LIB_NAME)
     srcs = [os.path.join(src_dir, s) for s in SOURCES]
-    if (not force and os.path.exists(out_path)
+    if (not force and os.path.exists(out_path) and _native(out_path)
             and all(os.path.getmtime(out_path) >= os.path.getmtime(s)
                     for s in srcs + [os.path.join(src_dir, "oracle.h")])):
         return out_path
