@@ -1,0 +1,78 @@
+"""Randomised properties of the library's host logic, against the oracle (no GPU).
+
+The row count and reduction plan for arbitrary segment tables and sizes, the skip /
+clip decision over the whole input range, and the shard split used by several ranks.
+"""
+
+import numpy as np
+import pytest
+
+hypothesis = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st  # noqa: E402
+
+import amsgrad_optimizer_step_gb300 as fa  # noqa: E402
+from amsgrad_optimizer_step_gb300 import sharded  # noqa: E402
+
+MAX_ROWS = 4_194_304
+SETTINGS = settings(max_examples=150, deadline=None)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from amsgrad_optimizer_step_gb300 import build
+    build.build()
+
+
+@SETTINGS
+@given(sizes=st.lists(st.integers(0, 4000), min_size=1, max_size=40),
+       row_len=st.integers(1, 700))
+def test_rows_and_plan_match_the_oracle(sizes, row_len, oracle_lib):
+    seg = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    n = int(seg[-1])
+    rows = fa.fa_stats_rows(n, row_len, [int(x) for x in seg])
+    want_rows = oracle_lib.row_stats(np.zeros(n, np.float32), "f32", row_len, seg)[0].shape[0] \
+        if n else 0
+    assert rows == want_rows
+    if rows >= 1:
+        assert fa.fa_stats_plan(rows) == oracle_lib.stats_plan(rows)[:2]
+
+
+@SETTINGS
+@given(rows=st.one_of(st.integers(-5, 5000), st.integers(1_000_000, MAX_ROWS + 5)))
+def test_plan_matches_the_oracle_or_both_reject(rows, oracle_lib):
+    want = oracle_lib.stats_plan(rows)
+    if want is None:
+        with pytest.raises(fa.FusedAdamWError, match="FA_ERR_PLAN"):
+            fa.fa_stats_plan(rows)
+    else:
+        assert fa.fa_stats_plan(rows) == want[:2]
+
+
+@SETTINGS
+# (normal-range sums: the oracle is handed sum / scale^2, which a subnormal sum underflows)
+@given(sum_sq=st.one_of(st.just(0.0), st.floats(1e-250, 1e30)),
+       count=st.integers(0, 3),
+       scale=st.sampled_from([1.0, 2.0, 128.0, 65536.0, 0.5, 3.0]),
+       max_norm=st.one_of(st.just(0.0), st.floats(1e-6, 1e6)))
+def test_clip_decision_matches_the_oracle(sum_sq, count, scale, max_norm, oracle_lib):
+    skip, norm, coef = fa.fa_clip_decision(sum_sq, count, scale, max_norm)
+    o_skip, o_norm, o_coef = oracle_lib.clip_decision(sum_sq / (scale * scale), count, max_norm)
+    assert skip == o_skip == (count > 0)
+    assert norm == pytest.approx(o_norm, rel=1e-14, abs=1e-300)
+    if not skip:
+        assert coef == pytest.approx(o_coef, rel=1e-14)
+        assert 0.0 < coef <= 1.0
+
+
+@SETTINGS
+@given(n=st.integers(0, 10 ** 10), world=st.integers(1, 64))
+def test_shards_are_contiguous_aligned_and_balanced(n, world):
+    bounds = [sharded.shard_range(n, r, world) for r in range(world)]
+    assert bounds[0][0] == 0 and bounds[-1][1] == n
+    for (a0, a1), (b0, b1) in zip(bounds, bounds[1:]):
+        assert a1 == b0
+    for lo, hi in bounds:
+        assert lo <= hi and lo % 8 == 0 and (hi % 8 == 0 or hi == n)
+    lens = [hi - lo for lo, hi in bounds]
+    # shards hold floor or ceil of ceil(n/8)/world 8-element units; the last may be short
+    assert max(lens) - min(lens) <= 16
