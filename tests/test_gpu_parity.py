@@ -164,6 +164,31 @@ def test_more_than_2_31_elements_sampled():
     assert all(r[1] > 1.0 for r in s["reports"])  # the clip is active
 
 
+def _random_case(k):
+    rng = np.random.default_rng(1000 + k)
+    n = int(rng.choice([1, 7, 4097, 65_537, 300_001, 1_000_003, 3_000_017]))
+    scale = float(2.0 ** rng.integers(-2, 8))
+    return dataclasses.replace(
+        CONFIG2, name=f"random{k}", seed=int(rng.integers(1, 10_000)),
+        grad_dtype=str(rng.choice(["f32", "f16", "bf16"])), amsgrad=bool(rng.integers(2)),
+        maximize=bool(rng.integers(2)), lr=float(10 ** rng.uniform(-5, -1)),
+        beta1=float(rng.choice([0.0, 0.5, 0.9, 0.95])),
+        beta2=float(rng.choice([0.9, 0.99, 0.999, 0.9999])),
+        eps=float(10 ** rng.uniform(-10, -3)), weight_decay=float(rng.choice([0.0, 1e-4, 0.1])),
+        gradient_scale=scale, grad_premul=scale, calls=int(rng.integers(2, 5)),
+        skip_calls=(2,) if rng.integers(3) == 0 else (), inplace=True).scaled(n)
+
+
+@pytest.mark.parametrize("k", range(24))
+def test_random_configurations_vs_oracle(k):
+    """Seeded random combinations of size, gradient dtype, AMSGrad, maximize, lr, betas,
+    eps, decay, power-of-two loss scale, call count and an occasional skip, each against
+    the oracle (one step from identical state and along the trajectory)."""
+    w = _random_case(k)
+    s = run_workload(w, w.n, "inplace", DEV, guard=64)
+    assert s["t"] == w.calls - len(w.skip_calls)
+
+
 # ---- degenerate hyper-parameters ------------------------------------------------
 
 DEGENERATE = {
