@@ -473,6 +473,49 @@ def test_analyze_rows_match_oracle(gdt, n, row_len, segs, oracle_lib):
     assert np.all(np.abs(dev_s + dev_lo - rs)[ok] <= 2e-6 * rs[ok] + 1e-30)
 
 
+@pytest.mark.parametrize("k", range(16))
+def test_random_statistics_vs_oracle(k, oracle_lib):
+    """Seeded random analyses: size, gradient dtype, row length (fast and generic kernels),
+    segment tables with empty segments, and 0-5 planted NaN/+-Inf values.  Every row
+    record against the oracle (counts exact), then the merged report (count exact, sum
+    within the merge's error) and the skip / clip decision."""
+    import math
+    rng = np.random.default_rng(5000 + k)
+    gdt = str(rng.choice(["f32", "f16", "bf16"]))
+    n = int(rng.integers(1, 2_000_000))
+    row_len = int(rng.choice([1, 7, 100, 256, 512, 1000, 1024, 2048]))
+    segs = None
+    if rng.integers(2):
+        cuts = np.sort(rng.integers(0, n + 1, int(rng.integers(1, 40))))
+        segs = [0] + [int(x) for x in cuts] + [n]
+    rows = fa.fa_stats_rows(n, row_len, segs)
+    if rows > 4_194_304:
+        row_len, rows = 1024, fa.fa_stats_rows(n, 1024, segs)
+    bad = [int(i) for i in rng.integers(0, n, int(rng.integers(0, 6)))]
+    g, bits = _planted_grad(n, gdt, 6000 + k, bad)
+    buf = fa.stats_buffer(rows, DEV)
+    assert fa.fa_analyze_gradient(g, row_len, buf, segs) == rows
+    scratch = fa.scratch_buffer(rows, DEV)
+    report = fa.stats_buffer(1, DEV)
+    fa.fa_merge_gradient_stats(buf, rows, scratch, report)
+    torch.cuda.synchronize()
+    rs, rc = oracle_lib.row_stats(bits, gdt, row_len, segs)
+    host = buf.cpu()
+    dev_s = host[:rows, 0].view(torch.float32).double().numpy()
+    dev_c = host[:rows, 1].numpy().astype(np.int64)
+    dev_lo = host[:rows, 2].view(torch.float32).double().numpy()
+    assert np.array_equal(dev_c, rc.astype(np.int64))
+    ok = rc == 0
+    assert np.all(np.abs(dev_s + dev_lo - rs)[ok] <= 2e-6 * rs[ok] + 1e-30)
+    h = fa.fa_read_report(report)
+    s_or, c_or = oracle_lib.gradient_stats(bits, gdt)
+    assert h.nonfinite == c_or
+    if c_or == 0:
+        exact_rows = math.fsum((dev_s + dev_lo).tolist())
+        assert abs(float(h.sum_sq) + float(h.sum_sq_lo) - exact_rows) <= 1e-12 * exact_rows
+        assert abs(float(h.sum_sq) + float(h.sum_sq_lo) - s_or) <= 2e-6 * s_or + 1e-30
+
+
 @pytest.mark.parametrize("rows", [1, 2, 1023, 1024, 1025, 4096, 1_048_575, 1_048_576,
                                   1_048_577, 4_194_304])
 def test_merge_matches_exact_sum(rows):
