@@ -27,9 +27,9 @@ from typing import Optional
 
 import torch
 
-from . import (fa_analyze_gradient, fa_bucket_step, fa_bucket_step_writeback,
-               fa_merge_gradient_stats, fa_read_report, fa_stats_rows, options,
-               control, scratch_buffer, stats_buffer)
+from . import (FaStats, fa_analyze_gradient, fa_bucket_step, fa_bucket_step_gated,
+               fa_bucket_step_writeback, fa_clip_decision, fa_merge_gradient_stats,
+               fa_read_report, fa_stats_rows, options, control, scratch_buffer, stats_buffer)
 from . import sharded
 
 MAX_ROWS = 4_194_304
@@ -229,8 +229,8 @@ class FusedAdamW(torch.optim.Optimizer):
     def _rows(self, b: _Bucket) -> int:
         return fa_stats_rows(b.n, self.row_len, b.segments)
 
-    def statistics(self, gradient_scale: float = 1.0):
-        """Analyse every group, merge, read back: (skip, global norm, clip coefficient)."""
+    def _enqueue_statistics(self) -> torch.Tensor:
+        """Analyses every group and merges into the one 12-byte device report."""
         total, rows_buf, scratch, report = self._stats_buffers()
         off = 0
         for b in self._buckets:
@@ -238,7 +238,11 @@ class FusedAdamW(torch.optim.Optimizer):
             fa_analyze_gradient(b.grad, self.row_len, rows_buf[off:off + r], b.segments)
             off += r
         fa_merge_gradient_stats(rows_buf, total, scratch, report)
-        rep = fa_read_report(report)
+        return report
+
+    def statistics(self, gradient_scale: float = 1.0):
+        """Analyse every group, merge, read back: (skip, global norm, clip coefficient)."""
+        rep = fa_read_report(self._enqueue_statistics())
         skip, norm, coef = sharded.global_clip_decision(
             rep, gradient_scale, self.max_grad_norm if self.max_grad_norm else 0.0)
         return skip, norm, coef, int(rep.nonfinite)
@@ -253,8 +257,12 @@ class FusedAdamW(torch.optim.Optimizer):
         for b in self._buckets:
             b.gather_grads()
         report = {"skipped": bool(found_inf), "nonfinite": 0, "grad_norm": None, "clip_coef": 1.0}
-        if not found_inf and (self.max_grad_norm is not None or self.hierarchical_stats
-                              or check_finite):
+        use_stats = not found_inf and (self.max_grad_norm is not None or self.hierarchical_stats
+                                       or check_finite)
+        if use_stats and self._can_gate():
+            self.last_report = self._gated_step(gradient_scale)
+            return loss
+        if use_stats:
             skip, norm, coef, bad = self.statistics(gradient_scale)
             report.update(skipped=skip, nonfinite=bad, grad_norm=norm, clip_coef=coef)
         if not report["skipped"]:
@@ -272,6 +280,46 @@ class FusedAdamW(torch.optim.Optimizer):
                                             b.t, o, ctl, report["clip_coef"])
         self.last_report = report
         return loss
+
+    def _options(self, group):
+        return options(lr=group["lr"], beta1=group["betas"][0], beta2=group["betas"][1],
+                       eps=group["eps"], weight_decay=group["weight_decay"],
+                       amsgrad=group["amsgrad"], maximize=group["maximize"])
+
+    def _can_gate(self) -> bool:
+        """The device can take the decision itself when every group updates FP32
+        parameters in place and this process holds the whole gradient (several ranks
+        need every rank's totals first)."""
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+            return False
+        return not any(b.master_separate for b in self._buckets)
+
+    def _gated_step(self, gradient_scale: float) -> dict:
+        """Statistics, then every group's update gated on the device by the same report
+        (bit-identical to deciding on the host), while the host reads the report back
+        through pinned memory to advance the step counts."""
+        report_dev = self._enqueue_statistics()
+        if getattr(self, "_pinned_report", None) is None:
+            self._pinned_report = torch.empty((1, 3), dtype=torch.int32).pin_memory()
+            self._report_event = torch.cuda.Event()
+        stream = torch.cuda.current_stream(report_dev.device)
+        self._pinned_report.copy_(report_dev, non_blocking=True)
+        self._report_event.record(stream)
+        ctl = control(gradient_scale)
+        max_norm = self.max_grad_norm if self.max_grad_norm else 0.0
+        for group, b in zip(self.param_groups, self._buckets):
+            fa_bucket_step_gated(b.segments, b.master, b.grad, b.m, b.v, b.vmax, b.t,
+                                 self._options(group), ctl, report_dev, max_norm)
+        self._report_event.synchronize()
+        rep = FaStats.from_buffer_copy(self._pinned_report.numpy().tobytes())
+        total = float(rep.sum_sq) + float(rep.sum_sq_lo)
+        skip, norm, coef = fa_clip_decision(total, int(rep.nonfinite), gradient_scale, max_norm)
+        if not skip:
+            for b in self._buckets:
+                b.t += 1
+        return {"skipped": skip, "nonfinite": int(rep.nonfinite), "grad_norm": norm,
+                "clip_coef": coef}
 
 
 class GradScaler:
