@@ -30,6 +30,7 @@ __all__ = [
     "fa_merge_gradient_stats_chunks", "fa_bucket_step_segment_scaled",
     "fa_bucket_step_clipped_per_segment", "segment_rows",
     "fa_clip_decide", "fa_bucket_step_clipped", "fa_bucket_step_gated",
+    "fa_bucket_step_writeback_gated",
     "fa_bucket_step_clipped_gated", "options", "control", "stats_buffer",
     "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
 ]
@@ -303,6 +304,27 @@ def fa_bucket_step_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
     check("fa_bucket_step_gated", _L().fa_bucket_step_gated(
         seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
         ctypes.byref(opts), ctl, _ptr(report), max_grad_norm, _stream(stream)))
+
+
+def fa_bucket_step_writeback_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                                   ctl: FaStepControl, report: torch.Tensor,
+                                   max_grad_norm: float, p_model: torch.Tensor,
+                                   stream=None) -> None:
+    """Enqueues the write-back update gated on the device report; the caller advances t."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _dense("p_model", p_model, n, (torch.float16, torch.bfloat16), p.device)
+    _stats_tensor("report", report)
+    seg, nseg = _segments(seg_offsets)
+    check("fa_bucket_step_writeback_gated", _L().fa_bucket_step_writeback_gated(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
+        ctypes.byref(opts), ctl, _ptr(report), max_grad_norm, _ptr(p_model),
+        _TORCH_GRAD[p_model.dtype], _stream(stream)))
 
 
 def fa_bucket_step_clipped_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,

@@ -71,6 +71,9 @@ SIGNATURES = {
                                      P]),
     "fa_bucket_step_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, c_u64,
                                      ctypes.POINTER(FaOptions), FaStepControl, P, c_f64, P]),
+    "fa_bucket_step_writeback_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, c_u64,
+                                               ctypes.POINTER(FaOptions), FaStepControl, P,
+                                               c_f64, P, c_i32, P]),
     "fa_bucket_step_clipped_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
                                              ctypes.POINTER(FaOptions), FaStepControl, c_f64,
                                              c_i32, P, c_i64, P, c_i64, P,

@@ -597,6 +597,38 @@ fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t
                           max_grad_norm);
 }
 
+fa_status fa_bucket_step_writeback_gated(const int64_t *seg_offsets, int32_t nseg,
+                                         int64_t n_total, float *p, const void *g, fa_dtype gdt,
+                                         float *m, float *v, float *vmax, uint64_t t,
+                                         const fa_options *options, fa_step_control ctl,
+                                         const fa_stats *report_dev, double max_grad_norm,
+                                         void *p_model, fa_dtype model_dtype, void *stream) {
+    TraceRange trace("fa_bucket_step_writeback_gated");
+    fa_status st;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
+    if (model_dtype != FA_F16 && model_dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (n_total == 0 || ctl.skip_update) return FA_OK;
+    if (t == UINT64_MAX) return FA_ERR_OPTION;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(p_model, dev, 2)) != FA_OK) return st;
+    const size_t b = static_cast<size_t>(n_total) * 4;
+    const Range r[] = {{report_dev, 12}, {p_model, static_cast<size_t>(n_total) * 2}, {p, b},
+                       {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b}, {v, b},
+                       {options->amsgrad ? vmax : nullptr, b}};
+    // the report and the model copy must stay clear of every buffer the update writes
+    for (int i = 0; i < 2; ++i)
+        for (int j = i + 1; j < 7; ++j)
+            if (overlap(r[i], r[j])) return FA_ERR_ALIAS;
+    return enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, t + 1,
+                          ctl.gradient_scale, 1.0, stream, p_model, model_dtype, report_dev,
+                          max_grad_norm);
+}
+
 namespace {
 
 // Per host thread: a pinned staging record for report read-backs that must not

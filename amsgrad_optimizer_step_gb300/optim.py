@@ -28,7 +28,8 @@ from typing import Optional
 import torch
 
 from . import (FaStats, fa_analyze_gradient, fa_bucket_step, fa_bucket_step_gated,
-               fa_bucket_step_writeback, fa_clip_decision, fa_merge_gradient_stats,
+               fa_bucket_step_writeback, fa_bucket_step_writeback_gated, fa_clip_decision,
+               fa_merge_gradient_stats,
                fa_read_report, fa_stats_rows, options, control, scratch_buffer, stats_buffer)
 from . import sharded
 
@@ -287,13 +288,10 @@ class FusedAdamW(torch.optim.Optimizer):
                        amsgrad=group["amsgrad"], maximize=group["maximize"])
 
     def _can_gate(self) -> bool:
-        """The device can take the decision itself when every group updates FP32
-        parameters in place and this process holds the whole gradient (several ranks
-        need every rank's totals first)."""
+        """The device can take the decision itself when this process holds the whole
+        gradient (several ranks need every rank's totals first)."""
         import torch.distributed as dist
-        if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
-            return False
-        return not any(b.master_separate for b in self._buckets)
+        return not (dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1)
 
     def _gated_step(self, gradient_scale: float) -> dict:
         """Statistics, then every group's update gated on the device by the same report
@@ -309,8 +307,13 @@ class FusedAdamW(torch.optim.Optimizer):
         ctl = control(gradient_scale)
         max_norm = self.max_grad_norm if self.max_grad_norm else 0.0
         for group, b in zip(self.param_groups, self._buckets):
-            fa_bucket_step_gated(b.segments, b.master, b.grad, b.m, b.v, b.vmax, b.t,
-                                 self._options(group), ctl, report_dev, max_norm)
+            if b.master_separate:
+                fa_bucket_step_writeback_gated(b.segments, b.master, b.grad, b.m, b.v, b.vmax,
+                                               b.t, self._options(group), ctl, report_dev,
+                                               max_norm, b.model)
+            else:
+                fa_bucket_step_gated(b.segments, b.master, b.grad, b.m, b.v, b.vmax, b.t,
+                                     self._options(group), ctl, report_dev, max_norm)
         self._report_event.synchronize()
         rep = FaStats.from_buffer_copy(self._pinned_report.numpy().tobytes())
         total = float(rep.sum_sq) + float(rep.sum_sq_lo)

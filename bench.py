@@ -712,6 +712,22 @@ def run_ours(args):
         del dopt, dparams
         torch.cuda.empty_cache()
 
+        # the same model in mixed precision: BF16 parameters and gradients, FP32 masters
+        # and moments, the BF16 copy written back in the update's pass
+        dparams = [torch.nn.Parameter(torch.zeros(shape, device=dev, dtype=torch.bfloat16))
+                   for _, shape in decoder_bucket_shapes()]
+        dopt = FusedAdamW(dparams, lr=1e-3, max_grad_norm=1.0)
+        dopt._buckets[0].grad.normal_(0.0, 1e-3)
+        ms = timed(dopt.step, args.next_rows_steps)
+        b4 = fa.bytes_per_param(2, False, False) + 2 + 2  # update + model copy + analysis
+        rows_out["f4_fused_adamw_decoder1.1B_bf16_params_clip"] = {
+            "ms": ms, "params": dn, "tensors": len(dparams), "row_len": dopt.row_len,
+            "bytes_per_param": b4, "achieved_gbs": b4 * dn / (ms * 1e-3) / 1e9,
+            "frac": b4 * dn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+            "params_per_s": dn / (ms * 1e-3), "skipped": dopt.last_report["skipped"]}
+        del dopt, dparams
+        torch.cuda.empty_cache()
+
         # f3: per-parameter clipping on the decoder-shaped bucket (199 segments,
         # FP16 gradients, AMSGrad): segment-aligned analysis, one report per
         # segment, 199 x 12 bytes read back, per-segment clip, update.

@@ -273,6 +273,22 @@ fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t
                                double max_grad_norm, void *stream);
 
 /*
+ * fa_bucket_step_writeback gated on the device report, as fa_bucket_step_gated
+ * is for fa_bucket_step: the update (FP32 masters and the FP16/BF16 model copy
+ * p_model, written in the same pass) skips when the report counts a non-finite
+ * value and otherwise applies the host formula's clip coefficient, bit-identical
+ * to reading the report back and calling fa_bucket_step_writeback.  ``t`` is the
+ * completed step count and is not changed.  p_model as in
+ * fa_bucket_step_writeback; a skipped update writes nothing, p_model included.
+ */
+fa_status fa_bucket_step_writeback_gated(const int64_t *seg_offsets, int32_t nseg,
+                                         int64_t n_total, float *p, const void *g, fa_dtype gdt,
+                                         float *m, float *v, float *vmax, uint64_t t,
+                                         const fa_options *options, fa_step_control ctl,
+                                         const fa_stats *report_dev, double max_grad_norm,
+                                         void *p_model, fa_dtype model_dtype, void *stream);
+
+/*
  * fa_bucket_step_clipped with the update gated on the device: the analysis
  * and merge are enqueued, then the 12-byte report's copy into pinned host
  * memory, then the gated update, so the update does not wait for the host.

@@ -849,6 +849,49 @@ def test_gated_step_full_size_bitwise():
     assert states[0]["t"] == 4
 
 
+@pytest.mark.parametrize("model_dtype", [torch.bfloat16, torch.float16])
+def test_gated_writeback_equals_host_decided_writeback_bitwise(model_dtype):
+    """The model-copy update gated on the device report: parameters, moments and the
+    low-precision copy bit-identical to deciding on the host, the +Inf call included."""
+    n = 256 * 4000 + 33
+    w = CONFIG5.scaled(n, calls=4, inf_call=2)
+    states = []
+    for gated in (False, True):
+        p = torch.empty(n, device=DEV)
+        w.fill_params_device(p)
+        m, v = torch.empty_like(p), torch.empty_like(p)
+        model = torch.zeros(n, dtype=model_dtype, device=DEV)
+        g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+        rows = fa.fa_stats_rows(n, 256)
+        rb, sc, rep = (fa.stats_buffer(rows, DEV), fa.scratch_buffer(rows, DEV),
+                       fa.stats_buffer(1, DEV))
+        t = 0
+        for call in range(1, w.calls + 1):
+            w.fill_grad_device(call, g)
+            fa.fa_analyze_gradient(g, 256, rb)
+            fa.fa_merge_gradient_stats(rb, rows, sc, rep)
+            o = fa.options(**w.options())
+            if gated:
+                fa.fa_bucket_step_writeback_gated(None, p, g, m, v, None, t, o, fa.control(),
+                                                  rep, 0.5, model)
+                h = fa.fa_read_report(rep)
+                skip, _, _ = fa.fa_clip_decision(float(h.sum_sq) + float(h.sum_sq_lo),
+                                                 h.nonfinite, 1.0, 0.5)
+                t += 0 if skip else 1
+            else:
+                skip, _, coef = fa.fa_clip_decide(rep, 1.0, 0.5)
+                if not skip:
+                    t, _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, t, o,
+                                                       fa.control(), model, coef)
+        torch.cuda.synchronize()
+        states.append((t, p.clone(), m.clone(), v.clone(), model.clone()))
+    (ta, *a), (tb, *b) = states
+    assert ta == tb == 3
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16) if x.element_size() == 2 else x.view(torch.int32),
+                           y.view(torch.int16) if y.element_size() == 2 else y.view(torch.int32))
+
+
 def test_gated_update_skips_on_non_finite_report():
     n = 4_000_000
     p = torch.randn(n, device=DEV)
