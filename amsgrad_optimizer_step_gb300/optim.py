@@ -15,10 +15,13 @@ GB300 layout: every parameter group is packed into one contiguous bucket.  The
 parameters (or, for BF16/FP16 parameters, an FP32 master copy) and their
 gradients become views into flat device buffers, so a step is one analysis and
 one update launch per group over the whole bucket (the pages launch one update
-per parameter).  Elements of a bucket share the group's options and step count,
-as a pre-flattened bucket must ("実験的なデバイス上の融合 AdamW / AMSGrad", section
-"サポートされている契約").  All arithmetic runs in the library's kernels; this
-module only allocates buffers and calls the C ABI.
+per active parameter).  Elements of one launch share the group's options and step
+count, as a pre-flattened bucket must ("実験的なデバイス上の融合 AdamW / AMSGrad",
+section "サポートされている契約").  Each parameter keeps its own step count: a
+parameter whose ``.grad`` is None is inactive, is not updated and does not advance,
+as in torch.optim; the update then covers each run of consecutive active
+parameters with equal counts in one launch.  All arithmetic runs in the library's
+kernels; this module only allocates buffers and calls the C ABI.
 """
 
 from __future__ import annotations
@@ -36,6 +39,28 @@ from . import sharded
 MAX_ROWS = 4_194_304
 STEP_OPTIONS_VERSION_HIERARCHICAL = 2
 STEP_OPTIONS_VERSION_PLAIN = 1
+
+
+def active_runs(active: list[bool], steps: list[int], offsets: list[int],
+                n: int) -> list[tuple[int, int, int, int]]:
+    """Maximal runs of consecutive active parameters with equal step counts, as
+    (first parameter, end parameter, first element, end element): each run is one
+    update launch over a contiguous slice of the bucket, and when every parameter is
+    active with one step count (the usual case) the single run is the whole bucket.
+    A run ends at the next parameter's offset, so it includes its alignment padding."""
+    out = []
+    i = 0
+    count = len(active)
+    while i < count:
+        if not active[i]:
+            i += 1
+            continue
+        j = i + 1
+        while j < count and active[j] and steps[j] == steps[i]:
+            j += 1
+        out.append((i, j, offsets[i], offsets[j] if j < count else n))
+        i = j
+    return out
 
 
 class _Bucket:
@@ -81,24 +106,41 @@ class _Bucket:
                 if p.grad is not None:
                     self.grad[off:off + k].copy_(p.grad.reshape(-1))
                 p.grad = self.grad[off:off + k].view_as(p)
-        self.t = 0
+        # one step count per parameter: a parameter without a gradient is not updated
+        # and its count does not advance, as in torch.optim and the pages' adapter
+        self.steps = [0] * len(params)
 
     def view(self, buf: torch.Tensor, i: int) -> torch.Tensor:
         p = self.params[i]
         return buf[self.offsets[i]:self.offsets[i] + p.numel()].view_as(p)
 
-    def gather_grads(self) -> None:
+    def gather_grads(self) -> list[bool]:
         """Autograd normally accumulates into the bucket views in place; a gradient
-        that was replaced by a new tensor is copied back into the bucket."""
+        that was replaced by a new tensor is copied back into the bucket.  Returns
+        which parameters are active (have a gradient); an inactive one's slice of the
+        bucket gradient is zeroed, so it adds nothing to the statistics."""
+        active = []
         with torch.no_grad():
             for i, p in enumerate(self.params):
                 mine = self.view(self.grad, i)
                 if p.grad is None:
                     mine.zero_()
-                    p.grad = mine
-                elif p.grad.data_ptr() != mine.data_ptr():
+                    active.append(False)
+                    continue
+                if p.grad.data_ptr() != mine.data_ptr():
                     mine.copy_(p.grad)
                     p.grad = mine
+                active.append(True)
+        return active
+
+    def runs(self, active: list[bool]) -> list[tuple[int, int, int, int]]:
+        return active_runs(active, self.steps, self.offsets, self.n)
+
+    def slices(self, lo: int, hi: int):
+        """(master, grad, m, v, vmax, model) views of elements [lo, hi)."""
+        cut = lambda t: None if t is None else t[lo:hi]  # noqa: E731
+        return (cut(self.master), cut(self.grad), cut(self.m), cut(self.v), cut(self.vmax),
+                cut(self.model))
 
 
 class FusedAdamW(torch.optim.Optimizer):
@@ -137,7 +179,7 @@ class FusedAdamW(torch.optim.Optimizer):
         """Per-parameter state entries are views into the group buckets."""
         for b in self._buckets:
             for i, p in enumerate(b.params):
-                st = {"step": torch.tensor(float(b.t)),
+                st = {"step": torch.tensor(float(b.steps[i])),
                       "exp_avg": b.view(b.m, i), "exp_avg_sq": b.view(b.v, i)}
                 if b.vmax is not None:
                     st["max_exp_avg_sq"] = b.view(b.vmax, i)
@@ -147,8 +189,8 @@ class FusedAdamW(torch.optim.Optimizer):
 
     def _sync_steps(self) -> None:
         for b in self._buckets:
-            for p in b.params:
-                self.state[p]["step"] = torch.tensor(float(b.t))
+            for i, p in enumerate(b.params):
+                self.state[p]["step"] = torch.tensor(float(b.steps[i]))
 
     def state_dict(self):
         self._sync_steps()
@@ -188,25 +230,25 @@ class FusedAdamW(torch.optim.Optimizer):
                 for k, val in saved.items():
                     if k != "params":
                         group[k] = tuple(val) if k == "betas" else val
-                steps = set()
                 for i, idx in enumerate(saved["params"]):
                     st = saved_state.get(idx, {})
-                    steps.add(int(float(st.get("step", 0))))
+                    b.steps[i] = int(float(st.get("step", 0)))
                     for key, buf in (("exp_avg", b.m), ("exp_avg_sq", b.v),
                                      ("max_exp_avg_sq", b.vmax), ("master_param", b.master)):
                         if buf is not None and key in st:
                             b.view(buf, i).copy_(st[key])
-                if len(steps) > 1:
-                    raise ValueError("parameters of one group have different step counts")
-                b.t = steps.pop() if steps else 0
         self._bind_state()
 
     def zero_grad(self, set_to_none: bool = False) -> None:
-        """Clears the bucket gradients (they stay allocated: the views are the bucket)."""
+        """Clears the bucket gradients.  By default ``.grad`` stays the bucket view, so
+        backward accumulates in place and every parameter counts as active.  With
+        ``set_to_none=True`` every ``.grad`` becomes None, as in torch.optim: a parameter
+        that backward then leaves without a gradient is skipped by the next step, at the
+        cost of one copy of each new gradient into the bucket."""
         for b in self._buckets:
             b.grad.zero_()
             for i, p in enumerate(b.params):
-                p.grad = b.view(b.grad, i)
+                p.grad = None if set_to_none else b.view(b.grad, i)
 
     # ---- the step ------------------------------------------------------------------
     def _stats_buffers(self):
@@ -255,30 +297,30 @@ class FusedAdamW(torch.optim.Optimizer):
         if closure is not None:
             with torch.enable_grad():
                 loss = closure()
-        for b in self._buckets:
-            b.gather_grads()
+        active = [b.gather_grads() for b in self._buckets]
         report = {"skipped": bool(found_inf), "nonfinite": 0, "grad_norm": None, "clip_coef": 1.0}
         use_stats = not found_inf and (self.max_grad_norm is not None or self.hierarchical_stats
                                        or check_finite)
         if use_stats and self._can_gate():
-            self.last_report = self._gated_step(gradient_scale)
+            self.last_report = self._gated_step(gradient_scale, active)
             return loss
         if use_stats:
             skip, norm, coef, bad = self.statistics(gradient_scale)
             report.update(skipped=skip, nonfinite=bad, grad_norm=norm, clip_coef=coef)
         if not report["skipped"]:
-            for group, b in zip(self.param_groups, self._buckets):
-                o = options(lr=group["lr"], beta1=group["betas"][0], beta2=group["betas"][1],
-                            eps=group["eps"], weight_decay=group["weight_decay"],
-                            amsgrad=group["amsgrad"], maximize=group["maximize"])
-                ctl = control(gradient_scale)
-                if b.master_separate:
-                    b.t, _ = fa_bucket_step_writeback(b.segments, b.master, b.grad, b.m, b.v,
-                                                      b.vmax, b.t, o, ctl, b.model,
-                                                      report["clip_coef"])
-                else:
-                    b.t, _ = fa_bucket_step(b.segments, b.master, b.grad, b.m, b.v, b.vmax,
-                                            b.t, o, ctl, report["clip_coef"])
+            ctl = control(gradient_scale)
+            for group, b, act in zip(self.param_groups, self._buckets, active):
+                o = self._options(group)
+                for i, j, lo, hi in b.runs(act):
+                    pm, g, m, v, vm, model = b.slices(lo, hi)
+                    if b.master_separate:
+                        fa_bucket_step_writeback(None, pm, g, m, v, vm, b.steps[i], o, ctl,
+                                                 model, report["clip_coef"])
+                    else:
+                        fa_bucket_step(None, pm, g, m, v, vm, b.steps[i], o, ctl,
+                                       report["clip_coef"])
+                    for k in range(i, j):
+                        b.steps[k] += 1
         self.last_report = report
         return loss
 
@@ -293,7 +335,7 @@ class FusedAdamW(torch.optim.Optimizer):
         import torch.distributed as dist
         return not (dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1)
 
-    def _gated_step(self, gradient_scale: float) -> dict:
+    def _gated_step(self, gradient_scale: float, active: list[list[bool]]) -> dict:
         """Statistics, then every group's update gated on the device by the same report
         (bit-identical to deciding on the host), while the host reads the report back
         through pinned memory to advance the step counts."""
@@ -306,21 +348,26 @@ class FusedAdamW(torch.optim.Optimizer):
         self._report_event.record(stream)
         ctl = control(gradient_scale)
         max_norm = self.max_grad_norm if self.max_grad_norm else 0.0
-        for group, b in zip(self.param_groups, self._buckets):
-            if b.master_separate:
-                fa_bucket_step_writeback_gated(b.segments, b.master, b.grad, b.m, b.v, b.vmax,
-                                               b.t, self._options(group), ctl, report_dev,
-                                               max_norm, b.model)
-            else:
-                fa_bucket_step_gated(b.segments, b.master, b.grad, b.m, b.v, b.vmax, b.t,
-                                     self._options(group), ctl, report_dev, max_norm)
+        launched = []
+        for group, b, act in zip(self.param_groups, self._buckets, active):
+            o = self._options(group)
+            for i, j, lo, hi in b.runs(act):
+                pm, g, m, v, vm, model = b.slices(lo, hi)
+                if b.master_separate:
+                    fa_bucket_step_writeback_gated(None, pm, g, m, v, vm, b.steps[i], o, ctl,
+                                                   report_dev, max_norm, model)
+                else:
+                    fa_bucket_step_gated(None, pm, g, m, v, vm, b.steps[i], o, ctl, report_dev,
+                                         max_norm)
+                launched.append((b, i, j))
         self._report_event.synchronize()
         rep = FaStats.from_buffer_copy(self._pinned_report.numpy().tobytes())
         total = float(rep.sum_sq) + float(rep.sum_sq_lo)
         skip, norm, coef = fa_clip_decision(total, int(rep.nonfinite), gradient_scale, max_norm)
         if not skip:
-            for b in self._buckets:
-                b.t += 1
+            for b, i, j in launched:
+                for k in range(i, j):
+                    b.steps[k] += 1
         return {"skipped": skip, "nonfinite": int(rep.nonfinite), "grad_norm": norm,
                 "clip_coef": coef}
 

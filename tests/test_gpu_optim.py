@@ -234,31 +234,97 @@ def test_low_precision_params_keep_fp32_masters(dtype):
 def test_empty_and_gradless_parameters():
     """A zero-element parameter and one that never receives a gradient share a bucket
     with ordinary ones: the empty one is carried along untouched, the gradless one is
-    updated with a zero gradient (decay only, as the oracle does), the rest as usual."""
+    inactive (not updated, its step count stays 0, it adds nothing to the global norm),
+    the rest are updated as usual."""
     shapes = [(0,), (17,), (3, 5)]
     params = _params(13, shapes=shapes)
+    before = params[2].detach().clone()
     opt = FusedAdamW(params, lr=1e-2, weight_decay=0.1, max_grad_norm=1.0)
     lib = oracle.lib()
     oo = dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=0.1, amsgrad=False,
               maximize=False)
-    refs = [oracle.OracleAdamW(_host(p), oo, lib_=lib) for p in params]
+    ref = oracle.OracleAdamW(_host(params[1]), oo, lib_=lib)
     for step in range(1, 4):
         g17 = (torch.randn(17, generator=torch.Generator().manual_seed(step)) * 1e-2)
         params[0].grad = None
         params[1].grad = g17.to(DEV)        # a new tensor: gathered into the bucket
         params[2].grad = None               # never receives a gradient
         opt.step()
-        grads = [np.zeros(0, np.float32), g17.numpy(), np.zeros(15, np.float32)]
-        allg = np.concatenate(grads)
-        s, c = lib.gradient_stats(allg, "f32")
+        s, c = lib.gradient_stats(g17.numpy(), "f32")
         _, norm, coef = lib.clip_decision(s, c, 1.0)
-        for r, g in zip(refs, grads):
-            r.step(g, "f32", clip_coef=coef)
+        assert abs(opt.last_report["grad_norm"] - norm) <= 1e-5 * norm
+        ref.step(g17.numpy(), "f32", clip_coef=coef)
     torch.cuda.synchronize()
     assert params[0].numel() == 0
-    for p, r in zip(params[1:], refs[1:]):
-        gate(_host(p), r.p, 1e-5, "p")
-    assert float(opt.state_dict()["state"][1]["step"]) == 3
+    gate(_host(params[1]), ref.p, 1e-5, "p")
+    assert torch.equal(params[2], before)
+    assert not opt.state[params[2]]["exp_avg"].any()
+    steps = [float(st["step"]) for st in opt.state_dict()["state"].values()]
+    assert steps[1:] == [3.0, 0.0]
+
+
+ACTIVITY = [  # which of the five parameters have a gradient, step by step
+    [True, True, True, True, True],
+    [True, False, True, False, True],
+    [False, True, True, True, False],
+    [True, True, True, True, True],
+    [True, True, False, True, True],
+]
+
+
+@pytest.mark.parametrize("dtype,clip", [(torch.float32, None), (torch.float32, 0.05),
+                                        (torch.bfloat16, 0.05)])
+def test_intermittent_parameters_keep_their_own_step_counts(dtype, clip):
+    """Parameters that miss some steps are updated with their own step counts (their
+    own bias corrections), by one launch per run of active parameters with equal
+    counts; the global norm covers only the active parameters of each step."""
+    params = _params(15, dtype=dtype)
+    hp = dict(lr=2e-3, betas=(0.9, 0.99), eps=1e-6, weight_decay=0.01, amsgrad=True)
+    opt = FusedAdamW(params, max_grad_norm=clip, **hp)
+    lib = oracle.lib()
+    oo = dict(lr=2e-3, beta1=0.9, beta2=0.99, eps=1e-6, weight_decay=0.01, amsgrad=True,
+              maximize=False)
+    name = "f32" if dtype == torch.float32 else "bf16"
+    refs = [oracle.OracleAdamW(_host(p), oo, lib_=lib) for p in params]
+    for step, act in enumerate(ACTIVITY, start=1):
+        grads = _grads(15, step)
+        opt.zero_grad(set_to_none=True)
+        bits = []
+        for p, g, a in zip(params, grads, act):
+            if a:
+                p.grad = g.to(dtype).to(DEV)
+                bits.append(lib_bits(p.grad, name))
+        opt.step()
+        coef = 1.0
+        if clip is not None:
+            s, c = lib.gradient_stats(np.concatenate(bits), name)
+            _, norm, coef = lib.clip_decision(s, c, clip)
+            assert abs(opt.last_report["grad_norm"] - norm) <= 1e-5 * norm
+        k = 0
+        for r, a in zip(refs, act):
+            if a:
+                r.step(bits[k], name, clip_coef=coef)
+                k += 1
+    torch.cuda.synchronize()
+    for p, r in zip(params, refs):
+        st = opt.state[p]
+        master = st["master_param"] if dtype != torch.float32 else p
+        gate(_host(master), r.p, 1e-5, "p")
+        gate(_host(st["exp_avg"]), r.state.m, 1e-5, "m")
+        gate(_host(st["max_exp_avg_sq"]), r.state.vmax, 1e-5, "vmax")
+        if dtype != torch.float32:
+            got = p.detach().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
+            assert np.array_equal(got, lib.model_copy(_host(master), name))
+    want = [sum(a[i] for a in ACTIVITY) for i in range(5)]
+    assert [int(float(st["step"])) for st in opt.state_dict()["state"].values()] == want
+    assert want == [r.state.t for r in refs]
+
+
+def lib_bits(t, name):
+    """A gradient as the oracle takes it: FP32 values, or BF16 bit patterns."""
+    if name == "f32":
+        return _host(t)
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
 
 
 def test_replaced_gradients_are_gathered_into_the_bucket():

@@ -76,3 +76,26 @@ def test_shards_are_contiguous_aligned_and_balanced(n, world):
     lens = [hi - lo for lo, hi in bounds]
     # shards hold floor or ceil of ceil(n/8)/world 8-element units; the last may be short
     assert max(lens) - min(lens) <= 16
+
+
+@SETTINGS
+@given(data=st.lists(st.tuples(st.booleans(), st.integers(0, 3), st.integers(0, 40)),
+                     min_size=1, max_size=30))
+def test_active_runs_cover_exactly_the_active_parameters(data):
+    from amsgrad_optimizer_step_gb300.optim import active_runs
+    active = [a for a, _, _ in data]
+    steps = [s for _, s, _ in data]
+    offsets, pos = [], 0
+    for _, _, size in data:
+        offsets.append(pos)
+        pos += (size + 7) // 8 * 8
+    runs = active_runs(active, steps, offsets, pos)
+    covered = [i for i, j, _, _ in runs for i in range(i, j)]
+    assert covered == [i for i, a in enumerate(active) if a]
+    for i, j, lo, hi in runs:
+        assert len({steps[k] for k in range(i, j)}) == 1
+        assert lo == offsets[i] and hi == (offsets[j] if j < len(data) else pos)
+        # maximal: the next parameter is inactive or has another step count
+        assert j == len(data) or not active[j] or steps[j] != steps[i]
+    if all(active) and len(set(steps)) == 1:
+        assert runs == [(0, len(data), 0, pos)]
