@@ -21,8 +21,8 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
                    FaStepReport, FusedAdamWError, check)
 
 __all__ = [
-    "fa_abi_version", "fa_device_error", "fa_bounds_check_report", "fa_pipeline_selftest", "fa_options_default", "fa_step_coefficients", "fa_adamw_step",
-    "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback",
+    "fa_abi_version", "fa_device_error", "fa_bounds_check_report", "fa_pipeline_selftest",
+    "fa_options_default", "fa_step_coefficients", "fa_adamw_step", "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback",
     "fa_adamw_step_staged", "fa_stats_plan",
     "fa_stats_rows",
     "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",

@@ -320,6 +320,49 @@ def test_intermittent_parameters_keep_their_own_step_counts(dtype, clip):
     assert want == [r.state.t for r in refs]
 
 
+def _train_intermittent(opt, params, steps, first=1, dtype=torch.float32):
+    for step in range(first, first + steps):
+        act = ACTIVITY[(step - 1) % len(ACTIVITY)]
+        opt.zero_grad(set_to_none=True)
+        for p, g, a in zip(params, _grads(16, step), act):
+            if a:
+                p.grad = g.to(dtype).to(DEV)
+        opt.step()
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_state_dict_round_trip_with_different_step_counts(dtype):
+    """Parameters with different step counts survive save / load: 3 intermittent steps
+    (counts 2 and 3), a checkpoint into a fresh optimizer, 7 more, bit-identical to 10
+    uninterrupted."""
+    hp = dict(lr=1e-3, amsgrad=True, max_grad_norm=0.5)
+    ref_params = _params(16, dtype=dtype)
+    ref = FusedAdamW(ref_params, **hp)
+    _train_intermittent(ref, ref_params, 10, dtype=dtype)
+
+    params = _params(16, dtype=dtype)
+    opt = FusedAdamW(params, **hp)
+    _train_intermittent(opt, params, 3, dtype=dtype)
+    sd = opt.state_dict()
+    assert len({float(st["step"]) for st in sd["state"].values()}) > 1
+    fresh = _params(98, dtype=dtype)
+    with torch.no_grad():
+        for p, q in zip(fresh, params):
+            p.copy_(q)
+    opt2 = FusedAdamW(fresh, **hp)
+    opt2.load_state_dict(sd)
+    _train_intermittent(opt2, fresh, 7, first=4, dtype=dtype)
+    for p, q in zip(fresh, ref_params):
+        assert torch.equal(p, q)
+        for key in ("exp_avg", "exp_avg_sq", "max_exp_avg_sq"):
+            assert torch.equal(opt2.state[p][key], ref.state[q][key])
+        if dtype != torch.float32:
+            assert torch.equal(opt2.state[p]["master_param"], ref.state[q]["master_param"])
+    assert ([float(st["step"]) for st in opt2.state_dict()["state"].values()]
+            == [float(st["step"]) for st in ref.state_dict()["state"].values()])
+
+
 def lib_bits(t, name):
     """A gradient as the oracle takes it: FP32 values, or BF16 bit patterns."""
     if name == "f32":
