@@ -33,7 +33,44 @@
 #endif
 #endif
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization allowed (launch_dependent below) may be scheduled while the kernel
+// before it in the stream is still running, once every CTA of that kernel has
+// called fa_allow_dependents() or exited.  fa_grid_dependency_wait() then blocks
+// until the earlier kernel has completed and its writes are visible; in a kernel
+// launched the ordinary way it returns at once.  Every kernel launched through
+// launch_dependent calls it before its first global-memory access, so starting
+// early never reads anything stale: what overlaps is launch latency, CTA
+// scheduling and shared-memory setup.
+#if defined(__CUDACC__)
+__device__ __forceinline__ void fa_grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void fa_allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
 namespace fa {
+
+#if defined(__CUDACC__)
+// Launches ``kernel`` with programmatic stream serialization allowed.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block,
+                                    size_t smem, cudaStream_t stream, const Args &...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#endif
 
 constexpr int kThreads = 256;            // threads per CTA for every kernel here
 constexpr int kFanIn = 1024;             // merge fan-in

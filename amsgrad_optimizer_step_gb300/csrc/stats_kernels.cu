@@ -137,6 +137,7 @@ __device__ __forceinline__ int find_segment(const AnalyzeArgs &a, int64_t r) {
 template <int GT, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 analyze_kernel(const __grid_constant__ AnalyzeArgs a) {
+    fa_allow_dependents();  // the merge that follows waits for this grid to finish
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
@@ -262,6 +263,7 @@ __device__ __forceinline__ float transpose_reduce(const float (&s)[R], int lane)
 template <int GT, int CH, bool MULTI>
 __global__ void __launch_bounds__(kThreads)
 analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
+    fa_allow_dependents();  // the merge that follows waits for this grid to finish
     constexpr int R = 8 / CH;
     constexpr int kLog2R = R == 8 ? 3 : R == 4 ? 2 : R == 2 ? 1 : 0;
     constexpr int64_t kElemBytes = GT == FA_F32 ? 4 : 2;
@@ -441,6 +443,8 @@ __device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int
 // One CTA per group of kFanIn input records.
 __global__ void __launch_bounds__(kThreads)
 merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
+    fa_grid_dependency_wait();  // (launched early: the records are not ready before this)
+    fa_allow_dependents();
     const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kFanIn;
     const int64_t g1 = g0 + kFanIn < count ? g0 + kFanIn : count;
     block_merge(in, g0, g1, count, out + blockIdx.x);
@@ -459,6 +463,8 @@ __device__ __forceinline__ int find_chunk(const ChunkMergeArgs &a, int64_t group
 
 __global__ void __launch_bounds__(kThreads)
 merge_chunks_a_kernel(const __grid_constant__ ChunkMergeArgs a) {
+    fa_grid_dependency_wait();
+    fa_allow_dependents();
     const int64_t b = blockIdx.x;
     const int k = find_chunk(a, b);
     const int64_t lo = a.row_start[k] + (b - a.group_start[k]) * kFanIn;
@@ -470,6 +476,8 @@ merge_chunks_a_kernel(const __grid_constant__ ChunkMergeArgs a) {
 // zero record).
 __global__ void __launch_bounds__(kThreads)
 merge_chunks_b_kernel(const __grid_constant__ ChunkMergeArgs a) {
+    fa_grid_dependency_wait();
+    fa_allow_dependents();
     const int k = blockIdx.x;
     block_merge(a.partial, a.group_start[k], a.group_start[k + 1], a.group_start[a.nchunks],
                 a.out + k);
@@ -546,20 +554,25 @@ cudaError_t stats_bounds_violations(unsigned long long *count, bool clear) {
 
 cudaError_t launch_merge_chunks(const ChunkMergeArgs &a, cudaStream_t stream) {
     const int64_t groups = a.group_start[a.nchunks];
+    // both levels start early and wait for their input in the kernel
     if (groups > 0) {
-        merge_chunks_a_kernel<<<static_cast<unsigned>(groups), kThreads, 0, stream>>>(a);
-        const cudaError_t err = cudaGetLastError();
+        const cudaError_t err = launch_dependent(merge_chunks_a_kernel,
+                                                 dim3(static_cast<unsigned>(groups)),
+                                                 dim3(kThreads), 0, stream, a);
         if (err != cudaSuccess) return err;
     }
-    if (a.nchunks > 0) merge_chunks_b_kernel<<<a.nchunks, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    if (a.nchunks > 0)
+        return launch_dependent(merge_chunks_b_kernel, dim3(a.nchunks), dim3(kThreads), 0,
+                                stream, a);
+    return cudaSuccess;
 }
 
 cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream) {
     const int64_t grid = (count + kFanIn - 1) / kFanIn;
     if (grid <= 0) return cudaSuccess;
-    merge_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(in, count, out);
-    return cudaGetLastError();
+    // starts early and waits for its input in the kernel
+    return launch_dependent(merge_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
+                            stream, in, count, out);
 }
 
 // ---- fixed merge scratch for callers that cannot allocate ------------------------

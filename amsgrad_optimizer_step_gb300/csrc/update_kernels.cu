@@ -262,6 +262,7 @@ __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &
 template <int GT, bool AMS, bool FIRST, int UNROLL, int MD>
 __global__ void __launch_bounds__(kUThreads)
 update_vec_kernel(const UpdateArgs a, const Coef c0) {
+    fa_grid_dependency_wait();  // (a gated launch may start before the merge ends)
     Coef c = c0;
     if (a.gate && !gate_decision(a, &c.gmul)) return;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kUThreads + threadIdx.x;
@@ -314,6 +315,7 @@ update_vec_kernel(const UpdateArgs a, const Coef c0) {
 template <int GT, bool AMS, bool FIRST, int MD>
 __global__ void __launch_bounds__(kThreads)
 update_scalar_kernel(const UpdateArgs a, const Coef c0) {
+    fa_grid_dependency_wait();
     Coef c = c0;
     if (a.gate && !gate_decision(a, &c.gmul)) return;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -458,6 +460,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_t ntiles) {
     const UpdateArgs &a = sa.a;
     Coef c = c0;
+    fa_grid_dependency_wait();  // (a gated launch may start before the merge ends)
     // a skipped step returns before any copy is issued (every thread decides alike)
     if (a.gate && !gate_decision(a, &c.gmul)) return;
     using L = TmaLayout<GT, AMS, MD>;
@@ -692,8 +695,12 @@ cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vecto
         if (dev < 64) configured[dev].store(true, std::memory_order_release);
     }
     const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
-    kern<<<grid, kTmaThreads, L::kSmem, stream>>>(s, c, ntiles);
     *launched = true;
+    // gated: scheduled while the merge before it runs; the kernel waits for it
+    if (s.a.gate)
+        return launch_dependent(kern, dim3(grid), dim3(kTmaThreads), L::kSmem, stream, s, c,
+                                ntiles);
+    kern<<<grid, kTmaThreads, L::kSmem, stream>>>(s, c, ntiles);
     return cudaGetLastError();
 }
 #endif
@@ -810,11 +817,13 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
         const int grid = persistent_grid(kern, need, dev, kUThreads);
         if (grid == 0) return cudaSuccess;
+        if (a.gate) return launch_dependent(kern, dim3(grid), dim3(kUThreads), 0, stream, a, c);
         kern<<<grid, kUThreads, 0, stream>>>(a, c);
     } else {
         auto kern = update_scalar_kernel<GT, AMS, FIRST, MD>;
         const int grid = persistent_grid(kern, (a.n + kThreads - 1) / kThreads, dev);
         if (grid == 0) return cudaSuccess;
+        if (a.gate) return launch_dependent(kern, dim3(grid), dim3(kThreads), 0, stream, a, c);
         kern<<<grid, kThreads, 0, stream>>>(a, c);
     }
     return cudaGetLastError();
