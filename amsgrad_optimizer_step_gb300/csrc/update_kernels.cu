@@ -24,6 +24,7 @@
 // Elements before the first 16-byte boundary and after the last full vector or
 // tile go through the same arithmetic one at a time.
 #include <atomic>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -340,6 +341,15 @@ __device__ __forceinline__ int find_seg_in(const SegScaleArgs &s, int64_t e, int
     return lo;
 }
 
+// The same search over a copy of the segment starts in shared memory.
+__device__ __forceinline__ int find_seg_smem(const int64_t *seg_start, int64_t e, int lo, int hi) {
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seg_start[mid] <= e) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
 __device__ __forceinline__ int find_seg(const SegScaleArgs &s, int64_t e) {
     int lo = 0, hi = s.nseg - 1;
     while (lo < hi) {
@@ -373,6 +383,9 @@ __device__ __forceinline__ void scalar_element_seg(const SegScaleArgs &s, const 
 #endif
 constexpr int kTmaThreads = FA_TMA_THREADS;
 constexpr int kTmaSmemBudget = 226 * 1024;  // dynamic shared memory per CTA
+constexpr int kSmemPerCtaMax = 227 * 1024;  // the architectural limit, tables included
+// The per-segment table staged in shared memory: starts and multipliers.
+constexpr int kSegTableBytes = (kMaxSegPerLaunch + 1) * 8 + kMaxSegPerLaunch * 4;
 constexpr uint32_t kTmaSpinLimit = 1u << 20;   // tries per wait (x kTmaSuspendNs: ~1 s)
 constexpr uint32_t kTmaSuspendNs = 1000;
 
@@ -453,6 +466,15 @@ struct TmaLayout {
     static_assert(kStages >= 2, "at least two stages");
 };
 
+// Dynamic shared memory of one launch: the stages, their barriers and, with SEG,
+// the segment table (read at every segment crossing: in shared memory it costs a
+// few tens of cycles, where an indexed kernel-parameter read that misses the
+// constant cache stalled the tile loop for hundreds).
+template <int GT, bool AMS, int MD, bool SEG>
+constexpr int tma_smem_bytes() {
+    return TmaLayout<GT, AMS, MD>::kSmem + (SEG ? kSegTableBytes : 0);
+}
+
 // SEG: one gradient multiplier per segment from s's table (MD must be kNoModel);
 // otherwise s.nseg is 0 and c.gmul applies to every element.
 template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
@@ -469,6 +491,8 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
         L::kTile * (4 + L::kGB + (FIRST ? 0 : (AMS ? 12 : 8)));
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * L::kStage);
+    int64_t *s_seg = reinterpret_cast<int64_t *>(smem + S * L::kStage + S * 8);  // SEG only
+    float *s_gmul = reinterpret_cast<float *>(s_seg + kMaxSegPerLaunch + 1);
     const int tid = threadIdx.x;
 
     // thread 0's view of each stage: loads issued and consumed
@@ -498,6 +522,10 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(&bars[s]);
         fence_mbar_init();
+    }
+    if (SEG) {
+        for (int j = tid; j <= sa.nseg; j += kTmaThreads) s_seg[j] = sa.seg_start[j];
+        for (int j = tid; j < sa.nseg; j += kTmaThreads) s_gmul[j] = sa.gmul[j];
     }
     __syncthreads();
     if (tid == 0) {
@@ -533,14 +561,14 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
             if (t0 >= next_start) {
                 do {
                     ++k_lo;
-                    next_start = k_lo + 1 < sa.nseg ? sa.seg_start[k_lo + 1] : INT64_MAX;
+                    next_start = k_lo + 1 < sa.nseg ? s_seg[k_lo + 1] : INT64_MAX;
                 } while (t0 >= next_start);
-                seg_gmul = sa.gmul[k_lo];
+                seg_gmul = s_gmul[k_lo];
             }
             k_hi = k_lo;
             if (t0 + L::kTile > next_start) {  // the tile reaches into later segments
                 k_hi = k_lo + 1;
-                while (k_hi + 1 < sa.nseg && sa.seg_start[k_hi + 1] < t0 + L::kTile) ++k_hi;
+                while (k_hi + 1 < sa.nseg && s_seg[k_hi + 1] < t0 + L::kTile) ++k_hi;
             }
         }
         uint32_t it = 0;
@@ -551,8 +579,14 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
         if (tid == 0) consumed[s] = issued[s];
 
         unsigned char *b = smem + s * L::kStage;
-#pragma unroll
-        for (int h = 0; h < L::kChunks; ++h) {
+        Coef ct = c;
+        if (SEG) ct.gmul = seg_gmul;
+        // One 4-element chunk per call; PER_ELEM looks up each element's segment (a tile
+        // that straddles a boundary).  The branch between the two forms is taken once
+        // per tile, so a tile inside one segment runs the same straight-line code over
+        // all its chunks as the kernel without a segment table (a branch per chunk cost
+        // the per-segment update 1 % of its time).
+        auto chunk = [&](int h, auto per_elem) {
             const int j = h * 4 * kTmaThreads + 4 * tid;  // first element of this chunk
             float x[4], p[4], m[4], v[4], vm[4];
             if (GT == FA_F32) {
@@ -584,24 +618,18 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
                     vm[0] = w4.x; vm[1] = w4.y; vm[2] = w4.z; vm[3] = w4.w;
                 }
             }
-            if (SEG) {
-                Coef cc = c;
-                if (k_lo == k_hi) {  // the whole tile lies in one segment
-                    cc.gmul = seg_gmul;
+            if constexpr (decltype(per_elem)::value) {
+                const int64_t e = a.head + tile * L::kTile + j;
+                Coef cc = ct;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
-                } else {
-                    const int64_t e = a.head + tile * L::kTile + j;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        cc.gmul = sa.gmul[find_seg_in(sa, e + q, k_lo, k_hi)];
-                        adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    cc.gmul = s_gmul[find_seg_smem(s_seg, e + q, k_lo, k_hi)];
+                    adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
                 }
             } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) adamw_element<AMS, FIRST>(c, x[q], p[q], m[q], v[q], vm[q]);
+                for (int q = 0; q < 4; ++q)
+                    adamw_element<AMS, FIRST>(ct, x[q], p[q], m[q], v[q], vm[q]);
             }
             *pp = make_float4(p[0], p[1], p[2], p[3]);
             *mp = make_float4(m[0], m[1], m[2], m[3]);
@@ -613,6 +641,13 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
                 w.y = pack2<MD>(p[2], p[3]);
                 *reinterpret_cast<uint2 *>(b + L::kModel + 2 * j) = w;
             }
+        };
+        if (!SEG || k_lo == k_hi) {
+#pragma unroll
+            for (int h = 0; h < L::kChunks; ++h) chunk(h, std::false_type{});
+        } else {
+#pragma unroll 1
+            for (int h = 0; h < L::kChunks; ++h) chunk(h, std::true_type{});
         }
         fence_async_shared();
         __syncthreads();
@@ -681,6 +716,8 @@ template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
 cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vector_ok, int dev,
                                 cudaStream_t stream, bool *launched) {
     using L = TmaLayout<GT, AMS, MD>;
+    constexpr int kSmem = tma_smem_bytes<GT, AMS, MD, SEG>();
+    static_assert(kSmem <= kSmemPerCtaMax, "shared memory per CTA");
     *launched = false;
     const int64_t ntiles = (s.a.n - s.a.head) / L::kTile;
     const int64_t sms = sm_count(dev);
@@ -690,7 +727,7 @@ cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vecto
     static std::atomic<bool> configured[64] = {};
     if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         const cudaError_t err =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (err != cudaSuccess) return err;
         if (dev < 64) configured[dev].store(true, std::memory_order_release);
     }
@@ -698,9 +735,9 @@ cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vecto
     *launched = true;
     // gated: scheduled while the merge before it runs; the kernel waits for it
     if (s.a.gate)
-        return launch_dependent(kern, dim3(grid), dim3(kTmaThreads), L::kSmem, stream, s, c,
+        return launch_dependent(kern, dim3(grid), dim3(kTmaThreads), kSmem, stream, s, c,
                                 ntiles);
-    kern<<<grid, kTmaThreads, L::kSmem, stream>>>(s, c, ntiles);
+    kern<<<grid, kTmaThreads, kSmem, stream>>>(s, c, ntiles);
     return cudaGetLastError();
 }
 #endif
