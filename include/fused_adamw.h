@@ -12,7 +12,11 @@
  *     current device.  Host pointers are rejected with FA_ERR_POINTER
  *     ([FA-ja] "サポートされている契約": no arbitrary host pointers).
  *   - ``stream`` is a cudaStream_t passed as void*; NULL is the legacy default
- *     stream.  All device work is enqueued on it, in call order.
+ *     stream.  All device work is enqueued on it, in call order.  The merge
+ *     kernels and the gated update are launched as programmatic dependents:
+ *     they may be scheduled while the kernel before them on the stream is still
+ *     running, and wait for it to complete before touching any memory, so the
+ *     stream's order is unchanged for the caller.
  *   - FA_OK from an enqueuing call means the work was ENQUEUED, not that it
  *     finished ([FA-ja] "低レベルの使用"; [FA-zh] "用法"): check the stream's
  *     completion before trusting or checkpointing outputs; after a device

@@ -540,6 +540,33 @@ def test_merge_matches_exact_sum(rows):
     assert abs(got - exact) <= 1e-12 * exact
 
 
+def test_merges_see_the_writes_of_the_kernel_before_them():
+    """The merge kernels start early (programmatic dependent launch) and wait in the
+    kernel for the grid before them.  Here that grid is a torch kernel that rewrites the
+    row records right before each merge, many times over: every report must be the
+    exact sum of the records just written, never of the previous ones."""
+    import math
+    rows = 1_048_577  # three merge levels
+    rng = np.random.default_rng(31)
+    rows_in = fa.stats_buffer(rows, DEV)
+    scratch = fa.scratch_buffer(rows, DEV)
+    report = fa.stats_buffer(1, DEV)
+    base_h = (rng.random(rows) * 10).astype(np.float32)
+    base = torch.from_numpy(base_h).to(DEV)
+    rows_in.zero_()
+    for k in range(12):
+        # one elementwise kernel writes every sum, immediately before the merge
+        torch.mul(base, float(k + 1), out=rows_in[:, 0].view(torch.float32))
+        rows_in[k * 1000:(k + 1) * 1000, 1].fill_(k)
+        fa.fa_merge_gradient_stats(rows_in, rows, scratch, report)
+        h = fa.fa_read_report(report)
+        # the records as written: the FP32 product, correctly rounded on both sides
+        want = math.fsum((base_h * np.float32(k + 1)).astype(np.float64).tolist())
+        got = float(h.sum_sq) + float(h.sum_sq_lo)
+        assert abs(got - want) <= 1e-12 * want, (k, got, want)
+        assert h.nonfinite == sum(range(k + 1)) * 1000
+
+
 def test_statistics_capture_into_a_cuda_graph():
     """Analysis and merge captured once into a CUDA graph and replayed on new gradients
     give the same report, bit for bit, as the direct calls."""
