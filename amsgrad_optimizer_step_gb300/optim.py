@@ -143,6 +143,22 @@ class _Bucket:
                 cut(self.model))
 
 
+def statistics_decision(rep, gradient_scale: float, max_grad_norm: float,
+                        shard_group=None) -> tuple[bool, float, float]:
+    """(skip, norm, clip coefficient) from this process's 12-byte report.
+
+    Without ``shard_group`` the report covers the whole gradient: one process, or
+    data-parallel replicas whose gradients were already reduced (each replica's norm is
+    the global norm, as with ``torch.nn.utils.clip_grad_norm_``).  With a process group,
+    this optimizer's parameters are one rank's shard of the model: the ranks' totals
+    are summed in rank order and every rank takes the same decision.
+    """
+    if shard_group is None:
+        s, c = sharded.report_totals(rep)
+        return fa_clip_decision(s, c, gradient_scale, max_grad_norm)
+    return sharded.global_clip_decision(rep, gradient_scale, max_grad_norm, group=shard_group)
+
+
 class FusedAdamW(torch.optim.Optimizer):
     """AdamW / AMSGrad on GB300 through the fused step.
 
@@ -152,12 +168,19 @@ class FusedAdamW(torch.optim.Optimizer):
     ``GradScaler`` asks for it, the step first analyses every group's gradient,
     merges the statistics (fan-in 1024) and reads back the 12-byte report: a
     non-finite value skips the step, and the global norm sets the clip.
+
+    ``shard_group``: a ``torch.distributed`` process group when each rank's optimizer
+    holds a different shard of the model's parameters; the statistics are then summed
+    over the group before the decision.  Leave it None for one process or for
+    replicas with reduced gradients (the decision is then local, and taken on the
+    device).
     """
 
     def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-5,
                  weight_decay: float = 1e-4, amsgrad: bool = False, maximize: bool = False,
                  fused_step: bool = True, max_grad_norm: Optional[float] = None,
-                 hierarchical_stats: bool = False, row_len: Optional[int] = None):
+                 hierarchical_stats: bool = False, row_len: Optional[int] = None,
+                 shard_group=None):
         if not fused_step:
             raise ValueError("FusedAdamW implements the fused step only (fused_step=True)")
         if max_grad_norm is not None and not max_grad_norm > 0:
@@ -168,6 +191,7 @@ class FusedAdamW(torch.optim.Optimizer):
         self.fused_step = True
         self.max_grad_norm = max_grad_norm
         self.hierarchical_stats = hierarchical_stats
+        self.shard_group = shard_group
         self._buckets = [_Bucket(list(g["params"]), g["amsgrad"]) for g in self.param_groups]
         self.row_len = row_len if row_len is not None else self._auto_row_len()
         self._stats = None
@@ -284,10 +308,12 @@ class FusedAdamW(torch.optim.Optimizer):
         return report
 
     def statistics(self, gradient_scale: float = 1.0):
-        """Analyse every group, merge, read back: (skip, global norm, clip coefficient)."""
+        """Analyse every group, merge, read back: (skip, global norm, clip coefficient,
+        non-finite count), over every shard of ``shard_group`` when one is set."""
         rep = fa_read_report(self._enqueue_statistics())
-        skip, norm, coef = sharded.global_clip_decision(
-            rep, gradient_scale, self.max_grad_norm if self.max_grad_norm else 0.0)
+        skip, norm, coef = statistics_decision(
+            rep, gradient_scale, self.max_grad_norm if self.max_grad_norm else 0.0,
+            self.shard_group)
         return skip, norm, coef, int(rep.nonfinite)
 
     @torch.no_grad()
@@ -331,9 +357,8 @@ class FusedAdamW(torch.optim.Optimizer):
 
     def _can_gate(self) -> bool:
         """The device can take the decision itself when this process holds the whole
-        gradient (several ranks need every rank's totals first)."""
-        import torch.distributed as dist
-        return not (dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1)
+        gradient; shards need every rank's totals first."""
+        return self.shard_group is None
 
     def _gated_step(self, gradient_scale: float, active: list[list[bool]]) -> dict:
         """Statistics, then every group's update gated on the device by the same report

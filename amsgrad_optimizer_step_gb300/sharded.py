@@ -42,7 +42,10 @@ def gather_totals(sum_sq: float, nonfinite: int, group=None,
     if not (dist.is_available() and dist.is_initialized()):
         return sum_sq, nonfinite
     world = dist.get_world_size(group)
-    dev = device if device is not None else torch.device("cpu")
+    dev = device
+    if dev is None:  # NCCL exchanges device tensors, gloo host tensors
+        dev = (torch.device("cuda", torch.cuda.current_device())
+               if dist.get_backend(group) == "nccl" else torch.device("cpu"))
     mine = torch.tensor([sum_sq, float(nonfinite)], dtype=torch.float64, device=dev)
     parts = [torch.empty_like(mine) for _ in range(world)]
     dist.all_gather(parts, mine, group=group)

@@ -91,3 +91,47 @@ def test_shard_ranges_tile_the_bucket():
                 assert lo % 8 == 0 or lo == n
                 prev = hi
             assert prev == n
+
+
+def _optim_worker(rank, world, port, out_dir):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from amsgrad_optimizer_step_gb300 import FaStats, fa_clip_decision
+    from amsgrad_optimizer_step_gb300.optim import statistics_decision
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rep = FaStats()
+    rep.sum_sq = np.float32(3.0 + 5.0 * rank)  # rank 0: 3, rank 1: 8
+    rep.sum_sq_lo = np.float32(0.0)
+    rep.nonfinite = 0
+    local = statistics_decision(rep, 2.0, 0.5)
+    shards = statistics_decision(rep, 2.0, 0.5, shard_group=dist.group.WORLD)
+    want_local = fa_clip_decision(3.0 + 5.0 * rank, 0, 2.0, 0.5)
+    want_shards = fa_clip_decision(11.0, 0, 2.0, 0.5)
+    np.save(os.path.join(out_dir, f"o{rank}.npy"),
+            np.array([list(map(float, local)), list(map(float, shards)),
+                      list(map(float, want_local)), list(map(float, want_shards))]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_fused_adamw_sums_statistics_only_over_a_shard_group(tmp_path):
+    """FusedAdamW's decision with torch.distributed initialised: replicas (no
+    shard_group) decide from their own report, which already covers the whole reduced
+    gradient; shards (shard_group set) sum the ranks' totals first."""
+    from amsgrad_optimizer_step_gb300 import build
+    build.build()
+    world = 2
+    mp.start_processes(_optim_worker, args=(world, _free_port(), str(tmp_path)),
+                       nprocs=world, join=True, start_method="spawn")
+    res = [np.load(tmp_path / f"o{r}.npy") for r in range(world)]
+    for r in res:
+        local, shards, want_local, want_shards = r
+        assert np.array_equal(local, want_local)
+        assert np.array_equal(shards, want_shards)
+    # the sharded decision is the same on every rank; the local ones differ
+    assert np.array_equal(res[0][1], res[1][1])
+    assert not np.array_equal(res[0][0], res[1][0])
