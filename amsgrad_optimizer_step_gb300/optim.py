@@ -187,15 +187,30 @@ class FusedAdamW(torch.optim.Optimizer):
             raise ValueError("max_grad_norm must be positive or None")
         defaults = dict(lr=lr, betas=tuple(betas), eps=eps, weight_decay=weight_decay,
                         amsgrad=amsgrad, maximize=maximize)
+        self._buckets = None
         super().__init__(params, defaults)
         self.fused_step = True
         self.max_grad_norm = max_grad_norm
         self.hierarchical_stats = hierarchical_stats
         self.shard_group = shard_group
         self._buckets = [_Bucket(list(g["params"]), g["amsgrad"]) for g in self.param_groups]
+        self._row_len_fixed = row_len is not None
         self.row_len = row_len if row_len is not None else self._auto_row_len()
         self._stats = None
         self.last_report: dict = {}
+        self._bind_state()
+
+    def add_param_group(self, param_group: dict) -> None:
+        """As torch.optim: a group added after construction gets its own bucket (its
+        parameters become views into it) and starts at step 0."""
+        super().add_param_group(param_group)
+        if getattr(self, "_buckets", None) is None:  # called from the constructor
+            return
+        g = self.param_groups[-1]
+        self._buckets.append(_Bucket(list(g["params"]), g["amsgrad"]))
+        if not self._row_len_fixed:
+            self.row_len = self._auto_row_len()
+        self._stats = None
         self._bind_state()
 
     # ---- state -------------------------------------------------------------------

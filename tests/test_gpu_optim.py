@@ -363,6 +363,38 @@ def test_state_dict_round_trip_with_different_step_counts(dtype):
             == [float(st["step"]) for st in ref.state_dict()["state"].values()])
 
 
+def test_param_group_added_after_construction():
+    """A group added with add_param_group after two steps gets its own bucket and its
+    own step counts: both groups follow the oracle, and both share the global clip."""
+    first = _params(17, shapes=SHAPES[:3])
+    later = _params(18, shapes=SHAPES[3:])
+    opt = FusedAdamW(first, lr=1e-3, max_grad_norm=0.05)
+    lib = oracle.lib()
+    oo = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=1e-4, amsgrad=False,
+              maximize=False)
+    refs = [oracle.OracleAdamW(_host(p), oo, lib_=lib) for p in first + later]
+    for step in range(1, 6):
+        if step == 3:
+            opt.add_param_group({"params": later, "lr": 2e-3})
+            for r in refs[3:]:
+                r.opts = dict(oo, lr=2e-3)
+        params = first + (later if step >= 3 else [])
+        grads = _grads(17, step)[:len(params)]
+        _set_grads(params, grads)
+        opt.step()
+        allg = np.concatenate([g.numpy().reshape(-1) for g in grads])
+        s, c = lib.gradient_stats(allg, "f32")
+        _, norm, coef = lib.clip_decision(s, c, 0.05)
+        assert abs(opt.last_report["grad_norm"] - norm) <= 1e-5 * norm
+        for r, g in zip(refs, grads):
+            r.step(g.numpy().reshape(-1), "f32", clip_coef=coef)
+    torch.cuda.synchronize()
+    for p, r in zip(first + later, refs):
+        gate(_host(p), r.p, 1e-5, "p")
+    steps = [int(float(st["step"])) for st in opt.state_dict()["state"].values()]
+    assert steps == [5, 5, 5, 3, 3]
+
+
 def lib_bits(t, name):
     """A gradient as the oracle takes it: FP32 values, or BF16 bit patterns."""
     if name == "f32":
