@@ -70,6 +70,8 @@ class _Bucket:
         dev = params[0].device
         if dev.type != "cuda":
             raise ValueError("FusedAdamW needs CUDA parameters (there is no CPU path)")
+        if any(p.device != dev for p in params):
+            raise ValueError("a parameter group must hold parameters of one CUDA device")
         dtypes = {p.dtype for p in params}
         if len(dtypes) != 1 or not dtypes <= {torch.float32, torch.float16, torch.bfloat16}:
             raise TypeError("a parameter group must hold parameters of one float dtype "

@@ -395,6 +395,15 @@ def test_param_group_added_after_construction():
     assert steps == [5, 5, 5, 3, 3]
 
 
+def test_group_on_several_devices_or_on_the_cpu_is_rejected():
+    mixed = _params(19, shapes=SHAPES[:2])
+    mixed.append(torch.nn.Parameter(torch.zeros(3)))  # on the CPU
+    with pytest.raises(ValueError, match="one CUDA device"):
+        FusedAdamW(mixed)
+    with pytest.raises(ValueError, match="CUDA parameters"):
+        FusedAdamW([torch.nn.Parameter(torch.zeros(3))])
+
+
 def lib_bits(t, name):
     """A gradient as the oracle takes it: FP32 values, or BF16 bit patterns."""
     if name == "f32":
