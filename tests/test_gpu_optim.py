@@ -404,6 +404,31 @@ def test_group_on_several_devices_or_on_the_cpu_is_rejected():
         FusedAdamW([torch.nn.Parameter(torch.zeros(3))])
 
 
+def test_torch_lr_scheduler_drives_the_learning_rate():
+    """A torch LR scheduler changes param_groups[...]["lr"] between steps; every fused
+    step takes the group's current lr (each step vs the oracle with that lr)."""
+    params = _params(20)
+    opt = FusedAdamW(params, lr=1e-2, weight_decay=0.01)
+    sched = torch.optim.lr_scheduler.LambdaLR(opt, lambda k: 0.5 ** k)
+    lib = oracle.lib()
+    oo = dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=0.01, amsgrad=False,
+              maximize=False)
+    refs = [oracle.OracleAdamW(_host(p), oo, lib_=lib) for p in params]
+    for step in range(1, 5):
+        lr = opt.param_groups[0]["lr"]
+        assert lr == pytest.approx(1e-2 * 0.5 ** (step - 1))
+        grads = _grads(20, step)
+        _set_grads(params, grads)
+        opt.step()
+        sched.step()
+        for r, g in zip(refs, grads):
+            r.opts = dict(oo, lr=lr)
+            r.step(g.numpy().reshape(-1), "f32")
+    torch.cuda.synchronize()
+    for p, r in zip(params, refs):
+        gate(_host(p), r.p, 1e-5, "p")
+
+
 def lib_bits(t, name):
     """A gradient as the oracle takes it: FP32 values, or BF16 bit patterns."""
     if name == "f32":
@@ -426,3 +451,57 @@ def test_replaced_gradients_are_gathered_into_the_bucket():
     torch.cuda.synchronize()
     for p, q in zip(params, ref_params):
         assert torch.equal(p, q)
+
+
+def test_mixed_precision_decoder_full_size():
+    """FusedAdamW as the benchmark runs it, at full size: the 1,195,991,040-parameter
+    decoder in 199 BF16 tensors (FP32 masters and moments, BF16 gradients N(0, 1e-3)),
+    global clip 1.0, the update gated on the device with the BF16 copy written in the
+    same pass.  Three calls, the second with one +Inf (skipped).  Each call: the report
+    against the oracle's statistics over the whole gradient, the skip decision, and
+    40,000 sampled parameters plus every tensor's first and last element (master, m, v
+    along the trajectory; the BF16 copy bit for bit)."""
+    import dataclasses
+    from gpu_harness import check_model_copy, grad_bits_from_device
+    from synthetic.configs import CONFIG5, decoder_bucket_shapes
+    params = [torch.nn.Parameter(torch.zeros(shape, dtype=torch.bfloat16, device=DEV))
+              for _, shape in decoder_bucket_shapes()]
+    opt = FusedAdamW(params, lr=1e-3, weight_decay=1e-4, eps=1e-5, max_grad_norm=1.0)
+    b = opt._buckets[0]
+    n = b.n
+    assert n == 1_195_991_040 and b.offsets[-1] + params[-1].numel() == n
+    w = dataclasses.replace(CONFIG5.scaled(n), calls=3, inf_call=2)
+    w.fill_params_device(b.master)
+    ends = [o for o in b.offsets] + [o + p.numel() - 1 for o, p in zip(b.offsets, params)]
+    rng = np.random.default_rng(21)
+    idx = np.unique(np.concatenate([rng.integers(0, n, 40_000), ends, [w.inf_index()]]))
+    idx_t = torch.as_tensor(idx, device=DEV)
+    lib = oracle.lib()
+    traj = oracle.OracleAdamW(w.params_host(idx), w.options(), lib_=lib)
+    assert np.array_equal(b.master[idx_t].cpu().numpy(), w.params_host(idx))
+    for call in range(1, 4):
+        w.fill_grad_device(call, b.grad)
+        gh = w.grad_host(call, idx)
+        assert np.array_equal(grad_bits_from_device(b.grad[idx_t]), gh)
+        s_or, c_or = lib.gradient_stats(grad_bits_from_device(b.grad), "bf16", 1.0)
+        skip_or, norm_or, coef_or = lib.clip_decision(s_or, c_or, 1.0)
+        before = b.master[idx_t].cpu().numpy()
+        opt.step()
+        torch.cuda.synchronize()
+        rep = opt.last_report
+        assert rep["skipped"] == skip_or == (call == 2)
+        assert rep["nonfinite"] == c_or
+        if not skip_or:
+            assert abs(rep["grad_norm"] - norm_or) <= 1e-5 * norm_or
+            assert coef_or < 1.0
+        traj.step(gh, "bf16", 1.0, skip_update=skip_or, clip_coef=coef_or)
+        master = b.master[idx_t].cpu().numpy()
+        if skip_or:
+            assert np.array_equal(master, before)
+            continue
+        gate(master, traj.p, 1e-5, f"call {call} master")
+        gate(b.m[idx_t].cpu().numpy(), traj.state.m, 1e-5, f"call {call} m")
+        gate(b.v[idx_t].cpu().numpy(), traj.state.v, 1e-5, f"call {call} v")
+        check_model_copy(grad_bits_from_device(b.model[idx_t]), master, traj.p.astype(np.float32),
+                         "bf16", lib, f"call {call} model copy")
+    assert set(b.steps) == {2} and traj.state.t == 2
