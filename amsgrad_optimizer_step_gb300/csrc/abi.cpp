@@ -101,7 +101,6 @@ fa_status check_control(const fa_step_control &c) {
 bool valid_dtype(fa_dtype d) { return d == FA_F32 || d == FA_F16 || d == FA_BF16; }
 size_t dtype_bytes(fa_dtype d) { return d == FA_F32 ? 4 : 2; }
 
-// Device of the stream (current device for the legacy default stream).
 // Host-side trace ranges (NVTX): a profiler attached to the process shows each
 // entry point's span around the kernels it enqueues; without one they cost nothing.
 struct TraceRange {
@@ -111,6 +110,8 @@ struct TraceRange {
     TraceRange &operator=(const TraceRange &) = delete;
 };
 
+// The current device, checked against the stream's device (the legacy default
+// stream belongs to the current device).
 fa_status stream_device(void *stream, int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess) {
         cudaGetLastError();
