@@ -240,7 +240,7 @@ fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt,
     return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// Validates the in-place argument set; fills the ranges for alias checks.
+// Validates the in-place argument set: device pointers, alignment, and no overlap.
 fa_status check_inplace(int64_t n, float *p, const void *g, fa_dtype gdt, float *m, float *v,
                         float *vmax, const fa_options *o, int dev) {
     fa_status st;
