@@ -28,7 +28,8 @@ __all__ = [
     "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",
     "fa_read_report", "fa_clip_decision", "fa_stats_chunk_scratch",
     "fa_merge_gradient_stats_chunks", "fa_bucket_step_segment_scaled",
-    "fa_bucket_step_clipped_per_segment", "segment_rows",
+    "fa_bucket_step_clipped_per_segment", "fa_bucket_step_per_segment_gated",
+    "fa_bucket_step_clipped_per_segment_gated", "segment_rows",
     "fa_clip_decide", "fa_bucket_step_clipped", "fa_bucket_step_gated",
     "fa_bucket_step_writeback_gated",
     "fa_bucket_step_clipped_gated", "options", "control", "stats_buffer",
@@ -481,6 +482,54 @@ def fa_bucket_step_clipped_per_segment(seg_offsets, p, g, m, v, vmax, t: int, op
         rows_buf.shape[0], _ptr(scratch), scratch.numel(), _ptr(seg_reports), norms, coefs,
         ctypes.byref(rep), _stream(stream)))
     return tt.value, rep, list(norms), list(coefs)
+
+
+def fa_bucket_step_per_segment_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                                     ctl: FaStepControl, seg_reports: torch.Tensor,
+                                     max_grad_norm: float, stream=None) -> None:
+    """Enqueues the per-segment update decided on the device from ``seg_reports``; the
+    caller reads the reports and advances t unless one counts a non-finite value."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _stats_tensor("seg_reports", seg_reports)
+    seg, nseg = _segments(seg_offsets)
+    if seg_reports.shape[0] < nseg:
+        raise ValueError(f"seg_reports: {seg_reports.shape[0]} records for {nseg} segments")
+    check("fa_bucket_step_per_segment_gated", _L().fa_bucket_step_per_segment_gated(
+        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
+        ctypes.byref(opts), ctl, _ptr(seg_reports), max_grad_norm, _stream(stream)))
+
+
+def fa_bucket_step_clipped_per_segment_gated(seg_offsets, p, g, m, v, vmax, t: int,
+                                             opts: FaOptions, ctl: FaStepControl,
+                                             max_grad_norm: float, row_len: int,
+                                             rows_buf: torch.Tensor, scratch: torch.Tensor,
+                                             seg_reports: torch.Tensor, stream=None) -> None:
+    """Enqueues analysis, per-segment merges and the device-decided per-segment update;
+    nothing is read back.  The caller reads ``seg_reports`` and advances t."""
+    n = p.numel()
+    _dense("p", p, n, (torch.float32,))
+    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
+    _dense("m", m, n, (torch.float32,), p.device)
+    _dense("v", v, n, (torch.float32,), p.device)
+    if vmax is not None:
+        _dense("vmax", vmax, n, (torch.float32,), p.device)
+    _stats_tensor("rows_buf", rows_buf)
+    _stats_tensor("seg_reports", seg_reports)
+    seg, nseg = _segments(seg_offsets)
+    if seg_reports.shape[0] < nseg:
+        raise ValueError(f"seg_reports: {seg_reports.shape[0]} records for {nseg} segments")
+    check("fa_bucket_step_clipped_per_segment_gated",
+          _L().fa_bucket_step_clipped_per_segment_gated(
+              seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v),
+              _ptr(vmax), t, ctypes.byref(opts), ctl, max_grad_norm, row_len, _ptr(rows_buf),
+              rows_buf.shape[0], _ptr(scratch), scratch.numel(), _ptr(seg_reports),
+              _stream(stream)))
 
 
 def fa_read_report(report: torch.Tensor, stream=None) -> FaStats:

@@ -277,6 +277,67 @@ fa_status check_segments(const int64_t *seg, int32_t nseg, int64_t n) {
     return FA_OK;
 }
 
+// The per-segment update, one launch per kMaxSegPerLaunch segments (arguments
+// validated).  Each segment's multiplier comes from seg_grad_mult (decided on the
+// host) or, with ``reports`` (device, one record per segment), is decided in the
+// kernels from the records: any non-finite count skips every launch, and segment
+// k's clip coefficient is the host formula's with max_grad_norm.
+fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float *p,
+                                 const void *g, fa_dtype gdt, float *m, float *v, float *vmax,
+                                 uint64_t t_new, const fa_options *options, fa_step_control ctl,
+                                 const double *seg_grad_mult, const fa_stats *reports,
+                                 double max_grad_norm, void *stream) {
+    Coef c;
+    fa_status st = make_coef(options, t_new, ctl.gradient_scale, 1.0, &c);
+    if (st != FA_OK) return st;
+    const bool first = t_new == 1;
+    const bool ams = options->amsgrad != 0;
+    const double sign = options->maximize ? -1.0 : 1.0;
+    const size_t gb = dtype_bytes(gdt);
+    for (int32_t k0 = 0; k0 < nseg; k0 += fa::kMaxSegPerLaunch) {
+        const int32_t cnt = nseg - k0 < fa::kMaxSegPerLaunch ? nseg - k0 : fa::kMaxSegPerLaunch;
+        const int64_t e0 = seg_offsets[k0], e1 = seg_offsets[k0 + cnt];
+        if (e1 == e0) continue;
+        fa::SegScaleArgs sa;
+        fa::UpdateArgs &a = sa.a;
+        a.p_in = p + e0;
+        a.m_in = first ? nullptr : m + e0;
+        a.v_in = first ? nullptr : v + e0;
+        a.vmax_in = (first || !ams) ? nullptr : vmax + e0;
+        a.g = static_cast<const char *>(g) + e0 * gb;
+        a.p_out = p + e0;
+        a.m_out = m + e0;
+        a.v_out = v + e0;
+        a.vmax_out = ams ? vmax + e0 : nullptr;
+        a.p_model = nullptr;
+        a.extra_tx = 0;
+        a.gate = nullptr;
+        a.gate_scale = ctl.gradient_scale;
+        a.gate_max_norm = max_grad_norm;
+        a.gate_sign = sign;
+        a.n = e1 - e0;
+        const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g};
+        const size_t es[] = {4, 4, 4, 4, gb};
+        const int64_t head = vector_head(ptrs, es, 5, a.n);
+        const bool vec = head >= 0;
+        a.head = vec ? head : 0;
+        a.nvec = vec ? (a.n - a.head) / 8 : 0;
+        sa.nseg = cnt;
+        for (int32_t j = 0; j <= cnt; ++j) sa.seg_start[j] = seg_offsets[k0 + j] - e0;
+        for (int32_t j = 0; j < cnt; ++j)
+            sa.gmul[j] = seg_grad_mult
+                             ? static_cast<float>(sign * seg_grad_mult[k0 + j] / ctl.gradient_scale)
+                             : 0.0f;
+        sa.reports = reports;
+        sa.nreports = reports ? nseg : 0;
+        sa.k0 = k0;
+        if (fa::launch_update_segment_scaled(sa, c, gdt, ams, first, vec,
+                                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -980,46 +1041,9 @@ fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg
     int dev = 0;
     if ((st = stream_device(stream, &dev)) != FA_OK) return st;
     if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    Coef c;
-    if ((st = make_coef(options, *t + 1, ctl.gradient_scale, 1.0, &c)) != FA_OK) return st;
-    const bool first = *t == 0;
-    const bool ams = options->amsgrad != 0;
-    const size_t gb = dtype_bytes(gdt);
-    for (int32_t k0 = 0; k0 < nseg; k0 += fa::kMaxSegPerLaunch) {
-        const int32_t cnt = nseg - k0 < fa::kMaxSegPerLaunch ? nseg - k0 : fa::kMaxSegPerLaunch;
-        const int64_t e0 = seg_offsets[k0], e1 = seg_offsets[k0 + cnt];
-        if (e1 == e0) continue;
-        fa::SegScaleArgs sa;
-        fa::UpdateArgs &a = sa.a;
-        a.p_in = p + e0;
-        a.m_in = first ? nullptr : m + e0;
-        a.v_in = first ? nullptr : v + e0;
-        a.vmax_in = (first || !ams) ? nullptr : vmax + e0;
-        a.g = static_cast<const char *>(g) + e0 * gb;
-        a.p_out = p + e0;
-        a.m_out = m + e0;
-        a.v_out = v + e0;
-        a.vmax_out = ams ? vmax + e0 : nullptr;
-        a.p_model = nullptr;
-        a.extra_tx = 0;
-        a.gate = nullptr;
-        a.gate_scale = a.gate_max_norm = a.gate_sign = 0.0;
-        a.n = e1 - e0;
-        const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g};
-        const size_t es[] = {4, 4, 4, 4, gb};
-        const int64_t head = vector_head(ptrs, es, 5, a.n);
-        const bool vec = head >= 0;
-        a.head = vec ? head : 0;
-        a.nvec = vec ? (a.n - a.head) / 8 : 0;
-        sa.nseg = cnt;
-        for (int32_t j = 0; j <= cnt; ++j) sa.seg_start[j] = seg_offsets[k0 + j] - e0;
-        for (int32_t j = 0; j < cnt; ++j)
-            sa.gmul[j] = static_cast<float>((options->maximize ? -1.0 : 1.0) *
-                                            seg_grad_mult[k0 + j] / ctl.gradient_scale);
-        if (fa::launch_update_segment_scaled(sa, c, gdt, ams, first, vec,
-                                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
-            return FA_ERR_CUDA;
-    }
+    if ((st = enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, *t + 1, options,
+                                     ctl, seg_grad_mult, nullptr, 0.0, stream)) != FA_OK)
+        return st;
     *t += 1;
     *updated = 1;
     return FA_OK;
@@ -1099,6 +1123,73 @@ fa_status fa_bucket_step_clipped_per_segment(
     rep.updated = updated;
     *out = rep;
     return FA_OK;
+}
+
+fa_status fa_bucket_step_per_segment_gated(const int64_t *seg_offsets, int32_t nseg,
+                                           int64_t n_total, float *p, const void *g,
+                                           fa_dtype gdt, float *m, float *v, float *vmax,
+                                           uint64_t t, const fa_options *options,
+                                           fa_step_control ctl, const fa_stats *seg_reports,
+                                           double max_grad_norm, void *stream) {
+    TraceRange trace("fa_bucket_step_per_segment_gated");
+    fa_status st;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    if (nseg < 1) return FA_ERR_SEGMENTS;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (n_total == 0 || ctl.skip_update) return FA_OK;
+    if (t == UINT64_MAX) return FA_ERR_OPTION;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(seg_reports, dev, 4)) != FA_OK) return st;
+    const size_t b = static_cast<size_t>(n_total) * 4;
+    const Range rep{seg_reports, static_cast<size_t>(nseg) * 12};
+    const Range others[] = {{p, b}, {m, b}, {v, b}, {options->amsgrad ? vmax : nullptr, b}};
+    for (const Range &r : others)
+        if (overlap(rep, r)) return FA_ERR_ALIAS;
+    return enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, t + 1, options, ctl,
+                                  nullptr, seg_reports, max_grad_norm, stream);
+}
+
+fa_status fa_bucket_step_clipped_per_segment_gated(
+    const int64_t *seg_offsets, int32_t nseg, int64_t n_total, float *p, const void *g,
+    fa_dtype gdt, float *m, float *v, float *vmax, uint64_t t, const fa_options *options,
+    fa_step_control ctl, double max_grad_norm, int32_t row_len, fa_stats *rows_buf,
+    int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
+    void *stream) {
+    TraceRange trace("fa_bucket_step_clipped_per_segment_gated");
+    fa_status st;
+    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
+    if (row_len <= 0) return FA_ERR_SIZE;
+    if (nseg < 1) return FA_ERR_SEGMENTS;
+    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
+    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
+    if (t == UINT64_MAX) return FA_ERR_OPTION;
+    if (n_total == 0 || ctl.skip_update) return FA_OK;
+    std::vector<int64_t> chunk_rows(static_cast<size_t>(nseg) + 1, 0);
+    for (int32_t k = 0; k < nseg; ++k)
+        chunk_rows[k + 1] = chunk_rows[k] + (seg_offsets[k + 1] - seg_offsets[k] + row_len - 1) / row_len;
+    int64_t need = 0;
+    if ((st = fa_stats_chunk_scratch(chunk_rows.data(), nseg, &need)) != FA_OK) return st;
+    if (scratch_elements < need || rows_capacity < chunk_rows[nseg]) return FA_ERR_SIZE;
+    int dev = 0;
+    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
+    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
+    if ((st = check_device_ptr(seg_reports, dev, 4)) != FA_OK) return st;
+    const size_t b = static_cast<size_t>(n_total) * 4;
+    const Range rep{seg_reports, static_cast<size_t>(nseg) * 12};
+    const Range others[] = {{p, b}, {m, b}, {v, b}, {options->amsgrad ? vmax : nullptr, b}};
+    for (const Range &r : others)
+        if (overlap(rep, r)) return FA_ERR_ALIAS;
+    if ((st = fa_analyze_gradient(g, gdt, n_total, row_len, seg_offsets, nseg, rows_buf,
+                                  rows_capacity, stream)) != FA_OK)
+        return st;
+    if ((st = fa_merge_gradient_stats_chunks(rows_buf, chunk_rows.data(), nseg, scratch,
+                                             scratch_elements, seg_reports, stream)) != FA_OK)
+        return st;
+    return enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, t + 1, options, ctl,
+                                  nullptr, seg_reports, max_grad_norm, stream);
 }
 
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream) {

@@ -170,6 +170,13 @@ struct SegScaleArgs {
     int32_t nseg;
     int64_t seg_start[kMaxSegPerLaunch + 1];  // relative to the launch's first element
     float gmul[kMaxSegPerLaunch];             // (maximize ? -1 : 1) * multiplier / scale
+    // Device-side decision (reports == nullptr: gmul above is used).  reports holds
+    // one 12-byte record per segment of the whole bucket: any non-finite count skips
+    // the launch, and segment j of this launch takes the clip multiplier of record
+    // k0 + j, computed like the host's from a.gate_scale, a.gate_max_norm, a.gate_sign.
+    const fa_stats *reports;
+    int64_t nreports;
+    int32_t k0;
 };
 cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, fa_dtype gdt,
                                          bool amsgrad, bool first, bool vector_ok,

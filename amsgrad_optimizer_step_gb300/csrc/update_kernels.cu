@@ -360,11 +360,38 @@ __device__ __forceinline__ int find_seg(const SegScaleArgs &s, int64_t e) {
 }
 
 template <int GT, bool AMS, bool FIRST>
-__device__ __forceinline__ void scalar_element_seg(const SegScaleArgs &s, const Coef &c,
-                                                   int64_t i) {
+__device__ __forceinline__ void scalar_element_seg(const SegScaleArgs &s, const float *gm,
+                                                   const Coef &c, int64_t i) {
     Coef cc = c;
-    cc.gmul = s.gmul[find_seg(s, i)];
+    cc.gmul = gm[find_seg(s, i)];
     scalar_element<GT, AMS, FIRST, kNoModel>(s.a, cc, i);
+}
+
+// This launch's per-segment multipliers into gm[0, s.nseg), from the kernel
+// parameters or, with s.reports, decided on the device: false (skip the launch) when
+// any segment of the bucket counts a non-finite value, else each segment's clip
+// multiplier with the host's FP64 operations in the host's order (norm =
+// sqrt(sum) / scale; coef = max_norm / norm above max_norm; sign * coef / scale), so
+// every multiplier is bit-identical to the host-decided step's.  Every thread of the
+// CTA calls it (the skip is a CTA-wide vote); gm is read after the next barrier.
+__device__ __forceinline__ bool segment_multipliers(const SegScaleArgs &s, float *gm) {
+    if (!s.reports) {
+        for (int j = threadIdx.x; j < s.nseg; j += blockDim.x) gm[j] = s.gmul[j];
+        return true;
+    }
+    bool bad = false;
+    for (int64_t j = threadIdx.x; j < s.nreports; j += blockDim.x)
+        bad |= s.reports[j].nonfinite != 0;
+    if (__syncthreads_or(bad)) return false;
+    for (int j = threadIdx.x; j < s.nseg; j += blockDim.x) {
+        const fa_stats r = s.reports[s.k0 + j];
+        const double sum = static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
+        const double norm = sqrt(sum) / s.a.gate_scale;
+        double coef = 1.0;
+        if (s.a.gate_max_norm > 0 && norm > s.a.gate_max_norm) coef = s.a.gate_max_norm / norm;
+        gm[j] = static_cast<float>(s.a.gate_sign * coef / s.a.gate_scale);
+    }
+    return true;
 }
 
 #if FA_UPDATE_TMA
@@ -518,14 +545,15 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
         ++issued[s];
     };
 
+    if (SEG) {
+        // a launch skipped by the device-side decision returns before any copy
+        if (!segment_multipliers(sa, s_gmul)) return;
+        for (int j = tid; j <= sa.nseg; j += kTmaThreads) s_seg[j] = sa.seg_start[j];
+    }
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(&bars[s]);
         fence_mbar_init();
-    }
-    if (SEG) {
-        for (int j = tid; j <= sa.nseg; j += kTmaThreads) s_seg[j] = sa.seg_start[j];
-        for (int j = tid; j < sa.nseg; j += kTmaThreads) s_gmul[j] = sa.gmul[j];
     }
     __syncthreads();
     if (tid == 0) {
@@ -547,7 +575,7 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
     float seg_gmul = 0.f;
     if (SEG) {
         if (sa.nseg > 1) next_start = sa.seg_start[1];
-        seg_gmul = sa.gmul[0];
+        seg_gmul = s_gmul[0];
     }
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
         const int s = static_cast<int>(k % S);
@@ -699,8 +727,10 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
     const int64_t gsz = static_cast<int64_t>(gridDim.x) * kTmaThreads;
     const int64_t tail0 = a.head + ntiles * L::kTile;
     if (SEG) {
-        for (int64_t i = gtid; i < a.head; i += gsz) scalar_element_seg<GT, AMS, FIRST>(sa, c, i);
-        for (int64_t i = tail0 + gtid; i < a.n; i += gsz) scalar_element_seg<GT, AMS, FIRST>(sa, c, i);
+        for (int64_t i = gtid; i < a.head; i += gsz)
+            scalar_element_seg<GT, AMS, FIRST>(sa, s_gmul, c, i);
+        for (int64_t i = tail0 + gtid; i < a.n; i += gsz)
+            scalar_element_seg<GT, AMS, FIRST>(sa, s_gmul, c, i);
     } else {
         for (int64_t i = gtid; i < a.head; i += gsz) scalar_element<GT, AMS, FIRST, MD>(a, c, i);
         for (int64_t i = tail0 + gtid; i < a.n; i += gsz) scalar_element<GT, AMS, FIRST, MD>(a, c, i);
@@ -733,8 +763,9 @@ cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vecto
     }
     const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
     *launched = true;
-    // gated: scheduled while the merge before it runs; the kernel waits for it
-    if (s.a.gate)
+    // gated (one report, or one per segment): scheduled while the merge before it
+    // runs; the kernel waits for it
+    if (s.a.gate || s.reports)
         return launch_dependent(kern, dim3(grid), dim3(kTmaThreads), kSmem, stream, s, c,
                                 ntiles);
     kern<<<grid, kTmaThreads, kSmem, stream>>>(s, c, ntiles);
@@ -745,6 +776,10 @@ cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vecto
 template <int GT, bool AMS, bool FIRST>
 __global__ void __launch_bounds__(kThreads)
 update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
+    __shared__ float gm[kMaxSegPerLaunch];
+    fa_grid_dependency_wait();
+    if (!segment_multipliers(s, gm)) return;
+    __syncthreads();
     const UpdateArgs &a = s.a;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -763,13 +798,13 @@ update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
         while (k + 1 < s.nseg && s.seg_start[k + 1] <= e) ++k;
         Coef cc = c;
         if (e + kVec <= s.seg_start[k + 1]) {
-            cc.gmul = s.gmul[k];
+            cc.gmul = gm[k];
 #pragma unroll
             for (int q = 0; q < kVec; ++q) adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
         } else {
 #pragma unroll
             for (int q = 0; q < kVec; ++q) {
-                cc.gmul = s.gmul[find_seg_in(s, e + q, k, s.nseg - 1)];
+                cc.gmul = gm[find_seg_in(s, e + q, k, s.nseg - 1)];
                 adamw_element<AMS, FIRST>(cc, x[q], p[q], m[q], v[q], vm[q]);
             }
         }
@@ -778,18 +813,22 @@ update_segscaled_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
         store8f(a.v_out, e, v);
         if (AMS) store8f(a.vmax_out, e, vm);
     }
-    if (tid < a.head) scalar_element_seg<GT, AMS, FIRST>(s, c, tid);
+    if (tid < a.head) scalar_element_seg<GT, AMS, FIRST>(s, gm, c, tid);
     const int64_t tail0 = a.head + a.nvec * kVec;
-    if (tid < a.n - tail0) scalar_element_seg<GT, AMS, FIRST>(s, c, tail0 + tid);
+    if (tid < a.n - tail0) scalar_element_seg<GT, AMS, FIRST>(s, gm, c, tail0 + tid);
 }
 
 template <int GT, bool AMS, bool FIRST>
 __global__ void __launch_bounds__(kThreads)
 update_segscaled_scalar_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
+    __shared__ float gm[kMaxSegPerLaunch];
+    fa_grid_dependency_wait();
+    if (!segment_multipliers(s, gm)) return;
+    __syncthreads();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < s.a.n;
          i += stride)
-        scalar_element_seg<GT, AMS, FIRST>(s, c, i);
+        scalar_element_seg<GT, AMS, FIRST>(s, gm, c, i);
 }
 
 template <int GT, bool AMS, bool FIRST>
@@ -802,16 +841,22 @@ cudaError_t launch_seg_typed(const SegScaleArgs &s, const Coef &c, bool vec, cud
     err = launch_tma_if_large<GT, AMS, FIRST, kNoModel, true>(s, c, vec, dev, st, &launched);
     if (err != cudaSuccess || launched) return err;
 #endif
+    // decided on the device: scheduled while the merge before it runs
+    const bool dependent = s.reports != nullptr;
     if (vec) {
         auto kern = update_segscaled_kernel<GT, AMS, FIRST>;
         int64_t need = (s.a.nvec + kThreads - 1) / kThreads;
         if (need == 0 && s.a.n > 0) need = 1;
         const int grid = persistent_grid(kern, need, dev);
-        if (grid > 0) kern<<<grid, kThreads, 0, st>>>(s, c);
+        if (grid == 0) return cudaSuccess;
+        if (dependent) return launch_dependent(kern, dim3(grid), dim3(kThreads), 0, st, s, c);
+        kern<<<grid, kThreads, 0, st>>>(s, c);
     } else {
         auto kern = update_segscaled_scalar_kernel<GT, AMS, FIRST>;
         const int grid = persistent_grid(kern, (s.a.n + kThreads - 1) / kThreads, dev);
-        if (grid > 0) kern<<<grid, kThreads, 0, st>>>(s, c);
+        if (grid == 0) return cudaSuccess;
+        if (dependent) return launch_dependent(kern, dim3(grid), dim3(kThreads), 0, st, s, c);
+        kern<<<grid, kThreads, 0, st>>>(s, c);
     }
     return cudaGetLastError();
 }
@@ -842,6 +887,9 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         SegScaleArgs s;
         s.a = a;
         s.nseg = 0;
+        s.reports = nullptr;
+        s.nreports = 0;
+        s.k0 = 0;
         bool launched = false;
         err = launch_tma_if_large<GT, AMS, FIRST, MD, false>(s, c, vector_ok, dev, stream, &launched);
         if (err != cudaSuccess || launched) return err;
@@ -910,6 +958,9 @@ cudaError_t launch_pipeline_selftest(const UpdateArgs &a, const Coef &c, fa_dtyp
     SegScaleArgs s;
     s.a = a;
     s.nseg = 0;
+    s.reports = nullptr;
+    s.nreports = 0;
+    s.k0 = 0;
     switch (gdt) {
         case FA_F32:
             return launch_tma_if_large<FA_F32, false, false, kNoModel, false>(s, c, true, dev,

@@ -442,6 +442,44 @@ fa_status fa_bucket_step_clipped_per_segment(
     int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
     double *seg_norms, double *seg_coefs, fa_step_report *out, void *stream);
 
+/*
+ * fa_bucket_step_segment_scaled with the multipliers decided on the device:
+ * seg_reports (device, nseg records, as written by fa_merge_gradient_stats_chunks
+ * earlier on the same stream) are read by the update kernels themselves.  Any
+ * non-finite count skips the whole update; otherwise segment k's gradient is
+ * multiplied by the clip coefficient that fa_clip_decision computes from record k
+ * on the host (max_grad_norm <= 0: no clip), with the same FP64 operations in the
+ * same order, so the results are bit-identical to reading the reports back and
+ * calling fa_bucket_step_segment_scaled with those coefficients.  ``t`` is the
+ * completed step count and is not changed: the caller reads the reports and
+ * advances its count unless one counts a non-finite value.  Nothing is launched
+ * for n_total == 0 or ctl.skip_update.
+ */
+fa_status fa_bucket_step_per_segment_gated(const int64_t *seg_offsets, int32_t nseg,
+                                           int64_t n_total, float *p, const void *g,
+                                           fa_dtype gdt, float *m, float *v, float *vmax,
+                                           uint64_t t, const fa_options *options,
+                                           fa_step_control ctl, const fa_stats *seg_reports,
+                                           double max_grad_norm, void *stream);
+
+/*
+ * fa_bucket_step_clipped_per_segment with the decision on the device: the
+ * segment-aligned analysis, the per-segment merges into seg_reports and the
+ * update gated by fa_bucket_step_per_segment_gated are enqueued back to back;
+ * nothing is read back and the call does not wait.  Results are bit-identical to
+ * fa_bucket_step_clipped_per_segment.  ``t`` is the completed step count and is
+ * not changed (the caller reads seg_reports after the stream reaches them and
+ * advances its count unless one counts a non-finite value).  For n_total == 0
+ * or ctl.skip_update nothing is enqueued and seg_reports is not written.  Other
+ * arguments as fa_bucket_step_clipped_per_segment.
+ */
+fa_status fa_bucket_step_clipped_per_segment_gated(
+    const int64_t *seg_offsets, int32_t nseg, int64_t n_total, float *p, const void *g,
+    fa_dtype gdt, float *m, float *v, float *vmax, uint64_t t, const fa_options *options,
+    fa_step_control ctl, double max_grad_norm, int32_t row_len, fa_stats *rows_buf,
+    int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
+    void *stream);
+
 /* Copies the 12-byte device report to host memory and waits for the stream
  * ([TR-zh]: the report is read back before any update).  Synchronises. */
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream);

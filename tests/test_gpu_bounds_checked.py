@@ -64,6 +64,9 @@ CASES = [
         "bf16", 100, lib)),
     ("per-segment multipliers, shared-memory pipeline",
      lambda lib: S.test_segment_multipliers_mixed_sizes_vs_oracle("f16", False, lib)),
+    ("per-segment decision on the device",
+     lambda lib: [S.test_per_segment_gated_equals_host_decision_bitwise(*k) for k in (
+         ("mixed", "f16", False), ("many", "f32", False), ("offset", "bf16", False))]),
 ]
 
 

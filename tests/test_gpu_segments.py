@@ -217,6 +217,66 @@ def test_per_segment_clipped_step_vs_oracle(oracle_lib):
         gate(ph[a:b], refs[k].p, 1e-5, f"segment {k}")
 
 
+def _gated_layout(kind):
+    if kind == "mixed":  # steady steps on the shared-memory pipeline
+        rng = np.random.default_rng(41)
+        sizes = rng.integers(0, 3000, 230)
+        sizes[::11] = rng.integers(150_000, 450_000, len(sizes[::11]))
+        sizes[3::17] = 0
+        return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    if kind == "many":  # 300 segments: two launches, the skip vote over all of them
+        return _segments(42, 300, 4000, empty_every=7)
+    return _scaled_decoder_offsets()  # "small" and "offset": register and scalar kernels
+
+
+@pytest.mark.parametrize("kind,gdt,maximize", [("mixed", "f16", False), ("mixed", "bf16", True),
+                                               ("many", "f32", False), ("small", "f16", False),
+                                               ("offset", "bf16", False)])
+def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize):
+    """The per-segment step decided on the device (every segment's coefficient and the
+    skip taken in the update kernels from the device-resident reports) against the
+    host-decided per-segment step, over four calls with a +Inf in the third: reports,
+    parameters and every moment bit for bit, the +Inf call skipped by both."""
+    seg = _gated_layout(kind)
+    n = int(seg[-1])
+    w = dataclasses.replace(CONFIG4, segments=None, calls=4, inf_call=3, grad_sigma=1e-2,
+                            grad_dtype=gdt, maximize=maximize).scaled(n)
+    o = fa.options(**w.options())
+    off = 1 if kind == "offset" else 0  # state views 4 bytes off the gradient's alignment
+
+    def state():
+        full = [torch.zeros(n + off, device=DEV) for _ in range(4)]
+        w.fill_params_device(full[0][off:])
+        return full, [x[off:] for x in full]
+
+    _, (pa, ma, va, vma) = state()
+    _, (pb, mb, vb, vmb) = state()
+    g = torch.empty(n, dtype=TORCH_DT[gdt], device=DEV)
+    row_len = 256
+    crow = fa.segment_rows(list(seg), row_len)
+    bufs = [(fa.stats_buffer(crow[-1], DEV), torch.empty(fa.fa_stats_chunk_scratch(crow), device=DEV),
+             fa.stats_buffer(len(seg) - 1, DEV)) for _ in range(2)]
+    max_norm = 0.05
+    ta = tb = 0
+    for call in range(1, 5):
+        w.fill_grad_device(call, g)
+        ta, rep, _, coefs = fa.fa_bucket_step_clipped_per_segment(
+            list(seg), pa, g, ma, va, vma, ta, o, fa.control(), max_norm, row_len, *bufs[0])
+        fa.fa_bucket_step_clipped_per_segment_gated(
+            list(seg), pb, g, mb, vb, vmb, tb, o, fa.control(), max_norm, row_len, *bufs[1])
+        rb = bufs[1][2].cpu()
+        if not bool((rb[:, 1] != 0).any()):
+            tb += 1
+        torch.cuda.synchronize()
+        assert torch.equal(bufs[0][2], bufs[1][2]), f"call {call}: reports differ"
+        assert bool(rep.skipped_nonfinite) == (call == 3) and ta == tb
+        if call != 3:
+            assert min(coefs) < 1.0
+        for x, y, name in ((pa, pb, "p"), (ma, mb, "m"), (va, vb, "v"), (vma, vmb, "vmax")):
+            assert torch.equal(x, y), f"call {call}: {name} differs"
+    assert ta == tb == 3
+
+
 def test_per_segment_clipped_full_size_sampled(oracle_lib):
     """The per-parameter clipped step on the whole 1,195,991,040-parameter decoder bucket
     (199 segments, FP16 gradients, AMSGrad, rows of 512), in the launch configuration the
