@@ -440,14 +440,56 @@ __device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int
     }
 }
 
-// One CTA per group of kFanIn input records.
+// One warp per group of kFanIn input records, eight groups per CTA, so that the
+// 4096 groups of the largest plan run in a single wave (one CTA per group took
+// three and a half).  Lane l adds records l, l + 32, ... of its group as
+// double-float values (16 records' loads issued together), then the warp's
+// shuffle tree; lane 0 writes the group's (hi, lo) record.
 __global__ void __launch_bounds__(kThreads)
 merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
     fa_grid_dependency_wait();  // (launched early: the records are not ready before this)
     fa_allow_dependents();
-    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kFanIn;
-    const int64_t g1 = g0 + kFanIn < count ? g0 + kFanIn : count;
-    block_merge(in, g0, g1, count, out + blockIdx.x);
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kBatch = 16;
+    const int lane = threadIdx.x & 31;
+    const int64_t group = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int64_t lo = group * kFanIn;
+    if (lo >= count) return;  // the whole warp
+    int64_t hi = lo + kFanIn < count ? lo + kFanIn : count;
+    if (!fa_in_bounds(lo, hi - lo, count)) hi = lo;  // (bounds-checked build only)
+    float sh = 0.f, sl = 0.f;
+    unsigned long long c = 0;
+    for (int64_t base = lo + lane; base < hi; base += 32 * kBatch) {
+        fa_stats r[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int64_t i = base + static_cast<int64_t>(u) * 32;
+            if (i < hi) r[u] = in[i];
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int64_t i = base + static_cast<int64_t>(u) * 32;
+            if (i < hi) {
+                df_add(sh, sl, r[u].sum_sq, r[u].sum_sq_lo);
+                c += r[u].nonfinite;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
+        df_add(sh, sl, oh, ol);
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    if (lane == 0) {
+        const double ts = static_cast<double>(sh) + static_cast<double>(sl);
+        fa_stats rec;
+        rec.sum_sq = static_cast<float>(ts);
+        rec.sum_sq_lo = static_cast<float>(ts - static_cast<double>(rec.sum_sq));
+        rec.nonfinite = c > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(c);
+        out[group] = rec;
+    }
 }
 
 // Per-chunk merge, level A: one CTA per group of at most kFanIn records of one
@@ -568,7 +610,8 @@ cudaError_t launch_merge_chunks(const ChunkMergeArgs &a, cudaStream_t stream) {
 }
 
 cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream) {
-    const int64_t grid = (count + kFanIn - 1) / kFanIn;
+    const int64_t groups = (count + kFanIn - 1) / kFanIn;
+    const int64_t grid = (groups + kThreads / 32 - 1) / (kThreads / 32);
     if (grid <= 0) return cudaSuccess;
     // starts early and waits for its input in the kernel
     return launch_dependent(merge_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
