@@ -381,82 +381,17 @@ __device__ __forceinline__ void df_add(float &h, float &l, float bh, float bl) {
     two_sum(s, e, h, l);
 }
 
-// One CTA reduces records [lo, hi) into *out.  Sums travel as double-float
-// pairs (an FP32 value and its FP32 residual, combined with error-free
-// TwoSum) through the per-thread loop and the warp shuffles, which keeps
-// every operation on the FP32 units (GB300's FP64 rate is low); only the
-// per-warp partials are added in FP64.  The total leaves as an FP32 (hi, lo)
-// pair.
-__device__ __forceinline__ void block_merge(const fa_stats *__restrict__ in, int64_t lo,
-                                            int64_t hi, int64_t in_count,
-                                            fa_stats *__restrict__ out) {
-    __shared__ double s_sum[kThreads / 32];
-    __shared__ unsigned long long s_cnt[kThreads / 32];
-    constexpr int kU = kFanIn / kThreads;  // records per thread per pass, loaded together
-    float sh = 0.f, sl = 0.f;
-    unsigned long long c = 0;
-    if (!fa_in_bounds(lo, hi - lo, in_count)) hi = lo;  // (bounds-checked build only)
-    for (int64_t base = lo + threadIdx.x; base < hi; base += kThreads * kU) {
-        fa_stats r[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int64_t i = base + static_cast<int64_t>(u) * kThreads;
-            if (i < hi) r[u] = in[i];
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int64_t i = base + static_cast<int64_t>(u) * kThreads;
-            if (i < hi) {
-                df_add(sh, sl, r[u].sum_sq, r[u].sum_sq_lo);
-                c += r[u].nonfinite;
-            }
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
-        const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
-        df_add(sh, sl, oh, ol);
-        c += __shfl_xor_sync(0xffffffffu, c, o);
-    }
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        s_sum[w] = static_cast<double>(sh) + static_cast<double>(sl);
-        s_cnt[w] = c;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double ts = 0.0;
-        unsigned long long tc = 0;
-        for (int k = 0; k < kThreads / 32; ++k) {
-            ts += s_sum[k];
-            tc += s_cnt[k];
-        }
-        fa_stats rec;
-        rec.sum_sq = static_cast<float>(ts);
-        rec.sum_sq_lo = static_cast<float>(ts - static_cast<double>(rec.sum_sq));
-        rec.nonfinite = tc > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(tc);
-        *out = rec;
-    }
-}
-
-// One warp per group of kFanIn input records, eight groups per CTA, so that the
-// 4096 groups of the largest plan run in a single wave (one CTA per group took
-// three and a half).  Lane l adds records l, l + 32, ... of its group as
-// double-float values (16 records' loads issued together), then the warp's
-// shuffle tree; lane 0 writes the group's (hi, lo) record.
-__global__ void __launch_bounds__(kThreads)
-merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
-    fa_grid_dependency_wait();  // (launched early: the records are not ready before this)
-    fa_allow_dependents();
-    constexpr int kWarps = kThreads / 32;
+// One warp reduces records [lo, hi) into *out.  Lane l adds records l, l + 32, ...
+// as double-float values (an FP32 value and its FP32 residual, combined with
+// error-free TwoSum, so every operation stays on the FP32 units: GB300's FP64
+// rate made an FP64 first level compute-bound), 16 records' loads issued
+// together; then the warp's shuffle tree, and lane 0 writes the total as an FP32
+// (hi, lo) pair.  Every lane of the warp calls it.
+__device__ __forceinline__ void warp_merge(const fa_stats *__restrict__ in, int64_t lo, int64_t hi,
+                                           int64_t in_count, fa_stats *__restrict__ out) {
     constexpr int kBatch = 16;
     const int lane = threadIdx.x & 31;
-    const int64_t group = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const int64_t lo = group * kFanIn;
-    if (lo >= count) return;  // the whole warp
-    int64_t hi = lo + kFanIn < count ? lo + kFanIn : count;
-    if (!fa_in_bounds(lo, hi - lo, count)) hi = lo;  // (bounds-checked build only)
+    if (!fa_in_bounds(lo, hi - lo, in_count)) hi = lo;  // (bounds-checked build only)
     float sh = 0.f, sl = 0.f;
     unsigned long long c = 0;
     for (int64_t base = lo + lane; base < hi; base += 32 * kBatch) {
@@ -488,8 +423,24 @@ merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restric
         rec.sum_sq = static_cast<float>(ts);
         rec.sum_sq_lo = static_cast<float>(ts - static_cast<double>(rec.sum_sq));
         rec.nonfinite = c > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(c);
-        out[group] = rec;
+        *out = rec;
     }
+}
+
+constexpr int kMergeWarps = kThreads / 32;  // groups (or chunks) per CTA
+
+// One warp per group of kFanIn input records, eight groups per CTA, so that the
+// 4096 groups of the largest plan run in a single wave (one CTA per group took
+// three and a half).
+__global__ void __launch_bounds__(kThreads)
+merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
+    fa_grid_dependency_wait();  // (launched early: the records are not ready before this)
+    fa_allow_dependents();
+    const int64_t group = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    const int64_t lo = group * kFanIn;
+    if (lo >= count) return;  // the whole warp
+    const int64_t hi = lo + kFanIn < count ? lo + kFanIn : count;
+    warp_merge(in, lo, hi, count, out + group);
 }
 
 // Per-chunk merge, level A: one CTA per group of at most kFanIn records of one
@@ -507,22 +458,24 @@ __global__ void __launch_bounds__(kThreads)
 merge_chunks_a_kernel(const __grid_constant__ ChunkMergeArgs a) {
     fa_grid_dependency_wait();
     fa_allow_dependents();
-    const int64_t b = blockIdx.x;
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    if (b >= a.group_start[a.nchunks]) return;  // the whole warp
     const int k = find_chunk(a, b);
     const int64_t lo = a.row_start[k] + (b - a.group_start[k]) * kFanIn;
     const int64_t hi = lo + kFanIn < a.row_start[k + 1] ? lo + kFanIn : a.row_start[k + 1];
-    block_merge(a.in, lo, hi, a.row_start[a.nchunks], a.partial + b);
+    warp_merge(a.in, lo, hi, a.row_start[a.nchunks], a.partial + b);
 }
 
-// Level B: one CTA per chunk over its level-A records (an empty chunk gives a
+// Level B: one warp per chunk over its level-A records (an empty chunk gives a
 // zero record).
 __global__ void __launch_bounds__(kThreads)
 merge_chunks_b_kernel(const __grid_constant__ ChunkMergeArgs a) {
     fa_grid_dependency_wait();
     fa_allow_dependents();
-    const int k = blockIdx.x;
-    block_merge(a.partial, a.group_start[k], a.group_start[k + 1], a.group_start[a.nchunks],
-                a.out + k);
+    const int k = static_cast<int>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    if (k >= a.nchunks) return;  // the whole warp
+    warp_merge(a.partial, a.group_start[k], a.group_start[k + 1], a.group_start[a.nchunks],
+               a.out + k);
 }
 
 template <int GT, int CH, bool MULTI>
@@ -598,20 +551,21 @@ cudaError_t launch_merge_chunks(const ChunkMergeArgs &a, cudaStream_t stream) {
     const int64_t groups = a.group_start[a.nchunks];
     // both levels start early and wait for their input in the kernel
     if (groups > 0) {
-        const cudaError_t err = launch_dependent(merge_chunks_a_kernel,
-                                                 dim3(static_cast<unsigned>(groups)),
-                                                 dim3(kThreads), 0, stream, a);
+        const cudaError_t err = launch_dependent(
+            merge_chunks_a_kernel, dim3(static_cast<unsigned>((groups + kMergeWarps - 1) / kMergeWarps)),
+            dim3(kThreads), 0, stream, a);
         if (err != cudaSuccess) return err;
     }
     if (a.nchunks > 0)
-        return launch_dependent(merge_chunks_b_kernel, dim3(a.nchunks), dim3(kThreads), 0,
-                                stream, a);
+        return launch_dependent(merge_chunks_b_kernel,
+                                dim3(static_cast<unsigned>((a.nchunks + kMergeWarps - 1) / kMergeWarps)),
+                                dim3(kThreads), 0, stream, a);
     return cudaSuccess;
 }
 
 cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream) {
     const int64_t groups = (count + kFanIn - 1) / kFanIn;
-    const int64_t grid = (groups + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t grid = (groups + kMergeWarps - 1) / kMergeWarps;
     if (grid <= 0) return cudaSuccess;
     // starts early and waits for its input in the kernel
     return launch_dependent(merge_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
