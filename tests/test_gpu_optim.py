@@ -453,24 +453,27 @@ def test_replaced_gradients_are_gathered_into_the_bucket():
         assert torch.equal(p, q)
 
 
-def test_mixed_precision_decoder_full_size():
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_decoder_full_size(dtype):
     """FusedAdamW as the benchmark runs it, at full size: the 1,195,991,040-parameter
-    decoder in 199 BF16 tensors (FP32 masters and moments, BF16 gradients N(0, 1e-3)),
-    global clip 1.0, the update gated on the device with the BF16 copy written in the
-    same pass.  Three calls, the second with one +Inf (skipped).  Each call: the report
-    against the oracle's statistics over the whole gradient, the skip decision, and
-    40,000 sampled parameters plus every tensor's first and last element (master, m, v
+    decoder in 199 tensors, global clip 1.0, the update gated on the device.  BF16:
+    FP32 masters and moments, BF16 gradients, the BF16 copy written in the same pass.
+    FP32: parameters, gradients and moments in FP32.  Gradients N(0, 1e-3).  Three calls,
+    the second with one +Inf (skipped).  Each call: the report against the oracle's
+    statistics over the whole gradient, the skip decision, and 40,000 sampled
+    parameters plus every tensor's first and last element (parameters or masters, m, v
     along the trajectory; the BF16 copy bit for bit)."""
     import dataclasses
     from gpu_harness import check_model_copy, grad_bits_from_device
     from synthetic.configs import CONFIG5, decoder_bucket_shapes
-    params = [torch.nn.Parameter(torch.zeros(shape, dtype=torch.bfloat16, device=DEV))
+    name = "bf16" if dtype == torch.bfloat16 else "f32"
+    params = [torch.nn.Parameter(torch.zeros(shape, dtype=dtype, device=DEV))
               for _, shape in decoder_bucket_shapes()]
     opt = FusedAdamW(params, lr=1e-3, weight_decay=1e-4, eps=1e-5, max_grad_norm=1.0)
     b = opt._buckets[0]
     n = b.n
     assert n == 1_195_991_040 and b.offsets[-1] + params[-1].numel() == n
-    w = dataclasses.replace(CONFIG5.scaled(n), calls=3, inf_call=2)
+    w = dataclasses.replace(CONFIG5.scaled(n), calls=3, inf_call=2, grad_dtype=name)
     w.fill_params_device(b.master)
     ends = [o for o in b.offsets] + [o + p.numel() - 1 for o, p in zip(b.offsets, params)]
     rng = np.random.default_rng(21)
@@ -483,7 +486,7 @@ def test_mixed_precision_decoder_full_size():
         w.fill_grad_device(call, b.grad)
         gh = w.grad_host(call, idx)
         assert np.array_equal(grad_bits_from_device(b.grad[idx_t]), gh)
-        s_or, c_or = lib.gradient_stats(grad_bits_from_device(b.grad), "bf16", 1.0)
+        s_or, c_or = lib.gradient_stats(grad_bits_from_device(b.grad), name, 1.0)
         skip_or, norm_or, coef_or = lib.clip_decision(s_or, c_or, 1.0)
         before = b.master[idx_t].cpu().numpy()
         opt.step()
@@ -494,7 +497,7 @@ def test_mixed_precision_decoder_full_size():
         if not skip_or:
             assert abs(rep["grad_norm"] - norm_or) <= 1e-5 * norm_or
             assert coef_or < 1.0
-        traj.step(gh, "bf16", 1.0, skip_update=skip_or, clip_coef=coef_or)
+        traj.step(gh, name, 1.0, skip_update=skip_or, clip_coef=coef_or)
         master = b.master[idx_t].cpu().numpy()
         if skip_or:
             assert np.array_equal(master, before)
@@ -502,6 +505,7 @@ def test_mixed_precision_decoder_full_size():
         gate(master, traj.p, 1e-5, f"call {call} master")
         gate(b.m[idx_t].cpu().numpy(), traj.state.m, 1e-5, f"call {call} m")
         gate(b.v[idx_t].cpu().numpy(), traj.state.v, 1e-5, f"call {call} v")
-        check_model_copy(grad_bits_from_device(b.model[idx_t]), master, traj.p.astype(np.float32),
-                         "bf16", lib, f"call {call} model copy")
+        if b.model is not None:
+            check_model_copy(grad_bits_from_device(b.model[idx_t]), master,
+                             traj.p.astype(np.float32), name, lib, f"call {call} model copy")
     assert set(b.steps) == {2} and traj.state.t == 2
