@@ -251,3 +251,46 @@ def test_chunk_scratch_plan():
         with pytest.raises(fa.FusedAdamWError) as e:
             fa.fa_stats_chunk_scratch(bad)
         assert e.value.status == code
+
+
+def test_device_decided_calls_validate_on_the_host(lib):
+    """The gated calls (one report, one per segment) check options, control, dtype, the
+    segment table and max_grad_norm on the host, before any pointer is looked at, and
+    launch nothing for skip_update or an empty bucket."""
+    o = fa.options()
+    seg = (ctypes.c_int64 * 3)(0, 8, 16)
+    fake = ctypes.c_void_p(0x1000)
+    gated = (lib.fa_bucket_step_gated, lib.fa_bucket_step_writeback_gated)
+    per_seg = lib.fa_bucket_step_per_segment_gated
+
+    def one(fn, *, ctl=None, nseg=2, table=seg, n=16, dtype=0, max_norm=1.0, opts=o):
+        ctl = ctl or fa.control()
+        if fn is per_seg:
+            return fn(table, nseg, n, fake, fake, dtype, fake, fake, None, 3, ctypes.byref(opts),
+                      ctl, fake, max_norm, None)
+        if fn is lib.fa_bucket_step_writeback_gated:
+            return fn(table, nseg, n, fake, fake, dtype, fake, fake, None, 3, ctypes.byref(opts),
+                      ctl, fake, max_norm, fake, 2, None)
+        return fn(table, nseg, n, fake, fake, dtype, fake, fake, None, 3, ctypes.byref(opts),
+                  ctl, fake, max_norm, None)
+
+    bad_opts = fa.options(lr=-1.0)
+    for fn in gated + (per_seg,):
+        assert one(fn, opts=bad_opts) == 4
+        assert one(fn, ctl=fa.control(gradient_scale=0.0)) == 4
+        assert one(fn, dtype=7) == 2
+        assert one(fn, max_norm=float("nan")) == 4
+        assert one(fn, table=(ctypes.c_int64 * 3)(0, 9, 8), n=8) == 10  # FA_ERR_SEGMENTS
+        assert one(fn, ctl=fa.control(skip_update=True)) == 0  # nothing launched
+        assert one(fn, table=(ctypes.c_int64 * 3)(0, 0, 0), n=0) == 0
+    assert one(per_seg, nseg=0, table=None) == 10  # a segment table is required
+
+    # the one-call per-segment form: row length and scratch checked first as well
+    def clipped(row_len=256, scratch=1 << 20, ctl=None, nseg=2, table=seg):
+        return lib.fa_bucket_step_clipped_per_segment_gated(
+            table, nseg, 16, fake, fake, 0, fake, fake, None, 0, ctypes.byref(o),
+            ctl or fa.control(), 1.0, row_len, fake, 1 << 20, fake, scratch, fake, None)
+    assert clipped(row_len=0) == 3
+    assert clipped(nseg=0, table=None) == 10
+    assert clipped(scratch=0) == 3
+    assert clipped(ctl=fa.control(skip_update=True)) == 0
