@@ -6,10 +6,13 @@
  * the final p, m, v and the three step reports written to a binary file.
  *
  * Inputs are integer hashes scaled by powers of two, exact in FP32, so the test
- * that runs this program can rebuild them bit for bit.
+ * that runs this program can rebuild them bit for bit.  With "gated", every step
+ * goes through fa_bucket_step_clipped_gated (the update decides on the device)
+ * instead of fa_bucket_step_clipped; the results must be the same bits.
  *
- *   consumer <n> <output file>
+ *   consumer <n> <output file> [gated]
  */
+#include <string.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -52,10 +55,11 @@ static float sample(uint32_t stream, uint32_t i, float scale) {
     } while (0)
 
 int main(int argc, char **argv) {
-    if (argc != 3) {
-        fprintf(stderr, "usage: consumer <n> <output file>\n");
+    if (argc != 3 && !(argc == 4 && strcmp(argv[3], "gated") == 0)) {
+        fprintf(stderr, "usage: consumer <n> <output file> [gated]\n");
         return 1;
     }
+    const int gated = argc == 4;
     const int64_t n = atoll(argv[1]);
     if (n < 2) return 1;
     const int32_t row_len = 256;
@@ -94,9 +98,15 @@ int main(int argc, char **argv) {
         for (int64_t i = 0; i < n; ++i) h[i] = sample(100u + (uint32_t)call, (uint32_t)i, 0.0625f);
         if (call == 2) h[n / 2] = 1.0f / 0.0f; /* +Inf: this step is skipped */
         CHECK_CUDA(cudaMemcpy(g, h, (size_t)n * 4, cudaMemcpyHostToDevice));
-        CHECK_FA(fa_bucket_step_clipped(NULL, 0, n, p, g, FA_F32, m, v, NULL, &t, &o, ctl,
-                                        0.5, row_len, rows_buf, rows, scratch, scratch_elems,
-                                        report, &reps[call - 1], stream));
+        if (gated)
+            CHECK_FA(fa_bucket_step_clipped_gated(NULL, 0, n, p, g, FA_F32, m, v, NULL, &t, &o,
+                                                  ctl, 0.5, row_len, rows_buf, rows, scratch,
+                                                  scratch_elems, report, &reps[call - 1],
+                                                  stream));
+        else
+            CHECK_FA(fa_bucket_step_clipped(NULL, 0, n, p, g, FA_F32, m, v, NULL, &t, &o, ctl,
+                                            0.5, row_len, rows_buf, rows, scratch,
+                                            scratch_elems, report, &reps[call - 1], stream));
     }
     CHECK_CUDA(cudaStreamSynchronize(stream));
 
