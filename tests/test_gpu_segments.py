@@ -282,7 +282,9 @@ def test_per_segment_clipped_full_size_sampled(oracle_lib):
     (199 segments, FP16 gradients, AMSGrad, rows of 512), in the launch configuration the
     benchmark times. Every segment's report and clip coefficient is checked against the
     oracle over that segment's full gradient. Sampled elements are checked one step from
-    identical state and along the trajectory. Call 3 carries +Inf and is skipped."""
+    identical state and along the trajectory. Call 3 carries +Inf and is skipped.  The
+    same step decided on the device runs beside it on a copy of the state and must match
+    it bit for bit over every element after every call."""
     w = dataclasses.replace(CONFIG4, calls=4, inf_call=3)
     seg = np.asarray(w.segments, dtype=np.int64)
     n = w.n
@@ -297,6 +299,10 @@ def test_per_segment_clipped_full_size_sampled(oracle_lib):
     rows_buf = fa.stats_buffer(crow[-1], DEV)
     scratch = torch.empty(fa.fa_stats_chunk_scratch(crow), device=DEV)
     reports = fa.stats_buffer(len(seg) - 1, DEV)
+    dev_state = [x.clone() for x in (p, m, v, vm)]
+    dev_bufs = (fa.stats_buffer(crow[-1], DEV), torch.empty_like(scratch),
+                fa.stats_buffer(len(seg) - 1, DEV))
+    t_dev = 0
     rng = np.random.default_rng(40)
     ends = np.concatenate([seg[1:-1], seg[1:-1] - 1, [0, n - 1, w.inf_index()]])
     idx = np.unique(np.concatenate([rng.integers(0, n, 40000), ends]))
@@ -314,7 +320,15 @@ def test_per_segment_clipped_full_size_sampled(oracle_lib):
         t, rep, norms, coefs = fa.fa_bucket_step_clipped_per_segment(
             list(seg), p, g, m, v, vm, t, o, fa.control(), max_norm, row_len, rows_buf,
             scratch, reports)
+        pd, md, vd, vmd = dev_state
+        fa.fa_bucket_step_clipped_per_segment_gated(list(seg), pd, g, md, vd, vmd, t_dev, o,
+                                                    fa.control(), max_norm, row_len, *dev_bufs)
+        if not bool((dev_bufs[2][:, 1] != 0).any()):
+            t_dev += 1
         torch.cuda.synchronize()
+        assert t_dev == t and torch.equal(dev_bufs[2], reports)
+        for x, y, name in zip((p, m, v, vm), dev_state, ("p", "m", "v", "vmax")):
+            assert torch.equal(x, y), f"call {call}: decided on the device, {name} differs"
         bits = grad_bits_from_device(g)
         assert np.array_equal(bits[idx], w.grad_host(call, idx)), "device/host grads differ"
         stats = _slice_stats(oracle_lib, bits, "f16", seg)
