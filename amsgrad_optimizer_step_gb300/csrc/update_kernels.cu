@@ -10,7 +10,7 @@
 // inside the kernel without reading them).
 //
 // Design: one HBM pass per parameter.  The update is bandwidth bound (about
-// 0.7 flop per byte), so it is built for bytes in flight.  Two kernels share the
+// 0.7 flop per byte), so it is built for bytes in flight.  Three kernels share the
 // element arithmetic:
 //   - steady steps of large tensors: update_tma_kernel, one CTA per SM staging
 //     tiles of every stream through shared memory with 1-D TMA bulk copies and
@@ -22,7 +22,10 @@
 //     before any arithmetic;
 //   - views not co-aligned to 16 bytes: update_scalar_kernel.
 // Elements before the first 16-byte boundary and after the last full vector or
-// tile go through the same arithmetic one at a time.
+// tile go through the same arithmetic one at a time.  A gated launch takes the
+// skip / clip decision itself, from the 12-byte statistics report (or one report
+// per segment) that the merge before it wrote, and is launched as that merge's
+// programmatic dependent.
 #include <atomic>
 #include <type_traits>
 
