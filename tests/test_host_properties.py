@@ -99,3 +99,36 @@ def test_active_runs_cover_exactly_the_active_parameters(data):
         assert j == len(data) or not active[j] or steps[j] != steps[i]
     if all(active) and len(set(steps)) == 1:
         assert runs == [(0, len(data), 0, pos)]
+
+
+def _int_pow(beta, t):
+    """beta^t by repeated squaring in FP64 (the host's integer power)."""
+    r, b = 1.0, beta
+    while t:
+        if t & 1:
+            r *= b
+        b *= b
+        t >>= 1
+    return r
+
+
+@SETTINGS
+@given(lr=st.floats(0.0, 1.0), beta1=st.floats(0.0, 0.999999), beta2=st.floats(0.0, 0.999999),
+       eps=st.floats(0.0, 1e-2), wd=st.floats(0.0, 1.0), t=st.integers(1, 10 ** 12),
+       log2_scale=st.integers(-8, 16), mult=st.floats(0.0, 1.0), maximize=st.booleans())
+def test_step_coefficients_are_the_fp64_formula_cast_once(lr, beta1, beta2, eps, wd, t,
+                                                          log2_scale, mult, maximize):
+    """Every coefficient is the FP64 expression rounded once to FP32: exactly for the
+    ones without a power, and for the bias corrections to the FP32 rounding of the same
+    repeated-squaring power."""
+    scale = 2.0 ** log2_scale
+    o = fa.options(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=wd,
+                   maximize=maximize)
+    c = fa.fa_step_coefficients(o, t, gradient_scale=scale, grad_mult=mult)
+    f32 = lambda x: float(np.float32(x))  # noqa: E731
+    assert c[0] == f32(beta1) and c[1] == f32(1.0 - beta1)
+    assert c[2] == f32(beta2) and c[3] == f32(1.0 - beta2)
+    assert c[4] == f32(lr / (1.0 - _int_pow(beta1, t)))
+    assert c[5] == f32(1.0 / (1.0 - _int_pow(beta2, t)))
+    assert c[6] == f32(eps) and c[7] == f32(1.0 - lr * wd)
+    assert c[8] == f32((-1.0 if maximize else 1.0) * mult / scale)
