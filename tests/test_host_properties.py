@@ -132,3 +132,23 @@ def test_step_coefficients_are_the_fp64_formula_cast_once(lr, beta1, beta2, eps,
     assert c[5] == f32(1.0 / (1.0 - _int_pow(beta2, t)))
     assert c[6] == f32(eps) and c[7] == f32(1.0 - lr * wd)
     assert c[8] == f32((-1.0 if maximize else 1.0) * mult / scale)
+
+
+@SETTINGS
+@given(sizes=st.lists(st.integers(0, 200_000), min_size=1, max_size=60),
+       row_len=st.integers(1, 4096))
+def test_segment_rows_and_chunk_scratch(sizes, row_len):
+    """Per-segment rows (rows never span segments) and the per-segment merge scratch:
+    three FP32 words per group of at most 1024 rows inside each segment."""
+    seg = [0]
+    for s in sizes:
+        seg.append(seg[-1] + s)
+    crow = fa.segment_rows(seg, row_len)
+    assert crow == [0] + list(np.cumsum([-(-s // row_len) for s in sizes]))
+    if crow[-1] == 0 or crow[-1] > MAX_ROWS:
+        with pytest.raises(fa.FusedAdamWError):
+            fa.fa_stats_chunk_scratch(crow)
+        return
+    groups = sum(-(-(b - a) // 1024) for a, b in zip(crow[:-1], crow[1:]))
+    assert fa.fa_stats_chunk_scratch(crow) == 3 * groups
+    assert fa.fa_stats_rows(seg[-1], row_len, seg) == crow[-1]
