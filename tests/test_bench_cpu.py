@@ -39,3 +39,22 @@ def test_default_workload_is_the_1e9_bucket():
     assert cfg["workload"] == "flat1G_bf16_stats_clip" and cfg["params"] == 1_073_741_824
     assert cfg["grad_dtype"] == "bf16" and cfg["row_len"] == 256
     assert cfg["merge_fan_in"] == 1024 and cfg["max_grad_norm"] == 1.0
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores and prints one JSON
+    line with the arm's keys; it needs no GPU."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl",
+                        "reference", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=bench.ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "params/s" and line["value"] > 0
+    assert line["config"]["workload"] == "flat1G_bf16_stats_clip"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "params/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["higher_is_better"] is True and line["steps"] == 2 and line["warmup"] == 1
