@@ -443,7 +443,9 @@ fa_status fa_bucket_step_clipped_per_segment(
     double *seg_norms, double *seg_coefs, fa_step_report *out, void *stream);
 
 /*
- * fa_bucket_step_segment_scaled with the multipliers decided on the device:
+ * fa_bucket_step_segment_scaled with the multipliers decided on the device
+ * ([TR-zh] "FP32 主参数与混合参数存储": per-parameter clipping; [TR-zh] "在 ruda:0 上
+ * 进行原生 PyTorch 训练": any non-finite gradient skips the whole step):
  * seg_reports (device, nseg records, as written by fa_merge_gradient_stats_chunks
  * earlier on the same stream) are read by the update kernels themselves.  Any
  * non-finite count skips the whole update; otherwise segment k's gradient is
@@ -463,7 +465,9 @@ fa_status fa_bucket_step_per_segment_gated(const int64_t *seg_offsets, int32_t n
                                            double max_grad_norm, void *stream);
 
 /*
- * fa_bucket_step_clipped_per_segment with the decision on the device: the
+ * fa_bucket_step_clipped_per_segment with the decision on the device ([FA-ja]
+ * "ネイティブ PyTorch ストレージと階層統計": merge_gradient_stats_chunks; [TR-zh]
+ * "FP32 主参数与混合参数存储": per-parameter clipping): the
  * segment-aligned analysis, the per-segment merges into seg_reports and the
  * update gated by fa_bucket_step_per_segment_gated are enqueued back to back;
  * nothing is read back and the call does not wait.  Results are bit-identical to
