@@ -116,15 +116,23 @@ typedef struct fa_step_report {
 
 /* ---- host-only helpers ---------------------------------------------------- */
 
+/* FA_ABI_VERSION of the loaded library, for a caller to check against the
+ * header it was built with (library bookkeeping; the pages have no counterpart). */
 int32_t fa_abi_version(void);
+
+/* A static English description of a status code, never NULL (the status codes
+ * follow the error classes of [FA-ja] "低レベルの使用": invalid options, sizes,
+ * pointers and overlaps are rejected before anything runs). */
 const char *fa_status_string(fa_status status);
 
 /* Large updates stage tiles through shared memory with TMA bulk copies; every
  * wait in that pipeline is bounded (about a second), and a wait that gives up
  * sets a device flag, drains its own copies and ends the kernel early (its
- * outputs are then incomplete: discard them).  This reads the flag of the
- * current device into *flag (0 = no wait ever gave up) and clears it when
- * clear != 0.  Waits for the device; FA_ERR_CUDA if it cannot be read. */
+ * outputs are then incomplete: discard them, as [FA-ja] "低レベルの使用" asks of
+ * any device failure).  This reads the flag of the current device into *flag
+ * (0 = no wait ever gave up) and clears it when clear != 0.  Waits for the
+ * device; FA_ERR_CUDA if it cannot be read.  The pipeline is this library's;
+ * the pages have no counterpart. */
 fa_status fa_device_error(int32_t *flag, int32_t clear);
 
 /* Bounds-checked build (a test variant of the library compiled with
@@ -138,7 +146,8 @@ fa_status fa_device_error(int32_t *flag, int32_t clear);
  * FA_ERR_CUDA if the count cannot be read. */
 fa_status fa_bounds_check_report(int32_t *enabled, uint64_t *violations, int32_t clear);
 
-/* Self-test of the bounded waits above, with no fault: one steady-state update
+/* Self-test of the bounded waits above (the pages have no counterpart), with no
+ * fault: one steady-state update
  * of the n-element p, m, v (device, FP32) with gradient g, launched so that
  * every shared-memory stage waits for 16 bytes that never arrive.  Each wait
  * gives up after its limit (about a second), the kernel drains its own
@@ -258,7 +267,9 @@ fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt,
                                int32_t *updated, void *stream);
 
 /*
- * fa_bucket_step whose skip / clip decision is taken on the device: the
+ * fa_bucket_step whose skip / clip decision ([TR-zh] "在 ruda:0 上进行原生 PyTorch
+ * 训练": a non-finite gradient skips the whole step; the global L2 clip of the
+ * unscaled gradient) is taken on the device: the
  * update kernel reads ``report_dev`` (as produced by fa_merge_gradient_stats,
  * earlier on the same stream), skips when it counts a non-finite value, and
  * otherwise multiplies the unscaled gradient by the same coefficient that
@@ -278,7 +289,9 @@ fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t
 
 /*
  * fa_bucket_step_writeback gated on the device report, as fa_bucket_step_gated
- * is for fa_bucket_step: the update (FP32 masters and the FP16/BF16 model copy
+ * is for fa_bucket_step ([TR-zh] "FP32 主参数与混合参数存储": FP32 masters, parameters
+ * returned in their storage dtype; [TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": the
+ * skip and the clip): the update (FP32 masters and the FP16/BF16 model copy
  * p_model, written in the same pass) skips when the report counts a non-finite
  * value and otherwise applies the host formula's clip coefficient, bit-identical
  * to reading the report back and calling fa_bucket_step_writeback.  ``t`` is the
@@ -325,7 +338,8 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
  */
 fa_status fa_stats_plan(int64_t rows, int32_t *merge_kernels, int64_t *scratch_elements);
 
-/* Row count of an analysis: each segment [seg[k], seg[k+1]) is cut into rows
+/* Row count of an analysis ([FA-ja] "ネイティブ PyTorch ストレージと階層統計":
+ * analyze_gradient works in rows): each segment [seg[k], seg[k+1]) is cut into rows
  * of row_len elements, its last row possibly shorter; rows never span
  * segments.  seg_offsets NULL / nseg 0 means one segment [0, n).  Host only. */
 fa_status fa_stats_rows(int64_t n, int32_t row_len, const int64_t *seg_offsets, int32_t nseg,
@@ -385,7 +399,8 @@ fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
 
 /* ---- per-parameter statistics and clipping ---------------------------------- */
 
-/* Scratch (FP32 elements) for fa_merge_gradient_stats_chunks: 3 words for each
+/* Scratch (FP32 elements) for fa_merge_gradient_stats_chunks ([FA-ja]
+ * "ネイティブ PyTorch ストレージと階層統計": merge_gradient_stats_chunks): 3 words for each
  * group of at most 1024 rows within a chunk.  chunk_rows (host, nchunks+1
  * entries) are row offsets, non-decreasing from 0; their total must be a
  * valid plan size (FA_ERR_PLAN else).  Host only. */
@@ -423,7 +438,10 @@ fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg
                                         void *stream);
 
 /*
- * The statistics-guarded step with per-parameter clipping: analyse the bucket
+ * The statistics-guarded step with per-parameter clipping ([TR-zh] "FP32 主参数与
+ * 混合参数存储": Fp32MasterOptimizer clips each parameter by its own rule; [TR-zh]
+ * "在 ruda:0 上进行原生 PyTorch 训练": the report is read back first and a non-finite
+ * gradient skips the whole step): analyse the bucket
  * in segment-aligned rows, merge one report per segment into seg_reports
  * (device, nseg records), read them back (nseg * 12 bytes; synchronises),
  * skip the whole step when any value is non-finite, else clip each segment
@@ -501,7 +519,9 @@ fa_status fa_clip_decision(double sum_sq_stored, uint64_t nonfinite, double grad
                            double max_grad_norm, int32_t *skip, double *grad_norm,
                            double *clip_coef);
 
-/* fa_read_report followed by fa_clip_decision.  Synchronises the stream. */
+/* fa_read_report followed by fa_clip_decision ([TR-zh] "在 ruda:0 上进行原生 PyTorch
+ * 训练": the 12-byte report is read back, then the skip and the clip are decided).
+ * Synchronises the stream. */
 fa_status fa_clip_decide(const fa_stats *report_dev, double gradient_scale, double max_grad_norm,
                          int32_t *skip, double *grad_norm, double *clip_coef, void *stream);
 

@@ -294,3 +294,19 @@ def test_device_decided_calls_validate_on_the_host(lib):
     assert clipped(nseg=0, table=None) == 10
     assert clipped(scratch=0) == 3
     assert clipped(ctl=fa.control(skip_update=True)) == 0
+
+
+def test_every_entry_point_cites_its_passage():
+    """Each declaration in include/*.h is preceded by a comment that cites the page
+    passage defining the operation, or says that the pages have no counterpart."""
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        prev = 0
+        for m in re.finditer(r"^\w[\w \*]*?\b(fa_[a-z0-9_]+)\s*\(", text, flags=re.M):
+            comments = re.findall(r"/\*.*?\*/", text[prev:m.start()], flags=re.S)
+            last = comments[-1] if comments else ""
+            assert re.search(r"\[(FA-ja|FA-zh|TR-zh)\]|no counterpart", last), m.group(1)
+            prev = m.start()
