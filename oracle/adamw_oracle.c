@@ -59,6 +59,8 @@ static double widen_f16(uint16_t bits)
     return sign ? -mag : mag;
 }
 
+/* Element i of a stored gradient widened exactly to FP64 ("实验性融合 AdamW /
+ * AMSGrad", "增加的实际能力": gradients are FP32, FP16 or BF16). */
 double oracle_widen(const void *g, int dtype, int64_t i)
 {
     if (dtype == ORACLE_F32) {
@@ -73,7 +75,9 @@ double oracle_widen(const void *g, int dtype, int64_t i)
 
 /* ---- host coefficients ------------------------------------------------------ */
 
-/* beta^t by repeated multiplication in FP64 (an integer power, as the pages say). */
+/* beta^t by repeated multiplication in FP64 ("実験的なデバイス上の融合 AdamW / AMSGrad",
+ * "この演算子を使用する理由": the host forms the bias corrections from FP64 integer
+ * powers). */
 double oracle_int_pow(double beta, uint64_t t)
 {
     double r = 1.0;
@@ -96,7 +100,9 @@ static double store(double x, int round_fp32)
 }
 
 /*
- * One update call.  ``t`` is the 1-based step of this update (already
+ * One update call ("実験的なデバイス上の融合 AdamW / AMSGrad", "この演算子を使用する理由":
+ * the per-element formula block; "实验性融合 AdamW / AMSGrad", "增加的实际能力":
+ * maximize and the first update).  ``t`` is the 1-based step of this update (already
  * advanced by the caller).  ``have_state`` = 0 is the first update: the old
  * moments are taken as zero and the m/v/vmax arrays are only written.
  * ``clip_coef`` multiplies the unscaled gradient (1 = no clipping).
@@ -168,7 +174,10 @@ static double round_to_format(double x, int sig_bits, int emin, int emax)
     return y;
 }
 
-/* BF16: 8 significant bits, exponents -126..127 (same range as FP32). */
+/* BF16: 8 significant bits, exponents -126..127 (same range as FP32).  The model
+ * copies follow "训练与状态保存", "FP32 主参数与混合参数存储" (parameters return in their
+ * storage dtype); the pages name no rounding, and round-to-nearest-even, the IEEE
+ * default, is the reading taken. */
 uint16_t oracle_to_bf16(float x)
 {
     uint32_t b;
@@ -200,7 +209,8 @@ uint16_t oracle_to_f16(float x)
     return sign | (uint16_t)(expo << 10) | frac;
 }
 
-/* Model copies of n FP32 values: dtype ORACLE_BF16 or ORACLE_F16. */
+/* Model copies of n FP32 values: dtype ORACLE_BF16 or ORACLE_F16 ("训练与状态保存",
+ * "FP32 主参数与混合参数存储"; rounding to nearest even). */
 void oracle_model_copy(int64_t n, const float *p, int dtype, uint16_t *out)
 {
     for (int64_t i = 0; i < n; ++i)

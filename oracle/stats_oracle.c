@@ -32,7 +32,9 @@ static int is_nonfinite(double x)
     return isnan(x) || isinf(x);
 }
 
-/* Whole-gradient statistics: sum of (stored / scale)^2 and the non-finite count. */
+/* Whole-gradient statistics: sum of (stored / scale)^2 and the non-finite count
+ * ("训练与状态保存", "在 ruda:0 上进行原生 PyTorch 训练": the global L2 norm after
+ * unscale, and any non-finite value skips the step). */
 void oracle_gradient_stats(int64_t n, const void *g, int gdtype, double gradient_scale,
                            double *sum_sq, uint64_t *nonfinite)
 {
@@ -52,7 +54,8 @@ void oracle_gradient_stats(int64_t n, const void *g, int gdtype, double gradient
 }
 
 /*
- * Per-row statistics of the stored gradient.  The buffer is split into
+ * Per-row statistics of the stored gradient ("実験的なデバイス上の融合 AdamW / AMSGrad",
+ * "ネイティブ PyTorch ストレージと階層統計": analyze_gradient).  The buffer is split into
  * segments [seg[k], seg[k+1]) (one segment [0, n) when nseg == 0); each
  * segment is cut into rows of row_len elements, its last row possibly
  * shorter.  Rows never span two segments.  Returns the number of rows, or -1
@@ -97,7 +100,10 @@ int64_t oracle_row_stats(int64_t n, const void *g, int gdtype, int64_t row_len,
 }
 
 /*
- * Reduction plan for ``rows`` row records at fan-in ``fan_in``: each merge
+ * Reduction plan ("実験的なデバイス上の融合 AdamW / AMSGrad", "ネイティブ PyTorch
+ * ストレージと階層統計": StatsPlan; "训练与状态保存", "在 ruda:0 上进行原生 PyTorch
+ * 训练": at most two extra merge kernels and 49,200 bytes) for ``rows`` row
+ * records at fan-in ``fan_in``: each merge
  * kernel turns its input records into ceil(count / fan_in) records, until
  * one record -- the report -- is left.  Every record is three 4-byte words
  * (12 bytes).  The intermediate records live in scratch; the initial rows and
@@ -125,7 +131,8 @@ int oracle_stats_plan(int64_t rows, int64_t fan_in, int64_t max_rows,
 }
 
 /*
- * The host decision after the report is read back: skip on any non-finite
+ * The host decision after the report is read back ("训练与状态保存", "在 ruda:0 上
+ * 进行原生 PyTorch 训练"): skip on any non-finite
  * value; otherwise the global L2 norm of the unscaled gradient and the clip
  * coefficient min(1, max_grad_norm / norm) (max_grad_norm <= 0: no clip).
  */
