@@ -310,3 +310,10 @@ def test_every_entry_point_cites_its_passage():
             last = comments[-1] if comments else ""
             assert re.search(r"\[(FA-ja|FA-zh|TR-zh)\]|no counterpart", last), m.group(1)
             prev = m.start()
+
+
+def test_a_missing_library_fails_loudly(tmp_path):
+    """Without the built library nothing runs: loading raises and names the build step
+    (there is no CPU or library fallback to fall through to)."""
+    with pytest.raises(RuntimeError, match="is not built"):
+        _lib.open_library(str(tmp_path / "libfused_adamw.so"))
