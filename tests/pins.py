@@ -205,6 +205,58 @@ def pin_torch_adamw(L):
                                what="vmax " + tag)
 
 
+def _same_with_nan(a, b, rtol, what):
+    """Equal NaN positions, and the other values within rtol (``_close`` alone lets
+    a NaN on either side pass, because every comparison with NaN is false)."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    na, nb = np.isnan(a), np.isnan(b)
+    assert np.array_equal(na, nb), \
+        f"{what}: NaN at {np.flatnonzero(na ^ nb)[:5]} on one side only"
+    ok = ~nb
+    _close(a[ok], b[ok], rtol, 1e-13 * max(1e-300, np.abs(b[ok]).max(initial=0.0)), what=what)
+
+
+def pin_amsgrad_max_propagates_nan_like_torch(L):
+    """A NaN gradient under AMSGrad: the running max of v takes the NaN and keeps it, as
+    torch.maximum does in torch.optim.AdamW(amsgrad=True) (float64 CPU), for FP32 and
+    BF16 storage; the other elements follow torch as usual.  A max that drops a NaN
+    operand (C's fmax) keeps the old maximum there instead and fails."""
+    import torch
+    rng = _rng(31)
+    n = 96
+    nan_at = np.array([3, 17, 40, 95])
+    for dtype in ("f32", "bf16"):
+        opts = dict(BASE, amsgrad=True, beta2=0.99)
+        p0 = rng.normal(0, 0.02, n)
+        xs = [_grads(rng, n) * np.float32(2.0 if k == 0 else 0.5) for k in range(4)]
+        xs[1] = xs[1].copy()
+        xs[1][nan_at] = np.float32(np.nan)
+        if dtype == "bf16":
+            gs = [(x.view(np.uint32) >> 16).astype(np.uint16) for x in xs]
+            assert np.isnan(_widen_independent(gs[1], "bf16")[nan_at]).all()
+        else:
+            gs = xs
+        _, traj = _run(L, p0, gs, opts, dtype=dtype)
+        tp = torch.tensor(p0, dtype=torch.float64, requires_grad=True)
+        topt = torch.optim.AdamW([tp], lr=opts["lr"], betas=(opts["beta1"], opts["beta2"]),
+                                 eps=opts["eps"], weight_decay=opts["weight_decay"],
+                                 amsgrad=True, foreach=False)
+        for k, g in enumerate(gs):
+            tp.grad = torch.tensor(_widen_independent(g, dtype))
+            topt.step()
+            st = topt.state[tp]
+            pt, _, m, v, vmax = traj[k]
+            tag = f"{dtype} step {k + 1}"
+            _same_with_nan(vmax, st["max_exp_avg_sq"].numpy(), 1e-10, "vmax " + tag)
+            _same_with_nan(v, st["exp_avg_sq"].numpy(), 1e-10, "v " + tag)
+            _same_with_nan(m, st["exp_avg"].numpy(), 1e-10, "m " + tag)
+            _same_with_nan(pt, tp.detach().numpy(), 1e-11, "p " + tag)
+            if k >= 1:
+                assert np.isnan(vmax[nan_at]).all(), f"NaN dropped from the max, {tag}"
+                assert not np.isnan(np.delete(vmax, nan_at)).any()
+
+
 # ---------------------------------------------------------------------------
 # Update: invariants
 # ---------------------------------------------------------------------------

@@ -33,6 +33,8 @@ MUTANTS = {
                                "(1.0 - o->weight_decay)"),
     "no_amsgrad_max": ("adamw_oracle.c", "max_propagate_nan(vmax_old, v_new)", "v_new"),
     "amsgrad_min": ("adamw_oracle.c", "return a > b ? a : b;", "return a < b ? a : b;"),
+    "amsgrad_max_drops_nan": ("adamw_oracle.c", "if (isnan(a) || isnan(b))\n        return NAN;",
+                              "if (isnan(a) || isnan(b))\n        return isnan(a) ? b : a;"),
     "vmax_ignored_in_update": ("adamw_oracle.c", "v_used = vmax_new;", "v_used = v_new;"),
     "store_corrected_max": ("adamw_oracle.c", "vmax[i] = store(vmax_new,",
                             "vmax[i] = store(vmax_new / bc2,"),
