@@ -173,13 +173,21 @@ def check_model_copy(model_bits, p_dev_f32, p_oracle_f32, dtype, lib, what):
 
 def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None = None,
                  guard: int = 0, segments=None, row_len: int = 0, lib=None,
-                 full_grad_on_host: bool = True, step_check=True, model_dtype=None):
-    """Runs every call of ``w`` (at size n) and checks each one.  Returns a summary."""
+                 full_grad_on_host: bool = True, step_check=True, model_dtype=None,
+                 grad_mult: float = 1.0):
+    """Runs every call of ``w`` (at size n) and checks each one.  Returns a summary.
+
+    ``api``: "oop", "inplace", "bucket", "clipped" or "staged" (the 4/5-kernel
+    comparison, on in-place storage).  ``grad_mult`` is a fixed factor on the
+    unscaled gradient for "inplace" and "staged" (the oracle's clip coefficient)."""
+    import dataclasses
     lib = lib or oracle.lib()
     ws = w if n == w.n else w.scaled(n)
     if segments is not None and n != w.n:
-        import dataclasses
         ws = dataclasses.replace(ws, segments=tuple(segments))
+    if api == "staged" and not ws.inplace:
+        ws = dataclasses.replace(ws, inplace=True)
+    assert grad_mult == 1.0 or api in ("inplace", "staged")
     segs = list(ws.segments) if ws.segments is not None else None
     st = DeviceState(ws, n, device, guard=guard)
     opts = ws.options()
@@ -196,6 +204,8 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         full.view(torch.int16).fill_(0x7F7F)
         p_model = full[guard:guard + n]
         st._full["model"] = full
+    if api == "staged":
+        delta = torch.empty(n, dtype=torch.float32, device=device)
     if api == "clipped":
         rows = fa.fa_stats_rows(n, row_len, segs)
         rows_buf = fa.stats_buffer(rows, device)
@@ -211,9 +221,9 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         before = st.snapshot(idx_t)
         model_before = None if p_model is None else grad_bits_from_device(p_model[idx_t])
         t_before = st.t
-        coef_dev = 1.0
+        coef_dev = grad_mult
         expect_skip = skip
-        coef_or = 1.0
+        coef_or = grad_mult
         if api == "clipped":
             full_bits = (ws.grad_host(call, np.arange(n)) if full_grad_on_host
                          else grad_bits_from_device(st.g))
@@ -239,7 +249,10 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
             st.p, st.m, st.v, st.vmax = p2, m2, v2, vm2
         elif api == "inplace":
             t_new, updated = fa.fa_adamw_step_inplace(st.p, st.g, st.m, st.v, st.vmax, st.t,
-                                                      fopts, ctl)
+                                                      fopts, ctl, grad_mult=grad_mult)
+        elif api == "staged":
+            t_new, updated = fa.fa_adamw_step_staged(st.p, st.g, st.m, st.v, st.vmax, st.t,
+                                                     fopts, ctl, delta, grad_mult=grad_mult)
         elif api == "bucket" and p_model is not None:
             t_new, updated = fa.fa_bucket_step_writeback(segs, st.p, st.g, st.m, st.v, st.vmax,
                                                          st.t, fopts, ctl, p_model)

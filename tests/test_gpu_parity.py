@@ -790,6 +790,22 @@ def test_staged_equals_fused_bitwise(gdt, ams):
             assert torch.equal(x.view(torch.int32), y.view(torch.int32))
 
 
+@pytest.mark.parametrize("n", [70_001, 1_000_003])
+@pytest.mark.parametrize("ams", [False, True])
+@pytest.mark.parametrize("gdt", ["f32", "f16", "bf16"])
+def test_staged_vs_oracle(gdt, ams, n):
+    """The staged 4/5-kernel comparison against the oracle itself, not only against
+    the fused kernel: every element of every call, one step from identical state
+    (1e-6 and the FP32 error bound) and along the oracle's own trajectory (1e-5).
+    Lengths leave a scalar tail after the 4-element vectors; gradients stored x128
+    with gradient_scale 128, a clip factor of 0.75, a skipped third call, and
+    maximize on the FP16 runs."""
+    w = dataclasses.replace(CONFIG2, name=f"staged_{gdt}", grad_dtype=gdt, amsgrad=ams, calls=5,
+                            skip_calls=(3,), maximize=gdt == "f16")
+    s = run_workload(w, n, "staged", DEV, guard=1024, grad_mult=0.75)
+    assert s["updates"] == 4 and s["skips"] == 1 and s["t"] == 4
+
+
 def test_staged_rejects_unaligned_views():
     n = 4096
     full = torch.zeros(n + 4, device=DEV)
