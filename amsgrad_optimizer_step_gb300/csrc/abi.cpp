@@ -934,9 +934,19 @@ fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
     if ((st = check_device_ptr(rows_in, dev, 4)) != FA_OK) return st;
     if ((st = check_device_ptr(report, dev, 4)) != FA_OK) return st;
     if (overlap({rows_in, static_cast<size_t>(rows) * 12}, {report, 12})) return FA_ERR_ALIAS;
+    // While the stream is being captured, stream_device could not check the
+    // stream's device, and a first address lookup must not run inside the
+    // capture: only an address an earlier call looked up for the current device
+    // is used then; without one the call fails with nothing enqueued.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (stream && cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_POINTER;
+    }
     float *scratch = nullptr;
     int64_t capacity = 0;
-    if (fa::static_merge_scratch(dev, &scratch, &capacity) != cudaSuccess) {
+    if (fa::static_merge_scratch(dev, cs == cudaStreamCaptureStatusNone, &scratch, &capacity) !=
+        cudaSuccess) {
         cudaGetLastError();
         return FA_ERR_CUDA;
     }

@@ -186,9 +186,12 @@ cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, f
 cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream);
 
 // Device address and size of the library's fixed merge scratch on ``device``
-// (which must be the current device).  Looked up once per device.
+// (which must be the current device).  Looked up once per device; with
+// ``lookup_allowed`` false (the caller's stream is being captured) an address
+// not looked up yet is not looked up now: cudaErrorStreamCaptureUnsupported.
 constexpr int64_t kStaticMergeScratchFloats = 12300;  // 3 * (4096 + 4): the largest plan
-cudaError_t static_merge_scratch(int device, float **ptr, int64_t *capacity_floats);
+cudaError_t static_merge_scratch(int device, bool lookup_allowed, float **ptr,
+                                 int64_t *capacity_floats);
 
 // SM count of the current device (cached per device).
 int sm_count(int device);

@@ -582,12 +582,15 @@ cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaS
 
 static __device__ __align__(256) float g_static_merge_scratch[kStaticMergeScratchFloats];
 
-cudaError_t static_merge_scratch(int device, float **ptr, int64_t *capacity_floats) {
+cudaError_t static_merge_scratch(int device, bool lookup_allowed, float **ptr,
+                                 int64_t *capacity_floats) {
     static std::mutex mu;
     static float *addr[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[device]) {
+        // the first lookup may load the module; it must not happen inside a capture
+        if (!lookup_allowed) return cudaErrorStreamCaptureUnsupported;
         void *p = nullptr;
         const cudaError_t err = cudaGetSymbolAddress(&p, g_static_merge_scratch);
         if (err != cudaSuccess) return err;

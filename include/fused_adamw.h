@@ -388,7 +388,9 @@ fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the one array: the merge
+ * before any stream capture.  A call on a stream that is being captured, on a
+ * device where no earlier call has looked the address up, returns FA_ERR_CUDA
+ * with nothing enqueued and the capture left intact.  All calls share the one array: the merge
  * writes every scratch record before reading it, so leftovers from an
  * earlier call never leak into a result, but calls whose kernels overlap on
  * the GPU (different streams without ordering between them) race on the
