@@ -26,13 +26,13 @@ __all__ = [
     "fa_adamw_step_staged", "fa_stats_plan",
     "fa_stats_rows",
     "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",
-    "fa_read_report", "fa_clip_decision", "fa_stats_chunk_scratch",
+    "fa_read_report", "fa_stats_sum_sq", "fa_clip_decision", "fa_stats_chunk_scratch",
     "fa_merge_gradient_stats_chunks", "fa_bucket_step_segment_scaled",
     "fa_bucket_step_clipped_per_segment", "fa_bucket_step_per_segment_gated",
     "fa_bucket_step_clipped_per_segment_gated", "segment_rows",
     "fa_clip_decide", "fa_bucket_step_clipped", "fa_bucket_step_gated",
     "fa_bucket_step_writeback_gated",
-    "fa_bucket_step_clipped_gated", "options", "control", "stats_buffer",
+    "fa_bucket_step_clipped_gated", "report_mailbox", "options", "control", "stats_buffer",
     "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
 ]
 
@@ -160,6 +160,13 @@ def fa_stats_rows(n: int, row_len: int, seg_offsets: Optional[Sequence[int]] = N
     r = ctypes.c_int64()
     check("fa_stats_rows", _L().fa_stats_rows(n, row_len, seg, nseg, ctypes.byref(r)))
     return r.value
+
+
+def fa_stats_sum_sq(record: FaStats) -> float:
+    """The sum of squares a 12-byte record stands for (either of its two forms)."""
+    out = ctypes.c_double()
+    check("fa_stats_sum_sq", _L().fa_stats_sum_sq(ctypes.byref(record), ctypes.byref(out)))
+    return out.value
 
 
 def fa_clip_decision(sum_sq_stored: float, nonfinite: int, gradient_scale: float,
@@ -328,11 +335,22 @@ def fa_bucket_step_writeback_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: 
         _TORCH_GRAD[p_model.dtype], _stream(stream)))
 
 
+def report_mailbox() -> torch.Tensor:
+    """A report mailbox (fa_report_mailbox: the 12-byte report and a sequence word) in
+    pinned host memory, as int32 [4]; one per caller thread, reused across calls."""
+    return torch.zeros(4, dtype=torch.int32).pin_memory()
+
+
 def fa_bucket_step_clipped_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
                                  ctl: FaStepControl, max_grad_norm: float, row_len: int,
                                  rows_buf: torch.Tensor, scratch: Optional[torch.Tensor],
-                                 report: torch.Tensor, stream=None) -> tuple[int, FaStepReport]:
-    """The statistics-guarded step with the update gated on the device.  Returns (t, report)."""
+                                 report: torch.Tensor, mailbox: torch.Tensor,
+                                 stream=None) -> tuple[int, FaStepReport]:
+    """The statistics-guarded step with the update gated on the device; the report
+    comes back through ``mailbox`` (see ``report_mailbox``).  Returns (t, report)."""
+    if (not isinstance(mailbox, torch.Tensor) or mailbox.device.type != "cpu"
+            or mailbox.nbytes < 16 or not mailbox.is_contiguous() or not mailbox.is_pinned()):
+        raise ValueError("mailbox: expected a pinned, contiguous host tensor of 16 bytes")
     n = p.numel()
     _dense("p", p, n, (torch.float32,))
     _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
@@ -349,7 +367,7 @@ def fa_bucket_step_clipped_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: Fa
         seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
         ctypes.byref(tt), ctypes.byref(opts), ctl, max_grad_norm, row_len, _ptr(rows_buf),
         rows_buf.shape[0], _ptr(scratch), 0 if scratch is None else scratch.numel(),
-        _ptr(report), ctypes.byref(rep), _stream(stream)))
+        _ptr(report), _ptr(mailbox), ctypes.byref(rep), _stream(stream)))
     return tt.value, rep
 
 

@@ -50,6 +50,7 @@ PF64 = ctypes.POINTER(c_f64)
 # name -> (restype, argtypes)
 SIGNATURES = {
     "fa_abi_version": (c_i32, []),
+    "fa_stats_sum_sq": (c_i32, [ctypes.POINTER(FaStats), PF64]),
     "fa_status_string": (ctypes.c_char_p, [c_i32]),
     "fa_options_default": (FaOptions, []),
     "fa_device_error": (c_i32, [PI32, c_i32]),
@@ -76,7 +77,7 @@ SIGNATURES = {
                                                c_f64, P, c_i32, P]),
     "fa_bucket_step_clipped_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
                                              ctypes.POINTER(FaOptions), FaStepControl, c_f64,
-                                             c_i32, P, c_i64, P, c_i64, P,
+                                             c_i32, P, c_i64, P, c_i64, P, P,
                                              ctypes.POINTER(FaStepReport), P]),
     "fa_stats_plan": (c_i32, [c_i64, PI32, PI64]),
     "fa_stats_rows": (c_i32, [c_i64, c_i32, PI64, c_i32, PI64]),

@@ -14,11 +14,13 @@
 //   "训练与状态保存" (zh/docs/training): "在 ruda:0 上进行原生 PyTorch 训练" (12-byte
 //     report read back first, non-finite skip, global clip after unscale).
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <thread>
 #include <utility>
 #include <vector>
 
@@ -338,11 +340,41 @@ fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float
     return FA_OK;
 }
 
+// Enqueues the merge levels of ``rows`` records (``kernels`` of them, from the plan)
+// into ``report``; intermediate records go to ``scratch``.  The level that writes the
+// report also posts it to ``post`` (device address of a host mailbox) when given.
+fa_status enqueue_merge_levels(const fa_stats *rows_in, int64_t rows, int32_t kernels,
+                               float *scratch, fa_stats *report, fa_report_mailbox *post,
+                               uint32_t seq, cudaStream_t stream) {
+    const fa_stats *in = rows_in;
+    int64_t count = rows;
+    fa_stats *next = reinterpret_cast<fa_stats *>(scratch);
+    for (int32_t level = 0; level < kernels; ++level) {
+        const int64_t out_count = (count + fa::kFanIn - 1) / fa::kFanIn;
+        const bool last = out_count == 1;
+        fa_stats *out = last ? report : next;
+        if (fa::launch_merge(in, count, out, stream, last ? post : nullptr, seq) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_CUDA;
+        }
+        in = out;
+        count = out_count;
+        next = out + out_count;
+    }
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
 int32_t fa_abi_version(void) { return FA_ABI_VERSION; }
+
+fa_status fa_stats_sum_sq(const fa_stats *record, double *sum_sq) {
+    if (!record || !sum_sq) return FA_ERR_NULL;
+    *sum_sq = fa::record_sum_sq(*record);
+    return FA_OK;
+}
 
 const char *fa_status_string(fa_status s) {
     switch (s) {
@@ -693,30 +725,49 @@ fa_status fa_bucket_step_writeback_gated(const int64_t *seg_offsets, int32_t nse
 
 namespace {
 
-// Per host thread: a pinned staging record for report read-backs that must not
-// block the stream, and an event marking its arrival (per device).
-struct ReadbackSlot {
-    fa_stats *pinned = nullptr;
-    cudaEvent_t event[64] = {};
-};
-
-fa_status readback_slot(int dev, ReadbackSlot **out) {
-    thread_local ReadbackSlot slot;
-    if (dev < 0 || dev >= 64) return FA_ERR_POINTER;
-    if (!slot.pinned) {
-        void *ptr = nullptr;
-        if (cudaHostAlloc(&ptr, 64, cudaHostAllocPortable) != cudaSuccess) {
-            cudaGetLastError();
-            return FA_ERR_CUDA;
-        }
-        slot.pinned = static_cast<fa_stats *>(ptr);
-    }
-    if (!slot.event[dev] &&
-        cudaEventCreateWithFlags(&slot.event[dev], cudaEventDisableTiming) != cudaSuccess) {
+// The device address of a caller's report mailbox: pinned host memory that the
+// device can write (cudaHostAlloc, or registered and mapped, with unified
+// addressing).  Pageable or device memory: FA_ERR_POINTER.
+fa_status mailbox_device_ptr(fa_report_mailbox *mailbox, fa_report_mailbox **dev_ptr) {
+    if (!mailbox) return FA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(mailbox) % 4) return FA_ERR_ALIGN;
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, mailbox) != cudaSuccess) {
         cudaGetLastError();
-        return FA_ERR_CUDA;
+        return FA_ERR_POINTER;
     }
-    *out = &slot;
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return FA_ERR_POINTER;
+    *dev_ptr = static_cast<fa_report_mailbox *>(attr.devicePointer);
+    return FA_OK;
+}
+
+// Waits until the device has posted report ``seq`` to the mailbox, then copies the
+// report out.  The wait ends early with FA_ERR_CUDA when the stream reports an
+// error, or when the stream has finished without the report having been posted;
+// and in any case after five minutes.
+fa_status wait_for_post(const fa_report_mailbox *mailbox, uint32_t seq, cudaStream_t stream,
+                        fa_stats *out) {
+    const uint32_t *seq_word = &mailbox->seq;
+    const auto deadline = std::chrono::steady_clock::now() + std::chrono::minutes(5);
+    for (uint64_t it = 0;; ++it) {
+        if (__atomic_load_n(seq_word, __ATOMIC_ACQUIRE) == seq) break;
+        if (it % 4096 == 4095) {  // now and then: is the stream still able to post it?
+            const cudaError_t q = cudaStreamQuery(stream);
+            if (q != cudaSuccess && q != cudaErrorNotReady) {
+                cudaGetLastError();
+                return FA_ERR_CUDA;
+            }
+            if (q == cudaSuccess && __atomic_load_n(seq_word, __ATOMIC_ACQUIRE) != seq)
+                return FA_ERR_CUDA;  // all work done and nothing posted
+            if (std::chrono::steady_clock::now() > deadline) return FA_ERR_CUDA;
+        }
+        if (it > 256) std::this_thread::yield();
+    }
+    const volatile uint32_t *w = reinterpret_cast<const volatile uint32_t *>(&mailbox->report);
+    const uint32_t words[3] = {w[0], w[1], w[2]};
+    std::memcpy(&out->sum_sq, &words[0], 4);
+    out->nonfinite = words[1];
+    std::memcpy(&out->sum_sq_lo, &words[2], 4);
     return FA_OK;
 }
 
@@ -729,7 +780,8 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
                                        int32_t row_len, fa_stats *rows_buf,
                                        int64_t rows_capacity, float *scratch,
                                        int64_t scratch_elements, fa_stats *report_dev,
-                                       fa_step_report *out, void *stream) {
+                                       fa_report_mailbox *mailbox, fa_step_report *out,
+                                       void *stream) {
     TraceRange trace("fa_bucket_step_clipped_gated");
     fa_status st;
     if (!t || !out) return FA_ERR_NULL;
@@ -757,36 +809,31 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
                        {rows_buf, static_cast<size_t>(rows) * 12},
                        {scratch, static_cast<size_t>(need) * 4}, {report_dev, 12}};
     if (any_overlap(r, 8)) return FA_ERR_ALIAS;
-    ReadbackSlot *slot = nullptr;
-    if ((st = readback_slot(dev, &slot)) != FA_OK) return st;
+    if (need > 0 && (st = check_device_ptr(scratch, dev, 4)) != FA_OK) return st;
+    if ((st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
+    fa_report_mailbox *post = nullptr;
+    if ((st = mailbox_device_ptr(mailbox, &post)) != FA_OK) return st;
+    const uint32_t seq = __atomic_load_n(&mailbox->seq, __ATOMIC_ACQUIRE) + 1;
 
     if ((st = fa_analyze_gradient(g, gdt, n_total, row_len, seg_offsets, nseg, rows_buf,
                                   rows_capacity, stream)) != FA_OK)
         return st;
-    if ((st = fa_merge_gradient_stats(rows_buf, rows, scratch, scratch_elements, report_dev,
-                                      stream)) != FA_OK)
+    // the merge that writes the report also posts it to the mailbox; no stream
+    // operation sits between it and the update, which starts as its dependent
+    if ((st = enqueue_merge_levels(rows_buf, rows, kernels, scratch, report_dev, post, seq,
+                                   static_cast<cudaStream_t>(stream))) != FA_OK)
         return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(slot->pinned, report_dev, sizeof(fa_stats), cudaMemcpyDeviceToHost, s) !=
-            cudaSuccess ||
-        cudaEventRecord(slot->event[dev], s) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-    }
-    // the update follows in stream order and decides on the device
     if ((st = enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, *t + 1,
                              ctl.gradient_scale, 1.0, stream, nullptr, fa::kNoModel, report_dev,
                              max_grad_norm)) != FA_OK)
         return st;
     // meanwhile the host reads the same report and takes the same decision
-    if (cudaEventSynchronize(slot->event[dev]) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-    }
-    const fa_stats h = *slot->pinned;
+    fa_stats h{};
+    if ((st = wait_for_post(mailbox, seq, static_cast<cudaStream_t>(stream), &h)) != FA_OK)
+        return st;
     int32_t skip = 0;
     double norm = 0, coef = 1;
-    const double sum = static_cast<double>(h.sum_sq) + static_cast<double>(h.sum_sq_lo);
+    const double sum = fa::record_sum_sq(h);
     if ((st = fa_clip_decision(sum, h.nonfinite, ctl.gradient_scale, max_grad_norm, &skip, &norm,
                                &coef)) != FA_OK)
         return st;
@@ -906,20 +953,8 @@ fa_status fa_merge_gradient_stats(const fa_stats *rows_in, int64_t rows, float *
                        {scratch, static_cast<size_t>(need) * 4},
                        {report, 12}};
     if (any_overlap(r, 3)) return FA_ERR_ALIAS;
-
-    const fa_stats *in = rows_in;
-    int64_t count = rows;
-    fa_stats *next = reinterpret_cast<fa_stats *>(scratch);
-    for (int32_t level = 0; level < kernels; ++level) {
-        const int64_t out_count = (count + fa::kFanIn - 1) / fa::kFanIn;
-        fa_stats *out = out_count == 1 ? report : next;
-        cudaError_t err = fa::launch_merge(in, count, out, static_cast<cudaStream_t>(stream));
-        if (err != cudaSuccess) return FA_ERR_CUDA;
-        in = out;
-        count = out_count;
-        next = out + out_count;
-    }
-    return FA_OK;
+    return enqueue_merge_levels(rows_in, rows, kernels, scratch, report, nullptr, 0,
+                                static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
@@ -951,20 +986,8 @@ fa_status fa_merge_gradient_stats_static(const fa_stats *rows_in, int64_t rows,
         return FA_ERR_CUDA;
     }
     if (need > capacity) return FA_ERR_SIZE;
-
-    const fa_stats *in = rows_in;
-    int64_t count = rows;
-    fa_stats *next = reinterpret_cast<fa_stats *>(scratch);
-    for (int32_t level = 0; level < kernels; ++level) {
-        const int64_t out_count = (count + fa::kFanIn - 1) / fa::kFanIn;
-        fa_stats *out = out_count == 1 ? report : next;
-        cudaError_t err = fa::launch_merge(in, count, out, static_cast<cudaStream_t>(stream));
-        if (err != cudaSuccess) return FA_ERR_CUDA;
-        in = out;
-        count = out_count;
-        next = out + out_count;
-    }
-    return FA_OK;
+    return enqueue_merge_levels(rows_in, rows, kernels, scratch, report, nullptr, 0,
+                                static_cast<cudaStream_t>(stream));
 }
 
 // ---- per-chunk (per-parameter) statistics and clipping ------------------------
@@ -1106,7 +1129,7 @@ fa_status fa_bucket_step_clipped_per_segment(
     double total = 0.0, min_coef = 1.0;
     uint64_t bad = 0;
     for (int32_t k = 0; k < nseg; ++k) {
-        const double sum = static_cast<double>(host[k].sum_sq) + static_cast<double>(host[k].sum_sq_lo);
+        const double sum = fa::record_sum_sq(host[k]);
         int32_t skip = 0;
         double norm = 0.0;
         if ((st = fa_clip_decision(sum, host[k].nonfinite, ctl.gradient_scale, max_grad_norm, &skip,
@@ -1242,7 +1265,7 @@ fa_status fa_clip_decide(const fa_stats *report_dev, double gradient_scale, doub
     fa_stats h;
     fa_status st = fa_read_report(report_dev, &h, stream);
     if (st != FA_OK) return st;
-    const double sum = static_cast<double>(h.sum_sq) + static_cast<double>(h.sum_sq_lo);
+    const double sum = fa::record_sum_sq(h);
     return fa_clip_decision(sum, h.nonfinite, gradient_scale, max_grad_norm, skip, grad_norm,
                             clip_coef);
 }
@@ -1292,7 +1315,7 @@ fa_status fa_bucket_step_clipped(const int64_t *seg_offsets, int32_t nseg, int64
     if ((st = fa_read_report(report_dev, &h, stream)) != FA_OK) return st;
     int32_t skip = 0;
     double norm = 0, coef = 1;
-    const double sum = static_cast<double>(h.sum_sq) + static_cast<double>(h.sum_sq_lo);
+    const double sum = fa::record_sum_sq(h);
     if ((st = fa_clip_decision(sum, h.nonfinite, ctl.gradient_scale, max_grad_norm, &skip, &norm,
                                &coef)) != FA_OK)
         return st;

@@ -77,6 +77,22 @@ constexpr int kFanIn = 1024;             // merge fan-in
 constexpr int64_t kMaxRows = 4194304;    // largest statistics plan
 constexpr int kMaxSegPerLaunch = 240;    // segment table entries carried in kernel parameters
 
+// The sum of squares a statistics record stands for.  A row whose FP32 sum of
+// squares overflows while it holds no NaN or +-Inf (a finite value above about
+// 1.8e19 squares past FP32's range) is summed again with every value multiplied
+// by 2^-96 first, so its record carries the sum times 2^-192; such a record, and
+// every merge that takes one in, is stored negated, its sign marking the form:
+//   sum_sq >= 0:  sum = sum_sq + sum_sq_lo
+//   sum_sq <  0:  sum = -(sum_sq + sum_sq_lo) * 2^192
+// (an exact power-of-two scaling, so the decoded FP64 value has the precision of
+// the stored one).  The host decision and the device-side gates decode with this
+// one function: the same FP64 operations in the same order.
+constexpr int kRescueValueExp = 96;  // values of a rescued row are multiplied by 2^-96
+__host__ __device__ inline double record_sum_sq(const fa_stats &r) {
+    const double s = static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
+    return r.sum_sq < 0.0f ? -s * 0x1p192 : s;
+}
+
 // FP32 coefficients of one update, computed on the host in FP64.
 struct Coef {
     float b1, omb1, b2, omb2;
@@ -183,7 +199,10 @@ cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, f
                                          cudaStream_t stream);
 
 // One merge level: ceil(count / kFanIn) output records from count input records.
-cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream);
+// ``post`` (device address of a pinned host mailbox, final level only) also receives
+// the single output record, followed by ``seq``.
+cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream,
+                         fa_report_mailbox *post = nullptr, uint32_t seq = 0);
 
 // Device address and size of the library's fixed merge scratch on ``device``
 // (which must be the current device).  Looked up once per device; with

@@ -13,6 +13,15 @@
 // below 1e-6.  Merges add (hi, lo) pairs as double-float values with
 // error-free FP32 transformations and hand each total to the next level as a
 // (hi, lo) pair of floats, so later levels lose nothing.
+//
+// Finite values whose squares leave FP32's range: a row whose FP32 sum comes
+// out non-finite while it holds no NaN or +-Inf is summed again with every
+// value multiplied by 2^-96 (squares by 2^-192: a square of any FP32 value is
+// then at most 2^64), and its record stores that sum negated.  A merge works in
+// the scaled domain as soon as one of its inputs is scaled or a partial sum
+// reaches 2^126 (below that two partial sums cannot overflow), and then
+// multiplies unscaled inputs by 2^-192 as it takes them in; its output is
+// negated in turn.  record_sum_sq (internal.h) decodes both forms.
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -51,6 +60,9 @@ struct StatIO<FA_F32> {
     static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
         acc1(__ldcs(reinterpret_cast<const unsigned int *>(g) + i), s, c);
     }
+    static __device__ __forceinline__ float load1(const void *g, int64_t i) {
+        return __uint_as_float(__ldcs(reinterpret_cast<const unsigned int *>(g) + i));
+    }
     static __device__ __forceinline__ void acc16(const uint4 &r, float &s, uint32_t &c) {
         acc1(r.x, s, c); acc1(r.y, s, c); acc1(r.z, s, c); acc1(r.w, s, c);
     }
@@ -75,6 +87,10 @@ struct StatIO<FA_BF16> {
     }
     static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
         acc1(__ldcs(static_cast<const unsigned short *>(g) + i), s, c);
+    }
+    static __device__ __forceinline__ float load1(const void *g, int64_t i) {
+        return __uint_as_float(static_cast<uint32_t>(__ldcs(static_cast<const unsigned short *>(g) + i))
+                               << 16);
     }
     static __device__ __forceinline__ void acc16(const uint4 &r, float &s, uint32_t &c) {
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
@@ -106,6 +122,9 @@ struct StatIO<FA_F16> {
     static __device__ __forceinline__ void accs(const void *g, int64_t i, float &s, uint32_t &c) {
         acc1(__ldcs(static_cast<const unsigned short *>(g) + i), s, c);
     }
+    static __device__ __forceinline__ float load1(const void *g, int64_t i) {
+        return __half2float(__ushort_as_half(__ldcs(static_cast<const unsigned short *>(g) + i)));
+    }
     static __device__ __forceinline__ void acc16(const uint4 &r, float &s, uint32_t &c) {
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -115,6 +134,10 @@ struct StatIO<FA_F16> {
         }
     }
 };
+
+// Values of a rescued row are multiplied by 2^-96 before they are squared.
+constexpr float kRescueScale = 0x1p-96f;
+static_assert(kRescueValueExp == 96, "kRescueScale and record_sum_sq must agree");
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -130,6 +153,23 @@ __device__ __forceinline__ int find_segment(const AnalyzeArgs &a, int64_t r) {
         if (a.row_start[mid] <= r) lo = mid; else hi = mid - 1;
     }
     return lo;
+}
+
+// Scaled sum of squares of elements [start, end) of one row, lane-strided and
+// summed over the warp: values multiplied by 2^-96 before squaring (the
+// rescue of a row whose FP32 sum overflowed without any NaN or +-Inf).  Every
+// lane of the warp calls it; rare, so it simply reads the row again.
+template <int GT>
+__device__ __noinline__ float rescued_row_sum(const void *g, int64_t start, int64_t end, int64_t n,
+                                              int lane) {
+    float s = 0.f;
+    for (int64_t i = start + lane; i < end; i += 32) {
+        if (fa_in_bounds(i, 1, n)) {
+            const float x = StatIO<GT>::load1(g, i) * kRescueScale;
+            s = fmaf(x, x, s);
+        }
+    }
+    return warp_sum(s);
 }
 
 // One warp per row, kRowsPerWarp rows in flight per warp.  Lane l reads
@@ -168,9 +208,16 @@ analyze_kernel(const __grid_constant__ AnalyzeArgs a) {
         }
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) {
-            const float tot = warp_sum(s[j]);
+            float tot = warp_sum(s[j]);
             const uint32_t cnt = __reduce_add_sync(0xffffffffu, c[j]);
             const int64_t r = r0 + j;
+            if (!isfinite(tot) && cnt == 0 && r < a.rows) {  // (warp-uniform)
+                const int k = a.nseg == 1 ? 0 : find_segment(a, r);
+                const int64_t start = a.seg_start[k] + (r - a.row_start[k]) * a.row_len;
+                const int64_t seg_end = a.seg_start[k + 1];
+                const int64_t end = start + a.row_len < seg_end ? start + a.row_len : seg_end;
+                tot = -rescued_row_sum<GT>(a.g, start, end, a.n, lane);
+            }
             if (lane == j && r < a.rows && fa_in_bounds(r, 1, a.rows)) {
                 fa_stats rec;
                 rec.sum_sq = tot;
@@ -182,22 +229,32 @@ analyze_kernel(const __grid_constant__ AnalyzeArgs a) {
     }
 }
 
-// Squares of one 16-byte word, added unconditionally (no finiteness test).
-template <int GT>
+// Squares of one 16-byte word, added unconditionally (no finiteness test);
+// RESCUE: each value multiplied by 2^-96 first.
+template <int GT, bool RESCUE = false>
 __device__ __forceinline__ void sq16(const uint4 &r, float &s) {
+    const float k = RESCUE ? kRescueScale : 1.0f;
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int q = 0; q < 4; ++q) {
         if (GT == FA_F32) {
-            const float x = __uint_as_float(w[k]);
+            const float x = RESCUE ? __uint_as_float(w[q]) * k : __uint_as_float(w[q]);
             s = fmaf(x, x, s);
         } else if (GT == FA_BF16) {
-            const float lo = __uint_as_float(w[k] << 16);
-            const float hi = __uint_as_float(w[k] & 0xffff0000u);
+            float lo = __uint_as_float(w[q] << 16);
+            float hi = __uint_as_float(w[q] & 0xffff0000u);
+            if (RESCUE) {
+                lo *= k;
+                hi *= k;
+            }
             s = fmaf(lo, lo, s);
             s = fmaf(hi, hi, s);
         } else {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[q]));
+            if (RESCUE) {
+                f.x *= k;
+                f.y *= k;
+            }
             s = fmaf(f.x, f.x, s);
             s = fmaf(f.y, f.y, s);
         }
@@ -331,6 +388,13 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
                     for (int ch = 0; ch < CH; ++ch) c += count_nonfinite16<GT>(buf[j][ch]);
                     c = __reduce_add_sync(0xffffffffu, c);
                     if (my_row == j) cnt = c;
+                    if (c == 0) {  // finite values whose squares overflowed: rescue
+                        float sr = 0.f;
+#pragma unroll
+                        for (int ch = 0; ch < CH; ++ch) sq16<GT, true>(buf[j][ch], sr);
+                        sr = warp_sum(sr);
+                        if (my_row == j) tot = -sr;
+                    }
                 }
             }
         }
@@ -349,6 +413,8 @@ analyze_fast_kernel(const __grid_constant__ AnalyzeArgs a) {
                     if (fa_in_bounds(i, 1, a.n)) StatIO<GT>::accs(a.g, i, sj, c);
                 sj = warp_sum(sj);
                 c = __reduce_add_sync(0xffffffffu, c);
+                if (!isfinite(sj) && c == 0)  // (warp-uniform) rescue
+                    sj = -rescued_row_sum<GT>(a.g, start, end, a.n, lane);
                 if (my_row == j) {
                     tot = sj;
                     cnt = c;
@@ -381,19 +447,41 @@ __device__ __forceinline__ void df_add(float &h, float &l, float bh, float bl) {
     two_sum(s, e, h, l);
 }
 
-// One warp reduces records [lo, hi) into *out.  Lane l adds records l, l + 32, ...
-// as double-float values (an FP32 value and its FP32 residual, combined with
-// error-free TwoSum, so every operation stays on the FP32 units: GB300's FP64
-// rate made an FP64 first level compute-bound), 16 records' loads issued
-// together; then the warp's shuffle tree, and lane 0 writes the total as an FP32
-// (hi, lo) pair.  Every lane of the warp calls it.
-__device__ __forceinline__ void warp_merge(const fa_stats *__restrict__ in, int64_t lo, int64_t hi,
-                                           int64_t in_count, fa_stats *__restrict__ out) {
-    constexpr int kBatch = 16;
-    const int lane = threadIdx.x & 31;
-    if (!fa_in_bounds(lo, hi - lo, in_count)) hi = lo;  // (bounds-checked build only)
-    float sh = 0.f, sl = 0.f;
-    unsigned long long c = 0;
+// Partial sums at or above this switch a merge to the scaled domain: two
+// unscaled partial sums below it add up to less than 2^127, which cannot overflow.
+constexpr float kScaleSwitch = 0x1p126f;
+
+// Multiplies a double-float by 2^-192 (two exact power-of-two steps; only values
+// that fall below FP32's normal range lose bits, and those are negligible next
+// to the sum that caused the switch, which is at least 2^-66 after scaling).
+__device__ __forceinline__ void df_scale_down(float &h, float &l) {
+    h = h * kRescueScale * kRescueScale;
+    l = l * kRescueScale * kRescueScale;
+}
+
+// Adds (bh, bl) -- scaled when bs -- into the double-float (h, l) -- scaled when
+// *hs -- moving the accumulator to the scaled domain first when either side is
+// scaled or either partial sum has reached kScaleSwitch.
+__device__ __forceinline__ void df_add_domain(float &h, float &l, bool &hs, float bh, float bl,
+                                              bool bs) {
+    const bool scaled = hs || bs || h >= kScaleSwitch || bh >= kScaleSwitch;
+    if (scaled && !hs) df_scale_down(h, l);
+    if (scaled && !bs) df_scale_down(bh, bl);
+    hs = scaled;
+    df_add(h, l, bh, bl);
+}
+
+// Lane sums below this let a warp's 32-lane shuffle tree stay below kScaleSwitch.
+constexpr float kWarpTreeLimit = 0x1p121f;
+
+// Adds records [lo + lane, hi) with stride 32 into (sh, sl): plain records with plain
+// double-float additions, marking in *special any record that is scaled, at or above
+// kScaleSwitch, or NaN; or (DOMAIN) with the domain-aware addition, tracking *ss.
+template <bool DOMAIN>
+__device__ __forceinline__ void lane_merge(const fa_stats *__restrict__ in, int64_t lo, int64_t hi,
+                                           int lane, float &sh, float &sl, bool &ss,
+                                           bool &special, unsigned long long &c) {
+    constexpr int kBatch = DOMAIN ? 4 : 16;  // (the rare path: fewer registers)
     for (int64_t base = lo + lane; base < hi; base += 32 * kBatch) {
         fa_stats r[kBatch];
 #pragma unroll
@@ -405,23 +493,68 @@ __device__ __forceinline__ void warp_merge(const fa_stats *__restrict__ in, int6
         for (int u = 0; u < kBatch; ++u) {
             const int64_t i = base + static_cast<int64_t>(u) * 32;
             if (i < hi) {
-                df_add(sh, sl, r[u].sum_sq, r[u].sum_sq_lo);
-                c += r[u].nonfinite;
+                if (DOMAIN) {
+                    const bool rs = r[u].sum_sq < 0.f;
+                    df_add_domain(sh, sl, ss, rs ? -r[u].sum_sq : r[u].sum_sq,
+                                  rs ? -r[u].sum_sq_lo : r[u].sum_sq_lo, rs);
+                } else {
+                    special |= !(r[u].sum_sq >= 0.f && r[u].sum_sq < kScaleSwitch);
+                    df_add(sh, sl, r[u].sum_sq, r[u].sum_sq_lo);
+                    c += r[u].nonfinite;
+                }
             }
         }
     }
+}
+
+// One warp reduces records [lo, hi) into *out.  Lane l adds records l, l + 32, ...
+// as double-float values (an FP32 value and its FP32 residual, combined with
+// error-free TwoSum, so every operation stays on the FP32 units: GB300's FP64
+// rate made an FP64 first level compute-bound), 16 records' loads issued
+// together; then the warp's shuffle tree, and lane 0 writes the total as an FP32
+// (hi, lo) pair.  When a lane met a scaled record, a record at or above
+// kScaleSwitch or a NaN, or holds a sum that could overflow the tree, the warp
+// adds its records again with the domain-aware addition (rare: it needs a finite
+// value above about 1.8e19 in the gradient), and the total is negated when it is
+// in the scaled domain.  Every lane of the warp calls it.
+__device__ __forceinline__ void warp_merge(const fa_stats *__restrict__ in, int64_t lo, int64_t hi,
+                                           int64_t in_count, fa_stats *__restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    if (!fa_in_bounds(lo, hi - lo, in_count)) hi = lo;  // (bounds-checked build only)
+    float sh = 0.f, sl = 0.f;
+    bool ss = false;       // (sh, sl) in the scaled domain
+    bool special = false;  // this lane's records need the domain-aware addition
+    unsigned long long c = 0;
+    lane_merge<false>(in, lo, hi, lane, sh, sl, ss, special, c);
+    if (__any_sync(0xffffffffu, special || !(sh < kWarpTreeLimit))) {
+        sh = sl = 0.f;
+        lane_merge<true>(in, lo, hi, lane, sh, sl, ss, special, c);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
-        const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
-        df_add(sh, sl, oh, ol);
-        c += __shfl_xor_sync(0xffffffffu, c, o);
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
+            const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
+            const bool os = __shfl_xor_sync(0xffffffffu, static_cast<int>(ss), o) != 0;
+            df_add_domain(sh, sl, ss, oh, ol, os);
+        }
+    } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
+            const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
+            df_add(sh, sl, oh, ol);
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     if (lane == 0) {
         const double ts = static_cast<double>(sh) + static_cast<double>(sl);
         fa_stats rec;
         rec.sum_sq = static_cast<float>(ts);
         rec.sum_sq_lo = static_cast<float>(ts - static_cast<double>(rec.sum_sq));
+        if (ss) {
+            rec.sum_sq = -rec.sum_sq;
+            rec.sum_sq_lo = -rec.sum_sq_lo;
+        }
         rec.nonfinite = c > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(c);
         *out = rec;
     }
@@ -432,8 +565,12 @@ constexpr int kMergeWarps = kThreads / 32;  // groups (or chunks) per CTA
 // One warp per group of kFanIn input records, eight groups per CTA, so that the
 // 4096 groups of the largest plan run in a single wave (one CTA per group took
 // three and a half).
+// ``post`` (the final level only; nullptr otherwise) is the device address of a
+// report mailbox in pinned host memory: the report is also stored there, then, after
+// a system-wide fence, ``seq``, so a host that sees seq reads the whole report.
 __global__ void __launch_bounds__(kThreads)
-merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out) {
+merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restrict__ out,
+             fa_report_mailbox *post, uint32_t seq) {
     fa_grid_dependency_wait();  // (launched early: the records are not ready before this)
     fa_allow_dependents();
     const int64_t group = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
@@ -441,6 +578,15 @@ merge_kernel(const fa_stats *__restrict__ in, int64_t count, fa_stats *__restric
     if (lo >= count) return;  // the whole warp
     const int64_t hi = lo + kFanIn < count ? lo + kFanIn : count;
     warp_merge(in, lo, hi, count, out + group);
+    if (post != nullptr && group == 0 && (threadIdx.x & 31) == 0) {
+        const fa_stats rec = out[0];  // written by this thread just above
+        volatile uint32_t *w = reinterpret_cast<volatile uint32_t *>(&post->report);
+        w[0] = __float_as_uint(rec.sum_sq);
+        w[1] = rec.nonfinite;
+        w[2] = __float_as_uint(rec.sum_sq_lo);
+        __threadfence_system();
+        *reinterpret_cast<volatile uint32_t *>(&post->seq) = seq;
+    }
 }
 
 // Per-chunk merge, level A: one CTA per group of at most kFanIn records of one
@@ -563,13 +709,15 @@ cudaError_t launch_merge_chunks(const ChunkMergeArgs &a, cudaStream_t stream) {
     return cudaSuccess;
 }
 
-cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream) {
+cudaError_t launch_merge(const fa_stats *in, int64_t count, fa_stats *out, cudaStream_t stream,
+                         fa_report_mailbox *post, uint32_t seq) {
     const int64_t groups = (count + kFanIn - 1) / kFanIn;
     const int64_t grid = (groups + kMergeWarps - 1) / kMergeWarps;
     if (grid <= 0) return cudaSuccess;
+    if (post != nullptr && groups != 1) return cudaErrorInvalidValue;  // final level only
     // starts early and waits for its input in the kernel
     return launch_dependent(merge_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
-                            stream, in, count, out);
+                            stream, in, count, out, post, seq);
 }
 
 // ---- fixed merge scratch for callers that cannot allocate ------------------------

@@ -180,7 +180,7 @@ __device__ __forceinline__ void adamw_element(const Coef &c, float x, float &p, 
 __device__ __forceinline__ bool gate_decision(const UpdateArgs &a, float *gmul) {
     const fa_stats r = *a.gate;
     if (r.nonfinite > 0) return false;
-    const double sum = static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
+    const double sum = record_sum_sq(r);
     const double norm = sqrt(sum) / a.gate_scale;
     double coef = 1.0;
     if (a.gate_max_norm > 0 && norm > a.gate_max_norm) coef = a.gate_max_norm / norm;
@@ -388,7 +388,7 @@ __device__ __forceinline__ bool segment_multipliers(const SegScaleArgs &s, float
     if (__syncthreads_or(bad)) return false;
     for (int j = threadIdx.x; j < s.nseg; j += blockDim.x) {
         const fa_stats r = s.reports[s.k0 + j];
-        const double sum = static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
+        const double sum = record_sum_sq(r);
         const double norm = sqrt(sum) / s.a.gate_scale;
         double coef = 1.0;
         if (s.a.gate_max_norm > 0 && norm > s.a.gate_max_norm) coef = s.a.gate_max_norm / norm;

@@ -32,6 +32,7 @@ import torch
 
 from . import (FaStats, fa_analyze_gradient, fa_bucket_step, fa_bucket_step_gated,
                fa_bucket_step_writeback, fa_bucket_step_writeback_gated, fa_clip_decision,
+               fa_stats_sum_sq,
                fa_merge_gradient_stats,
                fa_read_report, fa_stats_rows, options, control, scratch_buffer, stats_buffer)
 from . import sharded
@@ -404,7 +405,7 @@ class FusedAdamW(torch.optim.Optimizer):
                 launched.append((b, i, j))
         self._report_event.synchronize()
         rep = FaStats.from_buffer_copy(self._pinned_report.numpy().tobytes())
-        total = float(rep.sum_sq) + float(rep.sum_sq_lo)
+        total = fa_stats_sum_sq(rep)
         skip, norm, coef = fa_clip_decision(total, int(rep.nonfinite), gradient_scale, max_norm)
         if not skip:
             for b, i, j in launched:

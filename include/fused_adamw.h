@@ -23,13 +23,12 @@
  *     failure discard them.
  *   - Validation happens before anything is enqueued or written; on any
  *     error no output (host or device) is modified ([FA-ja] "低レベルの使用").
- *   - The library never allocates device memory: buffers (outputs, row
- *     statistics, scratch, report) belong to the caller.  Its only state is
+ *   - The library allocates nothing, on the device or pinned on the host, and
+ *     creates no stream or event: buffers (outputs, row statistics, scratch,
+ *     report, the report mailbox) belong to the caller.  Its only state is
  *     caches of device properties, a device flag for the update pipeline's
- *     bounded waits (fa_device_error), one fixed merge scratch array
- *     (fa_merge_gradient_stats_static) and, per host thread that calls
- *     fa_bucket_step_clipped_gated, a 64-byte pinned host staging record and
- *     one event per device, allocated on first use and kept until exit.
+ *     bounded waits (fa_device_error) and one fixed merge scratch array
+ *     (fa_merge_gradient_stats_static), all part of the loaded library.
  *   - A stream that is being captured into a CUDA graph is accepted without
  *     the device check (CUDA cannot report a capturing stream's device).
  *     fa_analyze_gradient and fa_merge_gradient_stats (and the chunk merge) may
@@ -95,15 +94,33 @@ typedef struct fa_step_control {
 /* 12-byte statistics record ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": a 12-byte
  * report).  Row records, intermediate merge records and the final report all
  * use it.  nonfinite counts stored NaN and +-Inf values exactly (saturating
- * at 2^32-1).  When nonfinite == 0, sum_sq + sum_sq_lo (added in FP64) is the
- * sum of squares of the STORED (still scaled) gradient values; when
- * nonfinite > 0 the sum is unspecified (it may be Inf or NaN) -- the step is
- * skipped then and the sum is never used. */
+ * at 2^32-1).  When nonfinite == 0 the record holds the sum of squares of the
+ * STORED (still scaled) gradient values in one of two forms:
+ *   sum_sq >= 0: the sum is sum_sq + sum_sq_lo (added in FP64);
+ *   sum_sq <  0: the sum is -(sum_sq + sum_sq_lo) * 2^192 -- the form taken
+ *                when the sum would overflow FP32 (a finite value above about
+ *                1.8e19 has a square beyond FP32's range): the values are
+ *                multiplied by 2^-96 before they are squared.
+ * fa_stats_sum_sq decodes either form.  When nonfinite > 0 the sum is
+ * unspecified (it may be Inf or NaN) -- the step is skipped then and the sum
+ * is never used. */
 typedef struct fa_stats {
     float sum_sq;
     uint32_t nonfinite;
     float sum_sq_lo;
 } fa_stats;
+
+/* A report mailbox: 16 bytes of pinned host memory that the device can write
+ * (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped; with unified
+ * addressing every pinned allocation qualifies), 4-byte aligned, owned by the
+ * caller.  The merge that produces a step's final report also stores it here and
+ * then, after a system-wide fence, its sequence number, so that the host can read
+ * the report without a copy or an event on the stream.  One mailbox serves one call
+ * at a time; its initial contents do not matter. */
+typedef struct fa_report_mailbox {
+    fa_stats report;
+    uint32_t seq;
+} fa_report_mailbox;
 
 /* Outcome of a step that ran the statistics path. */
 typedef struct fa_step_report {
@@ -115,6 +132,13 @@ typedef struct fa_step_report {
 } fa_step_report;
 
 /* ---- host-only helpers ---------------------------------------------------- */
+
+/* The sum of squares a statistics record stands for ([TR-zh] "在 ruda:0 上进行原生
+ * PyTorch 训练": the 12-byte report; the pages fix its size, not its encoding):
+ * either form above, in FP64, into *sum_sq -- the value that fa_clip_decision
+ * takes (the total of several ranks' or segments' records is the sum of these).
+ * Host only; FA_ERR_NULL for a NULL pointer. */
+fa_status fa_stats_sum_sq(const fa_stats *record, double *sum_sq);
 
 /* FA_ABI_VERSION of the loaded library, for a caller to check against the
  * header it was built with (library bookkeeping; the pages have no counterpart). */
@@ -307,14 +331,18 @@ fa_status fa_bucket_step_writeback_gated(const int64_t *seg_offsets, int32_t nse
 
 /*
  * fa_bucket_step_clipped with the update gated on the device: the analysis
- * and merge are enqueued, then the 12-byte report's copy into pinned host
- * memory, then the gated update, so the update does not wait for the host.
- * The host waits only for the report, takes the same decision from it
+ * and the merge are enqueued, the merge that writes report_dev also posting the
+ * report to ``mailbox`` (see fa_report_mailbox), then the gated update, which
+ * starts as the merge's programmatic dependent: nothing waits for the host.
+ * The host waits only for the posted report, takes the same decision from it
  * ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": the report is read back and a
  * non-finite gradient skips the whole step) and advances *t unless the step
  * was skipped.  Returns once the report is read; the update may still run
  * (FA_OK means enqueued).  Results are bit-identical to
- * fa_bucket_step_clipped.  Arguments as fa_bucket_step_clipped.
+ * fa_bucket_step_clipped.  The wait for the report gives up with FA_ERR_CUDA
+ * when the stream reports an error or finishes without posting it (and after
+ * five minutes in any case).  mailbox: pageable or device memory is
+ * FA_ERR_POINTER, NULL FA_ERR_NULL.  Other arguments as fa_bucket_step_clipped.
  */
 fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
                                        float *p, const void *g, fa_dtype gdt, float *m, float *v,
@@ -323,7 +351,8 @@ fa_status fa_bucket_step_clipped_gated(const int64_t *seg_offsets, int32_t nseg,
                                        int32_t row_len, fa_stats *rows_buf,
                                        int64_t rows_capacity, float *scratch,
                                        int64_t scratch_elements, fa_stats *report_dev,
-                                       fa_step_report *out, void *stream);
+                                       fa_report_mailbox *mailbox, fa_step_report *out,
+                                       void *stream);
 
 /* ---- gradient statistics -------------------------------------------------- */
 
@@ -512,7 +541,7 @@ fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void
  * Host decision ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": any non-finite gradient
  * skips the whole step; optional global L2 clipping after unscale).
  * sum_sq_stored is the sum of squares of the stored gradient (a report's
- * sum_sq + sum_sq_lo, or the sum of several ranks' reports).  Outputs:
+ * fa_stats_sum_sq, or the sum of several ranks' reports).  Outputs:
  * skip = nonfinite > 0; grad_norm = sqrt(sum_sq_stored)/gradient_scale;
  * clip_coef = max_grad_norm/grad_norm when max_grad_norm > 0 and the norm
  * exceeds it, else 1.  Host only.

@@ -64,7 +64,8 @@ class Workload:
     outlier_per_10000: int = 0          # Bernoulli mask rate, in 1/10000
     outlier_mult: float = 1.0
     skip_calls: tuple[int, ...] = ()    # 1-based call indices with skip_update = true
-    inf_call: Optional[int] = None      # 1-based call whose gradient holds one +Inf
+    inf_call: Optional[int] = None      # 1-based call whose gradient holds one planted value
+    inf_value: float = float("inf")     # the planted value (+Inf, or a large finite one)
     inplace: bool = False
     row_len: int = 0                    # > 0: analyze rows of this length
     max_grad_norm: float = 0.0          # > 0: global L2 clip
@@ -102,7 +103,7 @@ class Workload:
                                   G.stream_key(self.seed, STREAM_OUTLIER, call))
             x = np.where(mask, x * np.float32(self.outlier_mult), x).astype(np.float32)
         if self.inf_call is not None and call == self.inf_call:
-            x = np.where(idx == self.inf_index(), np.float32(np.inf), x).astype(np.float32)
+            x = np.where(idx == self.inf_index(), np.float32(self.inf_value), x).astype(np.float32)
         return x
 
     def grad_host(self, call: int, idx) -> np.ndarray:
@@ -138,7 +139,7 @@ class Workload:
             if self.inf_call is not None and call == self.inf_call:
                 k = self.inf_index()
                 if s <= k < s + c:
-                    x[k - s] = float("inf")
+                    x[k - s] = float(np.float32(self.inf_value))
             if self.grad_dtype == F32:
                 out[s:s + c].copy_(x)
             elif self.grad_dtype == BF16:

@@ -82,6 +82,8 @@ int main(int argc, char **argv) {
     if (scratch_elems > 0) CHECK_CUDA(cudaMalloc((void **)&scratch, (size_t)scratch_elems * 4));
     cudaStream_t stream;
     CHECK_CUDA(cudaStreamCreate(&stream));
+    fa_report_mailbox *mailbox = NULL; /* pinned host memory the device posts the report to */
+    CHECK_CUDA(cudaHostAlloc((void **)&mailbox, sizeof *mailbox, cudaHostAllocDefault));
 
     for (int64_t i = 0; i < n; ++i) h[i] = sample(1u, (uint32_t)i, 0.03125f);
     CHECK_CUDA(cudaMemcpy(p, h, (size_t)n * 4, cudaMemcpyHostToDevice));
@@ -101,8 +103,8 @@ int main(int argc, char **argv) {
         if (gated)
             CHECK_FA(fa_bucket_step_clipped_gated(NULL, 0, n, p, g, FA_F32, m, v, NULL, &t, &o,
                                                   ctl, 0.5, row_len, rows_buf, rows, scratch,
-                                                  scratch_elems, report, &reps[call - 1],
-                                                  stream));
+                                                  scratch_elems, report, mailbox,
+                                                  &reps[call - 1], stream));
         else
             CHECK_FA(fa_bucket_step_clipped(NULL, 0, n, p, g, FA_F32, m, v, NULL, &t, &o, ctl,
                                             0.5, row_len, rows_buf, rows, scratch,
@@ -128,6 +130,7 @@ int main(int argc, char **argv) {
     cudaFree(report);
     cudaFree(scratch);
     cudaStreamDestroy(stream);
+    cudaFreeHost(mailbox);
     free(h);
     return 0;
 }

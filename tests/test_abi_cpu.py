@@ -106,6 +106,32 @@ def test_clip_decision_matches_oracle(oracle_lib):
         assert math.isclose(coef, o_coef, rel_tol=1e-15)
 
 
+def test_stats_sum_sq_decodes_both_record_forms(lib):
+    """A plain record is hi + lo; a record whose sum left FP32's range is stored
+    negated at 2^-192 (its values scaled by 2^-96 before squaring): -(hi + lo) * 2^192.
+    Checked against exact rational arithmetic on the record's two floats."""
+    from fractions import Fraction
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        hi = np.float32(rng.uniform(0, 1e30))
+        lo = np.float32(rng.uniform(-1, 1) * float(np.spacing(hi)) / 2)
+        for scaled in (False, True):
+            rec = fa.FaStats()
+            rec.nonfinite = 0
+            rec.sum_sq = float(-hi if scaled else hi)
+            rec.sum_sq_lo = float(-lo if scaled else lo)
+            want = Fraction(float(hi)) + Fraction(float(lo))
+            if scaled:
+                want *= Fraction(2) ** 192
+            assert fa.fa_stats_sum_sq(rec) == float(want)
+    # the largest square of an FP32 value, scaled: finite in FP64
+    big = np.float32(3.4028235e38)
+    rec = fa.FaStats()
+    rec.sum_sq = -float(np.float32(float(big) * 2.0 ** -96) ** 2)
+    assert math.isclose(fa.fa_stats_sum_sq(rec), float(big) ** 2, rel_tol=1e-7)
+    assert lib.fa_stats_sum_sq(None, ctypes.byref(ctypes.c_double())) == 1  # FA_ERR_NULL
+
+
 def test_step_coefficients_are_fp64_then_fp32():
     o = fa.options(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=0.01,
                    maximize=True)
@@ -294,6 +320,29 @@ def test_device_decided_calls_validate_on_the_host(lib):
     assert clipped(nseg=0, table=None) == 10
     assert clipped(scratch=0) == 3
     assert clipped(ctl=fa.control(skip_update=True)) == 0
+
+
+def test_library_allocates_nothing():
+    """The library never allocates (device memory, pinned or managed host memory) and
+    creates no stream or event: none of the CUDA runtime or driver calls that do is
+    among the symbols it imports (it links the runtime as a shared library, so every
+    runtime call it makes is an undefined dynamic symbol).  Both builds."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm (binutils) not available")
+    forbidden = re.compile(r"^(cuda(Malloc\w*|HostAlloc|HostRegister|Free\w*|EventCreate\w*|"
+                           r"StreamCreate\w*|MemPool\w*|GraphCreate)|cuMem(Alloc|Create|Map)\w*|"
+                           r"cu(Event|Stream)Create\w*)$")
+    for variant in ("normal", "checked"):
+        path = build.build(variant=variant)
+        out = subprocess.run([nm, "-D", "--undefined-only", path], capture_output=True,
+                             text=True, check=True).stdout
+        names = [line.split()[-1].split("@")[0] for line in out.splitlines() if line.strip()]
+        assert any(n.startswith("cudaLaunchKernel") for n in names)  # the runtime is dynamic
+        bad = sorted(n for n in names if forbidden.match(n))
+        assert not bad, f"{variant} build imports allocating calls: {bad}"
 
 
 def test_every_entry_point_cites_its_passage():

@@ -832,6 +832,7 @@ def test_gated_step_equals_host_decided_step_bitwise(max_norm):
     n = 256 * 5000 + 77
     w = CONFIG5.scaled(n, calls=4, inf_call=2)
     dev_state = []
+    mailbox = fa.report_mailbox()
     for gated in (False, True):
         p = torch.empty(n, device=DEV)
         w.fill_params_device(p)
@@ -843,7 +844,8 @@ def test_gated_step_equals_host_decided_step_bitwise(max_norm):
         reports = []
         for call in range(1, w.calls + 1):
             w.fill_grad_device(call, g)
-            fn = fa.fa_bucket_step_clipped_gated if gated else fa.fa_bucket_step_clipped
+            fn = (lambda *a: fa.fa_bucket_step_clipped_gated(*a, mailbox)) if gated \
+                else fa.fa_bucket_step_clipped
             t, r = fn(None, p, g, m, v, None, t, fa.options(**w.options()), fa.control(),
                       max_norm, 256, rb, sc, rep)
             reports.append((r.updated, r.skipped_nonfinite, r.nonfinite, repr(r.grad_norm),
@@ -874,10 +876,12 @@ def test_gated_step_full_size_bitwise():
                        "rows": fa.stats_buffer(rows, DEV), "scr": fa.scratch_buffer(rows, DEV),
                        "rep": fa.stats_buffer(1, DEV)})
     o = fa.options(**w.options())
+    mailbox = fa.report_mailbox()
+    gated = lambda *a: fa.fa_bucket_step_clipped_gated(*a, mailbox)  # noqa: E731
     for call in range(1, w.calls + 1):
         w.fill_grad_device(call, g)
         reps = []
-        for s_, fn in zip(states, (fa.fa_bucket_step_clipped, fa.fa_bucket_step_clipped_gated)):
+        for s_, fn in zip(states, (fa.fa_bucket_step_clipped, gated)):
             s_["t"], r = fn(None, s_["p"], g, s_["m"], s_["v"], None, s_["t"], o, fa.control(),
                             w.max_grad_norm, w.row_len, s_["rows"], s_["scr"], s_["rep"])
             reps.append((r.updated, r.skipped_nonfinite, r.nonfinite, repr(r.grad_norm),
