@@ -106,3 +106,115 @@ def test_two_logical_ranks_match_the_oracle(tmp_path, oracle_lib):
     for name, want in (("p", ref.p), ("m", ref.state.m), ("v", ref.state.v)):
         got = np.concatenate([sh[name] for sh in shards])
         gate(got, want, 1e-5, f"two ranks, {name}")
+
+
+def _zero1_rank(rank, world, port, n, dtype, ams, inf, out_dir):
+    import sys
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import torch
+    import torch.distributed as dist
+    import amsgrad_optimizer_step_gb300 as fa
+    from amsgrad_optimizer_step_gb300 import sharded
+    import zero1_inputs as Z
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    opts = fa.options(lr=2e-3, weight_decay=0.01, amsgrad=ams)
+    step = sharded.Zero1Step(n, opts, tdt, dev, max_grad_norm=0.5, gradient_scale=2.0)
+    p = torch.zeros(step.padded, device=dev)
+    p[:n] = torch.from_numpy(Z.params(n)).to(dev)
+    g = torch.empty(step.padded, dtype=tdt, device=dev)
+    decisions = []
+    for call in range(1, 5):
+        at = inf[2] if inf is not None and inf[0] == call and inf[1] == rank else None
+        bits = Z.rank_gradient(n, step.padded, rank, call, dtype, at)
+        host = torch.from_numpy(bits) if dtype == "f32" else \
+            torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+        g.copy_(host)
+        d = step.step(p, g)
+        decisions.append([d["skipped"], d["nonfinite"], repr(d["grad_norm"]),
+                          repr(d["clip_coef"])])
+    torch.cuda.synchronize()
+    np.savez(os.path.join(out_dir, f"z{rank}.npz"), p=p.cpu().numpy(),
+             m=step.m[:step.k].cpu().numpy(), v=step.v[:step.k].cpu().numpy(),
+             vmax=(step.vmax[:step.k].cpu().numpy() if ams else np.zeros(0)), t=step.t)
+    with open(os.path.join(out_dir, f"z{rank}.json"), "w") as f:
+        json.dump(decisions, f)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,n,dtype,ams,inf", [
+    (2, 2_000_017, "bf16", False, None),
+    (3, 3_000_001, "f32", True, (3, 2, 2_999_999)),  # uneven split; +Inf in rank 2's gradient
+])
+def test_zero1_step_logical_ranks_match_the_whole_bucket_oracle(tmp_path, oracle_lib, world, n,
+                                                                dtype, ams, inf):
+    """The ZeRO-1 data-parallel step with logical ranks sharing cuda:0 (gloo collectives
+    staged through the host, so no kernel waits on another rank): reduce-scatter of the
+    ranks' gradients, each shard analysed, merged and updated in the library's kernels,
+    the 12-byte totals exchanged, the parameters all-gathered.  Every rank's full
+    parameters and the shards' moments against the oracle over the whole bucket on the
+    exact sum of the gradients with gradient_scale x world (the mean), the trajectory
+    within 1e-5; the decisions identical on every rank and the norm within 1e-5 of the
+    oracle's; a +Inf in one rank's gradient skips the step everywhere."""
+    import oracle
+    import zero1_inputs as Z
+    from amsgrad_optimizer_step_gb300 import build
+    from gpu_harness import gate
+    build.build()
+    mp.spawn(_zero1_rank, args=(world, _free_port(), n, dtype, ams, inf, str(tmp_path)),
+             nprocs=world, join=True)
+    res = [np.load(tmp_path / f"z{r}.npz") for r in range(world)]
+    dec = [json.load(open(tmp_path / f"z{r}.json")) for r in range(world)]
+    assert all(d == dec[0] for d in dec), "the ranks decided differently"
+    opts = dict(lr=2e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=0.01, amsgrad=ams,
+                maximize=False)
+    ref = oracle.OracleAdamW(Z.params(n).astype(np.float64), opts, storage="f32",
+                             lib_=oracle_lib)
+    for call in range(1, 5):
+        bits = Z.reduced_gradient(n, world, call, dtype, inf)
+        s, c = oracle_lib.gradient_stats(bits, dtype, 2.0 * world)
+        skip, norm, coef = oracle_lib.clip_decision(s, c, 0.5)
+        got = dec[0][call - 1]
+        assert got[0] == skip and got[1] == c, (call, got, skip, c)
+        if not skip:
+            assert abs(float(got[2]) - norm) <= 1e-5 * norm
+        ref.step(bits, dtype, 2.0 * world, skip_update=skip, clip_coef=coef)
+    for r in res:
+        assert int(r["t"]) == ref.state.t
+        gate(r["p"][:n], ref.p, 1e-5, "gathered p")
+        assert not r["p"][n:].any(), "padding written"
+    gate(np.concatenate([r["m"] for r in res]), ref.state.m, 1e-5, "sharded m")
+    gate(np.concatenate([r["v"] for r in res]), ref.state.v, 1e-5, "sharded v")
+    if ams:
+        gate(np.concatenate([r["vmax"] for r in res]), ref.state.vmax, 1e-5, "sharded vmax")
+
+
+def test_bench_runs_the_zero1_step_with_two_ranks_on_one_gpu():
+    """bench.py --gpus 2 under torchrun, the two ranks sharing cuda:0 with gloo
+    collectives staged through the host: the ZeRO-1 step runs and rank 0 prints one
+    JSON line for the whole job (both ranks' parameters counted), with the data-parallel
+    configuration named and the step's kernel launches counted."""
+    import subprocess
+    import sys
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "3", "--warmup", "3",
+           "--params", "1048576", "--e2e-steps", "2", "--next-rows-steps", "0",
+           "--no-cpu-baseline", "--dist-backend", "gloo"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, (r.stdout[-2000:], r.stderr[-3000:])
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["value"] > 0 and line["scaling"] == "weak"
+    assert line["config"]["parallelism"].startswith("dp2, ZeRO-1")
+    # per step: one analysis, two merge levels (4096 rows), one update
+    assert line["gpu_launches"] == 3 * 4
+    assert line["e2e"]["h2d_bytes_per_step"] == 2 * 1048576 * 2
