@@ -58,3 +58,45 @@ def test_reference_arm_prints_the_contract_line():
     assert line["e2e"] == {"value": line["value"], "unit": "params/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["higher_is_better"] is True and line["steps"] == 2 and line["warmup"] == 1
+
+
+def _oracle_snapshot(w, steps):
+    """What a correct device run would leave at the sampled indices: the oracle's own
+    trajectory (built here from the oracle, as a stand-in for the GPU's results)."""
+    import numpy as np
+    import oracle
+    lib = oracle.lib()
+    idx = bench.parity_indices(w.n, k=500)
+    g_all = w.grad_host(1, np.arange(w.n))
+    s, c = lib.gradient_stats(g_all, "bf16", w.gradient_scale)
+    skip, norm, coef = lib.clip_decision(s, c, w.max_grad_norm)
+    o = oracle.OracleAdamW(w.params_host(idx), w.options(), storage="f32", lib_=lib)
+    for _ in range(steps):
+        o.step(w.grad_host(1, idx), "bf16", w.gradient_scale, skip_update=skip, clip_coef=coef)
+    return {"idx": idx, "p": o.p.astype(np.float32), "m": o.state.m.astype(np.float32),
+            "v": o.state.v.astype(np.float32), "norm": norm, "nonfinite": c, "skipped": skip,
+            "t": steps, "g_bits": g_all}
+
+
+def test_bench_parity_check_passes_the_oracle_and_catches_errors():
+    """The bench's end-of-run parity check: a snapshot equal to the oracle's trajectory
+    passes; a parameter off by 1e-4, a moment off by 2e-5, a norm off by 1e-4 relative,
+    a wrong count, a wrong step count or a gradient that differs from the generator
+    each fail it."""
+    import dataclasses
+    w = bench.workload(256 * 40 + 3)
+    w = dataclasses.replace(w, max_grad_norm=0.05)  # so the clip is active at this size
+    snap = _oracle_snapshot(w, 4)
+    good = bench.parity_check(w, snap, 4)
+    assert good["ok"] and good["max_rel_err"] <= 1e-6 and good["elements"] == len(snap["idx"])
+    assert good["norm_rel_err"] <= 1e-12
+    bad_cases = [("p", lambda s: s["p"].__setitem__(3, s["p"][3] + 1e-4)),
+                 ("m", lambda s: s["m"].__setitem__(-1, s["m"][-1] + 2e-5)),
+                 ("norm", lambda s: s.__setitem__("norm", s["norm"] * (1 + 1e-4))),
+                 ("nonfinite", lambda s: s.__setitem__("nonfinite", 1)),
+                 ("t", lambda s: s.__setitem__("t", 3)),
+                 ("g", lambda s: s["g_bits"].__setitem__(int(s["idx"][5]), 0x7f80))]
+    for name, spoil in bad_cases:
+        s = {k: (v.copy() if hasattr(v, "copy") else v) for k, v in snap.items()}
+        spoil(s)
+        assert not bench.parity_check(w, s, 4)["ok"], name
