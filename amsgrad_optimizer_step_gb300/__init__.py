@@ -22,18 +22,15 @@ from ._lib import (FA_BF16, FA_F16, FA_F32, FaOptions, FaStats, FaStepControl,  
 
 __all__ = [
     "fa_abi_version", "fa_device_error", "fa_bounds_check_report", "fa_pipeline_selftest",
-    "fa_options_default", "fa_step_coefficients", "fa_adamw_step", "fa_adamw_step_inplace", "fa_bucket_step", "fa_bucket_step_writeback",
-    "fa_adamw_step_staged", "fa_stats_plan",
-    "fa_stats_rows",
-    "fa_analyze_gradient", "fa_merge_gradient_stats", "fa_merge_gradient_stats_static",
-    "fa_read_report", "fa_stats_sum_sq", "fa_clip_decision", "fa_stats_chunk_scratch",
-    "fa_merge_gradient_stats_chunks", "fa_bucket_step_segment_scaled",
-    "fa_bucket_step_clipped_per_segment", "fa_bucket_step_per_segment_gated",
-    "fa_bucket_step_clipped_per_segment_gated", "segment_rows",
-    "fa_clip_decide", "fa_bucket_step_clipped", "fa_bucket_step_gated",
-    "fa_bucket_step_writeback_gated",
-    "fa_bucket_step_clipped_gated", "report_mailbox", "options", "control", "stats_buffer",
-    "scratch_buffer", "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
+    "fa_options_default", "fa_step_coefficients", "fa_adamw_step", "fa_adamw_step_inplace",
+    "fa_bucket_step", "fa_bucket_update", "fa_adamw_step_staged", "fa_stats_plan",
+    "fa_stats_rows", "fa_analyze_gradient", "fa_merge_gradient_stats",
+    "fa_merge_gradient_stats_static", "fa_read_report", "fa_stats_sum_sq", "fa_clip_decision",
+    "fa_stats_chunk_scratch", "fa_merge_gradient_stats_chunks",
+    "fa_bucket_step_clipped_per_segment", "fa_bucket_step_clipped_per_segment_gated",
+    "segment_rows", "fa_clip_decide", "fa_bucket_step_clipped", "fa_bucket_step_clipped_gated",
+    "report_mailbox", "options", "control", "stats_buffer", "scratch_buffer",
+    "FusedAdamWError", "FaStats", "FaStepReport", "bytes_per_param",
 ]
 
 _TORCH_GRAD = {torch.float32: FA_F32, torch.float16: FA_F16, torch.bfloat16: FA_BF16}
@@ -252,13 +249,17 @@ def fa_bucket_step(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions, ctl: 
     return tt.value, bool(upd.value)
 
 
-def fa_bucket_step_writeback(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
-                             ctl: FaStepControl, p_model: torch.Tensor, grad_mult: float = 1.0,
-                             stream=None) -> tuple[int, bool]:
-    """fa_bucket_step that also writes the BF16/FP16 model copy ``p_model``.
-
-    Returns (t, updated).
-    """
+def fa_bucket_update(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
+                     ctl: FaStepControl, *, grad_mult: float = 1.0,
+                     seg_grad_mult: Optional[Sequence[float]] = None,
+                     report: Optional[torch.Tensor] = None,
+                     seg_reports: Optional[torch.Tensor] = None, max_grad_norm: float = 0.0,
+                     p_model: Optional[torch.Tensor] = None, stream=None) -> bool:
+    """One update of a pre-flattened bucket in any variant (the fa_bucket_update_args record):
+    a host multiplier (``grad_mult``, or ``seg_grad_mult`` per segment) or the decision on
+    the device from ``report`` / ``seg_reports`` with ``max_grad_norm``, and optionally the
+    BF16/FP16 model copy ``p_model``.  The update is step t + 1; t is not changed.
+    Returns True when an update kernel was enqueued."""
     n = p.numel()
     _dense("p", p, n, (torch.float32,))
     _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
@@ -266,14 +267,30 @@ def fa_bucket_step_writeback(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOpti
     _dense("v", v, n, (torch.float32,), p.device)
     if vmax is not None:
         _dense("vmax", vmax, n, (torch.float32,), p.device)
-    _dense("p_model", p_model, n, (torch.float16, torch.bfloat16), p.device)
+    if p_model is not None:
+        _dense("p_model", p_model, n, (torch.float16, torch.bfloat16), p.device)
+    if report is not None:
+        _stats_tensor("report", report)
     seg, nseg = _segments(seg_offsets)
-    tt, upd = ctypes.c_uint64(t), ctypes.c_int32()
-    check("fa_bucket_step_writeback", _L().fa_bucket_step_writeback(
-        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
-        ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, _ptr(p_model),
-        _TORCH_GRAD[p_model.dtype], ctypes.byref(upd), _stream(stream)))
-    return tt.value, bool(upd.value)
+    if seg_reports is not None:
+        _stats_tensor("seg_reports", seg_reports)
+        if seg_reports.shape[0] < nseg:
+            raise ValueError(f"seg_reports: {seg_reports.shape[0]} records for {nseg} segments")
+    mult = None
+    if seg_grad_mult is not None:
+        if len(seg_grad_mult) != nseg:
+            raise ValueError("one multiplier per segment")
+        mult = (ctypes.c_double * nseg)(*[float(x) for x in seg_grad_mult])
+    u = _lib.FaBucketUpdate(
+        seg_offsets=seg, nseg=nseg, n_total=n, p=_ptr(p), g=_ptr(g), gdt=_TORCH_GRAD[g.dtype],
+        m=_ptr(m), v=_ptr(v), vmax=_ptr(vmax), t=t, grad_mult=grad_mult, seg_grad_mult=mult,
+        report=_ptr(report), seg_reports=_ptr(seg_reports), max_grad_norm=max_grad_norm,
+        p_model=_ptr(p_model),
+        model_dtype=_TORCH_GRAD[p_model.dtype] if p_model is not None else FA_BF16)
+    enq = ctypes.c_int32()
+    check("fa_bucket_update", _L().fa_bucket_update(ctypes.byref(u), ctypes.byref(opts), ctl,
+                                                    ctypes.byref(enq), _stream(stream)))
+    return bool(enq.value)
 
 
 def fa_adamw_step_staged(p, g, m, v, vmax, t: int, opts: FaOptions, ctl: FaStepControl,
@@ -294,45 +311,6 @@ def fa_adamw_step_staged(p, g, m, v, vmax, t: int, opts: FaOptions, ctl: FaStepC
         ctypes.byref(tt), ctypes.byref(opts), ctl, grad_mult, _ptr(delta), ctypes.byref(upd),
         _stream(stream)))
     return tt.value, bool(upd.value)
-
-
-def fa_bucket_step_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
-                         ctl: FaStepControl, report: torch.Tensor, max_grad_norm: float,
-                         stream=None) -> None:
-    """Enqueues the update gated on the device report; the caller advances t."""
-    n = p.numel()
-    _dense("p", p, n, (torch.float32,))
-    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
-    _dense("m", m, n, (torch.float32,), p.device)
-    _dense("v", v, n, (torch.float32,), p.device)
-    if vmax is not None:
-        _dense("vmax", vmax, n, (torch.float32,), p.device)
-    _stats_tensor("report", report)
-    seg, nseg = _segments(seg_offsets)
-    check("fa_bucket_step_gated", _L().fa_bucket_step_gated(
-        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
-        ctypes.byref(opts), ctl, _ptr(report), max_grad_norm, _stream(stream)))
-
-
-def fa_bucket_step_writeback_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
-                                   ctl: FaStepControl, report: torch.Tensor,
-                                   max_grad_norm: float, p_model: torch.Tensor,
-                                   stream=None) -> None:
-    """Enqueues the write-back update gated on the device report; the caller advances t."""
-    n = p.numel()
-    _dense("p", p, n, (torch.float32,))
-    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
-    _dense("m", m, n, (torch.float32,), p.device)
-    _dense("v", v, n, (torch.float32,), p.device)
-    if vmax is not None:
-        _dense("vmax", vmax, n, (torch.float32,), p.device)
-    _dense("p_model", p_model, n, (torch.float16, torch.bfloat16), p.device)
-    _stats_tensor("report", report)
-    seg, nseg = _segments(seg_offsets)
-    check("fa_bucket_step_writeback_gated", _L().fa_bucket_step_writeback_gated(
-        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
-        ctypes.byref(opts), ctl, _ptr(report), max_grad_norm, _ptr(p_model),
-        _TORCH_GRAD[p_model.dtype], _stream(stream)))
 
 
 def report_mailbox() -> torch.Tensor:
@@ -453,28 +431,6 @@ def fa_merge_gradient_stats_chunks(rows_in: torch.Tensor, chunk_rows: Sequence[i
         _ptr(chunk_reports), _stream(stream)))
 
 
-def fa_bucket_step_segment_scaled(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
-                                  ctl: FaStepControl, seg_grad_mult: Sequence[float],
-                                  stream=None) -> tuple[int, bool]:
-    """Bucket update with one gradient multiplier per segment.  Returns (t, updated)."""
-    n = p.numel()
-    _dense("p", p, n, (torch.float32,))
-    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
-    _dense("m", m, n, (torch.float32,), p.device)
-    _dense("v", v, n, (torch.float32,), p.device)
-    if vmax is not None:
-        _dense("vmax", vmax, n, (torch.float32,), p.device)
-    seg, nseg = _segments(seg_offsets)
-    if len(seg_grad_mult) != nseg:
-        raise ValueError("one multiplier per segment")
-    mult = (ctypes.c_double * nseg)(*[float(x) for x in seg_grad_mult])
-    tt, upd = ctypes.c_uint64(t), ctypes.c_int32()
-    check("fa_bucket_step_segment_scaled", _L().fa_bucket_step_segment_scaled(
-        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax),
-        ctypes.byref(tt), ctypes.byref(opts), ctl, mult, ctypes.byref(upd), _stream(stream)))
-    return tt.value, bool(upd.value)
-
-
 def fa_bucket_step_clipped_per_segment(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
                                        ctl: FaStepControl, max_grad_norm: float, row_len: int,
                                        rows_buf: torch.Tensor, scratch: torch.Tensor,
@@ -500,27 +456,6 @@ def fa_bucket_step_clipped_per_segment(seg_offsets, p, g, m, v, vmax, t: int, op
         rows_buf.shape[0], _ptr(scratch), scratch.numel(), _ptr(seg_reports), norms, coefs,
         ctypes.byref(rep), _stream(stream)))
     return tt.value, rep, list(norms), list(coefs)
-
-
-def fa_bucket_step_per_segment_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
-                                     ctl: FaStepControl, seg_reports: torch.Tensor,
-                                     max_grad_norm: float, stream=None) -> None:
-    """Enqueues the per-segment update decided on the device from ``seg_reports``; the
-    caller reads the reports and advances t unless one counts a non-finite value."""
-    n = p.numel()
-    _dense("p", p, n, (torch.float32,))
-    _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
-    _dense("m", m, n, (torch.float32,), p.device)
-    _dense("v", v, n, (torch.float32,), p.device)
-    if vmax is not None:
-        _dense("vmax", vmax, n, (torch.float32,), p.device)
-    _stats_tensor("seg_reports", seg_reports)
-    seg, nseg = _segments(seg_offsets)
-    if seg_reports.shape[0] < nseg:
-        raise ValueError(f"seg_reports: {seg_reports.shape[0]} records for {nseg} segments")
-    check("fa_bucket_step_per_segment_gated", _L().fa_bucket_step_per_segment_gated(
-        seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v), _ptr(vmax), t,
-        ctypes.byref(opts), ctl, _ptr(seg_reports), max_grad_norm, _stream(stream)))
 
 
 def fa_bucket_step_clipped_per_segment_gated(seg_offsets, p, g, m, v, vmax, t: int,

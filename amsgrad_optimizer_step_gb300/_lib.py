@@ -36,6 +36,15 @@ class FaStats(ctypes.Structure):
                 ("sum_sq_lo", ctypes.c_float)]
 
 
+class FaBucketUpdate(ctypes.Structure):
+    _fields_ = [("seg_offsets", ctypes.POINTER(c_i64)), ("nseg", c_i32), ("n_total", c_i64),
+                ("p", c_vp), ("g", c_vp), ("gdt", c_i32), ("m", c_vp), ("v", c_vp),
+                ("vmax", c_vp), ("t", c_u64), ("grad_mult", c_f64),
+                ("seg_grad_mult", ctypes.POINTER(c_f64)), ("report", c_vp),
+                ("seg_reports", c_vp), ("max_grad_norm", c_f64), ("p_model", c_vp),
+                ("model_dtype", c_i32)]
+
+
 class FaStepReport(ctypes.Structure):
     _fields_ = [("updated", c_i32), ("skipped_nonfinite", c_i32), ("nonfinite", c_u64),
                 ("grad_norm", c_f64), ("clip_coef", c_f64)]
@@ -64,17 +73,11 @@ SIGNATURES = {
                                       ctypes.POINTER(FaOptions), FaStepControl, c_f64, PI32, P]),
     "fa_bucket_step": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
                                ctypes.POINTER(FaOptions), FaStepControl, c_f64, PI32, P]),
-    "fa_bucket_step_writeback": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
-                                         ctypes.POINTER(FaOptions), FaStepControl, c_f64, P,
-                                         c_i32, PI32, P]),
+    "fa_bucket_update": (c_i32, [ctypes.POINTER(FaBucketUpdate), ctypes.POINTER(FaOptions),
+                                 FaStepControl, PI32, P]),
     "fa_adamw_step_staged": (c_i32, [c_i64, P, P, c_i32, P, P, P, PU64,
                                      ctypes.POINTER(FaOptions), FaStepControl, c_f64, P, PI32,
                                      P]),
-    "fa_bucket_step_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, c_u64,
-                                     ctypes.POINTER(FaOptions), FaStepControl, P, c_f64, P]),
-    "fa_bucket_step_writeback_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, c_u64,
-                                               ctypes.POINTER(FaOptions), FaStepControl, P,
-                                               c_f64, P, c_i32, P]),
     "fa_bucket_step_clipped_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
                                              ctypes.POINTER(FaOptions), FaStepControl, c_f64,
                                              c_i32, P, c_i64, P, c_i64, P, P,
@@ -86,17 +89,11 @@ SIGNATURES = {
     "fa_merge_gradient_stats_static": (c_i32, [P, c_i64, P, P]),
     "fa_stats_chunk_scratch": (c_i32, [PI64, c_i32, PI64]),
     "fa_merge_gradient_stats_chunks": (c_i32, [P, PI64, c_i32, P, c_i64, P, P]),
-    "fa_bucket_step_segment_scaled": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P, PU64,
-                                              ctypes.POINTER(FaOptions), FaStepControl, PF64,
-                                              PI32, P]),
     "fa_bucket_step_clipped_per_segment": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P,
                                                    PU64, ctypes.POINTER(FaOptions),
                                                    FaStepControl, c_f64, c_i32, P, c_i64, P,
                                                    c_i64, P, PF64, PF64,
                                                    ctypes.POINTER(FaStepReport), P]),
-    "fa_bucket_step_per_segment_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P, P,
-                                                 c_u64, ctypes.POINTER(FaOptions),
-                                                 FaStepControl, P, c_f64, P]),
     "fa_bucket_step_clipped_per_segment_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P,
                                                          P, c_u64, ctypes.POINTER(FaOptions),
                                                          FaStepControl, c_f64, c_i32, P, c_i64,

@@ -591,38 +591,65 @@ fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_tot
                                  updated, stream);
 }
 
-fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                                   float *p, const void *g, fa_dtype gdt, float *m, float *v,
-                                   float *vmax, uint64_t *t, const fa_options *options,
-                                   fa_step_control ctl, double grad_mult, void *p_model,
-                                   fa_dtype model_dtype, int32_t *updated, void *stream) {
-    TraceRange trace("fa_bucket_step_writeback");
+fa_status fa_bucket_update(const fa_bucket_update_args *u, const fa_options *options,
+                           fa_step_control ctl, int32_t *enqueued, void *stream) {
+    TraceRange trace("fa_bucket_update");
     fa_status st;
-    if (!t || !updated) return FA_ERR_NULL;
-    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
-    if (model_dtype != FA_F16 && model_dtype != FA_BF16) return FA_ERR_DTYPE;
-    if (!is_finite(grad_mult) || grad_mult < 0) return FA_ERR_OPTION;
-    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
-    if (n_total == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
-        *updated = 0;
+    if (!u || !enqueued) return FA_ERR_NULL;
+    if ((st = check_step_args(options, ctl, u->gdt, u->n_total)) != FA_OK) return st;
+    const bool per_segment = u->seg_grad_mult || u->seg_reports;
+    const bool on_device = u->report || u->seg_reports;
+    const int sources = (u->seg_grad_mult != nullptr) + (u->report != nullptr) +
+                        (u->seg_reports != nullptr);
+    if (sources > 1) return FA_ERR_OPTION;
+    if (!is_finite(u->grad_mult) || u->grad_mult < 0) return FA_ERR_OPTION;
+    if (sources == 1 && u->grad_mult != 1.0) return FA_ERR_OPTION;
+    if (on_device && std::isnan(u->max_grad_norm)) return FA_ERR_OPTION;
+    if (u->p_model) {
+        if (u->model_dtype != FA_F16 && u->model_dtype != FA_BF16) return FA_ERR_DTYPE;
+        if (per_segment) return FA_ERR_OPTION;  // no per-segment kernel writes a model copy
+    }
+    if (per_segment && u->nseg < 1) return FA_ERR_SEGMENTS;
+    if ((st = check_segments(u->seg_offsets, u->nseg, u->n_total)) != FA_OK) return st;
+    if (u->seg_grad_mult)
+        for (int32_t k = 0; k < u->nseg; ++k)
+            if (!is_finite(u->seg_grad_mult[k]) || u->seg_grad_mult[k] < 0) return FA_ERR_OPTION;
+    if (u->n_total == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
+        *enqueued = 0;
         return FA_OK;
     }
-    if (*t == UINT64_MAX) return FA_ERR_OPTION;
+    if (u->t == UINT64_MAX) return FA_ERR_OPTION;
     int dev = 0;
     if ((st = stream_device(stream, &dev)) != FA_OK) return st;
-    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    if ((st = check_device_ptr(p_model, dev, 2)) != FA_OK) return st;
-    const size_t b = static_cast<size_t>(n_total) * 4;
-    const Range model{p_model, static_cast<size_t>(n_total) * 2};
-    const Range others[] = {{p, b}, {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b},
-                            {v, b}, {options->amsgrad ? vmax : nullptr, b}};
-    for (const Range &r : others)
-        if (overlap(model, r)) return FA_ERR_ALIAS;
-    st = enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, *t + 1,
-                        ctl.gradient_scale, grad_mult, stream, p_model, model_dtype);
+    if ((st = check_inplace(u->n_total, u->p, u->g, u->gdt, u->m, u->v, u->vmax, options, dev)) !=
+        FA_OK)
+        return st;
+    if (u->p_model && (st = check_device_ptr(u->p_model, dev, 2)) != FA_OK) return st;
+    const fa_stats *reports = u->report ? u->report : u->seg_reports;
+    if (reports && (st = check_device_ptr(reports, dev, 4)) != FA_OK) return st;
+    // the model copy and the reports must stay clear of every buffer the update touches
+    const size_t b = static_cast<size_t>(u->n_total) * 4;
+    const Range model{u->p_model, static_cast<size_t>(u->n_total) * 2};
+    const Range rep{reports, static_cast<size_t>(u->report ? 1 : u->nseg) * 12};
+    const Range state[] = {{u->p, b},
+                           {u->g, static_cast<size_t>(u->n_total) * dtype_bytes(u->gdt)},
+                           {u->m, b},
+                           {u->v, b},
+                           {options->amsgrad ? u->vmax : nullptr, b}};
+    for (const Range &r : state)
+        if (overlap(model, r) || overlap(rep, r)) return FA_ERR_ALIAS;
+    if (overlap(model, rep)) return FA_ERR_ALIAS;
+    if (per_segment)
+        st = enqueue_segment_update(u->seg_offsets, u->nseg, u->p, u->g, u->gdt, u->m, u->v,
+                                    u->vmax, u->t + 1, options, ctl, u->seg_grad_mult,
+                                    u->seg_reports, u->max_grad_norm, stream);
+    else
+        st = enqueue_update(u->n_total, u->p, u->g, u->gdt, u->m, u->v, u->vmax, u->p, u->m, u->v,
+                            u->vmax, options, u->t + 1, ctl.gradient_scale, u->grad_mult, stream,
+                            u->p_model, u->p_model ? u->model_dtype : fa::kNoModel, u->report,
+                            u->max_grad_norm);
     if (st != FA_OK) return st;
-    *t += 1;
-    *updated = 1;
+    *enqueued = 1;
     return FA_OK;
 }
 
@@ -663,64 +690,6 @@ fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt,
     *t += 1;
     *updated = 1;
     return FA_OK;
-}
-
-fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                               float *p, const void *g, fa_dtype gdt, float *m, float *v,
-                               float *vmax, uint64_t t, const fa_options *options,
-                               fa_step_control ctl, const fa_stats *report_dev,
-                               double max_grad_norm, void *stream) {
-    TraceRange trace("fa_bucket_step_gated");
-    fa_status st;
-    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
-    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
-    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
-    if (n_total == 0 || ctl.skip_update) return FA_OK;
-    if (t == UINT64_MAX) return FA_ERR_OPTION;
-    int dev = 0;
-    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
-    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    if ((st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
-    const size_t b = static_cast<size_t>(n_total) * 4;
-    const Range rep{report_dev, 12};
-    const Range others[] = {{p, b}, {m, b}, {v, b}, {options->amsgrad ? vmax : nullptr, b}};
-    for (const Range &r : others)
-        if (overlap(rep, r)) return FA_ERR_ALIAS;
-    return enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, t + 1,
-                          ctl.gradient_scale, 1.0, stream, nullptr, fa::kNoModel, report_dev,
-                          max_grad_norm);
-}
-
-fa_status fa_bucket_step_writeback_gated(const int64_t *seg_offsets, int32_t nseg,
-                                         int64_t n_total, float *p, const void *g, fa_dtype gdt,
-                                         float *m, float *v, float *vmax, uint64_t t,
-                                         const fa_options *options, fa_step_control ctl,
-                                         const fa_stats *report_dev, double max_grad_norm,
-                                         void *p_model, fa_dtype model_dtype, void *stream) {
-    TraceRange trace("fa_bucket_step_writeback_gated");
-    fa_status st;
-    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
-    if (model_dtype != FA_F16 && model_dtype != FA_BF16) return FA_ERR_DTYPE;
-    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
-    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
-    if (n_total == 0 || ctl.skip_update) return FA_OK;
-    if (t == UINT64_MAX) return FA_ERR_OPTION;
-    int dev = 0;
-    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
-    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    if ((st = check_device_ptr(report_dev, dev, 4)) != FA_OK) return st;
-    if ((st = check_device_ptr(p_model, dev, 2)) != FA_OK) return st;
-    const size_t b = static_cast<size_t>(n_total) * 4;
-    const Range r[] = {{report_dev, 12}, {p_model, static_cast<size_t>(n_total) * 2}, {p, b},
-                       {g, static_cast<size_t>(n_total) * dtype_bytes(gdt)}, {m, b}, {v, b},
-                       {options->amsgrad ? vmax : nullptr, b}};
-    // the report and the model copy must stay clear of every buffer the update writes
-    for (int i = 0; i < 2; ++i)
-        for (int j = i + 1; j < 7; ++j)
-            if (overlap(r[i], r[j])) return FA_ERR_ALIAS;
-    return enqueue_update(n_total, p, g, gdt, m, v, vmax, p, m, v, vmax, options, t + 1,
-                          ctl.gradient_scale, 1.0, stream, p_model, model_dtype, report_dev,
-                          max_grad_norm);
 }
 
 namespace {
@@ -1051,37 +1020,6 @@ fa_status fa_merge_gradient_stats_chunks(const fa_stats *rows_in, const int64_t 
     return FA_OK;
 }
 
-fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                                        float *p, const void *g, fa_dtype gdt, float *m,
-                                        float *v, float *vmax, uint64_t *t,
-                                        const fa_options *options, fa_step_control ctl,
-                                        const double *seg_grad_mult, int32_t *updated,
-                                        void *stream) {
-    TraceRange trace("fa_bucket_step_segment_scaled");
-    fa_status st;
-    if (!t || !updated) return FA_ERR_NULL;
-    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
-    if (nseg < 1) return FA_ERR_SEGMENTS;
-    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
-    if (!seg_grad_mult) return FA_ERR_NULL;
-    for (int32_t k = 0; k < nseg; ++k)
-        if (!is_finite(seg_grad_mult[k]) || seg_grad_mult[k] < 0) return FA_ERR_OPTION;
-    if (n_total == 0 || ctl.skip_update) {  // nothing launched, no buffer touched or checked
-        *updated = 0;
-        return FA_OK;
-    }
-    if (*t == UINT64_MAX) return FA_ERR_OPTION;
-    int dev = 0;
-    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
-    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    if ((st = enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, *t + 1, options,
-                                     ctl, seg_grad_mult, nullptr, 0.0, stream)) != FA_OK)
-        return st;
-    *t += 1;
-    *updated = 1;
-    return FA_OK;
-}
-
 fa_status fa_bucket_step_clipped_per_segment(
     const int64_t *seg_offsets, int32_t nseg, int64_t n_total, float *p, const void *g,
     fa_dtype gdt, float *m, float *v, float *vmax, uint64_t *t, const fa_options *options,
@@ -1149,40 +1087,13 @@ fa_status fa_bucket_step_clipped_per_segment(
         *out = rep;
         return FA_OK;
     }
-    int32_t updated = 0;
-    if ((st = fa_bucket_step_segment_scaled(seg_offsets, nseg, n_total, p, g, gdt, m, v, vmax, t,
-                                            options, ctl, coef.data(), &updated, stream)) != FA_OK)
+    if ((st = enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, *t + 1, options,
+                                     ctl, coef.data(), nullptr, 0.0, stream)) != FA_OK)
         return st;
-    rep.updated = updated;
+    *t += 1;
+    rep.updated = 1;
     *out = rep;
     return FA_OK;
-}
-
-fa_status fa_bucket_step_per_segment_gated(const int64_t *seg_offsets, int32_t nseg,
-                                           int64_t n_total, float *p, const void *g,
-                                           fa_dtype gdt, float *m, float *v, float *vmax,
-                                           uint64_t t, const fa_options *options,
-                                           fa_step_control ctl, const fa_stats *seg_reports,
-                                           double max_grad_norm, void *stream) {
-    TraceRange trace("fa_bucket_step_per_segment_gated");
-    fa_status st;
-    if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
-    if (std::isnan(max_grad_norm)) return FA_ERR_OPTION;
-    if (nseg < 1) return FA_ERR_SEGMENTS;
-    if ((st = check_segments(seg_offsets, nseg, n_total)) != FA_OK) return st;
-    if (n_total == 0 || ctl.skip_update) return FA_OK;
-    if (t == UINT64_MAX) return FA_ERR_OPTION;
-    int dev = 0;
-    if ((st = stream_device(stream, &dev)) != FA_OK) return st;
-    if ((st = check_inplace(n_total, p, g, gdt, m, v, vmax, options, dev)) != FA_OK) return st;
-    if ((st = check_device_ptr(seg_reports, dev, 4)) != FA_OK) return st;
-    const size_t b = static_cast<size_t>(n_total) * 4;
-    const Range rep{seg_reports, static_cast<size_t>(nseg) * 12};
-    const Range others[] = {{p, b}, {m, b}, {v, b}, {options->amsgrad ? vmax : nullptr, b}};
-    for (const Range &r : others)
-        if (overlap(rep, r)) return FA_ERR_ALIAS;
-    return enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, t + 1, options, ctl,
-                                  nullptr, seg_reports, max_grad_norm, stream);
 }
 
 fa_status fa_bucket_step_clipped_per_segment_gated(

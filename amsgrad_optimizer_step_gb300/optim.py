@@ -30,10 +30,8 @@ from typing import Optional
 
 import torch
 
-from . import (FaStats, fa_analyze_gradient, fa_bucket_step, fa_bucket_step_gated,
-               fa_bucket_step_writeback, fa_bucket_step_writeback_gated, fa_clip_decision,
-               fa_stats_sum_sq,
-               fa_merge_gradient_stats,
+from . import (FaStats, fa_analyze_gradient, fa_bucket_step, fa_bucket_update,
+               fa_clip_decision, fa_stats_sum_sq, fa_merge_gradient_stats,
                fa_read_report, fa_stats_rows, options, control, scratch_buffer, stats_buffer)
 from . import sharded
 
@@ -358,8 +356,8 @@ class FusedAdamW(torch.optim.Optimizer):
                 for i, j, lo, hi in b.runs(act):
                     pm, g, m, v, vm, model = b.slices(lo, hi)
                     if b.master_separate:
-                        fa_bucket_step_writeback(None, pm, g, m, v, vm, b.steps[i], o, ctl,
-                                                 model, report["clip_coef"])
+                        fa_bucket_update(None, pm, g, m, v, vm, b.steps[i], o, ctl,
+                                         grad_mult=report["clip_coef"], p_model=model)
                     else:
                         fa_bucket_step(None, pm, g, m, v, vm, b.steps[i], o, ctl,
                                        report["clip_coef"])
@@ -397,11 +395,11 @@ class FusedAdamW(torch.optim.Optimizer):
             for i, j, lo, hi in b.runs(act):
                 pm, g, m, v, vm, model = b.slices(lo, hi)
                 if b.master_separate:
-                    fa_bucket_step_writeback_gated(None, pm, g, m, v, vm, b.steps[i], o, ctl,
-                                                   report_dev, max_norm, model)
+                    fa_bucket_update(None, pm, g, m, v, vm, b.steps[i], o, ctl,
+                                     report=report_dev, max_grad_norm=max_norm, p_model=model)
                 else:
-                    fa_bucket_step_gated(None, pm, g, m, v, vm, b.steps[i], o, ctl, report_dev,
-                                         max_norm)
+                    fa_bucket_update(None, pm, g, m, v, vm, b.steps[i], o, ctl,
+                                     report=report_dev, max_grad_norm=max_norm)
                 launched.append((b, i, j))
         self._report_event.synchronize()
         rep = FaStats.from_buffer_copy(self._pinned_report.numpy().tobytes())

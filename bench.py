@@ -398,7 +398,9 @@ def parity_check(w, snap, steps: int):
             "oracle_full_gradient_stats_s": stats_s,
             "what": "p, m, v at the sampled elements after the warm-up and timed steps vs the "
                     "oracle's own trajectory; its decision from its FP64 sum over every "
-                    "gradient value"}
+                    "gradient value.  Sampling is exact for the update: each element's update "
+                    "depends only on its own values and the shared decision; the statistics "
+                    "that couple the elements are checked over the whole gradient"}
 
 
 def run_reference(args):
@@ -527,8 +529,8 @@ def run_ours(args):
             rep_pinned.copy_(report, non_blocking=True)
             rep_arrived.record(stream)
             if ev: ev[2].record(stream)
-            fa.fa_bucket_step_gated(None, p, g, m, v, None, state["t"], opts, ctl, report,
-                                    w.max_grad_norm)
+            fa.fa_bucket_update(None, p, g, m, v, None, state["t"], opts, ctl, report=report,
+                                max_grad_norm=w.max_grad_norm)
             launches["n"] += 1
             if ev: ev[3].record(stream)
             rep_arrived.synchronize()
@@ -728,8 +730,9 @@ def run_ours(args):
             fa.fa_bucket_step(None, p, g, m, v, None, 0, opts, ctl, 1.0)
 
         def writeback():
-            state["t"], _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, state["t"], opts,
-                                                        ctl, p_model, 1.0)
+            if fa.fa_bucket_update(None, p, g, m, v, None, state["t"], opts, ctl,
+                                   p_model=p_model):
+                state["t"] += 1
 
         peak, peak_kind = measured_peaks()
         rows_out = {}
@@ -885,8 +888,8 @@ def run_ours(args):
             fa.fa_merge_gradient_stats_chunks(srows, crow, sscr, srep)
             srep_pinned.copy_(srep, non_blocking=True)
             srep_ready.record(stream)
-            fa.fa_bucket_step_per_segment_gated(seg, sp, sg, sm, sv, svm, sstate["t"], so, ctl,
-                                                srep, 0.01)
+            fa.fa_bucket_update(seg, sp, sg, sm, sv, svm, sstate["t"], so, ctl, seg_reports=srep,
+                                max_grad_norm=0.01)
             srep_ready.synchronize()
             if not bool((srep_pinned[:, 1] != 0).any()):
                 sstate["t"] += 1

@@ -257,21 +257,71 @@ fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_tot
                          void *stream);
 
 /*
- * fa_bucket_step that also writes the low-precision model copy of the updated
- * parameters in the same HBM pass ([TR-zh] "FP32 主参数与混合参数存储": the FP32
- * master is updated in FP32 and the parameters are returned in their storage
- * dtype; [FA-zh] "增加的实际能力": in the plain step that write-back is left to the
- * caller).  p_model (device, n_total elements of model_dtype = FA_F16 or
- * FA_BF16, 2-byte aligned, overlapping no other buffer) receives each updated
- * FP32 p rounded to nearest, ties to even; +2 bytes per parameter instead of
- * a separate 6-byte cast pass.  Skip / empty: nothing is written, p_model
- * included.  FA_ERR_DTYPE for any other model_dtype.
+ * One update of a pre-flattened bucket in any of its variants, described by
+ * one record (fa_bucket_update_args): where the gradient multiplier comes from,
+ * and whether the low-precision model copy is written in the same pass.  Every variant is the
+ * per-element update of fa_bucket_step over the flat buffers, identical to
+ * updating each tensor on its own ([FA-ja] "サポートされている契約").
+ *
+ * The multiplier of the unscaled gradient, from exactly one source:
+ *   - grad_mult (host): one factor, the global clip coefficient (1 = none;
+ *     finite, >= 0).  It must be 1 when another source is given.
+ *   - seg_grad_mult (host, nseg doubles, finite, >= 0): one factor per segment
+ *     ([TR-zh] "FP32 主参数与混合参数存储": Fp32MasterOptimizer clips each
+ *     parameter by its own rule).  One launch per 240 segments.
+ *   - report (device, one fa_stats as written by fa_merge_gradient_stats earlier
+ *     on the same stream): the decision is taken in the update kernel
+ *     ([TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": a non-finite gradient skips the
+ *     whole step; the global L2 clip of the unscaled gradient).  The kernel skips
+ *     when the report counts a non-finite value, and otherwise multiplies by the
+ *     coefficient fa_clip_decision computes (max_grad_norm <= 0: no clip), with
+ *     the same FP64 operations in the same order.  The results are therefore
+ *     bit-identical to reading the report back and passing that coefficient as
+ *     grad_mult.  The update is launched as a programmatic dependent of the kernel
+ *     before it.
+ *   - seg_reports (device, nseg fa_stats as written by
+ *     fa_merge_gradient_stats_chunks earlier on the same stream): the same per
+ *     segment.  Any non-finite count skips the whole update; segment k takes the
+ *     coefficient of record k.
+ *
+ * p_model (device, n_total elements of model_dtype = FA_F16 or FA_BF16, 2-byte
+ * aligned, overlapping no other buffer): each updated FP32 p rounded to nearest,
+ * ties to even, written in the same HBM pass; +2 bytes per parameter instead of a
+ * separate 6-byte cast pass ([TR-zh] "FP32 主参数与混合参数存储": the FP32 master
+ * is updated in FP32 and the parameters come back in their storage dtype).  Not
+ * with the per-segment sources (FA_ERR_OPTION).  FA_ERR_DTYPE for another dtype.
+ *
+ * ``t`` is the completed step count; the update is step t + 1.  This call changes
+ * no count.  On return *enqueued is 1 when an update kernel was enqueued, and 0
+ * for n_total == 0 or ctl.skip_update: then nothing is launched and no buffer is
+ * checked or touched.  With a host multiplier the caller advances its count by one
+ * when *enqueued.  With a device decision it reads the report and advances the
+ * count unless the report counts a non-finite value.  The reports and the model copy
+ * must not overlap the state, the gradient or each other (FA_ERR_ALIAS).
  */
-fa_status fa_bucket_step_writeback(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                                   float *p, const void *g, fa_dtype gdt, float *m, float *v,
-                                   float *vmax, uint64_t *t, const fa_options *options,
-                                   fa_step_control ctl, double grad_mult, void *p_model,
-                                   fa_dtype model_dtype, int32_t *updated, void *stream);
+typedef struct fa_bucket_update_args {
+    const int64_t *seg_offsets;   /* host, nseg + 1 offsets from 0 to n_total (NULL, 0: one) */
+    int32_t nseg;
+    int64_t n_total;
+    float *p;                     /* device FP32 parameters, updated in place        */
+    const void *g;                /* device gradient of type gdt                      */
+    fa_dtype gdt;
+    float *m, *v, *vmax;          /* device FP32 state; vmax only with AMSGrad        */
+    uint64_t t;                   /* completed updates                                */
+    double grad_mult;             /* host factor (1 = none)                           */
+    const double *seg_grad_mult;  /* host, one factor per segment, or NULL            */
+    const fa_stats *report;       /* device report: decision in the kernel, or NULL   */
+    const fa_stats *seg_reports;  /* device, one report per segment, or NULL          */
+    double max_grad_norm;         /* clip threshold of the device decisions (<= 0: none) */
+    void *p_model;                /* device FP16/BF16 copy of the updated p, or NULL  */
+    fa_dtype model_dtype;         /* FA_F16 or FA_BF16 when p_model is set            */
+} fa_bucket_update_args;
+
+/* Enqueues the bucket update that ``update`` describes ([FA-ja] "サポートされている
+ * 契約": a flattened bucket shares the options and the step count; the variants and
+ * their rules above).  *enqueued: 1 when an update kernel was enqueued. */
+fa_status fa_bucket_update(const fa_bucket_update_args *update, const fa_options *options,
+                           fa_step_control ctl, int32_t *enqueued, void *stream);
 
 /*
  * The staged comparison, for benchmarks only ([FA-ja] "割り当てとパフォーマンスのモデル";
@@ -289,45 +339,6 @@ fa_status fa_adamw_step_staged(int64_t n, float *p, const void *g, fa_dtype gdt,
                                float *v, float *vmax, uint64_t *t, const fa_options *options,
                                fa_step_control ctl, double grad_mult, float *delta,
                                int32_t *updated, void *stream);
-
-/*
- * fa_bucket_step whose skip / clip decision ([TR-zh] "在 ruda:0 上进行原生 PyTorch
- * 训练": a non-finite gradient skips the whole step; the global L2 clip of the
- * unscaled gradient) is taken on the device: the
- * update kernel reads ``report_dev`` (as produced by fa_merge_gradient_stats,
- * earlier on the same stream), skips when it counts a non-finite value, and
- * otherwise multiplies the unscaled gradient by the same coefficient that
- * fa_clip_decision computes on the host (max_grad_norm <= 0: no clip) --
- * the same FP64 operations in the same order, so the results are
- * bit-identical to reading the report back and calling fa_bucket_step.
- * ``t`` is the completed step count; the update uses step t+1 and this call
- * does not change any count: the caller reads the report and advances its
- * count by one unless the report shows a non-finite value.  Nothing is
- * launched for n_total == 0 or ctl.skip_update.
- */
-fa_status fa_bucket_step_gated(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                               float *p, const void *g, fa_dtype gdt, float *m, float *v,
-                               float *vmax, uint64_t t, const fa_options *options,
-                               fa_step_control ctl, const fa_stats *report_dev,
-                               double max_grad_norm, void *stream);
-
-/*
- * fa_bucket_step_writeback gated on the device report, as fa_bucket_step_gated
- * is for fa_bucket_step ([TR-zh] "FP32 主参数与混合参数存储": FP32 masters, parameters
- * returned in their storage dtype; [TR-zh] "在 ruda:0 上进行原生 PyTorch 训练": the
- * skip and the clip): the update (FP32 masters and the FP16/BF16 model copy
- * p_model, written in the same pass) skips when the report counts a non-finite
- * value and otherwise applies the host formula's clip coefficient, bit-identical
- * to reading the report back and calling fa_bucket_step_writeback.  ``t`` is the
- * completed step count and is not changed.  p_model as in
- * fa_bucket_step_writeback; a skipped update writes nothing, p_model included.
- */
-fa_status fa_bucket_step_writeback_gated(const int64_t *seg_offsets, int32_t nseg,
-                                         int64_t n_total, float *p, const void *g, fa_dtype gdt,
-                                         float *m, float *v, float *vmax, uint64_t t,
-                                         const fa_options *options, fa_step_control ctl,
-                                         const fa_stats *report_dev, double max_grad_norm,
-                                         void *p_model, fa_dtype model_dtype, void *stream);
 
 /*
  * fa_bucket_step_clipped with the update gated on the device: the analysis
@@ -454,21 +465,6 @@ fa_status fa_merge_gradient_stats_chunks(const fa_stats *rows_in, const int64_t 
                                          void *stream);
 
 /*
- * fa_bucket_step with one gradient multiplier per segment ([TR-zh] "FP32 主参数与
- * 混合参数存储": Fp32MasterOptimizer's clipping follows a per-parameter rule, not
- * a whole-model norm).  seg_grad_mult (host, nseg doubles, finite, >= 0)
- * multiplies the unscaled gradient of segment k's elements.  nseg >= 1.  One
- * launch per 240 segments.  Other arguments and the skip/empty rule as
- * fa_adamw_step_inplace.
- */
-fa_status fa_bucket_step_segment_scaled(const int64_t *seg_offsets, int32_t nseg, int64_t n_total,
-                                        float *p, const void *g, fa_dtype gdt, float *m,
-                                        float *v, float *vmax, uint64_t *t,
-                                        const fa_options *options, fa_step_control ctl,
-                                        const double *seg_grad_mult, int32_t *updated,
-                                        void *stream);
-
-/*
  * The statistics-guarded step with per-parameter clipping ([TR-zh] "FP32 主参数与
  * 混合参数存储": Fp32MasterOptimizer clips each parameter by its own rule; [TR-zh]
  * "在 ruda:0 上进行原生 PyTorch 训练": the report is read back first and a non-finite
@@ -492,33 +488,12 @@ fa_status fa_bucket_step_clipped_per_segment(
     double *seg_norms, double *seg_coefs, fa_step_report *out, void *stream);
 
 /*
- * fa_bucket_step_segment_scaled with the multipliers decided on the device
- * ([TR-zh] "FP32 主参数与混合参数存储": per-parameter clipping; [TR-zh] "在 ruda:0 上
- * 进行原生 PyTorch 训练": any non-finite gradient skips the whole step):
- * seg_reports (device, nseg records, as written by fa_merge_gradient_stats_chunks
- * earlier on the same stream) are read by the update kernels themselves.  Any
- * non-finite count skips the whole update; otherwise segment k's gradient is
- * multiplied by the clip coefficient that fa_clip_decision computes from record k
- * on the host (max_grad_norm <= 0: no clip), with the same FP64 operations in the
- * same order, so the results are bit-identical to reading the reports back and
- * calling fa_bucket_step_segment_scaled with those coefficients.  ``t`` is the
- * completed step count and is not changed: the caller reads the reports and
- * advances its count unless one counts a non-finite value.  Nothing is launched
- * for n_total == 0 or ctl.skip_update.
- */
-fa_status fa_bucket_step_per_segment_gated(const int64_t *seg_offsets, int32_t nseg,
-                                           int64_t n_total, float *p, const void *g,
-                                           fa_dtype gdt, float *m, float *v, float *vmax,
-                                           uint64_t t, const fa_options *options,
-                                           fa_step_control ctl, const fa_stats *seg_reports,
-                                           double max_grad_norm, void *stream);
-
-/*
  * fa_bucket_step_clipped_per_segment with the decision on the device ([FA-ja]
  * "ネイティブ PyTorch ストレージと階層統計": merge_gradient_stats_chunks; [TR-zh]
  * "FP32 主参数与混合参数存储": per-parameter clipping): the
  * segment-aligned analysis, the per-segment merges into seg_reports and the
- * update gated by fa_bucket_step_per_segment_gated are enqueued back to back;
+ * update deciding per segment on the device (fa_bucket_update with seg_reports)
+ * are enqueued back to back;
  * nothing is read back and the call does not wait.  Results are bit-identical to
  * fa_bucket_step_clipped_per_segment.  ``t`` is the completed step count and is
  * not changed (the caller reads seg_reports after the stream reaches them and

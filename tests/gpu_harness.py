@@ -254,8 +254,9 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
             t_new, updated = fa.fa_adamw_step_staged(st.p, st.g, st.m, st.v, st.vmax, st.t,
                                                      fopts, ctl, delta, grad_mult=grad_mult)
         elif api == "bucket" and p_model is not None:
-            t_new, updated = fa.fa_bucket_step_writeback(segs, st.p, st.g, st.m, st.v, st.vmax,
-                                                         st.t, fopts, ctl, p_model)
+            updated = fa.fa_bucket_update(segs, st.p, st.g, st.m, st.v, st.vmax, st.t, fopts,
+                                          ctl, p_model=p_model)
+            t_new = st.t + int(updated)
         elif api == "bucket":
             t_new, updated = fa.fa_bucket_step(segs, st.p, st.g, st.m, st.v, st.vmax, st.t,
                                                fopts, ctl)

@@ -251,22 +251,53 @@ def test_byte_model_matches_pages():
     assert fa.bytes_per_param(2, True, True) == 22
 
 
+def _update_record(**kw):
+    """A fa_bucket_update record with placeholder (never dereferenced) device pointers."""
+    from amsgrad_optimizer_step_gb300._lib import FaBucketUpdate
+    fake = 0x1000
+    base = dict(seg_offsets=None, nseg=0, n_total=16, p=fake, g=fake, gdt=0, m=fake, v=fake,
+                vmax=None, t=3, grad_mult=1.0, seg_grad_mult=None, report=None,
+                seg_reports=None, max_grad_norm=1.0, p_model=None, model_dtype=2)
+    base.update(kw)
+    return FaBucketUpdate(**base)
+
+
+def _update(lib, ctl=None, opts=None, **kw):
+    """Status and *enqueued of one fa_bucket_update call (no GPU: only host checks run)."""
+    u = _update_record(**kw)
+    enq = ctypes.c_int32(9)
+    st = lib.fa_bucket_update(ctypes.byref(u), ctypes.byref(opts or fa.options()),
+                              ctl or fa.control(), ctypes.byref(enq), None)
+    return st, enq.value
+
+
 def test_writeback_validation_without_gpu(lib):
-    o = fa.options()
-    t = ctypes.c_uint64(4)
-    upd = ctypes.c_int32(9)
     # model dtype must be FP16 or BF16: rejected before any pointer is looked at
-    st = lib.fa_bucket_step_writeback(None, 0, 16, None, None, 0, None, None, None,
-                                      ctypes.byref(t), ctypes.byref(o), fa.control(), 1.0,
-                                      None, 0, ctypes.byref(upd), None)
-    assert (st, t.value, upd.value) == (2, 4, 9)
+    assert _update(lib, p_model=0x2000, model_dtype=0) == (2, 9)
     # skip: nothing launched or written
-    st = lib.fa_bucket_step_writeback(None, 0, 16, None, None, 0, None, None, None,
-                                      ctypes.byref(t), ctypes.byref(o),
-                                      fa.control(skip_update=True), 1.0, None, 2,
-                                      ctypes.byref(upd), None)
-    assert (st, t.value, upd.value) == (0, 4, 0)
+    assert _update(lib, p_model=0x2000, ctl=fa.control(skip_update=True)) == (0, 0)
     assert fa.bytes_per_param(2, False, False) + 2 == 28  # write-back adds one 16-bit store
+
+
+def test_bucket_update_takes_one_multiplier_source(lib):
+    """fa_bucket_update: at most one of the per-segment factors, one report and the
+    per-segment reports; a host factor other than 1 only on its own; no model copy with
+    a per-segment source; a finite, non-negative host factor.  All checked on the host
+    before any pointer is looked at."""
+    seg = (ctypes.c_int64 * 3)(0, 8, 16)
+    mult = (ctypes.c_double * 2)(0.5, 1.0)
+    fake = 0x3000
+    assert _update(lib, report=fake, seg_reports=fake, seg_offsets=seg, nseg=2)[0] == 4
+    assert _update(lib, report=fake, seg_grad_mult=mult, seg_offsets=seg, nseg=2)[0] == 4
+    assert _update(lib, report=fake, grad_mult=0.5)[0] == 4
+    assert _update(lib, seg_grad_mult=mult, seg_offsets=seg, nseg=2, p_model=fake)[0] == 4
+    assert _update(lib, grad_mult=float("nan"))[0] == 4
+    assert _update(lib, grad_mult=-1.0)[0] == 4
+    bad = (ctypes.c_double * 2)(0.5, float("inf"))
+    assert _update(lib, seg_grad_mult=bad, seg_offsets=seg, nseg=2)[0] == 4
+    assert _update(lib, seg_grad_mult=mult)[0] == 10  # per segment needs a segment table
+    assert _update(lib, t=2 ** 64 - 1)[0] == 4          # the step count would overflow
+    assert _update(lib, ctl=fa.control(skip_update=True), report=fake) == (0, 0)
 
 
 def test_chunk_scratch_plan():
@@ -280,36 +311,30 @@ def test_chunk_scratch_plan():
 
 
 def test_device_decided_calls_validate_on_the_host(lib):
-    """The gated calls (one report, one per segment) check options, control, dtype, the
-    segment table and max_grad_norm on the host, before any pointer is looked at, and
-    launch nothing for skip_update or an empty bucket."""
+    """The device-decided updates (one report, one per segment, with or without the model
+    copy) check options, control, dtype, the segment table and max_grad_norm on the host,
+    before any pointer is looked at, and launch nothing for skip_update or an empty
+    bucket."""
     o = fa.options()
     seg = (ctypes.c_int64 * 3)(0, 8, 16)
     fake = ctypes.c_void_p(0x1000)
-    gated = (lib.fa_bucket_step_gated, lib.fa_bucket_step_writeback_gated)
-    per_seg = lib.fa_bucket_step_per_segment_gated
+    variants = (dict(report=0x1000), dict(report=0x1000, p_model=0x2000),
+                dict(seg_reports=0x1000))
 
-    def one(fn, *, ctl=None, nseg=2, table=seg, n=16, dtype=0, max_norm=1.0, opts=o):
-        ctl = ctl or fa.control()
-        if fn is per_seg:
-            return fn(table, nseg, n, fake, fake, dtype, fake, fake, None, 3, ctypes.byref(opts),
-                      ctl, fake, max_norm, None)
-        if fn is lib.fa_bucket_step_writeback_gated:
-            return fn(table, nseg, n, fake, fake, dtype, fake, fake, None, 3, ctypes.byref(opts),
-                      ctl, fake, max_norm, fake, 2, None)
-        return fn(table, nseg, n, fake, fake, dtype, fake, fake, None, 3, ctypes.byref(opts),
-                  ctl, fake, max_norm, None)
+    def one(v, *, ctl=None, nseg=2, table=seg, n=16, dtype=0, max_norm=1.0, opts=o):
+        return _update(lib, ctl=ctl, opts=opts, seg_offsets=table, nseg=nseg, n_total=n,
+                       gdt=dtype, max_grad_norm=max_norm, **v)[0]
 
     bad_opts = fa.options(lr=-1.0)
-    for fn in gated + (per_seg,):
-        assert one(fn, opts=bad_opts) == 4
-        assert one(fn, ctl=fa.control(gradient_scale=0.0)) == 4
-        assert one(fn, dtype=7) == 2
-        assert one(fn, max_norm=float("nan")) == 4
-        assert one(fn, table=(ctypes.c_int64 * 3)(0, 9, 8), n=8) == 10  # FA_ERR_SEGMENTS
-        assert one(fn, ctl=fa.control(skip_update=True)) == 0  # nothing launched
-        assert one(fn, table=(ctypes.c_int64 * 3)(0, 0, 0), n=0) == 0
-    assert one(per_seg, nseg=0, table=None) == 10  # a segment table is required
+    for v in variants:
+        assert one(v, opts=bad_opts) == 4
+        assert one(v, ctl=fa.control(gradient_scale=0.0)) == 4
+        assert one(v, dtype=7) == 2
+        assert one(v, max_norm=float("nan")) == 4
+        assert one(v, table=(ctypes.c_int64 * 3)(0, 9, 8), n=8) == 10  # FA_ERR_SEGMENTS
+        assert one(v, ctl=fa.control(skip_update=True)) == 0  # nothing launched
+        assert one(v, table=(ctypes.c_int64 * 3)(0, 0, 0), n=0) == 0
+    assert one(variants[2], nseg=0, table=None) == 10  # a segment table is required
 
     # the one-call per-segment form: row length and scratch checked first as well
     def clipped(row_len=256, scratch=1 << 20, ctl=None, nseg=2, table=seg):

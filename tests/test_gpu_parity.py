@@ -735,8 +735,9 @@ def test_writeback_misaligned_model_view(oracle_lib):
     t = 0
     for call in (1, 2):
         w.fill_grad_device(call, g)
-        t, _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, t, fa.options(**w.options()),
-                                           fa.control(), model)
+        assert fa.fa_bucket_update(None, p, g, m, v, None, t, fa.options(**w.options()),
+                                   fa.control(), p_model=model)
+        t += 1
     torch.cuda.synchronize()
     bits = model.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(bits, oracle_lib.model_copy(p.cpu().numpy(), "bf16"))
@@ -750,15 +751,16 @@ def test_writeback_rejections():
     o = fa.options()
     import ctypes
     from amsgrad_optimizer_step_gb300 import _lib
-    tt, up = ctypes.c_uint64(1), ctypes.c_int32()
-    st = _lib.load().fa_bucket_step_writeback(None, 0, n, p.data_ptr(), g.data_ptr(), 0,
-                                              m.data_ptr(), v.data_ptr(), None, ctypes.byref(tt),
-                                              ctypes.byref(o), fa.control(), 1.0,
-                                              model.data_ptr(), 0, ctypes.byref(up), None)
+    up = ctypes.c_int32()
+    u = _lib.FaBucketUpdate(n_total=n, p=p.data_ptr(), g=g.data_ptr(), gdt=0, m=m.data_ptr(),
+                            v=v.data_ptr(), t=1, grad_mult=1.0, p_model=model.data_ptr(),
+                            model_dtype=0)
+    st = _lib.load().fa_bucket_update(ctypes.byref(u), ctypes.byref(o), fa.control(),
+                                      ctypes.byref(up), None)
     assert st == 2  # FP32 is not a model-copy dtype
     with pytest.raises(fa.FusedAdamWError) as e:
-        fa.fa_bucket_step_writeback(None, p, g, m, v, None, 1, o, fa.control(),
-                                    p.view(torch.bfloat16)[:n])
+        fa.fa_bucket_update(None, p, g, m, v, None, 1, o, fa.control(),
+                            p_model=p.view(torch.bfloat16)[:n])
     assert e.value.status == 5
     assert not model.view(torch.int16).any()
 
@@ -919,17 +921,17 @@ def test_gated_writeback_equals_host_decided_writeback_bitwise(model_dtype):
             fa.fa_merge_gradient_stats(rb, rows, sc, rep)
             o = fa.options(**w.options())
             if gated:
-                fa.fa_bucket_step_writeback_gated(None, p, g, m, v, None, t, o, fa.control(),
-                                                  rep, 0.5, model)
+                fa.fa_bucket_update(None, p, g, m, v, None, t, o, fa.control(), report=rep,
+                                    max_grad_norm=0.5, p_model=model)
                 h = fa.fa_read_report(rep)
-                skip, _, _ = fa.fa_clip_decision(float(h.sum_sq) + float(h.sum_sq_lo),
-                                                 h.nonfinite, 1.0, 0.5)
+                skip, _, _ = fa.fa_clip_decision(fa.fa_stats_sum_sq(h), h.nonfinite, 1.0, 0.5)
                 t += 0 if skip else 1
             else:
                 skip, _, coef = fa.fa_clip_decide(rep, 1.0, 0.5)
                 if not skip:
-                    t, _ = fa.fa_bucket_step_writeback(None, p, g, m, v, None, t, o,
-                                                       fa.control(), model, coef)
+                    assert fa.fa_bucket_update(None, p, g, m, v, None, t, o, fa.control(),
+                                               grad_mult=coef, p_model=model)
+                    t += 1
         torch.cuda.synchronize()
         states.append((t, p.clone(), m.clone(), v.clone(), model.clone()))
     (ta, *a), (tb, *b) = states
@@ -947,11 +949,13 @@ def test_gated_update_skips_on_non_finite_report():
     snap = [x.clone() for x in (p, m, v)]
     report = torch.zeros((1, 3), dtype=torch.int32, device=DEV)
     report[0, 1] = 2  # two non-finite values
-    fa.fa_bucket_step_gated(None, p, g, m, v, None, 4, fa.options(), fa.control(), report, 1.0)
+    fa.fa_bucket_update(None, p, g, m, v, None, 4, fa.options(), fa.control(), report=report,
+                        max_grad_norm=1.0)
     torch.cuda.synchronize()
     assert all(torch.equal(a, b) for a, b in zip((p, m, v), snap))
     report[0, 1] = 0
     report[0, 0] = torch.tensor([4.0], dtype=torch.float32).view(torch.int32)
-    fa.fa_bucket_step_gated(None, p, g, m, v, None, 4, fa.options(), fa.control(), report, 1.0)
+    fa.fa_bucket_update(None, p, g, m, v, None, 4, fa.options(), fa.control(), report=report,
+                        max_grad_norm=1.0)
     torch.cuda.synchronize()
     assert not torch.equal(p, snap[0])

@@ -91,8 +91,9 @@ def test_uniform_multipliers_equal_the_bucket_step_bitwise():
     for call in range(1, 4):
         w.fill_grad_device(call, g)
         ta, _ = fa.fa_bucket_step(list(seg), pa, g, *sa, ta, o, fa.control(2.0), 0.75)
-        tb, _ = fa.fa_bucket_step_segment_scaled(list(seg), pb, g, *sb, tb, o, fa.control(2.0),
-                                                 [0.75] * (len(seg) - 1))
+        assert fa.fa_bucket_update(list(seg), pb, g, *sb, tb, o, fa.control(2.0),
+                                   seg_grad_mult=[0.75] * (len(seg) - 1))
+        tb += 1
     torch.cuda.synchronize()
     assert ta == tb == 3
     assert torch.equal(pa, pb) and all(torch.equal(x, y) for x, y in zip(sa, sb))
@@ -114,7 +115,9 @@ def test_segment_multipliers_vs_oracle(gdt, oracle_lib):
     for call in range(1, 4):
         mult = rng.uniform(0.1, 1.0, len(seg) - 1)
         w.fill_grad_device(call, g)
-        t, _ = fa.fa_bucket_step_segment_scaled(list(seg), p, g, m, v, vm, t, o, fa.control(), mult)
+        assert fa.fa_bucket_update(list(seg), p, g, m, v, vm, t, o, fa.control(),
+                                   seg_grad_mult=mult)
+        t += 1
         bits = grad_bits_from_device(g)
         for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
             refs[k].step(bits[a:b], gdt, clip_coef=float(mult[k]))
@@ -150,7 +153,9 @@ def test_segment_multipliers_mixed_sizes_vs_oracle(gdt, maximize, oracle_lib):
     for call in range(1, 4):
         mult = rng.uniform(0.1, 1.0, len(seg) - 1)
         w.fill_grad_device(call, g)
-        t, _ = fa.fa_bucket_step_segment_scaled(list(seg), p, g, m, v, vm, t, o, fa.control(), mult)
+        assert fa.fa_bucket_update(list(seg), p, g, m, v, vm, t, o, fa.control(),
+                                   seg_grad_mult=mult)
+        t += 1
         bits = grad_bits_from_device(g)
         for k, (a, b) in enumerate(zip(seg[:-1], seg[1:])):
             refs[k].step(bits[a:b], gdt, clip_coef=float(mult[k]))
