@@ -340,6 +340,39 @@ def cpu_baseline(w, target_s=12.0):
     return out
 
 
+def hbm_mix_rates(dev, n: int = 1 << 30, reps: int = 5) -> dict:
+    """HBM rates (GB/s, best of ``reps``, CUDA events) of PyTorch's own streaming
+    kernels, one per read:write byte mix, on buffers of n FP32 values (4 GiB each, far
+    above L2): read only (sum), write only (fill), 1:1 (copy), 2:1 (add) and 1:2 (frexp:
+    an FP32 value in, its FP32 mantissa and int32 exponent out).  HBM does not move every
+    mix at the copy rate; these are the ceilings the fused kernels' own mixes are read
+    against (the first step moves 6 B in and 12 B out per parameter, the analysis
+    only reads)."""
+    import torch
+    a = torch.rand(n, device=dev)
+    b = torch.rand(n, device=dev)
+    c = torch.empty(n, device=dev)
+    e = torch.empty(n, dtype=torch.int32, device=dev)
+    ops = {"read_only": (lambda: a.sum(), 4), "write_only": (lambda: c.fill_(1.5), 4),
+           "copy_1r_1w": (lambda: c.copy_(a), 8), "add_2r_1w": (lambda: torch.add(a, b, out=c), 12),
+           "frexp_1r_2w": (lambda: torch.frexp(a, out=(c, e)), 12)}
+    out = {}
+    for name, (fn, bytes_per_elem) in ops.items():
+        fn()
+        best = float("inf")
+        for _ in range(reps):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            fn()
+            t1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, t0.elapsed_time(t1))
+        out[name] = bytes_per_elem * n / (best * 1e-3) / 1e9
+    del a, b, c, e
+    torch.cuda.empty_cache()
+    return out
+
+
 def parity_indices(n: int, k: int = 40_000, seed: int = 0):
     """Sorted sample of element indices checked against the oracle: k seeded random
     ones plus both ends, the first vectors and 16-byte boundaries, the neighbours of
@@ -747,6 +780,13 @@ def run_ours(args):
                               "params_per_s": n / (ms * 1e-3)}
         del p_model
 
+        # the HBM ceiling of each read:write mix, measured with PyTorch's kernels: the
+        # first step (6 B in, 12 B out per parameter) is read against the 1:2 mix
+        mixes = hbm_mix_rates(dev)
+        rows_out["hbm_mix_rates_gbs"] = mixes
+        rows_out["first_step"]["frac_of_1r_2w_mix"] = (rows_out["first_step"]["achieved_gbs"]
+                                                       / mixes["frexp_1r_2w"])
+
         # f2: the pages' staged baseline against the fused update, on FP32
         # gradients (the case their 48 -> 28 and 60 -> 36 B/param model is stated
         # for), AdamW and AMSGrad, same resident state.
@@ -956,7 +996,10 @@ def run_ours(args):
                            "what": "host clock over the timed steps: submission, the "
                                    "12-byte read-back and the decision included"},
             "stats_path": {"ms_median": st_ms, "analyze_bytes": n * 2 + rows * 12,
-                           "achieved_gbs": (n * 2 + rows * 12) / (st_ms * 1e-3) / 1e9},
+                           "achieved_gbs": (n * 2 + rows * 12) / (st_ms * 1e-3) / 1e9,
+                           "what": "analysis and merges, CUDA events inside the step (with "
+                                   "the reduce-scatter at N > 1); a read-only stream, read "
+                                   "against next_rows.hbm_mix_rates_gbs.read_only"},
             "gpu_launches": timed_launches,
             "clocks": clock_info,
             "host": host_info(),
