@@ -959,3 +959,58 @@ def test_gated_update_skips_on_non_finite_report():
                         max_grad_norm=1.0)
     torch.cuda.synchronize()
     assert not torch.equal(p, snap[0])
+
+
+def test_report_mailbox_rules():
+    """The one-call device-gated step reads its report through the caller's mailbox:
+    pageable host memory, device memory and NULL are rejected before anything is
+    enqueued (state untouched); a sequence word at 2^32 - 1 wraps to 0; calls in a row
+    on one mailbox each read their own report."""
+    import ctypes
+    from amsgrad_optimizer_step_gb300 import _lib
+    n = 256 * 4000 + 5
+    w = CONFIG5.scaled(n, calls=3, inf_call=2)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p)
+    m, v = torch.zeros_like(p), torch.zeros_like(p)
+    g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    w.fill_grad_device(1, g)
+    rows = fa.fa_stats_rows(n, 256)
+    rb, sc, rep = fa.stats_buffer(rows, DEV), fa.scratch_buffer(rows, DEV), fa.stats_buffer(1, DEV)
+    o = fa.options(**w.options())
+    lib = _lib.load()
+    snap = [x.clone() for x in (p, m, v)]
+
+    def raw(mailbox_ptr):
+        tt = ctypes.c_uint64(0)
+        out = fa.FaStepReport()
+        return lib.fa_bucket_step_clipped_gated(
+            None, 0, n, p.data_ptr(), g.data_ptr(), 2, m.data_ptr(), v.data_ptr(), None,
+            ctypes.byref(tt), ctypes.byref(o), fa.control(), w.max_grad_norm, 256,
+            rb.data_ptr(), rb.shape[0], sc.data_ptr(), sc.numel(), rep.data_ptr(),
+            mailbox_ptr, ctypes.byref(out), None)
+
+    pageable = np.zeros(4, np.uint32)
+    assert raw(pageable.ctypes.data) == 6            # FA_ERR_POINTER: not pinned
+    assert raw(torch.zeros(4, dtype=torch.int32, device=DEV).data_ptr()) == 6  # device memory
+    assert raw(None) == 1                             # FA_ERR_NULL
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip((p, m, v), snap))
+    with pytest.raises(ValueError):
+        fa.fa_bucket_step_clipped_gated(None, p, g, m, v, None, 0, o, fa.control(),
+                                        w.max_grad_norm, 256, rb, sc, rep,
+                                        torch.zeros(4, dtype=torch.int32))  # not pinned
+
+    mailbox = fa.report_mailbox()
+    mailbox[3] = -1  # sequence word 2^32 - 1: the next post is 0
+    t = 0
+    reports = []
+    for call in range(1, w.calls + 1):
+        w.fill_grad_device(call, g)
+        t, r = fa.fa_bucket_step_clipped_gated(None, p, g, m, v, None, t, o, fa.control(),
+                                               w.max_grad_norm, 256, rb, sc, rep, mailbox)
+        reports.append((r.skipped_nonfinite, r.nonfinite, r.grad_norm))
+        assert int(mailbox[3]) == call - 1  # 0, 1, 2
+    torch.cuda.synchronize()
+    assert t == 2 and [x[0] for x in reports] == [0, 1, 0] and reports[1][1] == 1
+    assert reports[0][2] > 0 and reports[2][2] > 0 and reports[0][2] != reports[2][2]
