@@ -562,9 +562,8 @@ __device__ __forceinline__ void warp_merge(const fa_stats *__restrict__ in, int6
 
 constexpr int kMergeWarps = kThreads / 32;  // groups (or chunks) per CTA
 
-// One warp per group of kFanIn input records, eight groups per CTA, so that the
-// 4096 groups of the largest plan run in a single wave (one CTA per group took
-// three and a half).
+// One warp per group of kFanIn input records, eight groups per CTA: the 4096
+// groups of the largest plan take 512 CTAs instead of 4096.
 // ``post`` (the final level only; nullptr otherwise) is the device address of a
 // report mailbox in pinned host memory: the report is also stored there, then, after
 // a system-wide fence, ``seq``, so a host that sees seq reads the whole report.
