@@ -79,6 +79,18 @@ def test_shards_are_contiguous_aligned_and_balanced(n, world):
 
 
 @SETTINGS
+@given(n=st.integers(0, 10 ** 10), world=st.integers(1, 64))
+def test_zero1_shards_cover_the_bucket_aligned_and_minimal(n, world):
+    """The ZeRO-1 shard length: world equal shards of S elements cover the n-element
+    bucket, S is a multiple of 8 (every shard starts 16-byte aligned in an aligned FP32
+    buffer), and S is the smallest such length, so the padding is under 8 * world."""
+    s = sharded.zero1_shard_len(n, world)
+    assert s % 8 == 0 and s * world >= n
+    assert s == 0 or (s - 8) * world < n
+    assert s * world - n < 8 * world or n == 0
+
+
+@SETTINGS
 @given(data=st.lists(st.tuples(st.booleans(), st.integers(0, 3), st.integers(0, 40)),
                      min_size=1, max_size=30))
 def test_active_runs_cover_exactly_the_active_parameters(data):
