@@ -16,8 +16,10 @@ import pytest
 import torch
 
 import amsgrad_optimizer_step_gb300 as fa
+import test_gpu_bucket_update as U
 import test_gpu_parity as P
 import test_gpu_segments as S
+import test_gpu_square_overflow as O
 from amsgrad_optimizer_step_gb300 import _lib, build
 from synthetic.configs import CONFIG3, CONFIG4
 
@@ -67,6 +69,17 @@ CASES = [
     ("per-segment decision on the device",
      lambda lib: [S.test_per_segment_gated_equals_host_decision_bitwise(*k) for k in (
          ("mixed", "f16", False), ("many", "f32", False), ("offset", "bf16", False))]),
+    ("staged comparison vs the oracle, scalar tail",
+     lambda lib: P.test_staged_vs_oracle("f16", True, 70_001)),
+    ("rows whose squares overflow FP32, rescued",
+     lambda lib: [O.test_rows_and_report_with_squares_beyond_fp32(gdt, *layout, lib)
+                  for gdt in ("f32", "bf16") for layout in O.LAYOUTS]),
+    ("merges in the scaled domain",
+     lambda lib: O.test_merge_moves_to_the_scaled_domain(5e37, 3000)),
+    ("device-decided steps with an overflowing value, report through the mailbox",
+     lambda lib: O.test_gated_steps_equal_host_decided_with_an_overflowing_value()),
+    ("the descriptor call in random variants",
+     lambda lib: [U.test_bucket_update_random_variant_vs_oracle(k, lib) for k in range(8)]),
 ]
 
 
