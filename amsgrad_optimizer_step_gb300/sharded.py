@@ -133,7 +133,7 @@ class Zero1Step:
 
     def _reduce_scatter(self, g: torch.Tensor) -> None:
         import torch.distributed as dist
-        if self.world == 1:
+        if not self.distributed:
             self.g_shard.copy_(g[:self.shard])
         elif self.nccl:
             dist.reduce_scatter_tensor(self.g_shard, g, op=dist.ReduceOp.SUM, group=self.group)
@@ -145,7 +145,7 @@ class Zero1Step:
     def _all_gather(self, p: torch.Tensor) -> None:
         import torch.distributed as dist
         mine = p[self.rank * self.shard:(self.rank + 1) * self.shard]
-        if self.world == 1:
+        if not self.distributed:
             return
         if self.nccl:  # in place: each rank's input is its own slice of the output
             dist.all_gather_into_tensor(p, mine, group=self.group)

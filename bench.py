@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--next-rows-steps", type=int, default=10)
     # gloo stages the collectives through the host: for ranks sharing one GPU (testing)
     ap.add_argument("--dist-backend", choices=["nccl", "gloo"], default="nccl")
+    # the ZeRO-1 step even on one rank (under torchrun: its collectives then stay on the GPU)
+    ap.add_argument("--zero1", action="store_true")
     # (under torchrun spell it --params: torchrun's own parser takes --n for one of its flags)
     ap.add_argument("--params", "--n", dest="n", type=int, default=0,
                     help="override the parameter count (testing)")
@@ -476,9 +478,11 @@ def run_ours(args):
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    distributed = world > 1 or (args.zero1 and "WORLD_SIZE" in os.environ)
+    zero1 = world > 1 or args.zero1
     # one rank per GPU; ranks beyond the visible GPUs share them (testing with gloo)
     local = int(os.environ.get("LOCAL_RANK", "0")) % max(1, torch.cuda.device_count())
-    if world > 1:
+    if distributed:
         torch.cuda.set_device(local)
         if args.dist_backend == "nccl":
             dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -500,7 +504,7 @@ def run_ours(args):
         return float(tt.item())
 
     zstep = None
-    if world == 1:
+    if not zero1:
         # resident inputs: the whole bucket
         p = torch.empty(n, dtype=torch.float32, device=dev)
         w.fill_params_device(p)
@@ -544,9 +548,9 @@ def run_ours(args):
         One GPU: the update is gated on the device by the same report, so it
         follows the merge without a host round trip; the host reads the report
         (pinned copy) meanwhile and advances t unless the step was skipped.
-        Several ranks: the ZeRO-1 step (reduce-scatter, shard statistics, the
-        exchange of the ranks' totals and one decision on the host, the shard's
-        update, all-gather)."""
+        Several ranks (or --zero1): the ZeRO-1 step (reduce-scatter, shard
+        statistics, the exchange of the ranks' totals and one decision on the host,
+        the shard's update, all-gather)."""
         if ev: ev[0].record(stream)
         if zstep is not None:
             d = zstep.step(p, g, events=ev[1:] if ev else None)
@@ -558,23 +562,21 @@ def run_ours(args):
         fa.fa_merge_gradient_stats(rows_buf, rows, scratch, report)
         if ev: ev[1].record(stream)
         launches["n"] += 1 + merge_kernels
-        if world == 1:
-            rep_pinned.copy_(report, non_blocking=True)
-            rep_arrived.record(stream)
-            if ev: ev[2].record(stream)
-            fa.fa_bucket_update(None, p, g, m, v, None, state["t"], opts, ctl, report=report,
-                                max_grad_norm=w.max_grad_norm)
-            launches["n"] += 1
-            if ev: ev[3].record(stream)
-            rep_arrived.synchronize()
-            h = fa.FaStats.from_buffer_copy(rep_pinned.numpy().tobytes())
-            skip, norm, _ = fa.fa_clip_decision(fa.fa_stats_sum_sq(h), int(h.nonfinite),
-                                                w.gradient_scale, w.max_grad_norm)
-            if not skip:
-                state["t"] += 1
-            state["last"] = (norm, int(h.nonfinite), bool(skip))
-            return norm
-        raise AssertionError("unreachable: several ranks run the ZeRO-1 step")
+        rep_pinned.copy_(report, non_blocking=True)
+        rep_arrived.record(stream)
+        if ev: ev[2].record(stream)
+        fa.fa_bucket_update(None, p, g, m, v, None, state["t"], opts, ctl, report=report,
+                            max_grad_norm=w.max_grad_norm)
+        launches["n"] += 1
+        if ev: ev[3].record(stream)
+        rep_arrived.synchronize()
+        h = fa.FaStats.from_buffer_copy(rep_pinned.numpy().tobytes())
+        skip, norm, _ = fa.fa_clip_decision(fa.fa_stats_sum_sq(h), int(h.nonfinite),
+                                            w.gradient_scale, w.max_grad_norm)
+        if not skip:
+            state["t"] += 1
+        state["last"] = (norm, int(h.nonfinite), bool(skip))
+        return norm
 
     for _ in range(args.warmup):
         step()
@@ -596,7 +598,7 @@ def run_ours(args):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     launches["n"] = 0
-    if world > 1:
+    if distributed:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
@@ -606,7 +608,7 @@ def run_ours(args):
     end.record(stream)
     torch.cuda.synchronize(dev)
     wall_ms = (time.perf_counter() - wall0) * 1e3
-    if world > 1:
+    if distributed:
         dist.barrier()
     total_ms = start.elapsed_time(end)
     clock_info = clocks.stop() if rank == 0 else None
@@ -615,7 +617,7 @@ def run_ours(args):
     stats_ms = [e[0].elapsed_time(e[1]) for e in evs]
     update_ms = [e[2].elapsed_time(e[3]) for e in evs]
     step_each = [e[0].elapsed_time(e[3]) for e in evs]
-    if world > 1:
+    if distributed:
         total_ms = max_over_ranks(total_ms)
 
     # The timed run's state at sampled elements, for the oracle replay at the end
@@ -708,7 +710,7 @@ def run_ours(args):
         # untimed warm-up through the same call
         run_e2e(min(args.warmup, args.e2e_steps))
         torch.cuda.synchronize(dev)
-        if world > 1:
+        if distributed:
             dist.barrier()
         t0 = time.perf_counter()
         host_step = run_e2e(args.e2e_steps)
@@ -716,7 +718,7 @@ def run_ours(args):
         e2e_s = time.perf_counter() - t0
         copy_ms = statistics.median(e[0].elapsed_time(e[1]) for e in cp_ev)
         step_ms = statistics.median(e[0].elapsed_time(e[1]) for e in st_ev)
-        if world > 1:
+        if distributed:
             e2e_s = max_over_ranks(e2e_s)
         e2e = {"value": world * n * args.e2e_steps / e2e_s, "unit": UNIT,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 12,
@@ -730,7 +732,7 @@ def run_ours(args):
                "what": ("pinned-host BF16 gradient copied in every step (side stream, double "
                         "buffered), then the C-ABI statistics-guarded step (analyse, merge, "
                         "12-byte report read back, update gated on the same decision); "
-                        "wall clock") if world == 1 else
+                        "wall clock") if zstep is None else
                        ("each rank's full pinned-host BF16 gradient copied in every step (side "
                         "stream, double buffered), then the ZeRO-1 step (reduce-scatter, shard "
                         "statistics, 12-byte exchange, shard update, all-gather); wall clock, "
@@ -740,7 +742,7 @@ def run_ours(args):
     # CUDA events per launch): the plain update and the fused low-precision
     # write-back (BF16 model copy, +2 B/param).
     next_rows = None
-    if args.next_rows_steps > 0 and world == 1:  # the single-GPU rows, at N = 1 only
+    if args.next_rows_steps > 0 and not zero1:  # the single-GPU rows, at N = 1 only
         p_model = torch.empty(n, dtype=torch.bfloat16, device=dev)
 
         def timed(fn, k):
@@ -1007,8 +1009,9 @@ def run_ours(args):
             "e2e": e2e,
             "next_rows": next_rows,
         }
-        if world > 1:
+        if zero1:
             line["config"]["parallelism"] = f"dp{world}, ZeRO-1 (optimizer state sharded)"
+        if world > 1:
             line["parity"] = {"ok": None, "checked": False,
                               "why": "the oracle runs in the CPU leg at N = 1 only; the "
                                      "ZeRO-1 step is checked against the oracle over the whole "
@@ -1029,7 +1032,7 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
         if rc:
             return rc
-    if world > 1:
+    if distributed:
         dist.barrier()
         dist.destroy_process_group()
     return 0

@@ -218,3 +218,92 @@ def test_bench_runs_the_zero1_step_with_two_ranks_on_one_gpu():
     # per step: one analysis, two merge levels (4096 rows), one update
     assert line["gpu_launches"] == 3 * 4
     assert line["e2e"]["h2d_bytes_per_step"] == 2 * 1048576 * 2
+
+
+def _zero1_nccl_rank(rank, port, n, out_dir):
+    import sys
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import torch
+    import torch.distributed as dist
+    import amsgrad_optimizer_step_gb300 as fa
+    from amsgrad_optimizer_step_gb300 import sharded
+    import zero1_inputs as Z
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    os.environ["NCCL_NVLS_ENABLE"] = "0"
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dist.init_process_group("nccl", rank=rank, world_size=1, device_id=dev)
+    opts = fa.options(lr=2e-3, weight_decay=0.01, amsgrad=True)
+    step = sharded.Zero1Step(n, opts, torch.bfloat16, dev, max_grad_norm=0.5, gradient_scale=2.0)
+    assert step.nccl and step.distributed
+    p = torch.zeros(step.padded, device=dev)
+    p[:n] = torch.from_numpy(Z.params(n)).to(dev)
+    g = torch.empty(step.padded, dtype=torch.bfloat16, device=dev)
+    decisions = []
+    for call in range(1, 4):
+        bits = Z.rank_gradient(n, step.padded, 0, call, "bf16", 77 if call == 2 else None)
+        g.copy_(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16))
+        d = step.step(p, g)
+        decisions.append([d["skipped"], d["nonfinite"], repr(d["grad_norm"])])
+    torch.cuda.synchronize()
+    np.savez(os.path.join(out_dir, "nccl.npz"), p=p.cpu().numpy(), m=step.m.cpu().numpy(),
+             v=step.v.cpu().numpy(), vmax=step.vmax.cpu().numpy(), t=step.t)
+    with open(os.path.join(out_dir, "nccl.json"), "w") as f:
+        json.dump(decisions, f)
+    dist.destroy_process_group()
+
+
+def test_zero1_step_on_a_one_rank_nccl_group_matches_the_oracle(tmp_path, oracle_lib):
+    """The ZeRO-1 step's NCCL branch on the one GPU there is: a one-rank NCCL group, so
+    reduce_scatter_tensor and the in-place all_gather_into_tensor run on the device buffers
+    (moving data within the GPU).  Against the oracle over the whole bucket, with a +Inf
+    in the second of three calls."""
+    import oracle
+    import zero1_inputs as Z
+    from amsgrad_optimizer_step_gb300 import build
+    from gpu_harness import gate
+    build.build()
+    n = 1_000_003
+    mp.spawn(_zero1_nccl_rank, args=(_free_port(), n, str(tmp_path)), nprocs=1, join=True)
+    res = np.load(tmp_path / "nccl.npz")
+    dec = json.load(open(tmp_path / "nccl.json"))
+    opts = dict(lr=2e-3, beta1=0.9, beta2=0.999, eps=1e-5, weight_decay=0.01, amsgrad=True,
+                maximize=False)
+    ref = oracle.OracleAdamW(Z.params(n).astype(np.float64), opts, storage="f32",
+                             lib_=oracle_lib)
+    inf = (2, 0, 77)
+    for call in range(1, 4):
+        bits = Z.reduced_gradient(n, 1, call, "bf16", inf)
+        s, c = oracle_lib.gradient_stats(bits, "bf16", 2.0)
+        skip, norm, coef = oracle_lib.clip_decision(s, c, 0.5)
+        assert dec[call - 1][0] == skip and dec[call - 1][1] == c
+        if not skip:
+            assert abs(float(dec[call - 1][2]) - norm) <= 1e-5 * norm
+        ref.step(bits, "bf16", 2.0, skip_update=skip, clip_coef=coef)
+    assert int(res["t"]) == ref.state.t == 2
+    gate(res["p"][:n], ref.p, 1e-5, "p")
+    gate(res["m"][:n], ref.state.m, 1e-5, "m")
+    gate(res["v"][:n], ref.state.v, 1e-5, "v")
+    gate(res["vmax"][:n], ref.state.vmax, 1e-5, "vmax")
+
+
+def test_bench_zero1_step_over_nccl_checks_its_own_parity():
+    """bench.py --zero1 under torchrun with one rank over NCCL: the ZeRO-1 step's NCCL
+    collectives on the device buffers, timed, and the bench's own oracle replay of the
+    timed run must pass (parity.ok)."""
+    import subprocess
+    import sys
+    env = dict(os.environ, NCCL_NVLS_ENABLE="0")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "1",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(ROOT, "bench.py"), "--gpus", "1", "--steps", "3", "--warmup", "3",
+           "--params", "1048576", "--e2e-steps", "2", "--no-cpu-baseline", "--zero1"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900, env=env)
+    assert r.returncode == 0, (r.stdout[-2000:], r.stderr[-3000:])
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    assert line["config"]["parallelism"].startswith("dp1, ZeRO-1")
+    assert line["parity"]["ok"] is True and line["parity"]["t"] == 6
+    assert line["value"] > 0 and line["gpu_launches"] == 3 * 4
