@@ -8,9 +8,12 @@
  * Inputs are integer hashes scaled by powers of two, exact in FP32, so the test
  * that runs this program can rebuild them bit for bit.  With "gated", every step
  * goes through fa_bucket_step_clipped_gated (the update decides on the device)
- * instead of fa_bucket_step_clipped; the results must be the same bits.
+ * instead of fa_bucket_step_clipped; with "descriptor", every step is composed
+ * from the separate calls: fa_analyze_gradient, fa_merge_gradient_stats,
+ * fa_bucket_update with the device report, fa_read_report, fa_stats_sum_sq and
+ * fa_clip_decision.  The results must be the same bits in every mode.
  *
- *   consumer <n> <output file> [gated]
+ *   consumer <n> <output file> [gated | descriptor]
  */
 #include <string.h>
 #include <stdint.h>
@@ -55,11 +58,13 @@ static float sample(uint32_t stream, uint32_t i, float scale) {
     } while (0)
 
 int main(int argc, char **argv) {
-    if (argc != 3 && !(argc == 4 && strcmp(argv[3], "gated") == 0)) {
-        fprintf(stderr, "usage: consumer <n> <output file> [gated]\n");
+    if (argc != 3 && !(argc == 4 && (strcmp(argv[3], "gated") == 0 ||
+                                     strcmp(argv[3], "descriptor") == 0))) {
+        fprintf(stderr, "usage: consumer <n> <output file> [gated | descriptor]\n");
         return 1;
     }
-    const int gated = argc == 4;
+    const int gated = argc == 4 && strcmp(argv[3], "gated") == 0;
+    const int descriptor = argc == 4 && strcmp(argv[3], "descriptor") == 0;
     const int64_t n = atoll(argv[1]);
     if (n < 2) return 1;
     const int32_t row_len = 256;
@@ -100,7 +105,43 @@ int main(int argc, char **argv) {
         for (int64_t i = 0; i < n; ++i) h[i] = sample(100u + (uint32_t)call, (uint32_t)i, 0.0625f);
         if (call == 2) h[n / 2] = 1.0f / 0.0f; /* +Inf: this step is skipped */
         CHECK_CUDA(cudaMemcpy(g, h, (size_t)n * 4, cudaMemcpyHostToDevice));
-        if (gated)
+        if (descriptor) {
+            /* the step from the separate calls; the update decides on the device */
+            CHECK_FA(fa_analyze_gradient(g, FA_F32, n, row_len, NULL, 0, rows_buf, rows, stream));
+            CHECK_FA(fa_merge_gradient_stats(rows_buf, rows, scratch, scratch_elems, report,
+                                             stream));
+            fa_bucket_update_args u;
+            memset(&u, 0, sizeof u);
+            u.n_total = n;
+            u.p = p;
+            u.g = g;
+            u.gdt = FA_F32;
+            u.m = m;
+            u.v = v;
+            u.t = t;
+            u.grad_mult = 1.0;
+            u.report = report;
+            u.max_grad_norm = 0.5;
+            u.model_dtype = FA_BF16;
+            int32_t enqueued = 0;
+            CHECK_FA(fa_bucket_update(&u, &o, ctl, &enqueued, stream));
+            fa_stats h;
+            double sum = 0.0, norm = 0.0, coef = 1.0;
+            int32_t skip = 0;
+            CHECK_FA(fa_read_report(report, &h, stream));
+            CHECK_FA(fa_stats_sum_sq(&h, &sum));
+            CHECK_FA(fa_clip_decision(sum, h.nonfinite, ctl.gradient_scale, 0.5, &skip, &norm,
+                                      &coef));
+            fa_step_report r;
+            memset(&r, 0, sizeof r);
+            r.updated = enqueued && !skip;
+            r.skipped_nonfinite = skip;
+            r.nonfinite = h.nonfinite;
+            r.grad_norm = norm;
+            r.clip_coef = coef;
+            reps[call - 1] = r;
+            if (!skip) t += 1;
+        } else if (gated)
             CHECK_FA(fa_bucket_step_clipped_gated(NULL, 0, n, p, g, FA_F32, m, v, NULL, &t, &o,
                                                   ctl, 0.5, row_len, rows_buf, rows, scratch,
                                                   scratch_elems, report, mailbox,

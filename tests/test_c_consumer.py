@@ -5,7 +5,9 @@ runtime, allocates its own device buffers and runs three statistics-guarded step
 (the second with a +Inf, so skipped).  On the CPU the header and the program must
 compile as strict C; on the GPU the program is built, linked against the library and
 run, and its output is compared with the oracle.  Run again with the update decided on
-the device (fa_bucket_step_clipped_gated), it must write the same bits.
+the device (fa_bucket_step_clipped_gated), and composed from the separate calls (the
+descriptor update fa_bucket_update deciding from the device report), it must write the
+same bits.
 """
 
 import os
@@ -87,6 +89,11 @@ def test_consumer_runs_and_matches_the_oracle(oracle_lib, tmp_path):
                        timeout=120)
     assert r.returncode == 0, r.stderr
     assert open(out_gated, "rb").read() == raw, "the device-decided steps wrote other bits"
+    out_desc = str(tmp_path / "out_descriptor.bin")
+    r = subprocess.run([exe, str(n), out_desc, "descriptor"], capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert open(out_desc, "rb").read() == raw, "the steps composed from the separate calls differ"
     t = struct.unpack_from("<Q", raw, 0)[0]
     reps = [struct.unpack_from("<iiQdd", raw, 8 + 32 * k) for k in range(3)]
     arrays = np.frombuffer(raw, dtype=np.float32, offset=8 + 96).reshape(3, n)
