@@ -439,6 +439,12 @@ def test_skip_and_empty_launch_nothing():
 
 # ---- statistics kernels ---------------------------------------------------------
 
+def grad_bits(t):
+    """Storage bits of a device gradient on the host: float32 values, or uint16 patterns."""
+    t = t.cpu()
+    return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
+
+
 def _planted_grad(n, gdt, seed, bad_idx, sigma=1e-2):
     rng = np.random.default_rng(seed)
     x = (rng.standard_normal(n) * sigma).astype(np.float32)
@@ -473,12 +479,26 @@ def test_analyze_rows_match_oracle(gdt, n, row_len, segs, oracle_lib):
     assert np.all(np.abs(dev_s + dev_lo - rs)[ok] <= 2e-6 * rs[ok] + 1e-30)
 
 
+def _decoded_records(host, rows):
+    """Sums of squares of the first ``rows`` records: plain ones added here, scaled ones
+    (negative first word) decoded by the library."""
+    hi = host[:rows, 0].view(torch.float32).double().numpy()
+    lo = host[:rows, 2].view(torch.float32).double().numpy()
+    out = hi + lo
+    for r in np.flatnonzero(hi < 0):
+        rec = fa.FaStats()
+        rec.sum_sq, rec.nonfinite, rec.sum_sq_lo = float(hi[r]), int(host[r, 1]), float(lo[r])
+        out[r] = fa.fa_stats_sum_sq(rec)
+    return out
+
+
 @pytest.mark.parametrize("k", range(16))
 def test_random_statistics_vs_oracle(k, oracle_lib):
     """Seeded random analyses: size, gradient dtype, row length (fast and generic kernels),
-    segment tables with empty segments, and 0-5 planted NaN/+-Inf values.  Every row
-    record against the oracle (counts exact), then the merged report (count exact, sum
-    within the merge's error) and the skip / clip decision."""
+    segment tables with empty segments, 0-5 planted NaN/+-Inf values and, in FP32 and BF16
+    cases, 0-3 finite values whose squares overflow FP32.  Every row record against the
+    oracle (counts exact), then the merged report (count exact, sum within the merge's
+    error) and the skip / clip decision."""
     import math
     rng = np.random.default_rng(5000 + k)
     gdt = str(rng.choice(["f32", "f16", "bf16"]))
@@ -493,6 +513,13 @@ def test_random_statistics_vs_oracle(k, oracle_lib):
         row_len, rows = 1024, fa.fa_stats_rows(n, 1024, segs)
     bad = [int(i) for i in rng.integers(0, n, int(rng.integers(0, 6)))]
     g, bits = _planted_grad(n, gdt, 6000 + k, bad)
+    if gdt != "f16":  # finite values beyond sqrt(FP32 max); FP16's largest squares fit
+        huge = [(int(i), float(v)) for i, v in zip(rng.integers(0, n, int(rng.integers(0, 4))),
+                                                   10.0 ** rng.uniform(19.5, 38.4, 4))
+                if int(i) not in bad]
+        for i, val in huge:
+            g[i] = val
+        bits = grad_bits(g)
     buf = fa.stats_buffer(rows, DEV)
     assert fa.fa_analyze_gradient(g, row_len, buf, segs) == rows
     scratch = fa.scratch_buffer(rows, DEV)
@@ -501,19 +528,19 @@ def test_random_statistics_vs_oracle(k, oracle_lib):
     torch.cuda.synchronize()
     rs, rc = oracle_lib.row_stats(bits, gdt, row_len, segs)
     host = buf.cpu()
-    dev_s = host[:rows, 0].view(torch.float32).double().numpy()
     dev_c = host[:rows, 1].numpy().astype(np.int64)
-    dev_lo = host[:rows, 2].view(torch.float32).double().numpy()
+    dev_sum = _decoded_records(host, rows)
     assert np.array_equal(dev_c, rc.astype(np.int64))
     ok = rc == 0
-    assert np.all(np.abs(dev_s + dev_lo - rs)[ok] <= 2e-6 * rs[ok] + 1e-30)
+    assert np.all(np.abs(dev_sum - rs)[ok] <= 2e-6 * rs[ok] + 1e-30)
     h = fa.fa_read_report(report)
     s_or, c_or = oracle_lib.gradient_stats(bits, gdt)
     assert h.nonfinite == c_or
     if c_or == 0:
-        exact_rows = math.fsum((dev_s + dev_lo).tolist())
-        assert abs(float(h.sum_sq) + float(h.sum_sq_lo) - exact_rows) <= 1e-12 * exact_rows
-        assert abs(float(h.sum_sq) + float(h.sum_sq_lo) - s_or) <= 2e-6 * s_or + 1e-30
+        got = fa.fa_stats_sum_sq(h)
+        exact_rows = math.fsum(dev_sum.tolist())
+        assert abs(got - exact_rows) <= 1e-12 * exact_rows
+        assert abs(got - s_or) <= 2e-6 * s_or + 1e-30
 
 
 @pytest.mark.parametrize("rows", [1, 2, 1023, 1024, 1025, 4096, 1_048_575, 1_048_576,
