@@ -12,14 +12,17 @@
 // Design: one HBM pass per parameter.  The update is bandwidth bound (about
 // 0.7 flop per byte), so it is built for bytes in flight.  Three kernels share the
 // element arithmetic:
-//   - steady steps of large tensors: update_tma_kernel, one CTA per SM staging
-//     tiles of every stream through shared memory with 1-D TMA bulk copies and
-//     mbarriers, several stages in flight, bounded waits (further below);
-//   - first steps, small tensors: update_vec_kernel, persistent CTAs grid-striding
-//     over 8-element vectors, every stream moved with 16-byte evict-first loads
-//     and stores (p, m, v, vmax as two float4; a BF16/FP16 gradient as one 16-byte
-//     word, an FP32 gradient as two float4), all loads of an iteration issued
-//     before any arithmetic;
+//   - update_vec_kernel: 8-element vectors, every stream moved with 16-byte
+//     evict-first loads and stores (p, m, v, vmax as two float4; a BF16/FP16
+//     gradient as one 16-byte word, an FP32 gradient as two float4), all loads of
+//     an iteration issued before any arithmetic.  A launch with its multiplier
+//     from the host runs a full grid of 64-thread CTAs, each covering one stretch
+//     of 1024 elements; a gated launch runs persistent 512-thread CTAs, so that the
+//     FP64 decision is taken once per CTA on few CTAs;
+//   - gated steady steps of large tensors: update_tma_kernel, one CTA per SM
+//     staging tiles of every stream through shared memory with 1-D TMA bulk
+//     copies and mbarriers, several stages in flight, bounded waits (further
+//     below);
 //   - views not co-aligned to 16 bytes: update_scalar_kernel.
 // Elements before the first 16-byte boundary and after the last full vector or
 // tile go through the same arithmetic one at a time.  A gated launch takes the
@@ -36,12 +39,16 @@
 #include "internal.h"
 
 // Tuning knobs (compile-time): vectors per thread per iteration, threads per
-// CTA, and an L2 256-byte prefetch hint on the vector loads.
+// CTA of the full-grid and of the persistent (gated) vector launches, and an L2
+// 256-byte prefetch hint on the vector loads.
 #ifndef FA_UPDATE_UNROLL
 #define FA_UPDATE_UNROLL 2
 #endif
 #ifndef FA_UPDATE_THREADS
-#define FA_UPDATE_THREADS 512
+#define FA_UPDATE_THREADS 64
+#endif
+#ifndef FA_UPDATE_GATED_THREADS
+#define FA_UPDATE_GATED_THREADS 512
 #endif
 #ifndef FA_UPDATE_L2_PREFETCH
 #define FA_UPDATE_L2_PREFETCH 0
@@ -61,6 +68,8 @@ namespace {
 
 constexpr int kVec = 8;  // elements per vector
 constexpr int kUThreads = FA_UPDATE_THREADS;
+constexpr int kUThreadsGated = FA_UPDATE_GATED_THREADS;
+constexpr int64_t kMaxGridX = 0x7fffffff;  // the launch limit on gridDim.x
 
 FA_BOUNDS_COUNTER(g_update_oob)
 
@@ -261,25 +270,25 @@ __device__ __forceinline__ void scalar_element(const UpdateArgs &a, const Coef &
 }
 
 // Vector body + scalar head/tail.  Each thread owns UNROLL vectors per
-// grid-stride iteration, spaced kThreads vectors apart so that a warp's
+// grid-stride iteration, spaced THREADS vectors apart so that a warp's
 // accesses to each stream are contiguous.
-template <int GT, bool AMS, bool FIRST, int UNROLL, int MD>
-__global__ void __launch_bounds__(kUThreads)
+template <int GT, bool AMS, bool FIRST, int UNROLL, int MD, int THREADS>
+__global__ void __launch_bounds__(THREADS)
 update_vec_kernel(const UpdateArgs a, const Coef c0) {
     fa_grid_dependency_wait();  // (a gated launch may start before the merge ends)
     Coef c = c0;
     if (a.gate && !gate_decision(a, &c.gmul)) return;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kUThreads + threadIdx.x;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kUThreads * UNROLL;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * THREADS * UNROLL;
 
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kUThreads * UNROLL + threadIdx.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * THREADS * UNROLL + threadIdx.x;
          base < a.nvec; base += stride) {
         float x[UNROLL][kVec], p[UNROLL][kVec], m[UNROLL][kVec], v[UNROLL][kVec],
             vm[UNROLL][kVec];
         bool ok[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t vi = base + static_cast<int64_t>(u) * kUThreads;
+            const int64_t vi = base + static_cast<int64_t>(u) * THREADS;
             ok[u] = vi < a.nvec && fa_in_bounds(a.head + vi * kVec, kVec, a.n);
             if (ok[u]) {
                 const int64_t e = a.head + vi * kVec;
@@ -294,7 +303,7 @@ update_vec_kernel(const UpdateArgs a, const Coef c0) {
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t vi = base + static_cast<int64_t>(u) * kUThreads;
+            const int64_t vi = base + static_cast<int64_t>(u) * THREADS;
             if (ok[u]) {
                 const int64_t e = a.head + vi * kVec;
 #pragma unroll
@@ -742,9 +751,10 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
 #endif  // FA_UPDATE_TMA
 
 #if FA_UPDATE_TMA
-// Steady steps of at least two tiles per SM take the TMA pipeline; the first
-// step (moments only written: 6 B in, 12 B out) measured faster through the
-// register kernel (3.0 vs 3.7 ms at 1.07e9), and so did small tensors.
+// Gated steady steps (and per-segment steady steps) of at least two tiles per SM
+// take the TMA pipeline, whose 152 CTAs take the FP64 decision once each; the
+// first step (moments only written: 6 B in, 12 B out) measured faster through
+// the register kernel (3.0 vs 3.7 ms at 1.07e9), and so did small tensors.
 template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
 cudaError_t launch_tma_if_large(const SegScaleArgs &s, const Coef &c, bool vector_ok, int dev,
                                 cudaStream_t stream, bool *launched) {
@@ -886,7 +896,7 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
     if (sm_count(dev) <= 0) return cudaErrorInvalidDevice;
 
 #if FA_UPDATE_TMA
-    {
+    if (a.gate) {
         SegScaleArgs s;
         s.a = a;
         s.nseg = 0;
@@ -898,14 +908,29 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         if (err != cudaSuccess || launched) return err;
     }
 #endif
-    if (vector_ok) {
-        auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD>;
+    if (vector_ok && a.gate) {
+        // Persistent CTAs: every CTA takes the FP64 decision before its first load, and
+        // GB300's FP64 rate makes a decision per small CTA of a full grid cost more
+        // than the grid gains (6.7 against 4.1 ms at 1.07e9 parameters).
+        auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD, kUThreadsGated>;
+        const int64_t per_cta = static_cast<int64_t>(kUThreadsGated) * kUnroll;
+        int64_t need = (a.nvec + per_cta - 1) / per_cta;
+        if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
+        const int grid = persistent_grid(kern, need, dev, kUThreadsGated);
+        if (grid == 0) return cudaSuccess;
+        return launch_dependent(kern, dim3(grid), dim3(kUThreadsGated), 0, stream, a, c);
+    } else if (vector_ok) {
+        // A full grid: one small CTA per kUThreads * kUnroll vectors, each CTA normally
+        // one iteration (the loop matters only for a grid capped at the launch limit).
+        // Measured on GB300 (1.07e9 parameters, CUDA events) against persistent grids
+        // of the same kernel and against the shared-memory (TMA) pipeline, it moves
+        // every byte mix fastest.
+        auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD, kUThreads>;
         const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
         int64_t need = (a.nvec + per_cta - 1) / per_cta;
         if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
-        const int grid = persistent_grid(kern, need, dev, kUThreads);
+        const int grid = static_cast<int>(need < kMaxGridX ? need : kMaxGridX);
         if (grid == 0) return cudaSuccess;
-        if (a.gate) return launch_dependent(kern, dim3(grid), dim3(kUThreads), 0, stream, a, c);
         kern<<<grid, kUThreads, 0, stream>>>(a, c);
     } else {
         auto kern = update_scalar_kernel<GT, AMS, FIRST, MD>;
