@@ -228,6 +228,7 @@ fa_status enqueue_update(int64_t n, const float *p, const void *g, fa_dtype gdt,
     a.gate_scale = scale;
     a.gate_max_norm = gate_max_norm;
     a.gate_sign = o->maximize ? -1.0 : 1.0;
+    a.gate_inv_scale = fa::power_of_two_inverse(scale);
     a.n = n;
     const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g,
                           a.p_out, a.m_out, a.v_out, a.vmax_out, a.p_model};
@@ -317,6 +318,7 @@ fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float
         a.gate_scale = ctl.gradient_scale;
         a.gate_max_norm = max_grad_norm;
         a.gate_sign = sign;
+        a.gate_inv_scale = fa::power_of_two_inverse(ctl.gradient_scale);
         a.n = e1 - e0;
         const void *ptrs[] = {a.p_in, a.m_in, a.v_in, a.vmax_in, a.g};
         const size_t es[] = {4, 4, 4, 4, gb};
@@ -449,7 +451,7 @@ fa_status fa_pipeline_selftest(int64_t n, float *p, const void *g, fa_dtype gdt,
     a.p_model = nullptr;
     a.extra_tx = 16;  // a barrier that waits for 16 bytes nobody sends
     a.gate = nullptr;
-    a.gate_scale = a.gate_max_norm = a.gate_sign = 0.0;
+    a.gate_scale = a.gate_max_norm = a.gate_sign = a.gate_inv_scale = 0.0;
     a.n = n;
     const void *ptrs[] = {p, m, v, g};
     const size_t es[] = {4, 4, 4, dtype_bytes(gdt)};

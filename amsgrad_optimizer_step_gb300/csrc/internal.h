@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI host layer (abi.cpp) and the kernels.
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -87,6 +88,17 @@ constexpr int kMaxSegPerLaunch = 240;    // segment table entries carried in ker
 // (an exact power-of-two scaling, so the decoded FP64 value has the precision of
 // the stored one).  The host decision and the device-side gates decode with this
 // one function: the same FP64 operations in the same order.
+// 1 / s when s is a power of two whose inverse is a normal double, else 0.  For such
+// an s, x / s and x * (1 / s) are the rounding of one and the same real number, so
+// IEEE arithmetic gives them the same bits for every x (subnormal, infinite and NaN
+// results included).
+inline double power_of_two_inverse(double s) {
+    int e = 0;
+    if (!(s > 0.0) || std::frexp(s, &e) != 0.5) return 0.0;  // s = 2^(e-1)
+    const int k = e - 1;
+    return (k < -1022 || k > 1022) ? 0.0 : std::ldexp(1.0, -k);
+}
+
 constexpr int kRescueValueExp = 96;  // values of a rescued row are multiplied by 2^-96
 __host__ __device__ inline double record_sum_sq(const fa_stats &r) {
     const double s = static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);
@@ -112,8 +124,10 @@ struct UpdateArgs {
     uint32_t extra_tx;  // self-test only: bytes a pipeline barrier waits for but never gets
     // Device-side decision (nullptr: none): skip when the report counts a
     // non-finite value, else gmul = sign * coef / scale with the host's formula.
+    // gate_inv_scale: power_of_two_inverse(gate_scale), so that the divisions by the
+    // scale can be multiplications with the same result.
     const fa_stats *gate;
-    double gate_scale, gate_max_norm, gate_sign;
+    double gate_scale, gate_max_norm, gate_sign, gate_inv_scale;
     int64_t n;     // elements
     int64_t head;  // scalar elements before the 16-byte aligned vector body
     int64_t nvec;  // 8-element vectors in the body

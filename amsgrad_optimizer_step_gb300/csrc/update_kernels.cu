@@ -17,12 +17,15 @@
 //     gradient as one 16-byte word, an FP32 gradient as two float4), all loads of
 //     an iteration issued before any arithmetic.  A launch with its multiplier
 //     from the host runs a full grid of 64-thread CTAs, each covering one stretch
-//     of 1024 elements; a gated launch runs persistent 512-thread CTAs, so that the
-//     FP64 decision is taken once per CTA on few CTAs;
-//   - gated steady steps of large tensors: update_tma_kernel, one CTA per SM
-//     staging tiles of every stream through shared memory with 1-D TMA bulk
-//     copies and mbarriers, several stages in flight, bounded waits (further
-//     below);
+//     of 1024 elements;
+//   - update_vec_cta_gate_kernel: the same full grid for a gated launch whose
+//     gradient scale is a power of two, thread 0 of each CTA taking the decision
+//     (with multiplications by the exact inverse scale) while the loads fly;
+//   - gated launches with any other scale: update_tma_kernel for steady steps of
+//     large tensors (one CTA per SM staging tiles of every stream through shared
+//     memory with 1-D TMA bulk copies and mbarriers, several stages in flight,
+//     bounded waits; further below), persistent 512-thread update_vec_kernel CTAs
+//     otherwise: few CTAs, each taking the FP64 decision once;
 //   - views not co-aligned to 16 bytes: update_scalar_kernel.
 // Elements before the first 16-byte boundary and after the last full vector or
 // tile go through the same arithmetic one at a time.  A gated launch takes the
@@ -183,6 +186,14 @@ __device__ __forceinline__ void adamw_element(const Coef &c, float x, float &p, 
     v = v_new;
 }
 
+// x / a.gate_scale.  For a power-of-two scale it is the multiplication by the exact
+// inverse, which gives the same bits; GB300's FP64 divisions are slow enough that two
+// of them per CTA of a full grid cost 5 % of a steady step (4.16 against 3.95 ms at
+// 1.07e9 parameters).
+__device__ __forceinline__ double gate_unscale(const UpdateArgs &a, double x) {
+    return a.gate_inv_scale != 0.0 ? x * a.gate_inv_scale : x / a.gate_scale;
+}
+
 // The host's skip / clip decision, taken on the device from the same report
 // with the same FP64 operations in the same order (so the multiplier is
 // bit-identical): false = skip the update.
@@ -190,10 +201,10 @@ __device__ __forceinline__ bool gate_decision(const UpdateArgs &a, float *gmul) 
     const fa_stats r = *a.gate;
     if (r.nonfinite > 0) return false;
     const double sum = record_sum_sq(r);
-    const double norm = sqrt(sum) / a.gate_scale;
+    const double norm = gate_unscale(a, sqrt(sum));
     double coef = 1.0;
     if (a.gate_max_norm > 0 && norm > a.gate_max_norm) coef = a.gate_max_norm / norm;
-    *gmul = static_cast<float>(a.gate_sign * coef / a.gate_scale);
+    *gmul = static_cast<float>(gate_unscale(a, a.gate_sign * coef));
     return true;
 }
 
@@ -324,6 +335,78 @@ update_vec_kernel(const UpdateArgs a, const Coef c0) {
     if (tid < a.n - tail0) scalar_element<GT, AMS, FIRST, MD>(a, c, tail0 + tid);
 }
 
+// The full-grid form of a gated launch: update_vec_kernel's body for one stretch
+// of THREADS * UNROLL vectors per CTA, with the decision taken once per CTA.  Every
+// thread first issues its loads; thread 0 then takes the decision and shares it
+// through shared memory, so that its latency hides behind the loads in flight.  The
+// barrier is reached by every thread of the CTA exactly once, before any exit.
+template <int GT, bool AMS, bool FIRST, int UNROLL, int MD, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+update_vec_cta_gate_kernel(const UpdateArgs a, const Coef c0) {
+    fa_grid_dependency_wait();  // (launched while the merge before it may still run)
+    __shared__ float s_gmul;
+    __shared__ int s_go;
+    Coef c = c0;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * THREADS * UNROLL;
+    int64_t base = static_cast<int64_t>(blockIdx.x) * THREADS * UNROLL + threadIdx.x;
+
+    float x[UNROLL][kVec], p[UNROLL][kVec], m[UNROLL][kVec], v[UNROLL][kVec], vm[UNROLL][kVec];
+    bool ok[UNROLL];
+    auto load_group = [&]() {
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t vi = base + static_cast<int64_t>(u) * THREADS;
+            ok[u] = vi < a.nvec && fa_in_bounds(a.head + vi * kVec, kVec, a.n);
+            if (ok[u]) {
+                const int64_t e = a.head + vi * kVec;
+                GradIO<GT>::load8(a.g, e, x[u]);
+                load8f(a.p_in, e, p[u]);
+                if (!FIRST) {
+                    load8f(a.m_in, e, m[u]);
+                    load8f(a.v_in, e, v[u]);
+                    if (AMS) load8f(a.vmax_in, e, vm[u]);
+                }
+            }
+        }
+    };
+    load_group();
+    if (threadIdx.x == 0) {
+        float gm = 0.f;
+        s_go = gate_decision(a, &gm) ? 1 : 0;
+        s_gmul = gm;
+    }
+    __syncthreads();
+    if (!s_go) return;  // the whole CTA: nothing is stored
+    c.gmul = s_gmul;
+    // One stretch per CTA unless the grid was capped at the launch limit.
+    for (;;) {
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t vi = base + static_cast<int64_t>(u) * THREADS;
+            if (ok[u]) {
+                const int64_t e = a.head + vi * kVec;
+#pragma unroll
+                for (int k = 0; k < kVec; ++k)
+                    adamw_element<AMS, FIRST>(c, x[u][k], p[u][k], m[u][k], v[u][k], vm[u][k]);
+                store8f(a.p_out, e, p[u]);
+                store8f(a.m_out, e, m[u]);
+                store8f(a.v_out, e, v[u]);
+                if (AMS) store8f(a.vmax_out, e, vm[u]);
+                if (MD != kNoModel) store8_model<MD>(a.p_model, e, p[u]);
+            }
+        }
+        base += stride;
+        if (base >= a.nvec) break;
+        load_group();
+    }
+
+    // Scalar head [0, head) and tail [head + 8*nvec, n).
+    if (tid < a.head) scalar_element<GT, AMS, FIRST, MD>(a, c, tid);
+    const int64_t tail0 = a.head + a.nvec * kVec;
+    if (tid < a.n - tail0) scalar_element<GT, AMS, FIRST, MD>(a, c, tail0 + tid);
+}
+
 // Every element one at a time (pointers not co-aligned to 16 bytes).
 template <int GT, bool AMS, bool FIRST, int MD>
 __global__ void __launch_bounds__(kThreads)
@@ -398,10 +481,10 @@ __device__ __forceinline__ bool segment_multipliers(const SegScaleArgs &s, float
     for (int j = threadIdx.x; j < s.nseg; j += blockDim.x) {
         const fa_stats r = s.reports[s.k0 + j];
         const double sum = record_sum_sq(r);
-        const double norm = sqrt(sum) / s.a.gate_scale;
+        const double norm = gate_unscale(s.a, sqrt(sum));
         double coef = 1.0;
         if (s.a.gate_max_norm > 0 && norm > s.a.gate_max_norm) coef = s.a.gate_max_norm / norm;
-        gm[j] = static_cast<float>(s.a.gate_sign * coef / s.a.gate_scale);
+        gm[j] = static_cast<float>(gate_unscale(s.a, s.a.gate_sign * coef));
     }
     return true;
 }
@@ -895,6 +978,17 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
     if (err != cudaSuccess) return err;
     if (sm_count(dev) <= 0) return cudaErrorInvalidDevice;
 
+    // A gated launch whose scale has an exact inverse: the full grid, deciding once
+    // per CTA (with multiplications instead of the FP64 divisions).
+    if (vector_ok && a.gate && a.gate_inv_scale != 0.0) {
+        auto kern = update_vec_cta_gate_kernel<GT, AMS, FIRST, kUnroll, MD, kUThreads>;
+        const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
+        int64_t need = (a.nvec + per_cta - 1) / per_cta;
+        if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
+        const int grid = static_cast<int>(need < kMaxGridX ? need : kMaxGridX);
+        if (grid == 0) return cudaSuccess;
+        return launch_dependent(kern, dim3(grid), dim3(kUThreads), 0, stream, a, c);
+    }
 #if FA_UPDATE_TMA
     if (a.gate) {
         SegScaleArgs s;
@@ -909,9 +1003,10 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
     }
 #endif
     if (vector_ok && a.gate) {
-        // Persistent CTAs: every CTA takes the FP64 decision before its first load, and
-        // GB300's FP64 rate makes a decision per small CTA of a full grid cost more
-        // than the grid gains (6.7 against 4.1 ms at 1.07e9 parameters).
+        // Other scales: persistent CTAs, each taking the decision (with its FP64
+        // divisions) once; GB300's FP64 rate makes those divisions in every small CTA
+        // of a full grid cost more than the grid gains (4.16 against 4.07 ms for the
+        // TMA pipeline at 1.07e9 parameters).
         auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD, kUThreadsGated>;
         const int64_t per_cta = static_cast<int64_t>(kUThreadsGated) * kUnroll;
         int64_t need = (a.nvec + per_cta - 1) / per_cta;

@@ -4,8 +4,9 @@ Every variant of the bucket update is one call with a descriptor: the multiplier
 a host factor, one host factor per segment, one device report or one device report
 per segment, and optionally the low-precision model copy.  Each case draws a variant,
 a size (1 to 2.5 million), a segment table with empty segments, the gradient dtype,
-AMSGrad, maximize, a power-of-two loss scale, a clip threshold (or none) and a
-skipped call, and runs three calls.  Each segment is compared with its own oracle run
+AMSGrad, maximize, a loss scale (a power of two in two cases of three, which a gated
+launch runs on the full grid; else 3, 0.3 or 1000, which it runs on the pipeline), a
+clip threshold (or none) and a skipped call, and runs three calls.  Each segment is compared with its own oracle run
 (trajectory within 1e-5 x max(1,|x|)), whose coefficient is the host factor, or the
 oracle's own decision from its FP64 statistics over the whole gradient or over the
 segment.  The model copy must be the encoding of the device's own parameters and a
@@ -43,7 +44,9 @@ def _case(k):
     # every source, and both model copies with each single-factor source, by case index
     source = ("host", "seg_host", "report", "seg_reports")[k % 4]
     model = ("none", "bf16", "f16")[(k // 4) % 3] if source in ("host", "report") else "none"
-    scale = float(2.0 ** rng.integers(-2, 7))
+    # powers of two (the gated full grid) and other scales (the gated pipeline)
+    scale = float(2.0 ** rng.integers(-2, 7)) if rng.integers(3) else float(
+        rng.choice([3.0, 0.3, 1000.0]))
     w = dataclasses.replace(
         CONFIG2, name=f"bucket_update{k}", seed=int(rng.integers(1, 10_000)),
         grad_dtype=str(rng.choice(["f32", "f16", "bf16"])), amsgrad=bool(rng.integers(2)),

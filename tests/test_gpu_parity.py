@@ -888,6 +888,44 @@ def test_gated_step_equals_host_decided_step_bitwise(max_norm):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
 
 
+@pytest.mark.parametrize("scale", [2.0 ** -3, 128.0, 2.0 ** 40, 3.0, 1000.0, 0.1])
+@pytest.mark.parametrize("amsgrad", [False, True])
+def test_gated_step_equals_host_decided_step_bitwise_at_any_scale(scale, amsgrad):
+    """The device takes the decision's divisions by the gradient scale as multiplications
+    by the exact inverse when the scale is a power of two (and then runs the full grid),
+    and as divisions otherwise (the TMA pipeline and persistent CTAs).  Either way the
+    steps are bit-identical to the host's decision, first step, clipped steady steps and
+    the skipped +Inf call alike."""
+    n = 256 * 5000 + 77  # more than two tiles per SM: the steady steps reach the pipeline
+    w = dataclasses.replace(CONFIG5, gradient_scale=scale, grad_premul=scale,
+                            amsgrad=amsgrad).scaled(n, calls=4, inf_call=2)
+    o = fa.options(**w.options())
+    mailbox = fa.report_mailbox()
+    states = []
+    for gated in (False, True):
+        p = torch.empty(n, device=DEV)
+        w.fill_params_device(p)
+        m, v = torch.empty_like(p), torch.empty_like(p)
+        vmax = torch.empty_like(p) if amsgrad else None
+        g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+        rows = fa.fa_stats_rows(n, 256)
+        rb, sc, rep = fa.stats_buffer(rows, DEV), fa.scratch_buffer(rows, DEV), fa.stats_buffer(1, DEV)
+        t, reports = 0, []
+        for call in range(1, w.calls + 1):
+            w.fill_grad_device(call, g)
+            fn = (lambda *a: fa.fa_bucket_step_clipped_gated(*a, mailbox)) if gated \
+                else fa.fa_bucket_step_clipped
+            t, r = fn(None, p, g, m, v, vmax, t, o, fa.control(scale), 0.05, 256, rb, sc, rep)
+            reports.append((r.updated, r.skipped_nonfinite, repr(r.grad_norm), repr(r.clip_coef)))
+        torch.cuda.synchronize()
+        states.append((t, reports, [x.clone() for x in (p, m, v, vmax) if x is not None]))
+    (ta, ra, sa), (tb, rb_, sb) = states
+    assert ta == tb == 3 and ra == rb_
+    assert ra[1][1] == 1 and all(0 < float(c) < 1 for _, s_, _, c in ra if not s_), ra
+    for x, y in zip(sa, sb):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
 def test_gated_step_full_size_bitwise():
     """The benchmark's launch configuration: the 1,073,741,824-parameter workload, rows of
     256, the update gated on the device report, five calls with the +Inf in call 3;
