@@ -27,6 +27,10 @@
 //     bounded waits; further below), persistent 512-thread update_vec_kernel CTAs
 //     otherwise: few CTAs, each taking the FP64 decision once;
 //   - views not co-aligned to 16 bytes: update_scalar_kernel.
+// The per-segment update (one multiplier per segment) runs update_seg_grid_kernel on
+// the full grid with multipliers from the host; decided on the device, it runs
+// update_tma_kernel<SEG> for steady steps of large buckets and the persistent
+// update_segscaled_kernel otherwise.
 // Elements before the first 16-byte boundary and after the last full vector or
 // tile go through the same arithmetic one at a time.  A gated launch takes the
 // skip / clip decision itself, from the 12-byte statistics report (or one report
@@ -73,6 +77,7 @@ constexpr int kVec = 8;  // elements per vector
 constexpr int kUThreads = FA_UPDATE_THREADS;
 constexpr int kUThreadsGated = FA_UPDATE_GATED_THREADS;
 constexpr int64_t kMaxGridX = 0x7fffffff;  // the launch limit on gridDim.x
+constexpr int kUnroll = FA_UPDATE_UNROLL;
 
 FA_BOUNDS_COUNTER(g_update_oob)
 
@@ -489,6 +494,82 @@ __device__ __forceinline__ bool segment_multipliers(const SegScaleArgs &s, float
     return true;
 }
 
+// The per-segment update with multipliers from the host, on the full grid: one
+// stretch of THREADS * UNROLL vectors per CTA (the launcher guarantees that the grid
+// covers every stretch), the body of update_vec_kernel.  A CTA copies the
+// multipliers of only the segments its elements fall in, [k_lo, k_hi] (usually one),
+// from the table in the kernel parameters into shared memory.  CTA 0 also takes the
+// scalar head and the last CTA the scalar tail, so their ranges include those
+// elements.  A vector finds its segment by a forward scan from k_lo; one that
+// straddles a boundary looks up each element.  (Decided on the device, with one
+// report per segment, this grid measured slower than the pipeline: 6.35-6.63 against
+// 6.11 ms for the 1.2e9-parameter, 199-segment FP16 AMSGrad bucket.)
+template <int GT, bool AMS, bool FIRST, int UNROLL, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+update_seg_grid_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
+    __shared__ float gm[kMaxSegPerLaunch];
+    fa_grid_dependency_wait();
+    const UpdateArgs &a = s.a;
+    const int64_t vb = static_cast<int64_t>(blockIdx.x) * THREADS * UNROLL;
+    float x[UNROLL][kVec], p[UNROLL][kVec], m[UNROLL][kVec], v[UNROLL][kVec], vm[UNROLL][kVec];
+    bool ok[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const int64_t vi = vb + threadIdx.x + static_cast<int64_t>(u) * THREADS;
+        ok[u] = vi < a.nvec && fa_in_bounds(a.head + vi * kVec, kVec, a.n);
+        if (ok[u]) {
+            const int64_t e = a.head + vi * kVec;
+            GradIO<GT>::load8(a.g, e, x[u]);
+            load8f(a.p_in, e, p[u]);
+            if (!FIRST) {
+                load8f(a.m_in, e, m[u]);
+                load8f(a.v_in, e, v[u]);
+                if (AMS) load8f(a.vmax_in, e, vm[u]);
+            }
+        }
+    }
+
+    // elements [e_lo, e_hi) of this CTA, and their segments [k_lo, k_hi]
+    const int64_t body_end = a.head + a.nvec * kVec;
+    const int64_t e_lo = blockIdx.x == 0 ? 0 : a.head + vb * kVec;
+    int64_t e_hi = a.head + (vb + static_cast<int64_t>(THREADS) * UNROLL) * kVec;
+    if (e_hi > body_end) e_hi = body_end;
+    if (blockIdx.x == gridDim.x - 1) e_hi = a.n;
+    const int k_lo = find_seg(s, e_lo);
+    const int k_hi = e_hi > e_lo ? find_seg(s, e_hi - 1) : k_lo;
+    for (int k = k_lo + threadIdx.x; k <= k_hi; k += THREADS) gm[k] = s.gmul[k];
+    __syncthreads();
+
+    int k = k_lo;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        if (!ok[u]) continue;
+        const int64_t e = a.head + (vb + threadIdx.x + static_cast<int64_t>(u) * THREADS) * kVec;
+        while (k < k_hi && s.seg_start[k + 1] <= e) ++k;
+        Coef cc = c;
+        if (e + kVec <= s.seg_start[k + 1]) {
+            cc.gmul = gm[k];
+#pragma unroll
+            for (int q = 0; q < kVec; ++q)
+                adamw_element<AMS, FIRST>(cc, x[u][q], p[u][q], m[u][q], v[u][q], vm[u][q]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) {
+                cc.gmul = gm[find_seg_in(s, e + q, k, k_hi)];
+                adamw_element<AMS, FIRST>(cc, x[u][q], p[u][q], m[u][q], v[u][q], vm[u][q]);
+            }
+        }
+        store8f(a.p_out, e, p[u]);
+        store8f(a.m_out, e, m[u]);
+        store8f(a.v_out, e, v[u]);
+        if (AMS) store8f(a.vmax_out, e, vm[u]);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < a.head)
+        scalar_element_seg<GT, AMS, FIRST>(s, gm, c, threadIdx.x);
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x < a.n - body_end)
+        scalar_element_seg<GT, AMS, FIRST>(s, gm, c, body_end + threadIdx.x);
+}
+
 #if FA_UPDATE_TMA
 // ---- shared-memory staging with 1-D TMA bulk copies ---------------------------
 //
@@ -834,8 +915,9 @@ update_tma_kernel(const __grid_constant__ SegScaleArgs sa, const Coef c0, int64_
 #endif  // FA_UPDATE_TMA
 
 #if FA_UPDATE_TMA
-// Gated steady steps (and per-segment steady steps) of at least two tiles per SM
-// take the TMA pipeline, whose 152 CTAs take the FP64 decision once each; the
+// Steady steps of at least two tiles per SM that are gated with a scale that is not a
+// power of two, or decided per segment on the device, take the TMA pipeline, whose
+// 152 CTAs take the decisions once each; the
 // first step (moments only written: 6 B in, 12 B out) measured faster through
 // the register kernel (3.0 vs 3.7 ms at 1.07e9), and so did small tensors.
 template <int GT, bool AMS, bool FIRST, int MD, bool SEG>
@@ -932,13 +1014,27 @@ cudaError_t launch_seg_typed(const SegScaleArgs &s, const Coef &c, bool vec, cud
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    // Multipliers from the host: the full grid.  Decided on the device: few CTAs (the
+    // pipeline, or persistent CTAs), each taking every segment's decision once.
+    if (vec && !s.reports) {
+        auto kern = update_seg_grid_kernel<GT, AMS, FIRST, kUnroll, kUThreads>;
+        const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
+        int64_t need = (s.a.nvec + per_cta - 1) / per_cta;
+        if (need == 0 && s.a.n > 0) need = 1;  // head/tail elements only
+        if (need <= kMaxGridX) {
+            const int grid = static_cast<int>(need);
+            if (grid == 0) return cudaSuccess;
+            kern<<<grid, kUThreads, 0, st>>>(s, c);
+            return cudaGetLastError();
+        }
+    }
+    // decided on the device: scheduled while the merge before it runs
+    const bool dependent = s.reports != nullptr;
 #if FA_UPDATE_TMA
     bool launched = false;
     err = launch_tma_if_large<GT, AMS, FIRST, kNoModel, true>(s, c, vec, dev, st, &launched);
     if (err != cudaSuccess || launched) return err;
 #endif
-    // decided on the device: scheduled while the merge before it runs
-    const bool dependent = s.reports != nullptr;
     if (vec) {
         auto kern = update_segscaled_kernel<GT, AMS, FIRST>;
         int64_t need = (s.a.nvec + kThreads - 1) / kThreads;
@@ -967,8 +1063,6 @@ cudaError_t launch_seg_gt(const SegScaleArgs &s, const Coef &c, bool ams, bool f
                  : launch_seg_typed<GT, false, false>(s, c, vec, st);
 }
 
-
-constexpr int kUnroll = FA_UPDATE_UNROLL;
 
 template <int GT, bool AMS, bool FIRST, int MD>
 cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,

@@ -45,7 +45,7 @@ def test_normal_build_has_no_checks():
 CASES = [
     ("config1 out of place", lambda lib: P.test_config1_out_of_place_full()),
     ("config2 with skip", lambda lib: P.test_config2_bf16_scaled_amsgrad_with_skip_full()),
-    ("config3 ragged, shared-memory pipeline", lambda lib: P.test_config3_scaled_ragged("inplace")),
+    ("config3 ragged, in place", lambda lib: P.test_config3_scaled_ragged("inplace")),
     ("config3 ragged out of place", lambda lib: P.test_config3_scaled_ragged("oop")),
     ("decoder bucket", lambda lib: P.test_config4_scaled_decoder_bucket(CONFIG4)),
     ("statistics, clip, +Inf skip", lambda lib: P.test_config5_scaled_stats_clip_and_inf_skip()),
@@ -64,11 +64,16 @@ CASES = [
                                 P.test_writeback_misaligned_model_view(lib)]),
     ("per-segment reports", lambda lib: S.test_chunk_reports_match_oracle_per_segment(
         "bf16", 100, lib)),
-    ("per-segment multipliers, shared-memory pipeline",
+    ("per-segment multipliers, mixed sizes",
      lambda lib: S.test_segment_multipliers_mixed_sizes_vs_oracle("f16", False, lib)),
-    ("per-segment decision on the device",
+    ("per-segment decision on the device, full grid and pipeline",
      lambda lib: [S.test_per_segment_gated_equals_host_decision_bitwise(*k) for k in (
-         ("mixed", "f16", False), ("many", "f32", False), ("offset", "bf16", False))]),
+         ("mixed", "f16", False, 1.0), ("many", "f32", False, 1.0),
+         ("offset", "bf16", False, 1.0), ("mixed", "f16", False, 3.0),
+         ("small", "f16", True, 2.0 ** -4))]),
+    ("gated step at scales with and without an exact inverse",
+     lambda lib: [P.test_gated_step_equals_host_decided_step_bitwise_at_any_scale(sc, ams)
+                  for sc in (128.0, 3.0) for ams in (False, True)]),
     ("staged comparison vs the oracle, scalar tail",
      lambda lib: P.test_staged_vs_oracle("f16", True, 70_001)),
     ("rows whose squares overflow FP32, rescued",

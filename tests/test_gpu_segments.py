@@ -234,10 +234,13 @@ def _gated_layout(kind):
     return _scaled_decoder_offsets()  # "small" and "offset": register and scalar kernels
 
 
-@pytest.mark.parametrize("kind,gdt,maximize", [("mixed", "f16", False), ("mixed", "bf16", True),
-                                               ("many", "f32", False), ("small", "f16", False),
-                                               ("offset", "bf16", False)])
-def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize):
+@pytest.mark.parametrize("kind,gdt,maximize,scale", [
+    ("mixed", "f16", False, 1.0), ("mixed", "bf16", True, 1.0), ("many", "f32", False, 1.0),
+    ("small", "f16", False, 1.0), ("offset", "bf16", False, 1.0),
+    # powers of two decide on the full grid; other scales keep the pipeline and the
+    # persistent kernel, whose few CTAs take the FP64 divisions
+    ("mixed", "f16", False, 3.0), ("many", "bf16", False, 0.1), ("small", "f16", True, 2.0 ** -4)])
+def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize, scale):
     """The per-segment step decided on the device (every segment's coefficient and the
     skip taken in the update kernels from the device-resident reports) against the
     host-decided per-segment step, over four calls with a +Inf in the third: reports,
@@ -245,7 +248,8 @@ def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize):
     seg = _gated_layout(kind)
     n = int(seg[-1])
     w = dataclasses.replace(CONFIG4, segments=None, calls=4, inf_call=3, grad_sigma=1e-2,
-                            grad_dtype=gdt, maximize=maximize).scaled(n)
+                            grad_dtype=gdt, maximize=maximize, gradient_scale=scale,
+                            grad_premul=scale).scaled(n)
     o = fa.options(**w.options())
     off = 1 if kind == "offset" else 0  # state views 4 bytes off the gradient's alignment
 
@@ -266,9 +270,9 @@ def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize):
     for call in range(1, 5):
         w.fill_grad_device(call, g)
         ta, rep, _, coefs = fa.fa_bucket_step_clipped_per_segment(
-            list(seg), pa, g, ma, va, vma, ta, o, fa.control(), max_norm, row_len, *bufs[0])
+            list(seg), pa, g, ma, va, vma, ta, o, fa.control(scale), max_norm, row_len, *bufs[0])
         fa.fa_bucket_step_clipped_per_segment_gated(
-            list(seg), pb, g, mb, vb, vmb, tb, o, fa.control(), max_norm, row_len, *bufs[1])
+            list(seg), pb, g, mb, vb, vmb, tb, o, fa.control(scale), max_norm, row_len, *bufs[1])
         rb = bufs[1][2].cpu()
         if not bool((rb[:, 1] != 0).any()):
             tb += 1
