@@ -177,8 +177,9 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
                  grad_mult: float = 1.0):
     """Runs every call of ``w`` (at size n) and checks each one.  Returns a summary.
 
-    ``api``: "oop", "inplace", "bucket", "clipped" or "staged" (the 4/5-kernel
-    comparison, on in-place storage).  ``grad_mult`` is a fixed factor on the
+    ``api``: "oop", "inplace", "bucket", "clipped", "gated" (the clipped step with the
+    update deciding on the device from the report, which the last merge also posts to a
+    pinned mailbox) or "staged" (the 4/5-kernel comparison, on in-place storage).  ``grad_mult`` is a fixed factor on the
     unscaled gradient for "inplace" and "staged" (the oracle's clip coefficient)."""
     import dataclasses
     lib = lib or oracle.lib()
@@ -206,7 +207,8 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         st._full["model"] = full
     if api == "staged":
         delta = torch.empty(n, dtype=torch.float32, device=device)
-    if api == "clipped":
+    if api in ("clipped", "gated"):
+        mailbox = fa.report_mailbox()
         rows = fa.fa_stats_rows(n, row_len, segs)
         rows_buf = fa.stats_buffer(rows, device)
         scratch = fa.scratch_buffer(rows, device)
@@ -224,14 +226,15 @@ def run_workload(w: Workload, n: int, api: str, device, idx: np.ndarray | None =
         coef_dev = grad_mult
         expect_skip = skip
         coef_or = grad_mult
-        if api == "clipped":
+        if api in ("clipped", "gated"):
             full_bits = (ws.grad_host(call, np.arange(n)) if full_grad_on_host
                          else grad_bits_from_device(st.g))
             s_or, c_or = lib.gradient_stats(full_bits, ORACLE_DT[ws.grad_dtype], ws.gradient_scale)
             skip_or, norm_or, coef_or = lib.clip_decision(s_or, c_or, ws.max_grad_norm)
-            t_new, rep = fa.fa_bucket_step_clipped(segs, st.p, st.g, st.m, st.v, st.vmax, st.t,
-                                                   fopts, ctl, ws.max_grad_norm, row_len,
-                                                   rows_buf, scratch, report)
+            step = fa.fa_bucket_step_clipped if api == "clipped" else \
+                (lambda *a: fa.fa_bucket_step_clipped_gated(*a, mailbox))
+            t_new, rep = step(segs, st.p, st.g, st.m, st.v, st.vmax, st.t, fopts, ctl,
+                              ws.max_grad_norm, row_len, rows_buf, scratch, report)
             torch.cuda.synchronize()
             if not skip:
                 assert rep.nonfinite == c_or, (call, rep.nonfinite, c_or)

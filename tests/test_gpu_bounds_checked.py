@@ -48,7 +48,8 @@ CASES = [
     ("config3 ragged, in place", lambda lib: P.test_config3_scaled_ragged("inplace")),
     ("config3 ragged out of place", lambda lib: P.test_config3_scaled_ragged("oop")),
     ("decoder bucket", lambda lib: P.test_config4_scaled_decoder_bucket(CONFIG4)),
-    ("statistics, clip, +Inf skip", lambda lib: P.test_config5_scaled_stats_clip_and_inf_skip()),
+    ("statistics, clip, +Inf skip, decided on the host and on the device",
+     lambda lib: [P.test_config5_scaled_stats_clip_and_inf_skip(api) for api in ("clipped", "gated")]),
     ("edge sizes", lambda lib: [P.test_edge_sizes(gdt, ams, n) for gdt in ("f32", "bf16")
                                 for ams in (False, True) for n in (1, 9, 4097, 65537)]),
     ("misaligned views", lambda lib: [P.test_misaligned_views(gdt, off) for gdt in ("f16",)

@@ -83,9 +83,10 @@ def test_config4_full_size_sampled(w):
     assert s["t"] == 10
 
 
-def test_config5_scaled_stats_clip_and_inf_skip():
+@pytest.mark.parametrize("api", ["clipped", "gated"])
+def test_config5_scaled_stats_clip_and_inf_skip(api):
     n = 256 * 5000 + 77
-    s = run_workload(CONFIG5, n, "clipped", DEV, row_len=256, guard=1024)
+    s = run_workload(CONFIG5, n, api, DEV, row_len=256, guard=1024)
     assert s["skips"] == 1 and s["updates"] == 4 and s["t"] == 4
     # norm well above 1: the clip is active in every update
     assert all(r[1] > 1.0 for r in s["reports"] if r[3] == 0)
@@ -147,11 +148,12 @@ def test_misaligned_views(gdt, offsets):
     gate(views["vmax"].cpu().numpy(), traj.state.vmax, 1e-6, "vmax")
 
 
-def test_more_than_2_31_elements_sampled():
+@pytest.mark.parametrize("api", ["clipped", "gated"])
+def test_more_than_2_31_elements_sampled(api):
     """A bucket of 2^31 + 777 parameters (8.6 GB per FP32 array): every element offset in
     the kernels is 64-bit; the norm matches the oracle's over the whole gradient, and
     sampled elements on both sides of 2^31, at the ragged end and at random match it too,
-    first step and steady steps."""
+    first step and steady steps, with the update decided on the host and on the device."""
     n = 2 ** 31 + 777
     w = dataclasses.replace(CONFIG3, calls=3, inplace=True, outlier_per_10000=0,
                             max_grad_norm=1.0, row_len=1024)
@@ -159,7 +161,7 @@ def test_more_than_2_31_elements_sampled():
     idx = sample_indices(n, k=20000, seed=31, extra=edges)
     # the whole statistics-guarded step: analysis in rows of 1024 (2,097,153 rows), the
     # merge, the norm against the oracle's sum over all 2^31 + 777 values, the clipped update
-    s = run_workload(w, n, "clipped", DEV, idx=idx, row_len=1024, full_grad_on_host=False)
+    s = run_workload(w, n, api, DEV, idx=idx, row_len=1024, full_grad_on_host=False)
     assert s["t"] == 3 and s["updates"] == 3
     assert all(r[1] > 1.0 for r in s["reports"])  # the clip is active
 
