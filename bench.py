@@ -440,6 +440,54 @@ def parity_check(w, snap, steps: int):
                     "that couple the elements are checked over the whole gradient"}
 
 
+def row_snapshot(idx, arrays, t):
+    """Host copies of a row's state at the sampled elements (device side of the row
+    checks); ``arrays`` maps a name to a device tensor or None."""
+    import torch
+    it = torch.as_tensor(idx, device=next(a for a in arrays.values() if a is not None).device)
+    out = {k: (a[it].cpu().numpy() if a is not None else None) for k, a in arrays.items()}
+    out["t"] = int(t)
+    return out
+
+
+def row_parity_check(rec):
+    """Replays one timed next-row batch through the oracle (the bench's CPU leg).
+
+    ``rec`` holds the row's workload recipe, the sampled indices, the device gradient
+    at them, and the device state there before and after the batch (warm-up calls
+    included).  The oracle starts from the state before, takes the batch's steps
+    (t after - t before) with the same gradient, and must land on the state after
+    within |d| <= 1e-5 * max(1, |x|); the sampled gradient must be the generator's."""
+    import numpy as np
+    import oracle
+    lib = oracle.lib()
+    w, idx, b, a = rec["w"], rec["idx"], rec["before"], rec["after"]
+    gh = w.grad_host(1, idx)
+    inputs_ok = bool(np.array_equal(rec["g_bits"], gh))
+    if rec.get("p0_from_generator"):
+        inputs_ok = inputs_ok and bool(np.array_equal(b["p"], w.params_host(idx)))
+    opts = w.options()
+    o = oracle.OracleAdamW(b["p"], opts, storage="f32", lib_=lib)
+    if b["t"] > 0:
+        o.state = oracle.OracleState(t=b["t"], m=b["m"], v=b["v"],
+                                     vmax=b.get("vmax") if opts["amsgrad"] else None)
+    steps = a["t"] - b["t"]
+    for _ in range(steps):
+        o.step(gh, rec["gdt"], w.gradient_scale)
+    refs = {"p": o.p, "m": o.state.m, "v": o.state.v}
+    if opts["amsgrad"]:
+        refs["vmax"] = o.state.vmax
+    errs = {}
+    for name, ref in refs.items():
+        ref = np.asarray(ref, np.float64)
+        e = np.abs(np.asarray(a[name], np.float64) - ref) / np.maximum(1.0, np.abs(ref))
+        errs[name] = float(np.max(e)) if np.all(np.isfinite(e)) else float("inf")
+    max_err = max(errs.values())
+    ok = inputs_ok and steps > 0 and max_err <= 1e-5
+    return {"ok": bool(ok), "elements": int(len(idx)), "steps": int(steps),
+            "max_rel_err": max_err, "per_array": errs, "inputs_match_generator": inputs_ok}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -744,7 +792,9 @@ def run_ours(args):
     # CUDA events per launch): the plain update and the fused low-precision
     # write-back (BF16 model copy, +2 B/param).
     next_rows = None
+    row_checks = {}  # next rows replayed through the oracle in the CPU leg
     if args.next_rows_steps > 0 and not zero1:  # the single-GPU rows, at N = 1 only
+        import numpy as np
         p_model = torch.empty(n, dtype=torch.bfloat16, device=dev)
 
         def timed(fn, k):
@@ -854,7 +904,15 @@ def run_ours(args):
         def inplace3():
             s3["t"], _ = fa.fa_adamw_step_inplace(p3, g3, m3, v3, None, s3["t"], o3, ctl)
 
+        idx3 = parity_indices(n3, k=20_000, seed=3)
+        arr3 = {"p": p3, "m": m3, "v": v3}
+        before3 = row_snapshot(idx3, arr3, s3["t"])
         ms = timed(inplace3, args.next_rows_steps)
+        row_checks["inplace_124M_bf16_adamw"] = {
+            "w": CONFIG3, "idx": idx3, "gdt": "bf16", "p0_from_generator": True,
+            "g_bits": g3[torch.as_tensor(idx3, device=dev)].view(torch.int16).cpu().numpy()
+                        .view("uint16"),
+            "before": before3, "after": row_snapshot(idx3, arr3, s3["t"])}
         b = fa.bytes_per_param(2, False, False)
         rows_out["inplace_124M_bf16_adamw"] = {
             "ms": ms, "params": n3, "bytes_per_param": b,
@@ -951,6 +1009,11 @@ def run_ours(args):
         # the same bucket without statistics (AMSGrad, FP16 gradients, one launch over
         # 199 tensors), maximize off and on
         from synthetic.configs import CONFIG4_MAX
+        edges4 = sorted({x + d for x in seg[1:-1] for d in (-1, 0)})
+        idx4 = np.unique(np.concatenate([parity_indices(sn, k=20_000, seed=4),
+                                         np.asarray(edges4, np.int64)]))
+        g4_bits = sg[torch.as_tensor(idx4, device=dev)].view(torch.int16).cpu().numpy().view("uint16")
+        arr4 = {"p": sp, "m": sm, "v": sv, "vmax": svm}
         for tag, cfg in (("", CONFIG4), ("_maximize", CONFIG4_MAX)):
             ob = fa.options(**cfg.options())
 
@@ -958,7 +1021,11 @@ def run_ours(args):
                 sstate["t"], _ = fa.fa_bucket_step(seg, sp, sg, sm, sv, svm, sstate["t"], ob,
                                                    ctl, 1.0)
 
+            before4 = row_snapshot(idx4, arr4, sstate["t"])
             ms = timed(bucket, args.next_rows_steps)
+            row_checks["bucket_decoder1.1B_f16_amsgrad" + tag] = {
+                "w": cfg, "idx": idx4, "gdt": "f16", "g_bits": g4_bits,
+                "before": before4, "after": row_snapshot(idx4, arr4, sstate["t"])}
             b = fa.bytes_per_param(2, True, False)
             rows_out["bucket_decoder1.1B_f16_amsgrad" + tag] = {
                 "ms": ms, "params": sn, "tensors": len(seg) - 1, "bytes_per_param": b,
@@ -1025,6 +1092,11 @@ def run_ours(args):
             if next_rows is not None:
                 par["f2_staged_equals_fused_bitwise"] = f2_bitwise
                 par["ok"] = par["ok"] and all(f2_bitwise.values())
+                rows_par = {name: row_parity_check(rec) for name, rec in row_checks.items()}
+                for name, rp in rows_par.items():
+                    next_rows[name]["parity"] = rp
+                par["next_rows_ok"] = {name: rp["ok"] for name, rp in rows_par.items()}
+                par["ok"] = par["ok"] and all(rp["ok"] for rp in rows_par.values())
             line["parity"] = par
             if not par["ok"]:  # an unchecked or failing number is never reported
                 line["value"] = None

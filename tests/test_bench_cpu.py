@@ -100,3 +100,61 @@ def test_bench_parity_check_passes_the_oracle_and_catches_errors():
         s = {k: (v.copy() if hasattr(v, "copy") else v) for k, v in snap.items()}
         spoil(s)
         assert not bench.parity_check(w, s, 4)["ok"], name
+
+
+def _row_record(w, idx, t0, steps):
+    """A next-row record as the bench builds it, with the device side played by the
+    oracle itself: the state after t0 steps from the generator's parameters, and after
+    t0 + steps."""
+    import numpy as np
+    import oracle
+    lib = oracle.lib()
+    gh = w.grad_host(1, idx)
+    o = oracle.OracleAdamW(w.params_host(idx), w.options(), storage="f32", lib_=lib)
+
+    def snap(t):
+        st = o.state
+        zero = np.zeros(len(idx), np.float32)
+        out = {"p": o.p.copy(), "m": zero if st.m is None else st.m.copy(),
+               "v": zero if st.v is None else st.v.copy(), "t": t}
+        if w.amsgrad:
+            out["vmax"] = zero if st.vmax is None else st.vmax.copy()
+        return out
+
+    for _ in range(t0):
+        o.step(gh, w.grad_dtype, w.gradient_scale)
+    before = snap(t0)
+    for _ in range(steps):
+        o.step(gh, w.grad_dtype, w.gradient_scale)
+    return {"w": w, "idx": idx, "gdt": w.grad_dtype, "g_bits": gh.copy(),
+            "p0_from_generator": t0 == 0, "before": before, "after": snap(t0 + steps)}
+
+
+def test_bench_next_row_replay_passes_the_oracle_and_catches_errors():
+    """The bench's next-row check (the in-place 124M row and the decoder bucket rows):
+    a batch equal to the oracle's replay passes, from the first step and from a state
+    mid-run, with AMSGrad and maximize; a parameter off by 1e-4, a moment or vmax off
+    by 2e-5, a step count off by one, or a gradient other than the generator's fails."""
+    import dataclasses
+    import numpy as np
+    from synthetic.configs import CONFIG3, CONFIG4_MAX
+    w3 = CONFIG3.scaled(4099)
+    w4 = dataclasses.replace(CONFIG4_MAX, segments=None).scaled(5003)
+    for w, t0 in ((w3, 0), (w4, 3)):
+        idx = np.unique(np.concatenate([np.arange(0, w.n, 7), [w.n - 1]])).astype(np.int64)
+        rec = _row_record(w, idx, t0, 4)
+        good = bench.row_parity_check(rec)
+        assert good["ok"] and good["steps"] == 4 and good["max_rel_err"] <= 1e-7, good
+        spoils = [("p", lambda r: r["after"]["p"].__setitem__(2, r["after"]["p"][2] + 1e-4)),
+                  ("m", lambda r: r["after"]["m"].__setitem__(-1, r["after"]["m"][-1] + 2e-5)),
+                  ("t", lambda r: r["after"].__setitem__("t", r["after"]["t"] - 1)),
+                  ("g", lambda r: r["g_bits"].__setitem__(5, r["g_bits"][5] ^ 1))]
+        if w.amsgrad:
+            spoils.append(("vmax", lambda r: r["after"]["vmax"].__setitem__(
+                0, r["after"]["vmax"][0] + 2e-5)))
+        for name, spoil in spoils:
+            r = {k: v for k, v in rec.items()}
+            r["after"] = {k: (v.copy() if hasattr(v, "copy") else v) for k, v in rec["after"].items()}
+            r["g_bits"] = rec["g_bits"].copy()
+            spoil(r)
+            assert not bench.row_parity_check(r)["ok"], (w.name, name)
