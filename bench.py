@@ -457,7 +457,10 @@ def row_parity_check(rec):
     at them, and the device state there before and after the batch (warm-up calls
     included).  The oracle starts from the state before, takes the batch's steps
     (t after - t before) with the same gradient, and must land on the state after
-    within |d| <= 1e-5 * max(1, |x|); the sampled gradient must be the generator's."""
+    within |d| <= 1e-5 * max(1, |x|); the sampled gradient must be the generator's.
+    A per-segment clipped row also carries the segment table, the clip threshold and
+    the whole gradient: each sampled element then takes its segment's coefficient
+    from the oracle's own decision over that segment."""
     import numpy as np
     import oracle
     lib = oracle.lib()
@@ -467,25 +470,46 @@ def row_parity_check(rec):
     if rec.get("p0_from_generator"):
         inputs_ok = inputs_ok and bool(np.array_equal(b["p"], w.params_host(idx)))
     opts = w.options()
-    o = oracle.OracleAdamW(b["p"], opts, storage="f32", lib_=lib)
-    if b["t"] > 0:
-        o.state = oracle.OracleState(t=b["t"], m=b["m"], v=b["v"],
-                                     vmax=b.get("vmax") if opts["amsgrad"] else None)
     steps = a["t"] - b["t"]
-    for _ in range(steps):
-        o.step(gh, rec["gdt"], w.gradient_scale)
-    refs = {"p": o.p, "m": o.state.m, "v": o.state.v}
+    # the elements' groups and their clip coefficients: one group without statistics,
+    # else one per segment, with the oracle's own per-segment decision from its FP64
+    # statistics over the segment's whole gradient
+    groups, extra = [(np.arange(len(idx)), 1.0)], {}
+    if rec.get("seg") is not None:
+        seg = np.asarray(rec["seg"], np.int64)
+        g_all = rec["g_full_bits"]
+        inputs_ok = inputs_ok and bool(np.array_equal(g_all[idx], gh))
+        decisions = [lib.clip_decision(*lib.gradient_stats(g_all[lo:hi], rec["gdt"],
+                                                           w.gradient_scale),
+                                       rec["max_grad_norm"])
+                     for lo, hi in zip(seg[:-1], seg[1:])]
+        inputs_ok = inputs_ok and not any(d[0] for d in decisions)  # none planted here
+        kseg = np.searchsorted(seg, idx, side="right") - 1
+        groups = [(np.flatnonzero(kseg == k), decisions[k][2]) for k in np.unique(kseg)]
+        coefs = [d[2] for d in decisions]
+        extra = {"segments": int(len(seg) - 1), "min_clip_coef_oracle": float(min(coefs))}
+    refs = {"p": np.empty(len(idx)), "m": np.empty(len(idx)), "v": np.empty(len(idx))}
     if opts["amsgrad"]:
-        refs["vmax"] = o.state.vmax
+        refs["vmax"] = np.empty(len(idx))
+    for sel, coef in groups:
+        o = oracle.OracleAdamW(b["p"][sel], opts, storage="f32", lib_=lib)
+        if b["t"] > 0:
+            o.state = oracle.OracleState(t=b["t"], m=b["m"][sel], v=b["v"][sel],
+                                         vmax=b["vmax"][sel] if opts["amsgrad"] else None)
+        for _ in range(steps):
+            o.step(gh[sel], rec["gdt"], w.gradient_scale, clip_coef=coef)
+        refs["p"][sel], refs["m"][sel], refs["v"][sel] = o.p, o.state.m, o.state.v
+        if opts["amsgrad"]:
+            refs["vmax"][sel] = o.state.vmax
     errs = {}
     for name, ref in refs.items():
-        ref = np.asarray(ref, np.float64)
         e = np.abs(np.asarray(a[name], np.float64) - ref) / np.maximum(1.0, np.abs(ref))
         errs[name] = float(np.max(e)) if np.all(np.isfinite(e)) else float("inf")
     max_err = max(errs.values())
     ok = inputs_ok and steps > 0 and max_err <= 1e-5
     return {"ok": bool(ok), "elements": int(len(idx)), "steps": int(steps),
-            "max_rel_err": max_err, "per_array": errs, "inputs_match_generator": inputs_ok}
+            "max_rel_err": max_err, "per_array": errs, "inputs_match_generator": inputs_ok,
+            **extra}
 
 
 def run_reference(args):
@@ -996,9 +1020,25 @@ def run_ours(args):
             if not bool((srep_pinned[:, 1] != 0).any()):
                 sstate["t"] += 1
 
+        from synthetic.configs import CONFIG4_MAX
+        edges4 = sorted({x + d for x in seg[1:-1] for d in (-1, 0)})
+        idx4 = np.unique(np.concatenate([parity_indices(sn, k=20_000, seed=4),
+                                         np.asarray(edges4, np.int64)]))
+        g4_bits = sg[torch.as_tensor(idx4, device=dev)].view(torch.int16).cpu().numpy().view("uint16")
+        g4_all = sg.view(torch.int16).cpu().numpy().view("uint16")  # the oracle's statistics
+        arr4 = {"p": sp, "m": sm, "v": sv, "vmax": svm}
+        seg_clip = {"seg": seg, "max_grad_norm": 0.01, "g_full_bits": g4_all}
+        before_f3 = row_snapshot(idx4, arr4, sstate["t"])
         ms_host = timed(per_segment_host, args.next_rows_steps)
         min_coef = sstate["rep"].clip_coef
+        after_f3_host = row_snapshot(idx4, arr4, sstate["t"])
         ms = timed(per_segment, args.next_rows_steps)
+        row_checks["f3_per_segment_clip_decoder1.1B_f16_amsgrad/host_decided"] = dict(
+            seg_clip, w=CONFIG4, idx=idx4, gdt="f16", g_bits=g4_bits, p0_from_generator=True,
+            before=before_f3, after=after_f3_host)
+        row_checks["f3_per_segment_clip_decoder1.1B_f16_amsgrad"] = dict(
+            seg_clip, w=CONFIG4, idx=idx4, gdt="f16", g_bits=g4_bits, before=after_f3_host,
+            after=row_snapshot(idx4, arr4, sstate["t"]))
         b3 = fa.bytes_per_param(2, True, False) + 2  # AMSGrad update + analysis read of the FP16 gradient
         rows_out["f3_per_segment_clip_decoder1.1B_f16_amsgrad"] = {
             "ms": ms, "params": sn, "segments": len(seg) - 1, "row_len": 512,
@@ -1008,12 +1048,6 @@ def run_ours(args):
             "decided": "on the device", "host_decided_ms": ms_host}
         # the same bucket without statistics (AMSGrad, FP16 gradients, one launch over
         # 199 tensors), maximize off and on
-        from synthetic.configs import CONFIG4_MAX
-        edges4 = sorted({x + d for x in seg[1:-1] for d in (-1, 0)})
-        idx4 = np.unique(np.concatenate([parity_indices(sn, k=20_000, seed=4),
-                                         np.asarray(edges4, np.int64)]))
-        g4_bits = sg[torch.as_tensor(idx4, device=dev)].view(torch.int16).cpu().numpy().view("uint16")
-        arr4 = {"p": sp, "m": sm, "v": sv, "vmax": svm}
         for tag, cfg in (("", CONFIG4), ("_maximize", CONFIG4_MAX)):
             ob = fa.options(**cfg.options())
 
@@ -1094,7 +1128,8 @@ def run_ours(args):
                 par["ok"] = par["ok"] and all(f2_bitwise.values())
                 rows_par = {name: row_parity_check(rec) for name, rec in row_checks.items()}
                 for name, rp in rows_par.items():
-                    next_rows[name]["parity"] = rp
+                    row, _, variant = name.partition("/")
+                    next_rows[row]["parity_" + variant if variant else "parity"] = rp
                 par["next_rows_ok"] = {name: rp["ok"] for name, rp in rows_par.items()}
                 par["ok"] = par["ok"] and all(rp["ok"] for rp in rows_par.values())
             line["parity"] = par

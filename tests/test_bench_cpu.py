@@ -158,3 +158,52 @@ def test_bench_next_row_replay_passes_the_oracle_and_catches_errors():
             r["g_bits"] = rec["g_bits"].copy()
             spoil(r)
             assert not bench.row_parity_check(r)["ok"], (w.name, name)
+
+
+def test_bench_next_row_replay_takes_per_segment_decisions():
+    """The per-segment clipped rows: each sampled element replays with its own
+    segment's coefficient, which the oracle decides from that segment's whole
+    gradient.  A device state made with those coefficients passes; one made with a
+    single global coefficient, or a gradient changed outside the sampled elements,
+    fails."""
+    import dataclasses
+    import numpy as np
+    import oracle
+    from synthetic.configs import CONFIG4
+    lib = oracle.lib()
+    seg = np.array([0, 700, 700, 2500, 2501, 6000], np.int64)  # one empty, one of 1 element
+    w = dataclasses.replace(CONFIG4, segments=None).scaled(int(seg[-1]))
+    g_all = w.grad_host(1, np.arange(w.n))
+    max_norm = 1e-3
+    coefs = [lib.clip_decision(*lib.gradient_stats(g_all[a:b], "f16", 1.0), max_norm)[2]
+             for a, b in zip(seg[:-1], seg[1:])]
+    assert min(coefs) < 1.0
+    idx = np.unique(np.concatenate([np.arange(0, w.n, 5), seg[1:-1], seg[1:-1] - 1]))
+    idx = idx[idx < w.n].astype(np.int64)
+    kseg = np.searchsorted(seg, idx, side="right") - 1
+
+    def device_like(coef_of):
+        p = np.empty(len(idx), np.float32)
+        m, v, vm = p.copy(), p.copy(), p.copy()
+        for k in np.unique(kseg):
+            sel = np.flatnonzero(kseg == k)
+            o = oracle.OracleAdamW(w.params_host(idx[sel]), w.options(), lib_=lib)
+            for _ in range(3):
+                o.step(w.grad_host(1, idx[sel]), "f16", clip_coef=coef_of(k))
+            p[sel], m[sel], v[sel], vm[sel] = o.p, o.state.m, o.state.v, o.state.vmax
+        return {"p": p, "m": m, "v": v, "vmax": vm, "t": 3}
+
+    zero = np.zeros(len(idx), np.float32)
+    before = {"p": w.params_host(idx), "m": zero, "v": zero, "vmax": zero, "t": 0}
+    rec = {"w": w, "idx": idx, "gdt": "f16", "g_bits": g_all[idx].copy(),
+           "p0_from_generator": True, "seg": seg, "max_grad_norm": max_norm,
+           "g_full_bits": g_all, "before": before, "after": device_like(lambda k: coefs[k])}
+    good = bench.row_parity_check(rec)
+    assert good["ok"] and good["segments"] == 5 and good["max_rel_err"] <= 1e-7, good
+    assert abs(good["min_clip_coef_oracle"] - min(coefs)) == 0
+    bad = dict(rec, after=device_like(lambda k: min(coefs)))
+    assert not bench.row_parity_check(bad)["ok"]
+    off = np.setdiff1d(np.arange(w.n), idx)[3]
+    g2 = g_all.copy()
+    g2[off] = np.uint16(0x3C00)  # 1.0 in FP16: a larger norm for that segment
+    assert not bench.row_parity_check(dict(rec, g_full_bits=g2))["ok"]
