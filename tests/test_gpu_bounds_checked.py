@@ -1,6 +1,6 @@
 """The bounds-checked build of the library: the CUDA path's own cases, rerun through it.
 
-`compute-sanitizer` is not available on this machine, so the library has a test variant
+In place of an external memory checker, the library has a test variant
 (-DFA_BOUNDS_CHECK=1) in which every kernel checks the element range it is about to
 touch against its array's length and counts, then skips, any access outside it.  The
 cases below are the parity tests of the other modules (each against the oracle, with
