@@ -72,6 +72,9 @@ CASES = [
          ("mixed", "f16", False, 1.0), ("many", "f32", False, 1.0),
          ("offset", "bf16", False, 1.0), ("mixed", "f16", False, 3.0),
          ("small", "f16", True, 2.0 ** -4))]),
+    ("full-grid stretch edges and scalar heads, decided on the host and on the device",
+     lambda lib: [P.test_full_grid_stretch_edges_and_scalar_heads(n, off, lib)
+                  for n in (1025, 3 * 1024 + 5) for off in (0, 3)]),
     ("gated step at scales with and without an exact inverse",
      lambda lib: [P.test_gated_step_equals_host_decided_step_bitwise_at_any_scale(sc, ams)
                   for sc in (128.0, 3.0) for ams in (False, True)]),

@@ -928,6 +928,58 @@ def test_gated_step_equals_host_decided_step_bitwise_at_any_scale(scale, amsgrad
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
 
 
+@pytest.mark.parametrize("off", [0, 1, 3])
+@pytest.mark.parametrize("n", [1023, 1025, 2049, 3 * 1024 + 5])
+def test_full_grid_stretch_edges_and_scalar_heads(n, off, oracle_lib):
+    """The full grid gives each 64-thread CTA 1024 elements.  Sizes on both sides of one,
+    two and three stretches, with p, m and v viewed ``off`` elements past a 16-byte
+    boundary and the BF16 gradient at the offset that keeps all four co-aligned, so that
+    a scalar head of (4 - off) % 4 elements comes before the vector body; the elements
+    around the views are guards.  Decided on the host and on the device (four calls, a
+    +Inf in the third, the clip active): the two bit-identical, and both on the oracle's
+    trajectory."""
+    import oracle
+    from gpu_harness import gate
+    goff = off + 4 if off % 4 else 0  # 2-byte elements: the same 16-byte phase as p's
+    w = CONFIG5.scaled(n, calls=4, inf_call=3)
+    w = dataclasses.replace(w, max_grad_norm=0.02)  # the clip is active at these sizes
+    opts = w.options()
+    idx = np.arange(n)
+    rows = fa.fa_stats_rows(n, 256)
+    states = []
+    mailbox = fa.report_mailbox()
+    for gated in (False, True):
+        full = [torch.full((n + 32,), -7.0, device=DEV) for _ in range(3)]
+        p, m, v = (x[off:off + n] for x in full)
+        w.fill_params_device(p)
+        gfull = torch.zeros(n + 32, dtype=torch.bfloat16, device=DEV)
+        g = gfull[goff:goff + n]
+        rb, sc, rep = fa.stats_buffer(rows, DEV), fa.scratch_buffer(rows, DEV), fa.stats_buffer(1, DEV)
+        ref = oracle.OracleAdamW(w.params_host(idx), opts, lib_=oracle_lib)
+        t = 0
+        for call in range(1, w.calls + 1):
+            w.fill_grad_device(call, g)
+            step = (lambda *a: fa.fa_bucket_step_clipped_gated(*a, mailbox)) if gated \
+                else fa.fa_bucket_step_clipped
+            t, r = step(None, p, g, m, v, None, t, fa.options(**opts), fa.control(),
+                        w.max_grad_norm, 256, rb, sc, rep)
+            gh = w.grad_host(call, idx)
+            st, c = oracle_lib.gradient_stats(gh, "bf16", 1.0)
+            skip, _, coef = oracle_lib.clip_decision(st, c, w.max_grad_norm)
+            assert bool(r.skipped_nonfinite) == skip == (call == 3)
+            ref.step(gh, "bf16", skip_update=skip, clip_coef=coef)
+        torch.cuda.synchronize()
+        assert t == ref.state.t == 3
+        for x in full:  # the elements around the view are untouched
+            assert torch.all(x[:off] == -7.0) and torch.all(x[off + n:] == -7.0)
+        gate(p.cpu().numpy(), ref.p, 1e-5, f"n={n} off={off} gated={gated} p")
+        gate(m.cpu().numpy(), ref.state.m, 1e-5, "m")
+        gate(v.cpu().numpy(), ref.state.v, 1e-5, "v")
+        states.append([x.clone() for x in (p, m, v)])
+    for a, b in zip(*states):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
 def test_gated_step_full_size_bitwise():
     """The benchmark's launch configuration: the 1,073,741,824-parameter workload, rows of
     256, the update gated on the device report, five calls with the +Inf in call 3;
