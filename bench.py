@@ -847,6 +847,24 @@ def run_ours(args):
 
         peak, peak_kind = measured_peaks()
         rows_out = {}
+        # the whole step as one C-ABI call (the form a user calls): the last merge posts
+        # the report to a pinned mailbox and the update decides on the device, so no
+        # stream operation sits between them
+        one_call_mailbox = fa.report_mailbox()
+
+        def one_call():
+            state["t"], _ = fa.fa_bucket_step_clipped_gated(
+                None, p, g, m, v, None, state["t"], opts, ctl, w.max_grad_norm, row_len,
+                rows_buf, scratch, report, one_call_mailbox)
+
+        ms = timed(one_call, args.next_rows_steps)
+        sb = fa.bytes_per_param(2, False, False) * n + 2 * n + rows * 12 * 2
+        rows_out["step_one_call_gated"] = {
+            "ms": ms, "params_per_s": n / (ms * 1e-3), "bytes": sb,
+            "achieved_gbs": sb / (ms * 1e-3) / 1e9, "frac": sb / (ms * 1e-3) / 1e9 / peak,
+            "peak_kind": peak_kind,
+            "what": "fa_bucket_step_clipped_gated: analysis, merges posting to the mailbox, "
+                    "the update deciding on the device; CUDA events per call"}
         for name, fn, bpp_k in (("update_only", plain, fa.bytes_per_param(2, False, False)),
                                 ("first_step", first, fa.bytes_per_param(2, False, True)),
                                 ("f1_writeback_bf16", writeback,
