@@ -282,14 +282,17 @@ fa_status check_segments(const int64_t *seg, int32_t nseg, int64_t n) {
 
 // The per-segment update, one launch per kMaxSegPerLaunch segments (arguments
 // validated).  Each segment's multiplier comes from seg_grad_mult (decided on the
-// host) or, with ``reports`` (device, one record per segment), is decided in the
-// kernels from the records: any non-finite count skips every launch, and segment
-// k's clip coefficient is the host formula's with max_grad_norm.
+// host) or, with ``reports`` (device, one record per segment), is decided on the
+// device from the records: any non-finite count skips every launch, and segment
+// k's clip coefficient is the host formula's with max_grad_norm.  ``decided``
+// (device, nseg + 1 floats, or nullptr): where the decisions are first taken once
+// for the whole bucket (launch_segment_decide), for the update kernels to read.
 fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float *p,
                                  const void *g, fa_dtype gdt, float *m, float *v, float *vmax,
                                  uint64_t t_new, const fa_options *options, fa_step_control ctl,
                                  const double *seg_grad_mult, const fa_stats *reports,
-                                 double max_grad_norm, void *stream) {
+                                 double max_grad_norm, void *stream,
+                                 float *decided = nullptr) {
     Coef c;
     fa_status st = make_coef(options, t_new, ctl.gradient_scale, 1.0, &c);
     if (st != FA_OK) return st;
@@ -297,6 +300,16 @@ fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float
     const bool ams = options->amsgrad != 0;
     const double sign = options->maximize ? -1.0 : 1.0;
     const size_t gb = dtype_bytes(gdt);
+    if (decided) {
+        fa::UpdateArgs gate{};
+        gate.gate_scale = ctl.gradient_scale;
+        gate.gate_max_norm = max_grad_norm;
+        gate.gate_sign = sign;
+        gate.gate_inv_scale = fa::power_of_two_inverse(ctl.gradient_scale);
+        if (fa::launch_segment_decide(gate, reports, nseg, decided,
+                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
     for (int32_t k0 = 0; k0 < nseg; k0 += fa::kMaxSegPerLaunch) {
         const int32_t cnt = nseg - k0 < fa::kMaxSegPerLaunch ? nseg - k0 : fa::kMaxSegPerLaunch;
         const int64_t e0 = seg_offsets[k0], e1 = seg_offsets[k0 + cnt];
@@ -335,6 +348,7 @@ fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float
         sa.reports = reports;
         sa.nreports = reports ? nseg : 0;
         sa.k0 = k0;
+        sa.decided = decided;
         if (fa::launch_update_segment_scaled(sa, c, gdt, ams, first, vec,
                                              static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return FA_ERR_CUDA;
@@ -1134,8 +1148,12 @@ fa_status fa_bucket_step_clipped_per_segment_gated(
     if ((st = fa_merge_gradient_stats_chunks(rows_buf, chunk_rows.data(), nseg, scratch,
                                              scratch_elements, seg_reports, stream)) != FA_OK)
         return st;
+    // The merges are done with the scratch once the reports are written: when it holds
+    // nseg + 1 floats, every segment's decision is taken there once, and the update
+    // runs on the full grid reading it.
+    float *decided = scratch_elements >= static_cast<int64_t>(nseg) + 1 ? scratch : nullptr;
     return enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, t + 1, options, ctl,
-                                  nullptr, seg_reports, max_grad_norm, stream);
+                                  nullptr, seg_reports, max_grad_norm, stream, decided);
 }
 
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream) {

@@ -207,10 +207,22 @@ struct SegScaleArgs {
     const fa_stats *reports;
     int64_t nreports;
     int32_t k0;
+    // With reports: the decisions already taken once for the whole bucket by
+    // launch_segment_decide (nullptr: each launch decides itself): decided[0] is the
+    // skip flag (non-zero: skip), decided[1 + k0 + j] segment j's multiplier.
+    const float *decided;
 };
 cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, fa_dtype gdt,
                                          bool amsgrad, bool first, bool vector_ok,
                                          cudaStream_t stream);
+
+// One CTA takes every segment's decision from its record (the host formula's FP64
+// operations with a.gate_scale, a.gate_inv_scale, a.gate_max_norm, a.gate_sign) into
+// decided[1 + k] for k < nseg, and the skip flag (any non-finite count) into
+// decided[0].  Launched as the programmatic dependent of the merge that wrote the
+// records.
+cudaError_t launch_segment_decide(const UpdateArgs &a, const fa_stats *reports, int32_t nseg,
+                                  float *decided, cudaStream_t stream);
 
 // One merge level: ceil(count / kFanIn) output records from count input records.
 // ``post`` (device address of a pinned host mailbox, final level only) also receives

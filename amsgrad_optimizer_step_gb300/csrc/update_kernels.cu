@@ -199,17 +199,24 @@ __device__ __forceinline__ double gate_unscale(const UpdateArgs &a, double x) {
     return a.gate_inv_scale != 0.0 ? x * a.gate_inv_scale : x / a.gate_scale;
 }
 
-// The host's skip / clip decision, taken on the device from the same report
-// with the same FP64 operations in the same order (so the multiplier is
-// bit-identical): false = skip the update.
-__device__ __forceinline__ bool gate_decision(const UpdateArgs &a, float *gmul) {
-    const fa_stats r = *a.gate;
-    if (r.nonfinite > 0) return false;
+// The gradient multiplier of a report without non-finite values: the host's clip
+// decision with the same FP64 operations in the same order (norm = sqrt(sum) /
+// scale; coef = max_norm / norm above max_norm; sign * coef / scale), so it is
+// bit-identical to the host-decided multiplier.
+__device__ __forceinline__ float decided_multiplier(const UpdateArgs &a, const fa_stats &r) {
     const double sum = record_sum_sq(r);
     const double norm = gate_unscale(a, sqrt(sum));
     double coef = 1.0;
     if (a.gate_max_norm > 0 && norm > a.gate_max_norm) coef = a.gate_max_norm / norm;
-    *gmul = static_cast<float>(gate_unscale(a, a.gate_sign * coef));
+    return static_cast<float>(gate_unscale(a, a.gate_sign * coef));
+}
+
+// The host's skip / clip decision, taken on the device from the same report:
+// false = skip the update.
+__device__ __forceinline__ bool gate_decision(const UpdateArgs &a, float *gmul) {
+    const fa_stats r = *a.gate;
+    if (r.nonfinite > 0) return false;
+    *gmul = decided_multiplier(a, r);
     return true;
 }
 
@@ -483,27 +490,39 @@ __device__ __forceinline__ bool segment_multipliers(const SegScaleArgs &s, float
     for (int64_t j = threadIdx.x; j < s.nreports; j += blockDim.x)
         bad |= s.reports[j].nonfinite != 0;
     if (__syncthreads_or(bad)) return false;
-    for (int j = threadIdx.x; j < s.nseg; j += blockDim.x) {
-        const fa_stats r = s.reports[s.k0 + j];
-        const double sum = record_sum_sq(r);
-        const double norm = gate_unscale(s.a, sqrt(sum));
-        double coef = 1.0;
-        if (s.a.gate_max_norm > 0 && norm > s.a.gate_max_norm) coef = s.a.gate_max_norm / norm;
-        gm[j] = static_cast<float>(gate_unscale(s.a, s.a.gate_sign * coef));
-    }
+    for (int j = threadIdx.x; j < s.nseg; j += blockDim.x)
+        gm[j] = decided_multiplier(s.a, s.reports[s.k0 + j]);
     return true;
 }
 
-// The per-segment update with multipliers from the host, on the full grid: one
-// stretch of THREADS * UNROLL vectors per CTA (the launcher guarantees that the grid
-// covers every stretch), the body of update_vec_kernel.  A CTA copies the
-// multipliers of only the segments its elements fall in, [k_lo, k_hi] (usually one),
-// from the table in the kernel parameters into shared memory.  CTA 0 also takes the
-// scalar head and the last CTA the scalar tail, so their ranges include those
-// elements.  A vector finds its segment by a forward scan from k_lo; one that
-// straddles a boundary looks up each element.  (Decided on the device, with one
-// report per segment, this grid measured slower than the pipeline: 6.35-6.63 against
-// 6.11 ms for the 1.2e9-parameter, 199-segment FP16 AMSGrad bucket.)
+// Every segment's decision, once for the whole bucket (see launch_segment_decide).
+constexpr int kDecideThreads = 256;
+__global__ void __launch_bounds__(kDecideThreads)
+segment_decide_kernel(const UpdateArgs a, const fa_stats *reports, int32_t nseg,
+                      float *decided) {
+    fa_grid_dependency_wait();  // the merge that writes the records may still run
+    bool bad = false;
+    for (int j = threadIdx.x; j < nseg; j += kDecideThreads) {
+        const fa_stats r = reports[j];
+        bad |= r.nonfinite != 0;
+        decided[1 + j] = decided_multiplier(a, r);
+    }
+    const int skip = __syncthreads_or(bad);
+    if (threadIdx.x == 0) decided[0] = skip ? 1.0f : 0.0f;
+}
+
+// The per-segment update on the full grid, with multipliers from the host or
+// decided once for the bucket on the device (s.decided): one stretch of THREADS *
+// UNROLL vectors per CTA (the launcher guarantees that the grid covers every
+// stretch), the body of update_vec_kernel.  A CTA copies the multipliers of only the
+// segments its elements fall in, [k_lo, k_hi] (usually one), from the kernel
+// parameters or the decided table into shared memory; a decided skip ends every
+// CTA before it stores anything.  CTA 0 also takes the scalar head and the last CTA
+// the scalar tail, so their ranges include those elements.  A vector finds its
+// segment by a forward scan from k_lo; one that straddles a boundary looks up each
+// element.  (Deciding in every CTA from the reports measured slower than the
+// pipeline: 6.35-6.63 against 6.11 ms for the 1.2e9-parameter, 199-segment FP16
+// AMSGrad bucket.)
 template <int GT, bool AMS, bool FIRST, int UNROLL, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 update_seg_grid_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
@@ -537,8 +556,13 @@ update_seg_grid_kernel(const __grid_constant__ SegScaleArgs s, const Coef c) {
     if (blockIdx.x == gridDim.x - 1) e_hi = a.n;
     const int k_lo = find_seg(s, e_lo);
     const int k_hi = e_hi > e_lo ? find_seg(s, e_hi - 1) : k_lo;
-    for (int k = k_lo + threadIdx.x; k <= k_hi; k += THREADS) gm[k] = s.gmul[k];
+    __shared__ int s_skip;
+    const float *decided = s.decided;
+    for (int k = k_lo + threadIdx.x; k <= k_hi; k += THREADS)
+        gm[k] = decided ? decided[1 + s.k0 + k] : s.gmul[k];
+    if (threadIdx.x == 0) s_skip = decided != nullptr && decided[0] != 0.0f;
     __syncthreads();
+    if (s_skip) return;  // the whole CTA: nothing is stored
 
     int k = k_lo;
 #pragma unroll
@@ -1014,9 +1038,10 @@ cudaError_t launch_seg_typed(const SegScaleArgs &s, const Coef &c, bool vec, cud
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    // Multipliers from the host: the full grid.  Decided on the device: few CTAs (the
-    // pipeline, or persistent CTAs), each taking every segment's decision once.
-    if (vec && !s.reports) {
+    // Multipliers from the host, or decided once for the bucket: the full grid.
+    // Decided by each launch from the reports: few CTAs (the pipeline, or persistent
+    // CTAs), each taking every segment's decision once.
+    if (vec && (!s.reports || s.decided)) {
         auto kern = update_seg_grid_kernel<GT, AMS, FIRST, kUnroll, kUThreads>;
         const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
         int64_t need = (s.a.nvec + per_cta - 1) / per_cta;
@@ -1024,6 +1049,8 @@ cudaError_t launch_seg_typed(const SegScaleArgs &s, const Coef &c, bool vec, cud
         if (need <= kMaxGridX) {
             const int grid = static_cast<int>(need);
             if (grid == 0) return cudaSuccess;
+            if (s.decided)  // scheduled while the decision kernel before it runs
+                return launch_dependent(kern, dim3(grid), dim3(kUThreads), 0, st, s, c);
             kern<<<grid, kUThreads, 0, st>>>(s, c);
             return cudaGetLastError();
         }
@@ -1091,6 +1118,7 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         s.reports = nullptr;
         s.nreports = 0;
         s.k0 = 0;
+        s.decided = nullptr;
         bool launched = false;
         err = launch_tma_if_large<GT, AMS, FIRST, MD, false>(s, c, vector_ok, dev, stream, &launched);
         if (err != cudaSuccess || launched) return err;
@@ -1154,6 +1182,12 @@ cudaError_t launch_gt(const UpdateArgs &a, const Coef &c, bool ams, bool first, 
 
 }  // namespace
 
+cudaError_t launch_segment_decide(const UpdateArgs &a, const fa_stats *reports, int32_t nseg,
+                                  float *decided, cudaStream_t stream) {
+    return launch_dependent(segment_decide_kernel, dim3(1), dim3(kDecideThreads), 0, stream, a,
+                            reports, nseg, decided);
+}
+
 cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, fa_dtype gdt,
                                          bool amsgrad, bool first, bool vector_ok,
                                          cudaStream_t stream) {
@@ -1178,6 +1212,7 @@ cudaError_t launch_pipeline_selftest(const UpdateArgs &a, const Coef &c, fa_dtyp
     s.reports = nullptr;
     s.nreports = 0;
     s.k0 = 0;
+    s.decided = nullptr;
     switch (gdt) {
         case FA_F32:
             return launch_tma_if_large<FA_F32, false, false, kNoModel, false>(s, c, true, dev,

@@ -492,9 +492,12 @@ fa_status fa_bucket_step_clipped_per_segment(
  * "ネイティブ PyTorch ストレージと階層統計": merge_gradient_stats_chunks; [TR-zh]
  * "FP32 主参数与混合参数存储": per-parameter clipping): the
  * segment-aligned analysis, the per-segment merges into seg_reports and the
- * update deciding per segment on the device (fa_bucket_update with seg_reports)
- * are enqueued back to back;
- * nothing is read back and the call does not wait.  Results are bit-identical to
+ * update deciding per segment on the device are enqueued back to back;
+ * nothing is read back and the call does not wait.  Once the merges are done
+ * with ``scratch``, and when it holds at least nseg + 1 elements, one small
+ * kernel takes every segment's decision there and the update reads it;
+ * otherwise the update decides from seg_reports itself (as fa_bucket_update
+ * with seg_reports).  Either way the results are bit-identical to
  * fa_bucket_step_clipped_per_segment.  ``t`` is the completed step count and is
  * not changed (the caller reads seg_reports after the stream reaches them and
  * advances its count unless one counts a non-finite value).  For n_total == 0

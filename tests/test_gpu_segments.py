@@ -231,6 +231,12 @@ def _gated_layout(kind):
         return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
     if kind == "many":  # 300 segments: two launches, the skip vote over all of them
         return _segments(42, 300, 4000, empty_every=7)
+    if kind == "sparse":  # 110 of 120 segments empty: the scratch (3 words per group of
+        # rows) is too small for the decided table, so every launch decides itself
+        rng = np.random.default_rng(43)
+        sizes = np.zeros(120, np.int64)
+        sizes[::12] = rng.integers(150_000, 250_000, 10)
+        return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
     return _scaled_decoder_offsets()  # "small" and "offset": register and scalar kernels
 
 
@@ -239,12 +245,14 @@ def _gated_layout(kind):
     ("small", "f16", False, 1.0), ("offset", "bf16", False, 1.0),
     # powers of two decide on the full grid; other scales keep the pipeline and the
     # persistent kernel, whose few CTAs take the FP64 divisions
-    ("mixed", "f16", False, 3.0), ("many", "bf16", False, 0.1), ("small", "f16", True, 2.0 ** -4)])
+    ("mixed", "f16", False, 3.0), ("many", "bf16", False, 0.1), ("small", "f16", True, 2.0 ** -4),
+    ("sparse", "bf16", False, 1.0), ("sparse", "f16", True, 3.0)])
 def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize, scale):
     """The per-segment step decided on the device (every segment's coefficient and the
-    skip taken in the update kernels from the device-resident reports) against the
-    host-decided per-segment step, over four calls with a +Inf in the third: reports,
-    parameters and every moment bit for bit, the +Inf call skipped by both."""
+    skip taken on the device from the device-resident reports: once for the bucket in
+    the scratch when it has room, else in each update launch) against the host-decided
+    per-segment step, over four calls with a +Inf in the third: reports, parameters and
+    every moment bit for bit, the +Inf call skipped by both."""
     seg = _gated_layout(kind)
     n = int(seg[-1])
     w = dataclasses.replace(CONFIG4, segments=None, calls=4, inf_call=3, grad_sigma=1e-2,
