@@ -464,7 +464,9 @@ def fa_bucket_step_clipped_per_segment_gated(seg_offsets, p, g, m, v, vmax, t: i
                                              rows_buf: torch.Tensor, scratch: torch.Tensor,
                                              seg_reports: torch.Tensor, stream=None) -> None:
     """Enqueues analysis, per-segment merges and the device-decided per-segment update;
-    nothing is read back.  The caller reads ``seg_reports`` and advances t."""
+    nothing is read back.  When ``scratch`` holds nseg + 1 elements, the decisions are
+    taken there once (its contents are scratch either way).  The caller reads
+    ``seg_reports`` and advances t."""
     n = p.numel()
     _dense("p", p, n, (torch.float32,))
     _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
