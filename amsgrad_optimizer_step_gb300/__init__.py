@@ -254,11 +254,14 @@ def fa_bucket_update(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
                      seg_grad_mult: Optional[Sequence[float]] = None,
                      report: Optional[torch.Tensor] = None,
                      seg_reports: Optional[torch.Tensor] = None, max_grad_norm: float = 0.0,
-                     p_model: Optional[torch.Tensor] = None, stream=None) -> bool:
+                     p_model: Optional[torch.Tensor] = None,
+                     seg_decided: Optional[torch.Tensor] = None, stream=None) -> bool:
     """One update of a pre-flattened bucket in any variant (the fa_bucket_update_args record):
     a host multiplier (``grad_mult``, or ``seg_grad_mult`` per segment) or the decision on
     the device from ``report`` / ``seg_reports`` with ``max_grad_norm``, and optionally the
-    BF16/FP16 model copy ``p_model``.  The update is step t + 1; t is not changed.
+    BF16/FP16 model copy ``p_model``.  ``seg_decided`` (FP32 device scratch of at least
+    nseg + 1 elements, with ``seg_reports``): where every segment's decision is taken once
+    before the update.  The update is step t + 1; t is not changed.
     Returns True when an update kernel was enqueued."""
     n = p.numel()
     _dense("p", p, n, (torch.float32,))
@@ -271,6 +274,8 @@ def fa_bucket_update(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
         _dense("p_model", p_model, n, (torch.float16, torch.bfloat16), p.device)
     if report is not None:
         _stats_tensor("report", report)
+    if seg_decided is not None:
+        _dense("seg_decided", seg_decided, seg_decided.numel(), (torch.float32,), p.device)
     seg, nseg = _segments(seg_offsets)
     if seg_reports is not None:
         _stats_tensor("seg_reports", seg_reports)
@@ -286,7 +291,9 @@ def fa_bucket_update(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
         m=_ptr(m), v=_ptr(v), vmax=_ptr(vmax), t=t, grad_mult=grad_mult, seg_grad_mult=mult,
         report=_ptr(report), seg_reports=_ptr(seg_reports), max_grad_norm=max_grad_norm,
         p_model=_ptr(p_model),
-        model_dtype=_TORCH_GRAD[p_model.dtype] if p_model is not None else FA_BF16)
+        model_dtype=_TORCH_GRAD[p_model.dtype] if p_model is not None else FA_BF16,
+        seg_decided=_ptr(seg_decided),
+        seg_decided_elements=seg_decided.numel() if seg_decided is not None else 0)
     enq = ctypes.c_int32()
     check("fa_bucket_update", _L().fa_bucket_update(ctypes.byref(u), ctypes.byref(opts), ctl,
                                                     ctypes.byref(enq), _stream(stream)))

@@ -42,7 +42,7 @@ class FaBucketUpdate(ctypes.Structure):
                 ("vmax", c_vp), ("t", c_u64), ("grad_mult", c_f64),
                 ("seg_grad_mult", ctypes.POINTER(c_f64)), ("report", c_vp),
                 ("seg_reports", c_vp), ("max_grad_norm", c_f64), ("p_model", c_vp),
-                ("model_dtype", c_i32)]
+                ("model_dtype", c_i32), ("seg_decided", c_vp), ("seg_decided_elements", c_i64)]
 
 
 class FaStepReport(ctypes.Structure):

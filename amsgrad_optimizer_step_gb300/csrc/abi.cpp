@@ -625,8 +625,11 @@ fa_status fa_bucket_update(const fa_bucket_update_args *u, const fa_options *opt
         if (u->model_dtype != FA_F16 && u->model_dtype != FA_BF16) return FA_ERR_DTYPE;
         if (per_segment) return FA_ERR_OPTION;  // no per-segment kernel writes a model copy
     }
+    if (u->seg_decided && !u->seg_reports) return FA_ERR_OPTION;
     if (per_segment && u->nseg < 1) return FA_ERR_SEGMENTS;
     if ((st = check_segments(u->seg_offsets, u->nseg, u->n_total)) != FA_OK) return st;
+    if (u->seg_decided && u->seg_decided_elements < static_cast<int64_t>(u->nseg) + 1)
+        return FA_ERR_SIZE;
     if (u->seg_grad_mult)
         for (int32_t k = 0; k < u->nseg; ++k)
             if (!is_finite(u->seg_grad_mult[k]) || u->seg_grad_mult[k] < 0) return FA_ERR_OPTION;
@@ -655,10 +658,17 @@ fa_status fa_bucket_update(const fa_bucket_update_args *u, const fa_options *opt
     for (const Range &r : state)
         if (overlap(model, r) || overlap(rep, r)) return FA_ERR_ALIAS;
     if (overlap(model, rep)) return FA_ERR_ALIAS;
+    if (u->seg_decided) {
+        if ((st = check_device_ptr(u->seg_decided, dev, 4)) != FA_OK) return st;
+        const Range dec{u->seg_decided, (static_cast<size_t>(u->nseg) + 1) * 4};
+        for (const Range &r : state)
+            if (overlap(dec, r)) return FA_ERR_ALIAS;
+        if (overlap(dec, rep)) return FA_ERR_ALIAS;
+    }
     if (per_segment)
         st = enqueue_segment_update(u->seg_offsets, u->nseg, u->p, u->g, u->gdt, u->m, u->v,
                                     u->vmax, u->t + 1, options, ctl, u->seg_grad_mult,
-                                    u->seg_reports, u->max_grad_norm, stream);
+                                    u->seg_reports, u->max_grad_norm, stream, u->seg_decided);
     else
         st = enqueue_update(u->n_total, u->p, u->g, u->gdt, u->m, u->v, u->vmax, u->p, u->m, u->v,
                             u->vmax, options, u->t + 1, ctl.gradient_scale, u->grad_mult, stream,

@@ -1021,18 +1021,21 @@ def run_ours(args):
             sstate["t"], sstate["rep"], _, _ = fa.fa_bucket_step_clipped_per_segment(
                 seg, sp, sg, sm, sv, svm, sstate["t"], so, ctl, 0.01, 512, srows, sscr, srep)
 
-        # the same step decided on the device, as one call: analysis, merges, every
-        # segment's decision taken once in the merge scratch, and the update on the full
-        # grid reading it, enqueued without waiting for the host; the host reads the
-        # 199 reports afterwards only to advance the step count
+        # the same step decided on the device: the 199 reports are copied to pinned
+        # memory right behind the merges; every segment's decision is then taken once in
+        # the merge scratch (free again) and the update runs on the full grid reading
+        # it, without waiting for the host, which reads the reports only to advance the
+        # step count
         srep_pinned = torch.empty(srep.shape, dtype=srep.dtype).pin_memory()
         srep_ready = torch.cuda.Event()
 
         def per_segment():
-            fa.fa_bucket_step_clipped_per_segment_gated(seg, sp, sg, sm, sv, svm, sstate["t"],
-                                                        so, ctl, 0.01, 512, srows, sscr, srep)
+            fa.fa_analyze_gradient(sg, 512, srows, seg)
+            fa.fa_merge_gradient_stats_chunks(srows, crow, sscr, srep)
             srep_pinned.copy_(srep, non_blocking=True)
             srep_ready.record(stream)
+            fa.fa_bucket_update(seg, sp, sg, sm, sv, svm, sstate["t"], so, ctl, seg_reports=srep,
+                                max_grad_norm=0.01, seg_decided=sscr)
             srep_ready.synchronize()
             if not bool((srep_pinned[:, 1] != 0).any()):
                 sstate["t"] += 1
@@ -1062,7 +1065,7 @@ def run_ours(args):
             "bytes_per_param": b3, "achieved_gbs": b3 * sn / (ms * 1e-3) / 1e9,
             "frac": b3 * sn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
             "params_per_s": sn / (ms * 1e-3), "min_clip_coef": min_coef,
-            "decided": "on the device, once per segment (one call)", "host_decided_ms": ms_host}
+            "decided": "on the device, once per segment", "host_decided_ms": ms_host}
         # the same bucket without statistics (AMSGrad, FP16 gradients, one launch over
         # 199 tensors), maximize off and on
         for tag, cfg in (("", CONFIG4), ("_maximize", CONFIG4_MAX)):

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 1
+#define FA_ABI_VERSION 2
 
 typedef enum fa_status {
     FA_OK = 0,
@@ -282,7 +282,13 @@ fa_status fa_bucket_step(const int64_t *seg_offsets, int32_t nseg, int64_t n_tot
  *   - seg_reports (device, nseg fa_stats as written by
  *     fa_merge_gradient_stats_chunks earlier on the same stream): the same per
  *     segment.  Any non-finite count skips the whole update; segment k takes the
- *     coefficient of record k.
+ *     coefficient of record k.  With seg_decided (device scratch of
+ *     seg_decided_elements >= nseg + 1 FP32 elements, FA_ERR_SIZE when fewer,
+ *     overlapping no other buffer; only with seg_reports, else FA_ERR_OPTION),
+ *     one small kernel first takes every segment's decision there, once for the
+ *     bucket, and the update kernels read it instead of each deciding from the
+ *     reports: the same bits, and faster on large buckets.  Its contents are
+ *     scratch.
  *
  * p_model (device, n_total elements of model_dtype = FA_F16 or FA_BF16, 2-byte
  * aligned, overlapping no other buffer): each updated FP32 p rounded to nearest,
@@ -315,6 +321,8 @@ typedef struct fa_bucket_update_args {
     double max_grad_norm;         /* clip threshold of the device decisions (<= 0: none) */
     void *p_model;                /* device FP16/BF16 copy of the updated p, or NULL  */
     fa_dtype model_dtype;         /* FA_F16 or FA_BF16 when p_model is set            */
+    float *seg_decided;           /* with seg_reports: device scratch for the decisions, or NULL */
+    int64_t seg_decided_elements; /* its FP32 elements (at least nseg + 1)            */
 } fa_bucket_update_args;
 
 /* Enqueues the bucket update that ``update`` describes ([FA-ja] "サポートされている

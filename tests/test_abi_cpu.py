@@ -49,7 +49,7 @@ def test_binding_names_match_header():
 
 
 def test_abi_version_and_defaults(lib):
-    assert fa.fa_abi_version() == 1
+    assert fa.fa_abi_version() == 2
     d = fa.fa_options_default()
     assert (d.beta1, d.beta2, d.eps, d.weight_decay, d.amsgrad, d.maximize) == \
         (0.9, 0.999, 1e-5, 1e-4, 0, 0)
@@ -257,7 +257,8 @@ def _update_record(**kw):
     fake = 0x1000
     base = dict(seg_offsets=None, nseg=0, n_total=16, p=fake, g=fake, gdt=0, m=fake, v=fake,
                 vmax=None, t=3, grad_mult=1.0, seg_grad_mult=None, report=None,
-                seg_reports=None, max_grad_norm=1.0, p_model=None, model_dtype=2)
+                seg_reports=None, max_grad_norm=1.0, p_model=None, model_dtype=2,
+                seg_decided=None, seg_decided_elements=0)
     base.update(kw)
     return FaBucketUpdate(**base)
 
@@ -298,6 +299,24 @@ def test_bucket_update_takes_one_multiplier_source(lib):
     assert _update(lib, seg_grad_mult=mult)[0] == 10  # per segment needs a segment table
     assert _update(lib, t=2 ** 64 - 1)[0] == 4          # the step count would overflow
     assert _update(lib, ctl=fa.control(skip_update=True), report=fake) == (0, 0)
+
+
+def test_bucket_update_decided_table_rules(lib):
+    """seg_decided, the scratch where every segment's decision is taken once: only with
+    seg_reports, and holding at least nseg + 1 elements; both checked on the host
+    before any pointer is looked at."""
+    seg = (ctypes.c_int64 * 3)(0, 8, 16)
+    mult = (ctypes.c_double * 2)(0.5, 1.0)
+    fake = 0x3000
+    assert _update(lib, seg_decided=fake, seg_decided_elements=3)[0] == 4
+    assert _update(lib, report=fake, seg_decided=fake, seg_decided_elements=3)[0] == 4
+    assert _update(lib, seg_grad_mult=mult, seg_offsets=seg, nseg=2, seg_decided=fake,
+                   seg_decided_elements=3)[0] == 4
+    assert _update(lib, seg_reports=fake, seg_offsets=seg, nseg=2, seg_decided=fake,
+                   seg_decided_elements=2)[0] == 3  # nseg + 1 = 3 needed
+    # skip: nothing launched, the table never looked at
+    assert _update(lib, seg_reports=fake, seg_offsets=seg, nseg=2, seg_decided=fake,
+                   seg_decided_elements=3, ctl=fa.control(skip_update=True)) == (0, 0)
 
 
 def test_chunk_scratch_plan():

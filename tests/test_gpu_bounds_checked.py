@@ -71,7 +71,9 @@ CASES = [
      lambda lib: [S.test_per_segment_gated_equals_host_decision_bitwise(*k) for k in (
          ("mixed", "f16", False, 1.0), ("many", "f32", False, 1.0),
          ("offset", "bf16", False, 1.0), ("mixed", "f16", False, 3.0),
-         ("small", "f16", True, 2.0 ** -4))]),
+         ("small", "f16", True, 2.0 ** -4))]
+                 + [S.test_composed_step_with_decided_table_equals_host_decision_bitwise(
+                     "many", "bf16")]),
     ("full-grid stretch edges and scalar heads, decided on the host and on the device",
      lambda lib: [P.test_full_grid_stretch_edges_and_scalar_heads(n, off, lib)
                   for n in (1025, 3 * 1024 + 5) for off in (0, 3)]),

@@ -3,7 +3,9 @@
 Every variant of the bucket update is one call with a descriptor: the multiplier from
 a host factor, one host factor per segment, one device report or one device report
 per segment, and optionally the low-precision model copy.  Each case draws a variant,
-a size (1 to 2.5 million), a segment table with empty segments, the gradient dtype,
+(one device report per segment, half of the time with the decisions taken once in a
+table first), a size (1 to 2.5 million), a segment table with empty segments, the
+gradient dtype,
 AMSGrad, maximize, a loss scale (a power of two in two cases of three, which a gated
 launch runs on the full grid; else 3, 0.3 or 1000, which it runs on the pipeline), a
 clip threshold (or none) and a skipped call, and runs three calls.  Each segment is compared with its own oracle run
@@ -79,6 +81,9 @@ def test_bucket_update_random_variant_vs_oracle(k, oracle_lib):
         rows_buf = fa.stats_buffer(crow[-1], DEV)
         scratch = torch.empty(max(1, fa.fa_stats_chunk_scratch(crow)), device=DEV)
         report = fa.stats_buffer(nseg, DEV)
+    # half of the per-segment device decisions take them once in a table first
+    decided = (torch.full((nseg + 1,), float("nan"), device=DEV)
+               if source == "seg_reports" and (k // 4) % 2 else None)
     t = 0
     for call in range(1, w.calls + 1):
         w.fill_grad_device(call, g)
@@ -108,7 +113,7 @@ def test_bucket_update_random_variant_vs_oracle(k, oracle_lib):
             if not skip:
                 fa.fa_analyze_gradient(g, 256, rows_buf, seg)
                 fa.fa_merge_gradient_stats_chunks(rows_buf, crow, scratch, report)
-            kw = dict(seg_reports=report, max_grad_norm=w.max_grad_norm)
+            kw = dict(seg_reports=report, max_grad_norm=w.max_grad_norm, seg_decided=decided)
         enq = fa.fa_bucket_update(seg, p, g, m, v, vmax, t, o, ctl, p_model=p_model, **kw)
         assert enq == (not skip and n > 0)
         t += int(enq)  # no gradient here is non-finite: a device decision never skips
@@ -137,7 +142,8 @@ def test_bucket_update_random_variant_vs_oracle(k, oracle_lib):
 
 def test_bucket_update_rejections_leave_everything_untouched():
     """Reports or a model copy overlapping the state or the gradient, a model copy with a
-    per-segment source, two sources at once, a host factor beside a device report: each
+    per-segment source, two sources at once, a host factor beside a device report, a
+    decision table without per-segment reports, too small or inside the state: each
     rejected before anything is enqueued, every buffer bit-identical afterwards."""
     n = 1 << 20
     p, m, v = (torch.randn(n, device=DEV) for _ in range(3))
@@ -156,6 +162,10 @@ def test_bucket_update_rejections_leave_everything_untouched():
         (4, dict(seg_grad_mult=[1.0, 1.0], p_model=model)),                  # no such kernel
         (4, dict(report=report[:1], seg_reports=report[:2])),                # two sources
         (4, dict(report=report[:1], grad_mult=0.5)),                         # factor + report
+        (4, dict(report=report[:1], seg_decided=torch.empty(3, device=DEV))),  # table, no seg
+        (3, dict(seg_reports=report[:2], max_grad_norm=1.0,
+                 seg_decided=torch.empty(2, device=DEV))),                   # table too small
+        (5, dict(seg_reports=report[:2], max_grad_norm=1.0, seg_decided=m[:3])),  # table in m
     ]
     for status, kw in cases:
         with pytest.raises(fa.FusedAdamWError) as e:

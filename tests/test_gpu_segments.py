@@ -294,6 +294,47 @@ def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize, sca
     assert ta == tb == 3
 
 
+@pytest.mark.parametrize("kind,gdt", [("mixed", "f16"), ("many", "bf16")])
+def test_composed_step_with_decided_table_equals_host_decision_bitwise(kind, gdt):
+    """The per-segment step composed from the public calls: the segment-aligned analysis,
+    the chunk merges, then fa_bucket_update with seg_reports and seg_decided, the merge
+    scratch reused as the decision table.  Against the host-decided one-call step over
+    four calls with a +Inf in the third: reports, p, m, v and vmax bit for bit."""
+    seg = _gated_layout(kind)
+    n = int(seg[-1])
+    w = dataclasses.replace(CONFIG4, segments=None, calls=4, inf_call=3, grad_sigma=1e-2,
+                            grad_dtype=gdt).scaled(n)
+    o = fa.options(**w.options())
+    sa = [torch.zeros(n, device=DEV) for _ in range(4)]
+    sb = [torch.zeros(n, device=DEV) for _ in range(4)]
+    w.fill_params_device(sa[0])
+    w.fill_params_device(sb[0])
+    g = torch.empty(n, dtype=TORCH_DT[gdt], device=DEV)
+    crow = fa.segment_rows(list(seg), 256)
+    nseg = len(seg) - 1
+    bufs = [(fa.stats_buffer(crow[-1], DEV), torch.empty(fa.fa_stats_chunk_scratch(crow), device=DEV),
+             fa.stats_buffer(nseg, DEV)) for _ in range(2)]
+    assert bufs[1][1].numel() >= nseg + 1
+    ta = tb = 0
+    for call in range(1, 5):
+        w.fill_grad_device(call, g)
+        ta, rep, _, _ = fa.fa_bucket_step_clipped_per_segment(
+            list(seg), sa[0], g, sa[1], sa[2], sa[3], ta, o, fa.control(), 0.05, 256, *bufs[0])
+        rows_b, scr_b, rep_b = bufs[1]
+        fa.fa_analyze_gradient(g, 256, rows_b, list(seg))
+        fa.fa_merge_gradient_stats_chunks(rows_b, crow, scr_b, rep_b)
+        fa.fa_bucket_update(list(seg), sb[0], g, sb[1], sb[2], sb[3], tb, o, fa.control(),
+                            seg_reports=rep_b, max_grad_norm=0.05, seg_decided=scr_b)
+        if not bool((rep_b.cpu()[:, 1] != 0).any()):
+            tb += 1
+        torch.cuda.synchronize()
+        assert torch.equal(bufs[0][2], rep_b), f"call {call}: reports differ"
+        assert bool(rep.skipped_nonfinite) == (call == 3) and ta == tb
+        for x, y, name in zip(sa, sb, ("p", "m", "v", "vmax")):
+            assert torch.equal(x, y), f"call {call}: {name} differs"
+    assert ta == tb == 3
+
+
 def test_per_segment_clipped_full_size_sampled(oracle_lib):
     """The per-parameter clipped step on the whole 1,195,991,040-parameter decoder bucket
     (199 segments, FP16 gradients, AMSGrad, rows of 512), in the launch configuration the
