@@ -99,6 +99,8 @@ inline double power_of_two_inverse(double s) {
     return (k < -1022 || k > 1022) ? 0.0 : std::ldexp(1.0, -k);
 }
 
+constexpr int64_t kMaxGridX = 0x7fffffff;  // the launch limit on gridDim.x
+
 constexpr int kRescueValueExp = 96;  // values of a rescued row are multiplied by 2^-96
 __host__ __device__ inline double record_sum_sq(const fa_stats &r) {
     const double s = static_cast<double>(r.sum_sq) + static_cast<double>(r.sum_sq_lo);

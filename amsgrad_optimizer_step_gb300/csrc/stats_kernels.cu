@@ -630,7 +630,6 @@ merge_chunks_b_kernel(const __grid_constant__ ChunkMergeArgs a) {
 // measured as fast or faster there (0.419 against 0.417-0.435 ms for the 199-segment
 // FP16 bucket of 1.2e9 parameters).
 constexpr int kFastFullThreads = 128;
-constexpr int64_t kMaxGridX = 0x7fffffff;  // the launch limit on gridDim.x
 
 template <int GT, int CH, bool MULTI>
 cudaError_t launch_fast(const AnalyzeArgs &a, int64_t need, int dev, cudaStream_t stream) {

@@ -76,8 +76,15 @@ namespace {
 constexpr int kVec = 8;  // elements per vector
 constexpr int kUThreads = FA_UPDATE_THREADS;
 constexpr int kUThreadsGated = FA_UPDATE_GATED_THREADS;
-constexpr int64_t kMaxGridX = 0x7fffffff;  // the launch limit on gridDim.x
 constexpr int kUnroll = FA_UPDATE_UNROLL;
+
+// CTAs of a full grid over nvec vectors: one per kUThreads * kUnroll vectors, and one
+// for a launch of scalar head and tail elements only (nvec == 0 < n).
+inline int64_t full_grid_ctas(int64_t nvec, int64_t n) {
+    const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
+    const int64_t need = (nvec + per_cta - 1) / per_cta;
+    return need == 0 && n > 0 ? 1 : need;
+}
 
 FA_BOUNDS_COUNTER(g_update_oob)
 
@@ -1043,10 +1050,8 @@ cudaError_t launch_seg_typed(const SegScaleArgs &s, const Coef &c, bool vec, cud
     // CTAs), each taking every segment's decision once.
     if (vec && (!s.reports || s.decided)) {
         auto kern = update_seg_grid_kernel<GT, AMS, FIRST, kUnroll, kUThreads>;
-        const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
-        int64_t need = (s.a.nvec + per_cta - 1) / per_cta;
-        if (need == 0 && s.a.n > 0) need = 1;  // head/tail elements only
-        if (need <= kMaxGridX) {
+        const int64_t need = full_grid_ctas(s.a.nvec, s.a.n);
+        if (need <= kMaxGridX) {  // the kernel has no loop: every stretch its own CTA
             const int grid = static_cast<int>(need);
             if (grid == 0) return cudaSuccess;
             if (s.decided)  // scheduled while the decision kernel before it runs
@@ -1103,9 +1108,7 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
     // per CTA (with multiplications instead of the FP64 divisions).
     if (vector_ok && a.gate && a.gate_inv_scale != 0.0) {
         auto kern = update_vec_cta_gate_kernel<GT, AMS, FIRST, kUnroll, MD, kUThreads>;
-        const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
-        int64_t need = (a.nvec + per_cta - 1) / per_cta;
-        if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
+        const int64_t need = full_grid_ctas(a.nvec, a.n);  // beyond the cap: the loop
         const int grid = static_cast<int>(need < kMaxGridX ? need : kMaxGridX);
         if (grid == 0) return cudaSuccess;
         return launch_dependent(kern, dim3(grid), dim3(kUThreads), 0, stream, a, c);
@@ -1143,9 +1146,7 @@ cudaError_t launch_typed(const UpdateArgs &a, const Coef &c, bool vector_ok,
         // of the same kernel and against the shared-memory (TMA) pipeline, it moves
         // every byte mix fastest.
         auto kern = update_vec_kernel<GT, AMS, FIRST, kUnroll, MD, kUThreads>;
-        const int64_t per_cta = static_cast<int64_t>(kUThreads) * kUnroll;
-        int64_t need = (a.nvec + per_cta - 1) / per_cta;
-        if (need == 0 && a.n > 0) need = 1;  // head/tail elements only
+        const int64_t need = full_grid_ctas(a.nvec, a.n);  // beyond the cap: the loop
         const int grid = static_cast<int>(need < kMaxGridX ? need : kMaxGridX);
         if (grid == 0) return cudaSuccess;
         kern<<<grid, kUThreads, 0, stream>>>(a, c);
