@@ -326,6 +326,12 @@ def report_mailbox() -> torch.Tensor:
     return torch.zeros(4, dtype=torch.int32).pin_memory()
 
 
+def _check_mailbox(mailbox) -> None:
+    if (not isinstance(mailbox, torch.Tensor) or mailbox.device.type != "cpu"
+            or mailbox.nbytes < 16 or not mailbox.is_contiguous() or not mailbox.is_pinned()):
+        raise ValueError("mailbox: expected a pinned, contiguous host tensor of 16 bytes")
+
+
 def fa_bucket_step_clipped_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: FaOptions,
                                  ctl: FaStepControl, max_grad_norm: float, row_len: int,
                                  rows_buf: torch.Tensor, scratch: Optional[torch.Tensor],
@@ -333,9 +339,7 @@ def fa_bucket_step_clipped_gated(seg_offsets, p, g, m, v, vmax, t: int, opts: Fa
                                  stream=None) -> tuple[int, FaStepReport]:
     """The statistics-guarded step with the update gated on the device; the report
     comes back through ``mailbox`` (see ``report_mailbox``).  Returns (t, report)."""
-    if (not isinstance(mailbox, torch.Tensor) or mailbox.device.type != "cpu"
-            or mailbox.nbytes < 16 or not mailbox.is_contiguous() or not mailbox.is_pinned()):
-        raise ValueError("mailbox: expected a pinned, contiguous host tensor of 16 bytes")
+    _check_mailbox(mailbox)
     n = p.numel()
     _dense("p", p, n, (torch.float32,))
     _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
@@ -469,11 +473,18 @@ def fa_bucket_step_clipped_per_segment_gated(seg_offsets, p, g, m, v, vmax, t: i
                                              opts: FaOptions, ctl: FaStepControl,
                                              max_grad_norm: float, row_len: int,
                                              rows_buf: torch.Tensor, scratch: torch.Tensor,
-                                             seg_reports: torch.Tensor, stream=None) -> None:
-    """Enqueues analysis, per-segment merges and the device-decided per-segment update;
-    nothing is read back.  When ``scratch`` holds nseg + 1 elements, the decisions are
-    taken there once (its contents are scratch either way).  The caller reads
-    ``seg_reports`` and advances t."""
+                                             seg_reports: torch.Tensor,
+                                             mailbox: Optional[torch.Tensor] = None,
+                                             stream=None) -> None:
+    """Enqueues analysis, per-segment merges and the device-decided per-segment update.
+    When ``scratch`` holds nseg + 1 elements, the decisions are taken there once (its
+    contents are scratch either way).  Without ``mailbox`` nothing is read back: the
+    caller reads ``seg_reports`` and advances t.  With a mailbox (``report_mailbox()``)
+    the call returns once the bucket's record is posted there (its count decides the
+    skip; ``fa_stats_sum_sq`` of it is the total sum of squares), while the update may
+    still run."""
+    if mailbox is not None:
+        _check_mailbox(mailbox)
     n = p.numel()
     _dense("p", p, n, (torch.float32,))
     _dense("g", g, n, tuple(_TORCH_GRAD), p.device)
@@ -491,7 +502,7 @@ def fa_bucket_step_clipped_per_segment_gated(seg_offsets, p, g, m, v, vmax, t: i
               seg, nseg, n, _ptr(p), _ptr(g), _TORCH_GRAD[g.dtype], _ptr(m), _ptr(v),
               _ptr(vmax), t, ctypes.byref(opts), ctl, max_grad_norm, row_len, _ptr(rows_buf),
               rows_buf.shape[0], _ptr(scratch), scratch.numel(), _ptr(seg_reports),
-              _stream(stream)))
+              _ptr(mailbox), _stream(stream)))
 
 
 def fa_read_report(report: torch.Tensor, stream=None) -> FaStats:

@@ -97,7 +97,7 @@ SIGNATURES = {
     "fa_bucket_step_clipped_per_segment_gated": (c_i32, [PI64, c_i32, c_i64, P, P, c_i32, P, P,
                                                          P, c_u64, ctypes.POINTER(FaOptions),
                                                          FaStepControl, c_f64, c_i32, P, c_i64,
-                                                         P, c_i64, P, P]),
+                                                         P, c_i64, P, P, P]),
     "fa_read_report": (c_i32, [P, ctypes.POINTER(FaStats), P]),
     "fa_clip_decision": (c_i32, [c_f64, c_u64, c_f64, c_f64, PI32, PF64, PF64]),
     "fa_clip_decide": (c_i32, [P, c_f64, c_f64, PI32, PF64, PF64, P]),

@@ -287,12 +287,15 @@ fa_status check_segments(const int64_t *seg, int32_t nseg, int64_t n) {
 // k's clip coefficient is the host formula's with max_grad_norm.  ``decided``
 // (device, nseg + 1 floats, or nullptr): where the decisions are first taken once
 // for the whole bucket (launch_segment_decide), for the update kernels to read.
+// ``post`` (device address of a pinned mailbox, or nullptr): where that kernel also
+// posts the bucket's record, then ``seq``.
 fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float *p,
                                  const void *g, fa_dtype gdt, float *m, float *v, float *vmax,
                                  uint64_t t_new, const fa_options *options, fa_step_control ctl,
                                  const double *seg_grad_mult, const fa_stats *reports,
                                  double max_grad_norm, void *stream,
-                                 float *decided = nullptr) {
+                                 float *decided = nullptr, fa_report_mailbox *post = nullptr,
+                                 uint32_t seq = 0) {
     Coef c;
     fa_status st = make_coef(options, t_new, ctl.gradient_scale, 1.0, &c);
     if (st != FA_OK) return st;
@@ -300,13 +303,13 @@ fa_status enqueue_segment_update(const int64_t *seg_offsets, int32_t nseg, float
     const bool ams = options->amsgrad != 0;
     const double sign = options->maximize ? -1.0 : 1.0;
     const size_t gb = dtype_bytes(gdt);
-    if (decided) {
+    if (decided || post) {
         fa::UpdateArgs gate{};
         gate.gate_scale = ctl.gradient_scale;
         gate.gate_max_norm = max_grad_norm;
         gate.gate_sign = sign;
         gate.gate_inv_scale = fa::power_of_two_inverse(ctl.gradient_scale);
-        if (fa::launch_segment_decide(gate, reports, nseg, decided,
+        if (fa::launch_segment_decide(gate, reports, nseg, decided, post, seq,
                                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return FA_ERR_CUDA;
     }
@@ -1127,7 +1130,7 @@ fa_status fa_bucket_step_clipped_per_segment_gated(
     fa_dtype gdt, float *m, float *v, float *vmax, uint64_t t, const fa_options *options,
     fa_step_control ctl, double max_grad_norm, int32_t row_len, fa_stats *rows_buf,
     int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
-    void *stream) {
+    fa_report_mailbox *mailbox, void *stream) {
     TraceRange trace("fa_bucket_step_clipped_per_segment_gated");
     fa_status st;
     if ((st = check_step_args(options, ctl, gdt, n_total)) != FA_OK) return st;
@@ -1152,6 +1155,12 @@ fa_status fa_bucket_step_clipped_per_segment_gated(
     const Range others[] = {{p, b}, {m, b}, {v, b}, {options->amsgrad ? vmax : nullptr, b}};
     for (const Range &r : others)
         if (overlap(rep, r)) return FA_ERR_ALIAS;
+    fa_report_mailbox *post = nullptr;
+    uint32_t seq = 0;
+    if (mailbox) {
+        if ((st = mailbox_device_ptr(mailbox, &post)) != FA_OK) return st;
+        seq = __atomic_load_n(&mailbox->seq, __ATOMIC_ACQUIRE) + 1;
+    }
     if ((st = fa_analyze_gradient(g, gdt, n_total, row_len, seg_offsets, nseg, rows_buf,
                                   rows_capacity, stream)) != FA_OK)
         return st;
@@ -1162,8 +1171,15 @@ fa_status fa_bucket_step_clipped_per_segment_gated(
     // nseg + 1 floats, every segment's decision is taken there once, and the update
     // runs on the full grid reading it.
     float *decided = scratch_elements >= static_cast<int64_t>(nseg) + 1 ? scratch : nullptr;
-    return enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, t + 1, options, ctl,
-                                  nullptr, seg_reports, max_grad_norm, stream, decided);
+    if ((st = enqueue_segment_update(seg_offsets, nseg, p, g, gdt, m, v, vmax, t + 1, options,
+                                     ctl, nullptr, seg_reports, max_grad_norm, stream, decided,
+                                     post, seq)) != FA_OK)
+        return st;
+    if (!mailbox) return FA_OK;
+    // the decision kernel posted the bucket's record before the update ran: wait for it
+    // only, so that the caller can advance its count while the update runs
+    fa_stats h{};
+    return wait_for_post(mailbox, seq, static_cast<cudaStream_t>(stream), &h);
 }
 
 fa_status fa_read_report(const fa_stats *report_dev, fa_stats *report_host, void *stream) {

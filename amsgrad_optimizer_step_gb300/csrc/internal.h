@@ -221,10 +221,13 @@ cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, f
 // One CTA takes every segment's decision from its record (the host formula's FP64
 // operations with a.gate_scale, a.gate_inv_scale, a.gate_max_norm, a.gate_sign) into
 // decided[1 + k] for k < nseg, and the skip flag (any non-finite count) into
-// decided[0].  Launched as the programmatic dependent of the merge that wrote the
-// records.
+// decided[0] (decided == nullptr: no table).  With ``post`` (device address of a
+// pinned host mailbox) it also posts the bucket's record there: the exact non-finite
+// count and the FP64 total of the segments' sums of squares, then ``seq``.  Launched as
+// the programmatic dependent of the merge that wrote the records.
 cudaError_t launch_segment_decide(const UpdateArgs &a, const fa_stats *reports, int32_t nseg,
-                                  float *decided, cudaStream_t stream);
+                                  float *decided, fa_report_mailbox *post, uint32_t seq,
+                                  cudaStream_t stream);
 
 // One merge level: ceil(count / kFanIn) output records from count input records.
 // ``post`` (device address of a pinned host mailbox, final level only) also receives

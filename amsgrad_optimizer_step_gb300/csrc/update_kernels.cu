@@ -503,19 +503,67 @@ __device__ __forceinline__ bool segment_multipliers(const SegScaleArgs &s, float
 }
 
 // Every segment's decision, once for the whole bucket (see launch_segment_decide).
+// The bucket's record from the FP64 total of its segments' sums of squares and their
+// non-finite count (saturating): a (hi, lo) pair of floats, scaled by 2^-192 and
+// negated once the total leaves the range where FP32 holds it safely, the two forms
+// that record_sum_sq decodes.
+__device__ __forceinline__ fa_stats bucket_record(double sum, unsigned long long count) {
+    fa_stats r;
+    r.nonfinite = count > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(count);
+    const bool scaled = !(sum < 0x1p126);
+    const double s = scaled ? sum * 0x1p-192 : sum;
+    const float hi = static_cast<float>(s);
+    const float lo = static_cast<float>(s - static_cast<double>(hi));
+    r.sum_sq = scaled ? -hi : hi;
+    r.sum_sq_lo = scaled ? -lo : lo;
+    return r;
+}
+
 constexpr int kDecideThreads = 256;
 __global__ void __launch_bounds__(kDecideThreads)
 segment_decide_kernel(const UpdateArgs a, const fa_stats *reports, int32_t nseg,
-                      float *decided) {
+                      float *decided, fa_report_mailbox *post, uint32_t seq) {
     fa_grid_dependency_wait();  // the merge that writes the records may still run
     bool bad = false;
+    double sum = 0.0;
+    unsigned long long count = 0;
     for (int j = threadIdx.x; j < nseg; j += kDecideThreads) {
         const fa_stats r = reports[j];
         bad |= r.nonfinite != 0;
-        decided[1 + j] = decided_multiplier(a, r);
+        count += r.nonfinite;
+        sum += record_sum_sq(r);
+        if (decided) decided[1 + j] = decided_multiplier(a, r);
     }
     const int skip = __syncthreads_or(bad);
-    if (threadIdx.x == 0) decided[0] = skip ? 1.0f : 0.0f;
+    if (decided && threadIdx.x == 0) decided[0] = skip ? 1.0f : 0.0f;
+    if (!post) return;
+    // the bucket's totals, in a fixed order: each warp by a shuffle tree, then the
+    // warps in turn
+    __shared__ double s_sum[kDecideThreads / 32];
+    __shared__ unsigned long long s_count[kDecideThreads / 32];
+    for (int d = 16; d > 0; d >>= 1) {
+        sum += __shfl_down_sync(0xffffffffu, sum, d);
+        count += __shfl_down_sync(0xffffffffu, count, d);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_sum[threadIdx.x >> 5] = sum;
+        s_count[threadIdx.x >> 5] = count;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    double total = 0.0;
+    unsigned long long total_count = 0;
+    for (int w = 0; w < kDecideThreads / 32; ++w) {
+        total += s_sum[w];
+        total_count += s_count[w];
+    }
+    const fa_stats rec = bucket_record(total, total_count);
+    volatile uint32_t *out = reinterpret_cast<volatile uint32_t *>(&post->report);
+    out[0] = __float_as_uint(rec.sum_sq);
+    out[1] = rec.nonfinite;
+    out[2] = __float_as_uint(rec.sum_sq_lo);
+    __threadfence_system();  // a host that sees seq reads the whole record
+    *reinterpret_cast<volatile uint32_t *>(&post->seq) = seq;
 }
 
 // The per-segment update on the full grid, with multipliers from the host or
@@ -1184,9 +1232,10 @@ cudaError_t launch_gt(const UpdateArgs &a, const Coef &c, bool ams, bool first, 
 }  // namespace
 
 cudaError_t launch_segment_decide(const UpdateArgs &a, const fa_stats *reports, int32_t nseg,
-                                  float *decided, cudaStream_t stream) {
+                                  float *decided, fa_report_mailbox *post, uint32_t seq,
+                                  cudaStream_t stream) {
     return launch_dependent(segment_decide_kernel, dim3(1), dim3(kDecideThreads), 0, stream, a,
-                            reports, nseg, decided);
+                            reports, nseg, decided, post, seq);
 }
 
 cudaError_t launch_update_segment_scaled(const SegScaleArgs &s, const Coef &c, fa_dtype gdt,

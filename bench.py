@@ -1049,10 +1049,22 @@ def run_ours(args):
         arr4 = {"p": sp, "m": sm, "v": sv, "vmax": svm}
         seg_clip = {"seg": seg, "max_grad_norm": 0.01, "g_full_bits": g4_all}
         before_f3 = row_snapshot(idx4, arr4, sstate["t"])
+        # and as one call, the host reading the bucket's record from a mailbox that the
+        # decision kernel posts before the update runs
+        f3_mailbox = fa.report_mailbox()
+
+        def per_segment_one_call():
+            fa.fa_bucket_step_clipped_per_segment_gated(seg, sp, sg, sm, sv, svm, sstate["t"],
+                                                        so, ctl, 0.01, 512, srows, sscr, srep,
+                                                        mailbox=f3_mailbox)
+            if int(f3_mailbox[1]) == 0:  # the bucket's non-finite count
+                sstate["t"] += 1
+
         ms_host = timed(per_segment_host, args.next_rows_steps)
         min_coef = sstate["rep"].clip_coef
         after_f3_host = row_snapshot(idx4, arr4, sstate["t"])
         ms = timed(per_segment, args.next_rows_steps)
+        ms_one_call = timed(per_segment_one_call, args.next_rows_steps)
         row_checks["f3_per_segment_clip_decoder1.1B_f16_amsgrad/host_decided"] = dict(
             seg_clip, w=CONFIG4, idx=idx4, gdt="f16", g_bits=g4_bits, p0_from_generator=True,
             before=before_f3, after=after_f3_host)
@@ -1065,7 +1077,8 @@ def run_ours(args):
             "bytes_per_param": b3, "achieved_gbs": b3 * sn / (ms * 1e-3) / 1e9,
             "frac": b3 * sn / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
             "params_per_s": sn / (ms * 1e-3), "min_clip_coef": min_coef,
-            "decided": "on the device, once per segment", "host_decided_ms": ms_host}
+            "decided": "on the device, once per segment", "host_decided_ms": ms_host,
+            "one_call_ms": ms_one_call}
         # the same bucket without statistics (AMSGrad, FP16 gradients, one launch over
         # 199 tensors), maximize off and on
         for tag, cfg in (("", CONFIG4), ("_maximize", CONFIG4_MAX)):

@@ -113,10 +113,11 @@ typedef struct fa_stats {
 /* A report mailbox: 16 bytes of pinned host memory that the device can write
  * (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped; with unified
  * addressing every pinned allocation qualifies), 4-byte aligned, owned by the
- * caller.  The merge that produces a step's final report also stores it here and
- * then, after a system-wide fence, its sequence number, so that the host can read
- * the report without a copy or an event on the stream.  One mailbox serves one call
- * at a time; its initial contents do not matter. */
+ * caller.  The kernel that produces a step's final record (the last merge, or the
+ * per-segment decision kernel) also stores it here and then, after a system-wide
+ * fence, its sequence number, so that the host can read the record without a copy
+ * or an event on the stream.  One mailbox serves one call at a time; its initial
+ * contents do not matter. */
 typedef struct fa_report_mailbox {
     fa_stats report;
     uint32_t seq;
@@ -501,23 +502,35 @@ fa_status fa_bucket_step_clipped_per_segment(
  * "FP32 主参数与混合参数存储": per-parameter clipping): the
  * segment-aligned analysis, the per-segment merges into seg_reports and the
  * update deciding per segment on the device are enqueued back to back;
- * nothing is read back and the call does not wait.  Once the merges are done
- * with ``scratch``, and when it holds at least nseg + 1 elements, one small
- * kernel takes every segment's decision there and the update reads it;
- * otherwise the update decides from seg_reports itself (as fa_bucket_update
- * with seg_reports).  Either way the results are bit-identical to
- * fa_bucket_step_clipped_per_segment.  ``t`` is the completed step count and is
- * not changed (the caller reads seg_reports after the stream reaches them and
- * advances its count unless one counts a non-finite value).  For n_total == 0
- * or ctl.skip_update nothing is enqueued and seg_reports is not written.  Other
- * arguments as fa_bucket_step_clipped_per_segment.
+ * nothing waits for the host.  Once the merges are done with ``scratch``, and
+ * when it holds at least nseg + 1 elements, one small kernel takes every
+ * segment's decision there and the update reads it; otherwise the update
+ * decides from seg_reports itself (as fa_bucket_update with seg_reports).
+ * Either way the results are bit-identical to fa_bucket_step_clipped_per_segment.
+ * ``t`` is the completed step count and is not changed: the caller advances
+ * its count unless the step counted a non-finite value.
+ *
+ * mailbox (optional, as in fa_bucket_step_clipped_gated): NULL returns once
+ * everything is enqueued, and the caller reads seg_reports after the stream
+ * reaches them.  Otherwise the kernel that takes the decisions, which runs
+ * before the update, posts the bucket's record to the mailbox: the exact count
+ * of non-finite values over all segments (saturating) and the FP64 total of
+ * the segments' sums of squares (decoded by fa_stats_sum_sq).  The call returns
+ * once that record is posted, while the update may still run, and the caller
+ * decides from mailbox->report.nonfinite.  The wait gives up with FA_ERR_CUDA
+ * as fa_bucket_step_clipped_gated's does; pageable or device memory is
+ * FA_ERR_POINTER.
+ *
+ * For n_total == 0 or ctl.skip_update nothing is enqueued, and neither
+ * seg_reports nor the mailbox is written.  Other arguments as
+ * fa_bucket_step_clipped_per_segment.
  */
 fa_status fa_bucket_step_clipped_per_segment_gated(
     const int64_t *seg_offsets, int32_t nseg, int64_t n_total, float *p, const void *g,
     fa_dtype gdt, float *m, float *v, float *vmax, uint64_t t, const fa_options *options,
     fa_step_control ctl, double max_grad_norm, int32_t row_len, fa_stats *rows_buf,
     int64_t rows_capacity, float *scratch, int64_t scratch_elements, fa_stats *seg_reports,
-    void *stream);
+    fa_report_mailbox *mailbox, void *stream);
 
 /* Copies the 12-byte device report to host memory and waits for the stream
  * ([TR-zh]: the report is read back before any update).  Synchronises. */

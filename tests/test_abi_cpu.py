@@ -359,7 +359,7 @@ def test_device_decided_calls_validate_on_the_host(lib):
     def clipped(row_len=256, scratch=1 << 20, ctl=None, nseg=2, table=seg):
         return lib.fa_bucket_step_clipped_per_segment_gated(
             table, nseg, 16, fake, fake, 0, fake, fake, None, 0, ctypes.byref(o),
-            ctl or fa.control(), 1.0, row_len, fake, 1 << 20, fake, scratch, fake, None)
+            ctl or fa.control(), 1.0, row_len, fake, 1 << 20, fake, scratch, fake, None, None)
     assert clipped(row_len=0) == 3
     assert clipped(nseg=0, table=None) == 10
     assert clipped(scratch=0) == 3

@@ -6,6 +6,7 @@ segment's update is the pinned update with that segment's coefficient.
 """
 
 import dataclasses
+import math
 
 import numpy as np
 import pytest
@@ -252,7 +253,10 @@ def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize, sca
     skip taken on the device from the device-resident reports: once for the bucket in
     the scratch when it has room, else in each update launch) against the host-decided
     per-segment step, over four calls with a +Inf in the third: reports, parameters and
-    every moment bit for bit, the +Inf call skipped by both."""
+    every moment bit for bit, the +Inf call skipped by both.  Two layouts read the
+    bucket's record through a mailbox (with the decision table, and without: the
+    scratch too small): when the call returns, the record holds the exact total count
+    and the total sum of squares within 1e-12 of the exact sum of the segments'."""
     seg = _gated_layout(kind)
     n = int(seg[-1])
     w = dataclasses.replace(CONFIG4, segments=None, calls=4, inf_call=3, grad_sigma=1e-2,
@@ -274,17 +278,31 @@ def test_per_segment_gated_equals_host_decision_bitwise(kind, gdt, maximize, sca
     bufs = [(fa.stats_buffer(crow[-1], DEV), torch.empty(fa.fa_stats_chunk_scratch(crow), device=DEV),
              fa.stats_buffer(len(seg) - 1, DEV)) for _ in range(2)]
     max_norm = 0.05
+    mailbox = fa.report_mailbox() if kind in ("mixed", "sparse") else None
     ta = tb = 0
     for call in range(1, 5):
         w.fill_grad_device(call, g)
         ta, rep, _, coefs = fa.fa_bucket_step_clipped_per_segment(
             list(seg), pa, g, ma, va, vma, ta, o, fa.control(scale), max_norm, row_len, *bufs[0])
         fa.fa_bucket_step_clipped_per_segment_gated(
-            list(seg), pb, g, mb, vb, vmb, tb, o, fa.control(scale), max_norm, row_len, *bufs[1])
+            list(seg), pb, g, mb, vb, vmb, tb, o, fa.control(scale), max_norm, row_len, *bufs[1],
+            mailbox=mailbox)
+        if mailbox is not None:  # posted before the call returned
+            words = mailbox.numpy().view(np.uint32)[:3].copy()
+            floats = words.view(np.float32)
+            posted = fa.FaStats(float(floats[0]), int(words[1]), float(floats[2]))
         rb = bufs[1][2].cpu()
         if not bool((rb[:, 1] != 0).any()):
             tb += 1
         torch.cuda.synchronize()
+        if mailbox is not None:
+            recs = [fa.FaStats(*x) for x in zip(rb[:, 0].view(torch.float32).tolist(),
+                                                 rb[:, 1].tolist(),
+                                                 rb[:, 2].view(torch.float32).tolist())]
+            assert posted.nonfinite == sum(r.nonfinite for r in recs)
+            if posted.nonfinite == 0:
+                exact = math.fsum(fa.fa_stats_sum_sq(r) for r in recs)
+                assert abs(fa.fa_stats_sum_sq(posted) - exact) <= 1e-12 * exact
         assert torch.equal(bufs[0][2], bufs[1][2]), f"call {call}: reports differ"
         assert bool(rep.skipped_nonfinite) == (call == 3) and ta == tb
         if call != 3:
@@ -333,6 +351,48 @@ def test_composed_step_with_decided_table_equals_host_decision_bitwise(kind, gdt
         for x, y, name in zip(sa, sb, ("p", "m", "v", "vmax")):
             assert torch.equal(x, y), f"call {call}: {name} differs"
     assert ta == tb == 3
+
+
+def test_per_segment_gated_mailbox_rules():
+    """The one-call per-segment step's optional mailbox: pageable host memory and device
+    memory are rejected (FA_ERR_POINTER) before anything is enqueued, with every buffer
+    untouched; NULL runs the call without waiting."""
+    import ctypes
+    from amsgrad_optimizer_step_gb300 import _lib
+    seg = _segments(44, 20, 3000)
+    n = int(seg[-1])
+    w = dataclasses.replace(CONFIG4, segments=None).scaled(n)
+    p = torch.empty(n, device=DEV)
+    w.fill_params_device(p)
+    m, v, vm = (torch.zeros(n, device=DEV) for _ in range(3))
+    g = torch.empty(n, dtype=torch.float16, device=DEV)
+    w.fill_grad_device(1, g)
+    crow = fa.segment_rows(list(seg), 256)
+    rows = fa.stats_buffer(crow[-1], DEV)
+    scr = torch.empty(fa.fa_stats_chunk_scratch(crow), device=DEV)
+    rep = fa.stats_buffer(len(seg) - 1, DEV)
+    rep.fill_(7)
+    o = fa.options(**w.options())
+    lib = _lib.load()
+    table = (ctypes.c_int64 * len(seg))(*[int(x) for x in seg])
+    snap = [x.clone() for x in (p, m, v, vm, rep)]
+
+    def raw(mailbox_ptr):
+        return lib.fa_bucket_step_clipped_per_segment_gated(
+            table, len(seg) - 1, n, p.data_ptr(), g.data_ptr(), 1, m.data_ptr(), v.data_ptr(),
+            vm.data_ptr(), 0, ctypes.byref(o), fa.control(), 0.05, 256, rows.data_ptr(),
+            rows.shape[0], scr.data_ptr(), scr.numel(), rep.data_ptr(), mailbox_ptr, None)
+
+    pageable = np.zeros(4, np.uint32)
+    assert raw(pageable.ctypes.data) == 6
+    on_device = torch.zeros(4, dtype=torch.int32, device=DEV)
+    assert raw(on_device.data_ptr()) == 6
+    torch.cuda.synchronize()
+    for a, b in zip((p, m, v, vm, rep), snap):
+        assert torch.equal(a, b)
+    assert raw(None) == 0
+    torch.cuda.synchronize()
+    assert not torch.equal(p, snap[0])  # the update ran
 
 
 def test_per_segment_clipped_full_size_sampled(oracle_lib):
