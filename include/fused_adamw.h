@@ -150,7 +150,9 @@ int32_t fa_abi_version(void);
  * pointers and overlaps are rejected before anything runs). */
 const char *fa_status_string(fa_status status);
 
-/* Large updates stage tiles through shared memory with TMA bulk copies; every
+/* Some large updates (steady steps decided on the device with a gradient scale
+ * that is not a power of two, or per segment from the reports in each launch)
+ * stage tiles through shared memory with TMA bulk copies; every
  * wait in that pipeline is bounded (about a second), and a wait that gives up
  * sets a device flag, drains its own copies and ends the kernel early (its
  * outputs are then incomplete: discard them, as [FA-ja] "低レベルの使用" asks of
